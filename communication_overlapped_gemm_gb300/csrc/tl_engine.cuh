@@ -1,0 +1,454 @@
+// Persistent, warp-specialised tcgen05 GEMM engine for sm_103a.
+//
+// One CTA per SM walks the global tile sequence t = blockIdx.x, blockIdx.x + grid, ...
+// Warp roles:
+//   warp 0      TMA producer.  Before a tile's loads it performs the consumer side
+//               of the tile-centric signal primitives (consumer_tile_wait /
+//               peer_tile_wait of "TileLink ...", §3.2 Table 3): the whole warp polls the
+//               tile's ready signals with acquire loads, then fences the async proxy,
+//               then lane 0 issues the TMA loads of the 4-stage A/B ring.
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and issues
+//               tcgen05.mma from one lane; tcgen05.commit frees smem stages and hands
+//               finished accumulators to the epilogue.
+//   warps 2-5   epilogue: tcgen05.ld -> registers -> per-op math -> swizzled smem
+//               staging -> TMA store / TMA bulk reduction; then the producer side of the
+//               signal primitives (producer_tile_notify) for tiles others wait on.
+//   warps 6..   shard mover (tile_pull_data of §3.2.2, pull mode): copies shard chunks
+//               between the emulated ranks' buffers and releases one signal per chunk.
+// The communication tile (mover chunk) and the compute tile (128x256) are chosen
+// independently, as in the decoupled design space of §3.1.
+//
+// Every wait is bounded by the context's timeout (on %globaltimer).  A signal wait that
+// runs out records TL_ERR_TIMEOUT in the status word and the producer continues, so the
+// pipeline drains normally; an mbarrier wait that runs out (an internal fault) records
+// the error and the role stops after draining its own copies in flight.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "tl_ptx.cuh"
+#include "tl_sched.h"
+
+namespace tl {
+
+constexpr int kStages = 4;
+constexpr int kAStageBytes = kBM * kBK * 2;               // 16 KB
+constexpr int kBStageBytes = kBN * kBK * 2;               // 32 KB
+constexpr int kStageBytes = kAStageBytes + kBStageBytes;  // 48 KB
+constexpr int kEpiBufBytes = 32 * 128;                    // 32 rows x 128 B
+constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;           // 4 warps x 2 buffers
+constexpr int kBarBytes = 256;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
+constexpr int kTmemCols = 512;
+constexpr int kCoreWarps = 6;  // producer, MMA, 4 epilogue
+constexpr int kMaxMoverWarps = 4;
+constexpr int kMaxThreads = (kCoreWarps + kMaxMoverWarps) * 32;
+
+// Status codes written to the device status word (host maps them to TL_ERR_*).
+constexpr unsigned kStatusTimeout = 4;
+// Places a wait can run out (recorded in DevStatus::where).
+enum WaitSite : unsigned {
+  kSiteSignal = 1, kSiteEmpty = 2, kSiteFull = 3, kSiteTmemEmpty = 4, kSiteTmemFull = 5,
+  kSitePeer = 6, kSiteDrain = 7, kSiteCombine = 8
+};
+
+struct DevStatus {
+  unsigned int code;
+  unsigned int where;
+  unsigned int abort;
+  unsigned int pad;
+  unsigned long long info;
+};
+
+struct Common {
+  DevStatus* status;
+  unsigned long long epoch;       // this call's signal value (never 0)
+  unsigned long long timeout_ns;  // bound of every wait
+  int mover_warps;
+};
+
+__device__ __forceinline__ void report_timeout(DevStatus* st, unsigned where, unsigned long long info) {
+  if (atomicCAS(&st->code, 0u, kStatusTimeout) == 0u) {
+    st->where = where;
+    st->info = info;
+  }
+  atomicExch(&st->abort, 1u);
+}
+
+__device__ __forceinline__ bool aborted(const DevStatus* st) {
+  return ld_relaxed_gpu_u32(&st->abort) != 0u;
+}
+
+// Bounded mbarrier wait.  Returns false (and records the site) when it runs out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Common& c, unsigned site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++n & 63u) == 0u && globaltimer() - t0 > 4ull * c.timeout_ns) {
+      report_timeout(c.status, site, 0);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Warp-collective signal wait: every lane polls its share of `count` signals at
+// flags[i] until each equals `want` (acquire), then the async proxy is fenced so the
+// TMA loads that follow observe the data the signals publish.  Returns false on
+// timeout (or if another wait already aborted the call); the caller proceeds anyway.
+__device__ __forceinline__ bool warp_wait_signals(const uint64_t* flags, int count, uint64_t want,
+                                                  const Common& c, int lane, unsigned site,
+                                                  unsigned long long info) {
+  bool ok = true;
+  uint64_t t0 = 0;
+  uint32_t n = 0;
+  for (;;) {
+    bool mine = true;
+    for (int i = lane; i < count; i += 32) mine &= (ld_acquire_gpu(flags + i) == want);
+    if (__all_sync(0xffffffffu, mine)) break;
+    if ((++n & 15u) == 0u) {
+      uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      const bool expired = (now - t0 > c.timeout_ns) || aborted(c.status);
+      if (__any_sync(0xffffffffu, expired)) {
+        if (lane == 0) report_timeout(c.status, site, info);
+        ok = false;
+        break;
+      }
+    }
+  }
+  fence_proxy_async_global();
+  return ok;
+}
+
+// Single-signal wait by every lane of a warp (used by epilogue warps for peer signals).
+__device__ __forceinline__ bool warp_wait_one(const uint64_t* flag, uint64_t want, const Common& c, int lane,
+                                              unsigned site, unsigned long long info) {
+  return warp_wait_signals(flag, 1, want, c, lane, site, info);
+}
+
+// Generic tile description produced by an op's scheduler.
+struct Job {
+  int kind;     // op-specific
+  int a_sel;    // which A tensor map
+  int a_row;    // A row coordinate
+  int b_sel;    // which B tensor map
+  int b_col;    // B column coordinate
+  int b_z;      // third B coordinate (expert), 0 if unused
+  int kblocks;  // K / 64, rounded up
+  int x0, x1, x2, x3;  // op-specific (ranks, owners, blocks)
+};
+
+struct Smem {
+  uint8_t* stages;
+  uint8_t* epi;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* tfull;
+  uint64_t* tempty;
+  uint64_t* drain;
+  uint32_t* tmem_slot;
+  uint32_t* epi_cnt;  // [2] publish-round counters, one per TMEM accumulator
+  __device__ uint8_t* a(int s) const { return stages + s * kStageBytes; }
+  __device__ uint8_t* b(int s) const { return stages + s * kStageBytes + kAStageBytes; }
+  __device__ uint8_t* epi_buf(int ew, int i) const { return epi + (ew * 2 + i) * kEpiBufBytes; }
+};
+
+// Write one 32-row x 128-byte chunk (lane = row) into a staging buffer laid out in the
+// TMA 128-byte swizzle: 16-byte piece j of row r lives at piece (j ^ (r & 7)).
+__device__ __forceinline__ void stage_row128(uint8_t* buf, int lane, const uint32_t (&w)[32]) {
+  const uint32_t base = smem_u32(buf) + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t piece = static_cast<uint32_t>(j ^ (lane & 7));
+    st_shared_v4(base + piece * 16, w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  }
+}
+
+// Epilogue staging state of one warp: double-buffered smem chunk + TMA bulk groups.
+struct EpiStage {
+  uint8_t* buf[2];
+  int idx;
+  // Get a free buffer: at most one bulk group of this warp may still be reading smem.
+  __device__ __forceinline__ uint8_t* acquire(int lane) {
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    return buf[idx];
+  }
+  __device__ __forceinline__ void flip() { idx ^= 1; }
+};
+
+template <class Op>
+__device__ __forceinline__ void role_producer(const typename Op::Params& p, const Smem& sm, int lane) {
+  const Common& c = p.common;
+  const int ntiles = Op::num_tiles(p);
+  uint32_t stage = 0, phase = 0;
+  uint32_t filled = 0, fill_parity = 0;  // per-stage: fill issued / parity of that fill
+  bool ok = true;
+  Op::producer_init(p);
+  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+    const Job j = Op::job(p, t);
+    for (int kb = 0; kb < j.kblocks; ++kb) {
+      Op::wait_deps(p, j, kb, lane);
+      if (lane == 0) {
+        ok = mbar_wait(&sm.empty[stage], phase ^ 1u, c, kSiteEmpty);
+        if (ok) {
+          mbar_arrive_expect_tx(&sm.full[stage], Op::kTxBytes);
+          Op::load(p, j, kb, sm.a(stage), sm.b(stage), &sm.full[stage]);
+          filled |= 1u << stage;
+          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    }
+  }
+  // Drain: every TMA fill this warp issued must have landed before the CTA exits.
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s)
+      if (filled & (1u << s)) mbar_wait(&sm.full[s], (fill_parity >> s) & 1u, c, kSiteDrain);
+  }
+  __syncwarp();
+}
+
+template <class Op>
+__device__ __forceinline__ void role_mma(const typename Op::Params& p, const Smem& sm, int lane,
+                                         uint32_t tmem_base) {
+  const Common& c = p.common;
+  const int ntiles = Op::num_tiles(p);
+  uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+  bool ok = true;
+  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+    const Job j = Op::job(p, t);
+    if (lane == 0) {
+      ok = mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, c, kSiteTmemEmpty);
+      tc_fence_after();
+      const uint32_t d = tmem_base + acc * kBN;
+      for (int kb = 0; kb < j.kblocks && ok; ++kb) {
+        ok = mbar_wait(&sm.full[stage], phase, c, kSiteFull);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sm.a(stage));
+        const uint32_t b0 = smem_u32(sm.b(stage));
+        Op::mma_stage(d, a0, b0, kb);
+        umma_commit(&sm.empty[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (ok) umma_commit(&sm.tfull[acc]);
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    acc ^= 1u;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+  // Drain: all MMAs this thread issued complete before TMEM is freed.
+  if (lane == 0) {
+    umma_commit(sm.drain);
+    mbar_wait(sm.drain, 0, c, kSiteDrain);
+  }
+  __syncwarp();
+}
+
+template <class Op>
+__device__ __forceinline__ void role_epilogue(const typename Op::Params& p, const Smem& sm, int warp,
+                                              int lane, uint32_t tmem_base) {
+  const Common& c = p.common;
+  const int ntiles = Op::num_tiles(p);
+  const int q = warp & 3;   // TMEM lane quadrant this warp may access
+  const int ew = warp - 2;  // epilogue warp index 0..3
+  EpiStage es;
+  es.buf[0] = sm.epi_buf(ew, 0);
+  es.buf[1] = sm.epi_buf(ew, 1);
+  es.idx = 0;
+  uint32_t acc = 0, acc_phase = 0;
+  bool ok = true;
+  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+    const Job j = Op::job(p, t);
+    ok = mbar_wait(&sm.tfull[acc], acc_phase, c, kSiteTmemFull);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t taddr = tmem_base + acc * kBN + (static_cast<uint32_t>(q * 32) << 16);
+    Op::epilogue(p, j, taddr, q, lane, es);
+    if (Op::publishes(p, j)) {
+      // producer_tile_notify: the last of the four warps to see its own stores of this
+      // tile complete publishes the tile's signal (release).  Each warp arrives here
+      // before it frees the accumulator, so arrivals of consecutive rounds on one TMEM
+      // buffer never interleave and a plain modulo-4 counter identifies the last one.
+      if (lane == 0) {
+        bulk_wait<0>();
+        fence_proxy_async_global();
+        __threadfence();
+        const uint32_t old = atomicAdd(&sm.epi_cnt[acc], 1u);
+        if ((old & 3u) == 3u) {
+          __threadfence();
+          Op::publish(p, j);
+        }
+      }
+      __syncwarp();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+    acc ^= 1u;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+  if (lane == 0) bulk_wait<0>();
+  __syncwarp();
+}
+
+template <class Op>
+__global__ void __launch_bounds__(kMaxThreads, 1) persistent_kernel(const __grid_constant__ typename Op::Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem sm;
+  sm.stages = base;
+  sm.epi = base + kStages * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm.epi + kEpiBytes);
+  sm.full = bars;
+  sm.empty = bars + kStages;
+  sm.tfull = bars + 2 * kStages;
+  sm.tempty = bars + 2 * kStages + 2;
+  sm.drain = bars + 2 * kStages + 4;
+  sm.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  sm.epi_cnt = sm.tmem_slot + 2;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.tfull[b], 1);
+      mbar_init(&sm.tempty[b], 4);
+    }
+    mbar_init(sm.drain, 1);
+    sm.epi_cnt[0] = 0;
+    sm.epi_cnt[1] = 0;
+    fence_mbar_init();
+    Op::prefetch(p);
+  }
+  if (warp == 1) {
+    tmem_alloc(sm.tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_slot;
+
+  if (warp == 0) {
+    role_producer<Op>(p, sm, lane);
+  } else if (warp == 1) {
+    role_mma<Op>(p, sm, lane, tmem_base);
+  } else if (warp < kCoreWarps) {
+    role_epilogue<Op>(p, sm, warp, lane, tmem_base);
+  } else {
+    Op::mover(p, warp - kCoreWarps, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ shared epilogue pieces
+
+// Load 64 accumulator columns [col, col+64) of this warp's 32 rows.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, int col, float (&v)[64]) {
+  float a[32], b[32];
+  tmem_ld32(taddr + col, a);
+  tmem_ld32(taddr + col + 32, b);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = a[i];
+    v[32 + i] = b[i];
+  }
+}
+
+__device__ __forceinline__ void pack64_bf16(const float (&v)[64], uint32_t (&w)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+}
+
+// Stage 64 bf16 columns of 32 rows and TMA-store them at (x, y) of `map`.
+__device__ __forceinline__ void store_bf16_chunk(const CUtensorMap* map, EpiStage& es, int lane,
+                                                 const float (&v)[64], int x, int y) {
+  uint32_t w[32];
+  pack64_bf16(v, w);
+  uint8_t* buf = es.acquire(lane);
+  stage_row128(buf, lane, w);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, buf, x, y);
+    bulk_commit();
+  }
+  es.flip();
+}
+
+// Stage 32 fp32 columns of 32 rows and TMA-store (reduce = false) or TMA-add (reduce = true).
+__device__ __forceinline__ void store_f32_chunk(const CUtensorMap* map, EpiStage& es, int lane,
+                                                const float (&v)[32], int x, int y, bool reduce) {
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+  uint8_t* buf = es.acquire(lane);
+  stage_row128(buf, lane, w);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (reduce)
+      tma_reduce_add_2d(map, buf, x, y);
+    else
+      tma_store_2d(map, buf, x, y);
+    bulk_commit();
+  }
+  es.flip();
+}
+
+// Operand layouts in shared memory (both written by TMA with the 128-byte swizzle):
+//   A (K-major): 128 rows x 128 B; 8-row core groups 1024 B apart (SBO); a K step of
+//     16 elements advances the start address by 32 B inside the swizzle atom.
+//   B (MN-major, B is K x N row-major): BN/64 column groups of [64 k-rows x 128 B]
+//     (8 KB each) -> LBO = 8192 B between 64-column groups, SBO = 1024 B between
+//     8-row K groups; a K step of 16 rows advances the start by 2048 B.
+#ifndef TL_B_LBO
+#define TL_B_LBO 8192
+#endif
+#ifndef TL_B_SBO
+#define TL_B_SBO 1024
+#endif
+
+// The standard single-accumulator MMA stage: 4 x (128x256x16) into d.
+__device__ __forceinline__ void mma_stage_256(uint32_t d, uint32_t a0, uint32_t b0, int kb) {
+  constexpr uint32_t idesc = umma_idesc_bf16(kBM, kBN, true);
+#pragma unroll
+  for (int k = 0; k < kBK / 16; ++k) {
+    const uint64_t ad = umma_desc_sw128(a0 + k * 32, 16, 1024);
+    const uint64_t bd = umma_desc_sw128(b0 + k * 2048, TL_B_LBO, TL_B_SBO);
+    umma_bf16(d, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+  }
+}
+
+// Mover copy of `bytes` (multiple of 16) from src to dst by `nthreads` threads.
+__device__ __forceinline__ void copy_chunk(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t nvec,
+                                           int tid, int nthreads) {
+  constexpr int U = 8;
+  size_t i = tid;
+  for (; i + (U - 1) * nthreads < nvec; i += U * nthreads) {
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) r[u] = __ldg(src + i + u * nthreads);
+#pragma unroll
+    for (int u = 0; u < U; ++u) dst[i + u * nthreads] = r[u];
+  }
+  for (; i < nvec; i += nthreads) dst[i] = __ldg(src + i);
+}
+
+}  // namespace tl

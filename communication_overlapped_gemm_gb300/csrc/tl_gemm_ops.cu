@@ -1,0 +1,573 @@
+// AllGather+GEMM, GEMM+ReduceScatter and the CTA-chained 2-layer MLP on the
+// persistent tcgen05 engine, plus their C-ABI entry points.
+#include <cuda_bf16.h>
+
+#include "tl_host.h"
+
+namespace tl {
+
+// ============================================================================ shared op pieces
+
+// Wait for the `chunks` mover signals of one slab.
+__device__ __forceinline__ void wait_slab(const uint64_t* flags, int chunks, const Common& c, int lane,
+                                          unsigned long long info) {
+  warp_wait_signals(flags, chunks, c.epoch, c, lane, kSiteSignal, info);
+}
+
+// Pull one chunk of a shard into the gathered buffer and release its signal
+// (tile_pull_data + producer notify of "TileLink ...", §3.2; pull-mode AllGather of
+// "Triton-distributed ...", §3.2 Algorithm 2, with the chunk as the communication tile).
+__device__ __forceinline__ void mover_chunk(const uint8_t* src, uint8_t* dst, size_t bytes, uint64_t* flag,
+                                            bool signal, const Common& c, int tid, int nthreads) {
+  copy_chunk(reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), bytes / 16, tid, nthreads);
+  __threadfence();
+  named_bar_sync(2, nthreads);
+  if (tid == 0 && signal) st_release_gpu(flag, c.epoch);
+}
+
+// GEMM+RS epilogue on one 128x256 partial tile of producer `prod` (of W), reduced into
+// the fp32 slot tile at (grow, n0); the last producer writes bf16 rows of `out` at orow.
+// Order of the fp32 sums is fixed: slot = P_0; slot += P_1; ...; out = slot + P_{W-1}.
+__device__ __forceinline__ void rs_epilogue(const CUtensorMap* acc_map, const float* acc_ptr,
+                                            const CUtensorMap* out_map, const uint64_t* flag, int prod, int W,
+                                            int grow, int orow, int n0, int n, const Common& c, uint32_t taddr,
+                                            int q, int lane, EpiStage& es) {
+  const bool first = prod == 0;
+  const bool last = prod == W - 1;
+  if (!first) {
+    // peer_tile_wait: producer prod-1 has finished its contribution to this tile.
+    warp_wait_one(flag, (c.epoch << 4) | static_cast<unsigned long long>(prod), c, lane, kSitePeer,
+                  static_cast<unsigned long long>(grow) << 20 | static_cast<unsigned>(n0));
+  }
+  if (!last) {
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      const int x = n0 + ch * 32;
+      if (x >= n) break;
+      float v[32];
+      tmem_ld32(taddr + ch * 32, v);
+      store_f32_chunk(acc_map, es, lane, v, x, grow + q * 32, !first);
+    }
+  } else {
+    const int row = grow + q * 32 + lane;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 64; ++ch) {
+      const int x = n0 + ch * 64;
+      if (x >= n) break;
+      float v[64];
+      tmem_ld64(taddr, ch * 64, v);
+      if (!first) {
+        const float* src = acc_ptr + static_cast<size_t>(row) * n + x;
+        if (x + 64 <= n) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float4 s = __ldcg(reinterpret_cast<const float4*>(src) + i);
+            v[4 * i] += s.x;
+            v[4 * i + 1] += s.y;
+            v[4 * i + 2] += s.z;
+            v[4 * i + 3] += s.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (x + i < n) v[i] += __ldcg(src + i);
+        }
+      }
+      store_bf16_chunk(out_map, es, lane, v, x, orow + q * 32);
+    }
+  }
+}
+
+// ============================================================================ AllGather + GEMM
+struct AgParams {
+  CUtensorMap a_local;  // shard `rank` read in place: {k, m_per_rank}, box {64, 128}
+  CUtensorMap a_gath;   // gathered buffer T: {k, W*m_per_rank}, box {64, 128}
+  CUtensorMap b;        // {n, k}, box {64, 64}
+  CUtensorMap c;        // {n, W*m_per_rank}, box {64, 32}
+  Common common;
+  const uint8_t* shard[8];
+  uint8_t* gath;
+  uint64_t* flags;  // [W][mps][chunks]
+  long long shard_bytes, slab_bytes;
+  int W, rank, m_per_rank, mps, n, nbk, kblocks, swizzle, chunks, skip_chunk;
+};
+
+struct AgOp {
+  using Params = AgParams;
+  static constexpr uint32_t kTxBytes = kStageBytes;
+  static __device__ int num_tiles(const Params& p) { return ag_num_tiles(p.W, p.mps, p.nbk); }
+  static __device__ Job job(const Params& p, int t) {
+    const AgTile a = ag_tile(t, p.W, p.rank, p.mps, p.nbk, p.swizzle);
+    Job j;
+    j.kind = 0;
+    j.a_sel = a.src == p.rank ? 0 : 1;
+    j.a_row = (a.src == p.rank ? 0 : a.src * p.m_per_rank) + a.mb * kBM;
+    j.b_sel = 0;
+    j.b_col = a.nb * kBN;
+    j.b_z = 0;
+    j.kblocks = p.kblocks;
+    j.x0 = a.src;
+    j.x1 = a.mb;
+    j.x2 = a.src * p.m_per_rank + a.mb * kBM;  // row of C
+    j.x3 = 0;
+    return j;
+  }
+  static __device__ void prefetch(const Params& p) {
+    tma_prefetch_map(&p.a_local);
+    tma_prefetch_map(&p.a_gath);
+    tma_prefetch_map(&p.b);
+    tma_prefetch_map(&p.c);
+  }
+  static __device__ void producer_init(const Params&) {}
+  // consumer_tile_wait: a remote row block is read only after every chunk of its slab
+  // has been released by the mover.
+  static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
+    if (kb != 0 || j.a_sel == 0) return;
+    const uint64_t* f = p.flags + (static_cast<size_t>(j.x0) * p.mps + j.x1) * p.chunks;
+    wait_slab(f, p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x0) << 32) | j.x1);
+  }
+  static __device__ void load(const Params& p, const Job& j, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+    tma_load_2d(sa, j.a_sel ? &p.a_gath : &p.a_local, bar, kb * kBK, j.a_row);
+#pragma unroll
+    for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.b, bar, j.b_col + g * 64, kb * kBK);
+  }
+  static __device__ void mma_stage(uint32_t d, uint32_t a0, uint32_t b0, int kb) { mma_stage_256(d, a0, b0, kb); }
+  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 64; ++ch) {
+      const int x = j.b_col + ch * 64;
+      if (x >= p.n) break;
+      float v[64];
+      tmem_ld64(taddr, ch * 64, v);
+      store_bf16_chunk(&p.c, es, lane, v, x, j.x2 + q * 32);
+    }
+  }
+  static __device__ bool publishes(const Params&, const Job&) { return false; }
+  static __device__ void publish(const Params&, const Job&) {}
+  static __device__ void mover(const Params& p, int mw, int lane) {
+    const int nthreads = p.common.mover_warps * 32;
+    const int tid = mw * 32 + lane;
+    const int per_shard = p.mps * p.chunks;
+    const int total = p.W * per_shard;
+    const size_t chunk_bytes = static_cast<size_t>(p.slab_bytes / p.chunks);
+    for (int g = blockIdx.x; g < total; g += gridDim.x) {
+      const int i = g / per_shard;
+      const int rem = g - i * per_shard;
+      const int slab = rem / p.chunks;
+      const int ch = rem - slab * p.chunks;
+      const int r = ag_mover_rank(p.W, p.rank, p.swizzle, i);
+      const size_t off = static_cast<size_t>(slab) * p.slab_bytes + static_cast<size_t>(ch) * chunk_bytes;
+      mover_chunk(p.shard[r] + off, p.gath + static_cast<size_t>(r) * p.shard_bytes + off, chunk_bytes,
+                  p.flags + (static_cast<size_t>(r) * p.mps + slab) * p.chunks + ch, g != p.skip_chunk, p.common,
+                  tid, nthreads);
+    }
+  }
+};
+
+// ============================================================================ GEMM + ReduceScatter
+struct RsParams {
+  CUtensorMap a[8];    // A_p: {k_r, m}, box {64, 128}
+  CUtensorMap b[8];    // B_p: {n, k_r}, box {64, 64}
+  CUtensorMap out[8];  // out_o: {n, m/W}, box {64, 32}
+  CUtensorMap acc;     // fp32 slot: {n, m}, box {32, 32}
+  Common common;
+  const float* acc_ptr;
+  uint64_t* flags;  // [m/128][nbk]
+  int W, m, mo, mbo, n, nbk, kblocks, swizzle;
+};
+
+struct RsOp {
+  using Params = RsParams;
+  static constexpr uint32_t kTxBytes = kStageBytes;
+  static __device__ int num_tiles(const Params& p) { return rs_num_tiles(p.W, p.mbo, p.nbk); }
+  static __device__ Job job(const Params& p, int t) {
+    const RsTile r = rs_tile(t, p.W, p.mbo, p.nbk, p.swizzle);
+    Job j;
+    j.kind = 0;
+    j.a_sel = r.p;
+    j.a_row = r.o * p.mo + r.mb * kBM;
+    j.b_sel = r.p;
+    j.b_col = r.nb * kBN;
+    j.b_z = 0;
+    j.kblocks = p.kblocks;
+    j.x0 = r.p;
+    j.x1 = r.o;
+    j.x2 = r.mb;
+    j.x3 = r.nb;
+    return j;
+  }
+  static __device__ void prefetch(const Params& p) { tma_prefetch_map(&p.acc); }
+  static __device__ void producer_init(const Params&) {}
+  static __device__ void wait_deps(const Params&, const Job&, int, int) {}
+  static __device__ void load(const Params& p, const Job& j, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+    tma_load_2d(sa, &p.a[j.a_sel], bar, kb * kBK, j.a_row);
+#pragma unroll
+    for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.b[j.b_sel], bar, j.b_col + g * 64, kb * kBK);
+  }
+  static __device__ void mma_stage(uint32_t d, uint32_t a0, uint32_t b0, int kb) { mma_stage_256(d, a0, b0, kb); }
+  static __device__ int tile_id(const Params& p, const Job& j) { return (j.a_row / kBM) * p.nbk + j.x3; }
+  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
+    rs_epilogue(&p.acc, p.acc_ptr, &p.out[j.x1], p.flags + tile_id(p, j), j.x0, p.W, j.a_row, j.x2 * kBM, j.b_col,
+                p.n, p.common, taddr, q, lane, es);
+  }
+  // peer_tile_notify: producer p's contribution to this slot tile is complete.
+  static __device__ bool publishes(const Params& p, const Job& j) { return j.x0 != p.W - 1; }
+  static __device__ void publish(const Params& p, const Job& j) {
+    st_release_gpu(p.flags + tile_id(p, j), (p.common.epoch << 4) | static_cast<unsigned long long>(j.x0 + 1));
+  }
+  static __device__ void mover(const Params&, int, int) {}
+};
+
+// ============================================================================ 2-layer MLP chain
+struct Mlp2Params {
+  CUtensorMap x_local[8];  // X_r in place: {h, Tr}, box {64, 128}
+  CUtensorMap w1[8];       // {f, h}, box {64, 64}
+  CUtensorMap w2[8];       // {h, f}, box {64, 64}
+  CUtensorMap out[8];      // {h, Tr}, box {64, 32}
+  CUtensorMap x_gath;      // per-rank gathered X: {h, W*T}, box {64, 128}
+  CUtensorMap h_st;        // H: {f, W*T}, box {64, 32}
+  CUtensorMap h_ld;        // H: {f, W*T}, box {64, 128}
+  CUtensorMap acc;         // fp32 slot {h, T}, box {32, 32}
+  Common common;
+  const uint8_t* x[8];
+  uint8_t* xg;
+  const float* acc_ptr;
+  uint64_t* ag_flags;  // [W gathering rank][W src][mps][chunks]
+  uint64_t* h_flags;   // [W][T/128][nb1]
+  uint64_t* rs_flags;  // [T/128][nb2]
+  long long shard_bytes, slab_bytes;
+  int W, T, Tr, h, f, mps, nb1, kb1, nb2, kb2, swizzle, chunks, skip_chunk;
+};
+
+struct Mlp2Op {
+  using Params = Mlp2Params;
+  static constexpr uint32_t kTxBytes = kStageBytes;
+  static __device__ int per_rank(const Params& p) { return p.W * p.mps * (p.nb1 + p.nb2); }
+  static __device__ int num_tiles(const Params& p) { return p.W * per_rank(p); }
+  // kind 1: layer-1 tile of rank x0 on shard x1, row block x2, column block (b_col)
+  // kind 2: layer-2 tile of producer x0 for owner x1, row block x2, column block x3
+  static __device__ Job job(const Params& p, int t) {
+    const int pr = per_rank(p);
+    const int r = t / pr;
+    const int u = t - r * pr;
+    const int n1 = p.W * p.mps * p.nb1;
+    Job j;
+    j.b_z = 0;
+    if (u < n1) {
+      const AgTile a = ag_tile(u, p.W, r, p.mps, p.nb1, p.swizzle);
+      j.kind = 1;
+      j.a_sel = a.src == r ? 0 : 1;
+      j.a_row = a.src == r ? a.mb * kBM : r * p.T + a.src * p.Tr + a.mb * kBM;
+      j.b_sel = r;
+      j.b_col = a.nb * kBN;
+      j.kblocks = p.kb1;
+      j.x0 = r;
+      j.x1 = a.src;
+      j.x2 = a.mb;
+      j.x3 = a.nb;
+    } else {
+      // this rank is the producer; it walks owners (r + 1 + step) mod W
+      const int per_owner = p.mps * p.nb2;
+      const int v = u - n1;
+      const int step = v / per_owner;
+      const int w = v - step * per_owner;
+      j.kind = 2;
+      j.x0 = r;
+      j.x1 = rs_owner(p.W, r, step, p.swizzle);
+      j.x2 = w / p.nb2;
+      j.x3 = w - j.x2 * p.nb2;
+      j.a_sel = 0;
+      j.a_row = r * p.T + j.x1 * p.Tr + j.x2 * kBM;
+      j.b_sel = r;
+      j.b_col = j.x3 * kBN;
+      j.kblocks = p.kb2;
+    }
+    return j;
+  }
+  static __device__ void prefetch(const Params& p) {
+    tma_prefetch_map(&p.x_gath);
+    tma_prefetch_map(&p.h_st);
+    tma_prefetch_map(&p.h_ld);
+    tma_prefetch_map(&p.acc);
+  }
+  static __device__ void producer_init(const Params&) {}
+  static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
+    if (kb != 0) return;
+    if (j.kind == 1) {
+      if (j.a_sel == 0) return;
+      const uint64_t* f =
+          p.ag_flags + ((static_cast<size_t>(j.x0) * p.W + j.x1) * p.mps + j.x2) * p.chunks;
+      wait_slab(f, p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x1) << 32) | j.x2);
+    } else {
+      // CTA-level chain: the layer-1 tiles that produce this row block of H_r are done.
+      const int rb = (j.x1 * p.Tr) / kBM + j.x2;
+      const uint64_t* f = p.h_flags + (static_cast<size_t>(j.x0) * (p.T / kBM) + rb) * p.nb1;
+      warp_wait_signals(f, p.nb1, p.common.epoch, p.common, lane, kSiteSignal,
+                        (2ull << 60) | (static_cast<unsigned long long>(j.x0) << 32) | rb);
+    }
+  }
+  static __device__ void load(const Params& p, const Job& j, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+    if (j.kind == 1) {
+      tma_load_2d(sa, j.a_sel ? &p.x_gath : &p.x_local[j.x0], bar, kb * kBK, j.a_row);
+#pragma unroll
+      for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.w1[j.b_sel], bar, j.b_col + g * 64, kb * kBK);
+    } else {
+      tma_load_2d(sa, &p.h_ld, bar, kb * kBK, j.a_row);
+#pragma unroll
+      for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.w2[j.b_sel], bar, j.b_col + g * 64, kb * kBK);
+    }
+  }
+  static __device__ void mma_stage(uint32_t d, uint32_t a0, uint32_t b0, int kb) { mma_stage_256(d, a0, b0, kb); }
+  static __device__ int h_row(const Params& p, const Job& j) { return j.x0 * p.T + j.x1 * p.Tr + j.x2 * kBM; }
+  static __device__ int rs_tile_id(const Params& p, const Job& j) {
+    return ((j.x1 * p.Tr) / kBM + j.x2) * p.nb2 + j.x3;
+  }
+  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
+    if (j.kind == 1) {
+      const int row = h_row(p, j) + q * 32;
+#pragma unroll 1
+      for (int ch = 0; ch < kBN / 64; ++ch) {
+        const int x = j.b_col + ch * 64;
+        if (x >= p.f) break;
+        float v[64];
+        tmem_ld64(taddr, ch * 64, v);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.70710678118654752f));
+        store_bf16_chunk(&p.h_st, es, lane, v, x, row);
+      }
+    } else {
+      rs_epilogue(&p.acc, p.acc_ptr, &p.out[j.x1], p.rs_flags + rs_tile_id(p, j), j.x0, p.W,
+                  j.x1 * p.Tr + j.x2 * kBM, j.x2 * kBM, j.b_col, p.h, p.common, taddr, q, lane, es);
+    }
+  }
+  static __device__ bool publishes(const Params& p, const Job& j) { return j.kind == 1 || j.x0 != p.W - 1; }
+  static __device__ void publish(const Params& p, const Job& j) {
+    if (j.kind == 1) {
+      const int rb = (j.x1 * p.Tr) / kBM + j.x2;
+      st_release_gpu(p.h_flags + (static_cast<size_t>(j.x0) * (p.T / kBM) + rb) * p.nb1 + j.x3, p.common.epoch);
+    } else {
+      st_release_gpu(p.rs_flags + rs_tile_id(p, j), (p.common.epoch << 4) | static_cast<unsigned long long>(j.x0 + 1));
+    }
+  }
+  // Every emulated rank r gathers the other ranks' X shards into its own copy of X
+  // (rows r*T ..), in its swizzled order; rank 0's gather first.
+  static __device__ void mover(const Params& p, int mw, int lane) {
+    const int nthreads = p.common.mover_warps * 32;
+    const int tid = mw * 32 + lane;
+    const int per_shard = p.mps * p.chunks;
+    const int per_rank = p.W * per_shard;
+    const int total = p.W * per_rank;
+    const size_t chunk_bytes = static_cast<size_t>(p.slab_bytes / p.chunks);
+    for (int g = blockIdx.x; g < total; g += gridDim.x) {
+      const int r = g / per_rank;
+      int rem = g - r * per_rank;
+      const int i = rem / per_shard;
+      rem -= i * per_shard;
+      const int slab = rem / p.chunks;
+      const int ch = rem - slab * p.chunks;
+      const int src = ag_mover_rank(p.W, r, p.swizzle, i);
+      const size_t off = static_cast<size_t>(slab) * p.slab_bytes + static_cast<size_t>(ch) * chunk_bytes;
+      uint8_t* dst = p.xg + (static_cast<size_t>(r) * p.T + static_cast<size_t>(src) * p.Tr) * p.h * 2 + off;
+      mover_chunk(p.x[src] + off, dst, chunk_bytes,
+                  p.ag_flags + ((static_cast<size_t>(r) * p.W + src) * p.mps + slab) * p.chunks + ch,
+                  g != p.skip_chunk, p.common, tid, nthreads);
+    }
+  }
+};
+
+}  // namespace tl
+
+using namespace tl;
+
+// ============================================================================ C ABI
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static bool ag_shape_ok(int W, int mpr, int n, int k) {
+  return W >= 1 && W <= 8 && mpr >= 0 && n >= 0 && k >= 0 && mpr % kBM == 0 && n % 8 == 0 && k % 8 == 0;
+}
+
+extern "C" size_t tl_ag_gemm_workspace_bytes(int W, int m_per_rank, int n, int k) {
+  if (!ag_shape_ok(W, m_per_rank, n, k)) return 0;
+  const size_t gath = static_cast<size_t>(W) * m_per_rank * k * 2;
+  const size_t flags = static_cast<size_t>(W) * (m_per_rank / kBM) * 32 * 8;
+  return align256(gath) + align256(flags);
+}
+
+extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b, void* c,
+                          void* workspace, size_t workspace_bytes, int m_per_rank, int n, int k,
+                          tl_stream_t stream) {
+  if (!ctx || !ag_shape_ok(W, m_per_rank, n, k) || rank < 0 || rank >= W) return TL_ERR_INVALID;
+  if (m_per_rank == 0 || n == 0 || k == 0) return TL_OK;
+  if (!a_shards || !b || !c || !workspace) return TL_ERR_INVALID;
+  for (int r = 0; r < W; ++r)
+    if (!a_shards[r] || !aligned16(a_shards[r])) return TL_ERR_INVALID;
+  if (!aligned16(b) || !aligned16(c) || !aligned16(workspace)) return TL_ERR_INVALID;
+  if (workspace_bytes < tl_ag_gemm_workspace_bytes(W, m_per_rank, n, k)) return TL_ERR_WORKSPACE;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
+
+  AgParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int M = W * m_per_rank;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t gath_bytes = static_cast<size_t>(M) * k * 2;
+  p.gath = ws;
+  p.flags = reinterpret_cast<uint64_t*>(ws + align256(gath_bytes));
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!tmap_2d(&p.a_local, BF, 2, a_shards[rank], k, m_per_rank, 64, 128) ||
+      !tmap_2d(&p.a_gath, BF, 2, p.gath, k, M, 64, 128) || !tmap_2d(&p.b, BF, 2, b, n, k, 64, 64) ||
+      !tmap_2d(&p.c, BF, 2, c, n, M, 64, 32))
+    return TL_ERR_CUDA;
+  p.common = make_common(ctx);
+  for (int r = 0; r < W; ++r) p.shard[r] = static_cast<const uint8_t*>(a_shards[r]);
+  p.W = W;
+  p.rank = rank;
+  p.m_per_rank = m_per_rank;
+  p.mps = m_per_rank / kBM;
+  p.n = n;
+  p.nbk = ceil_div(n, kBN);
+  p.kblocks = ceil_div(k, kBK);
+  p.swizzle = ctx->cfg.swizzle;
+  p.chunks = ctx->cfg.chunks_per_slab;
+  p.skip_chunk = ctx->cfg.debug_skip_chunk;
+  p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
+  p.slab_bytes = static_cast<long long>(kBM) * k * 2;
+  return launch_persistent<AgOp>(ctx, p, reinterpret_cast<cudaStream_t>(stream), ctx->cfg.mover_warps);
+}
+
+static bool rs_shape_ok(int W, int m, int n, int kr) {
+  return W >= 1 && W <= 8 && m >= 0 && n >= 0 && kr >= 0 && m % (kBM * W) == 0 && n % 8 == 0 && kr % 8 == 0;
+}
+
+extern "C" size_t tl_gemm_rs_workspace_bytes(int W, int m, int n, int k_r) {
+  if (!rs_shape_ok(W, m, n, k_r)) return 0;
+  const size_t acc = static_cast<size_t>(m) * n * 4;
+  const size_t flags = static_cast<size_t>(m / kBM) * ceil_div(n, kBN) * 8;
+  return align256(acc) + align256(flags);
+}
+
+extern "C" int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* const* b, void* const* out,
+                          void* workspace, size_t workspace_bytes, int m, int n, int k_r, tl_stream_t stream) {
+  if (!ctx || !rs_shape_ok(W, m, n, k_r)) return TL_ERR_INVALID;
+  if (m == 0 || n == 0) return TL_OK;
+  if (!a || !b || !out || !workspace || !aligned16(workspace)) return TL_ERR_INVALID;
+  for (int r = 0; r < W; ++r)
+    if (!a[r] || !b[r] || !out[r] || !aligned16(a[r]) || !aligned16(b[r]) || !aligned16(out[r]))
+      return TL_ERR_INVALID;
+  if (workspace_bytes < tl_gemm_rs_workspace_bytes(W, m, n, k_r)) return TL_ERR_WORKSPACE;
+  if (k_r == 0) return TL_ERR_INVALID;  // an empty reduction has no tiles to chain; reject
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
+
+  RsParams p;
+  std::memset(&p, 0, sizeof(p));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* acc = reinterpret_cast<float*>(ws);
+  p.acc_ptr = acc;
+  p.flags = reinterpret_cast<uint64_t*>(ws + align256(static_cast<size_t>(m) * n * 4));
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int mo = m / W;
+  for (int r = 0; r < W; ++r) {
+    if (!tmap_2d(&p.a[r], BF, 2, a[r], k_r, m, 64, 128) || !tmap_2d(&p.b[r], BF, 2, b[r], n, k_r, 64, 64) ||
+        !tmap_2d(&p.out[r], BF, 2, out[r], n, mo, 64, 32))
+      return TL_ERR_CUDA;
+  }
+  if (!tmap_2d(&p.acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, n, m, 32, 32)) return TL_ERR_CUDA;
+  p.common = make_common(ctx);
+  p.W = W;
+  p.m = m;
+  p.mo = mo;
+  p.mbo = mo / kBM;
+  p.n = n;
+  p.nbk = ceil_div(n, kBN);
+  p.kblocks = ceil_div(k_r, kBK);
+  p.swizzle = ctx->cfg.swizzle;
+  return launch_persistent<RsOp>(ctx, p, reinterpret_cast<cudaStream_t>(stream), 0);
+}
+
+static bool mlp2_shape_ok(int W, int T, int h, int f) {
+  return W >= 1 && W <= 8 && T >= 0 && h >= 0 && f >= 0 && T % (kBM * W) == 0 && h % 8 == 0 && f % 8 == 0;
+}
+
+struct Mlp2Layout {
+  size_t xg, hbuf, acc, agf, hf, rsf, total;
+};
+static Mlp2Layout mlp2_layout(int W, int T, int h, int f) {
+  Mlp2Layout L;
+  const size_t xg = static_cast<size_t>(W) * T * h * 2;
+  const size_t hb = static_cast<size_t>(W) * T * f * 2;
+  const size_t acc = static_cast<size_t>(T) * h * 4;
+  const size_t agf = static_cast<size_t>(W) * W * (T / W / kBM) * 32 * 8;
+  const size_t hf = static_cast<size_t>(W) * (T / kBM) * ceil_div(f, kBN) * 8;
+  const size_t rsf = static_cast<size_t>(T / kBM) * ceil_div(h, kBN) * 8;
+  L.xg = 0;
+  L.hbuf = align256(xg);
+  L.acc = L.hbuf + align256(hb);
+  L.agf = L.acc + align256(acc);
+  L.hf = L.agf + align256(agf);
+  L.rsf = L.hf + align256(hf);
+  L.total = L.rsf + align256(rsf);
+  return L;
+}
+
+extern "C" size_t tl_mlp2_workspace_bytes(int W, int tokens, int hidden, int f_r) {
+  if (!mlp2_shape_ok(W, tokens, hidden, f_r)) return 0;
+  return mlp2_layout(W, tokens, hidden, f_r).total;
+}
+
+extern "C" int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const void* const* w1,
+                       const void* const* w2, void* const* out, void* workspace, size_t workspace_bytes, int tokens,
+                       int hidden, int f_r, tl_stream_t stream) {
+  if (!ctx || !mlp2_shape_ok(W, tokens, hidden, f_r)) return TL_ERR_INVALID;
+  if (tokens == 0 || hidden == 0) return TL_OK;
+  if (f_r == 0) return TL_ERR_INVALID;
+  if (!x_shards || !w1 || !w2 || !out || !workspace || !aligned16(workspace)) return TL_ERR_INVALID;
+  for (int r = 0; r < W; ++r)
+    if (!x_shards[r] || !w1[r] || !w2[r] || !out[r] || !aligned16(x_shards[r]) || !aligned16(w1[r]) ||
+        !aligned16(w2[r]) || !aligned16(out[r]))
+      return TL_ERR_INVALID;
+  if (workspace_bytes < tl_mlp2_workspace_bytes(W, tokens, hidden, f_r)) return TL_ERR_WORKSPACE;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
+
+  const Mlp2Layout L = mlp2_layout(W, tokens, hidden, f_r);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Mlp2Params p;
+  std::memset(&p, 0, sizeof(p));
+  const int Tr = tokens / W;
+  p.xg = ws + L.xg;
+  uint8_t* hb = ws + L.hbuf;
+  float* acc = reinterpret_cast<float*>(ws + L.acc);
+  p.acc_ptr = acc;
+  p.ag_flags = reinterpret_cast<uint64_t*>(ws + L.agf);
+  p.h_flags = reinterpret_cast<uint64_t*>(ws + L.hf);
+  p.rs_flags = reinterpret_cast<uint64_t*>(ws + L.rsf);
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  for (int r = 0; r < W; ++r) {
+    if (!tmap_2d(&p.x_local[r], BF, 2, x_shards[r], hidden, Tr, 64, 128) ||
+        !tmap_2d(&p.w1[r], BF, 2, w1[r], f_r, hidden, 64, 64) ||
+        !tmap_2d(&p.w2[r], BF, 2, w2[r], hidden, f_r, 64, 64) ||
+        !tmap_2d(&p.out[r], BF, 2, out[r], hidden, Tr, 64, 32))
+      return TL_ERR_CUDA;
+    p.x[r] = static_cast<const uint8_t*>(x_shards[r]);
+  }
+  if (!tmap_2d(&p.x_gath, BF, 2, p.xg, hidden, static_cast<uint64_t>(W) * tokens, 64, 128) ||
+      !tmap_2d(&p.h_st, BF, 2, hb, f_r, static_cast<uint64_t>(W) * tokens, 64, 32) ||
+      !tmap_2d(&p.h_ld, BF, 2, hb, f_r, static_cast<uint64_t>(W) * tokens, 64, 128) ||
+      !tmap_2d(&p.acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, hidden, tokens, 32, 32))
+    return TL_ERR_CUDA;
+  p.common = make_common(ctx);
+  p.W = W;
+  p.T = tokens;
+  p.Tr = Tr;
+  p.h = hidden;
+  p.f = f_r;
+  p.mps = Tr / kBM;
+  p.nb1 = ceil_div(f_r, kBN);
+  p.kb1 = ceil_div(hidden, kBK);
+  p.nb2 = ceil_div(hidden, kBN);
+  p.kb2 = ceil_div(f_r, kBK);
+  p.swizzle = ctx->cfg.swizzle;
+  p.chunks = ctx->cfg.chunks_per_slab;
+  p.skip_chunk = ctx->cfg.debug_skip_chunk;
+  p.shard_bytes = static_cast<long long>(Tr) * hidden * 2;
+  p.slab_bytes = static_cast<long long>(kBM) * hidden * 2;
+  return launch_persistent<Mlp2Op>(ctx, p, reinterpret_cast<cudaStream_t>(stream), ctx->cfg.mover_warps);
+}

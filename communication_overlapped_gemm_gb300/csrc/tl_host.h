@@ -1,0 +1,76 @@
+// Host-side internals shared by the op translation units: the context, TMA
+// descriptor encoding (cuTensorMapEncodeTiled through the runtime's driver
+// entry point) and the cooperative persistent launch.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/tl.h"
+#include "tl_engine.cuh"
+
+struct tl_ctx {
+  int device;
+  int sms;
+  int ctas;
+  tl_config cfg;
+  tl::DevStatus* status;      // device status word (the only memory the library owns)
+  unsigned long long epoch;   // last signal value handed out
+};
+
+namespace tl {
+
+bool tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
+             uint64_t outer, uint32_t box_inner, uint32_t box_outer);
+bool tmap_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t d0, uint64_t d1,
+             uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Next signal value of this context (never 0; < 2^59 so that (epoch << 4) | 15 fits in 64 bits).
+inline unsigned long long next_epoch(tl_ctx* ctx) { return ++ctx->epoch; }
+
+inline Common make_common(tl_ctx* ctx) {
+  Common c;
+  c.status = ctx->status;
+  c.epoch = next_epoch(ctx);
+  c.timeout_ns = ctx->cfg.timeout_ns;
+  c.mover_warps = ctx->cfg.mover_warps;
+  return c;
+}
+
+int set_smem_attr(const void* kern);
+
+// Cooperative launch of one persistent CTA per SM (or cfg.grid_ctas), so that every CTA
+// that waits on a signal is co-resident with the CTAs that will set it.
+template <class Op>
+int launch_persistent(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t stream, int mover_warps) {
+  auto kern = persistent_kernel<Op>;
+  int rc = set_smem_attr(reinterpret_cast<const void*>(kern));
+  if (rc != TL_OK) return rc;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(ctx->ctas, 1, 1);
+  cfg.blockDim = dim3((kCoreWarps + mover_warps) * 32, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    (void)cudaGetLastError();
+    return TL_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TL_ERR_CUDA;
+  }
+  return TL_OK;
+}
+
+}  // namespace tl

@@ -1,0 +1,218 @@
+/*
+ * tl.h - C ABI of the GB300 (sm_103a) tile-centric communication-overlapped GEMM library.
+ *
+ * The library computes, on ONE GPU, the four overlapped operators of the pages it is
+ * built from, with the W tensor-parallel ranks emulated as W separate HBM buffers:
+ *
+ *   tl_ag_gemm      AllGather + GEMM:        C = [A_0; A_1; ...; A_{W-1}] . B
+ *   tl_gemm_rs      GEMM + ReduceScatter:    out_o = rows_o( sum_p A_p . B_p )
+ *   tl_mlp2         2-layer MLP chain:       out_o = rows_o( sum_r GELU(AG(X) . W1_r) . W2_r )
+ *   tl_moe_combine  top-k MoE layer:         out_t = sum_j g_tj * (SiLU(x_t Wg_e) * (x_t Wu_e)) Wd_e
+ *
+ * "Communication" is the movement of shards between the ranks' buffers inside one HBM,
+ * done by mover warps that publish per-chunk release flags; the persistent tcgen05 GEMM
+ * waits on those flags (acquire) before its TMA loads, walking its tiles in a rank-swizzled
+ * order that starts from the local shard.
+ *
+ * Sources (page titles; sections as printed on the pages):
+ *   [TL] TileLink: Generating Efficient Compute-Communication Overlapping Kernels using
+ *        Tile-Centric Primitives - §2.1 (tensor-parallel FFN), §3.1 (decoupled tile size /
+ *        order / resource binding), §3.2 Table 3 (producer_tile_notify, consumer_tile_wait,
+ *        peer_tile_notify/wait, tile_push_data, tile_pull_data), §4.1 (static and dynamic
+ *        tile-centric mapping), §4.2 (release/acquire lowering), §6 (BlockChannel context).
+ *   [TD] Triton-distributed: Programming Overlapping Kernels on Distributed AI Systems with
+ *        the Triton Compiler - §2.1 (symmetric memory, signal exchange, async tasks),
+ *        §3.2 Algorithm 2 (pull-mode AllGather), §3.3 Algorithm 3 (push-mode ReduceScatter),
+ *        §3.7 (tile swizzle for AG+GEMM and GEMM+RS), §3.8 (signal reset, resource partition).
+ *   [RA] Resource-aware Computation-Communication Overlap for multi-GPU ML Workloads -
+ *        CTA-pipelining abstract (2-layer GEMM with CTA-level dependencies) and the MoE
+ *        abstract (persistent expert producer, persistent combine consumer on a small
+ *        dedicated SM partition, tile-level signalling).
+ *
+ * Conventions for every entry point
+ *   - Matrices are row-major bf16 (IEEE bfloat16, passed as raw 16-bit storage), fp32 where
+ *     stated.  Every device pointer must be 16-byte aligned.  Accumulation is fp32.
+ *   - Ownership: the caller allocates every device buffer, including the workspace (size from
+ *     the matching *_workspace_bytes function).  The library owns only the context (a small
+ *     device status word).  No entry point allocates device memory.
+ *   - A workspace must be zero-filled once before its first use (e.g. cudaMemset) and again
+ *     after any call whose tl_ctx_check reported an error; between successful calls the
+ *     library keeps it valid itself (its signals are epoch-valued, never reset).
+ *   - Calls are asynchronous on `stream` and return once the work is enqueued.  Two calls that
+ *     share a workspace must be ordered (same stream, or events).
+ *   - Return values: TL_OK (0) or a negative TL_ERR_* code.  Argument errors are reported
+ *     before anything is enqueued.  Device-side errors (a bounded wait that ran out) are read
+ *     with tl_ctx_check after the stream has been synchronised.
+ *   - Threading: a context is not thread-safe; use one per host thread.
+ */
+#ifndef TL_GB300_H
+#define TL_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* == cudaStream_t / CUstream */
+typedef struct CUstream_st* tl_stream_t;
+
+/* ---------------------------------------------------------------- status codes */
+#define TL_OK 0
+#define TL_ERR_INVALID (-1)     /* null / misaligned pointer, unsupported shape, bad config      */
+#define TL_ERR_UNSUPPORTED (-2) /* device is not sm_103 / co-residency of the persistent grid fails */
+#define TL_ERR_CUDA (-3)        /* a CUDA runtime or driver call failed                          */
+#define TL_ERR_TIMEOUT (-4)     /* (tl_ctx_check) a bounded device wait on a signal ran out        */
+#define TL_ERR_WORKSPACE (-5)   /* workspace smaller than *_workspace_bytes                     */
+
+/* ---------------------------------------------------------------- configuration
+ * The BlockChannel-like launch context of [TL] §6: rank/world come per call; this struct
+ * carries the decoupled design-space choices of [TL] §3.1 (communication tile size = mover
+ * chunk, tile order = swizzle, resource binding = mover warps / combine partition) and the
+ * bound on every device-side wait.
+ */
+typedef struct tl_config {
+  int mover_warps;            /* warps per persistent CTA that move shards (1..4; default 2)          */
+  int chunks_per_slab;        /* mover chunks, hence signals, per 128-row slab (1..32; default 32)     */
+  int swizzle;                /* 0: identity tile order; 1: rank-swizzled ([TD] §3.7; default)          */
+  int grid_ctas;              /* persistent CTAs; 0 = one per SM (default)                              */
+  int combine_ctas;           /* MoE combine partition, CTAs = SMs ([RA]; default 8)                    */
+  int debug_skip_chunk;       /* fault injection: this mover chunk is copied but never signalled (-1 off) */
+  unsigned long long timeout_ns; /* bound of every device wait (default 2e9 ns)                       */
+} tl_config;
+
+typedef struct tl_ctx tl_ctx;
+
+/* Fill *cfg with the defaults above.  Returns TL_OK, or TL_ERR_INVALID for cfg == NULL. */
+int tl_config_default(tl_config* cfg);
+
+/* Create a context on `device` (must be compute capability 10.3, i.e. sm_103).  cfg may be
+ * NULL (defaults).  Allocates one small device status word.  On failure *out is NULL. */
+int tl_ctx_create(tl_ctx** out, int device, const tl_config* cfg);
+
+/* Destroy a context (NULL is ignored).  Synchronises the device first. */
+void tl_ctx_destroy(tl_ctx* ctx);
+
+/* Read and clear the device status word.  Call after synchronising the streams used with ctx.
+ * Returns TL_OK, or TL_ERR_TIMEOUT if a bounded wait ran out (the results of that call are
+ * undefined and its workspace must be zero-filled again), or TL_ERR_CUDA. */
+int tl_ctx_check(tl_ctx* ctx);
+
+/* Human-readable text for a status code (static storage). */
+const char* tl_strerror(int code);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int tl_version(void);
+
+/* Number of SMs / persistent CTAs the context launches with. */
+int tl_ctx_num_ctas(const tl_ctx* ctx);
+
+/* ---------------------------------------------------------------- AllGather + GEMM
+ * [TL] §2.1, [TD] §3.2 Algorithm 2 (pull mode) and §3.7 (AG+GEMM swizzle).
+ *
+ *   C[(W*m_per_rank) x n] = A . B,  A = [A_0; ...; A_{W-1}] (rank order), B [k x n].
+ *
+ * a_shards: host array of W device pointers, shard r is bf16 [m_per_rank x k] (rank r's
+ *           "local buffer").  b: bf16 [k x n].  c: bf16 [(W*m_per_rank) x n] (output).
+ * workspace: device buffer of tl_ag_gemm_workspace_bytes(); its first W*m_per_rank*k*2
+ *           bytes receive the gathered A (the symmetric buffer T of Algorithm 2, rank order),
+ *           the rest holds the per-chunk ready signals.
+ * The emulated self rank `rank` (0 <= rank < W) reads its own shard in place; the mover pulls
+ * shards (rank+1) mod W, (rank+2) mod W, ... into T in that order (its own shard last), and the
+ * GEMM visits row blocks of shard rank first, then (rank+1) mod W, ... waiting on each slab's
+ * signals before its first load.  The result does not depend on `rank` or the swizzle.
+ * Shapes: 1 <= W <= 8; m_per_rank % 128 == 0; n % 8 == 0; k % 8 == 0 (n, k need not be
+ * tile multiples: ragged edges are zero-filled by TMA on load and clipped on store).
+ * Any zero dimension is a no-op returning TL_OK.
+ */
+size_t tl_ag_gemm_workspace_bytes(int W, int m_per_rank, int n, int k);
+int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b, void* c,
+               void* workspace, size_t workspace_bytes, int m_per_rank, int n, int k, tl_stream_t stream);
+
+/* ---------------------------------------------------------------- GEMM + ReduceScatter
+ * [TD] §3.3 Algorithm 3 (each producer pushes its partial into the owner's slot, the owner
+ * accumulates), [TL] §5 / Figure 4 text (producer tiles notify; peer tiles chain the partial
+ * sums from rank to rank) and [TD] §3.7 (start at the next rank's chunk, own chunk last).
+ *
+ *   out_o [(m/W) x n] = rows [o*m/W, (o+1)*m/W) of  sum_{p=0}^{W-1} A_p . B_p
+ *
+ * a: W device pointers, A_p bf16 [m x k_r];  b: W device pointers, B_p bf16 [k_r x n];
+ * out: W device pointers, out_o bf16 [(m/W) x n].
+ * workspace: tl_gemm_rs_workspace_bytes(): an fp32 [m x n] accumulation slot (owner o owns
+ * rows o*m/W..) plus one signal per output tile.  Producers are visited p = 0..W-1; producer
+ * p walks owners (p+1) mod W, (p+2) mod W, ..., p (swizzle = 1) or 0..W-1 (swizzle = 0).
+ * Producer 0 stores its partial tile into the slot, producer p > 0 waits for producer p-1's
+ * signal on that tile (peer_tile_wait) and adds its partial with a TMA bulk reduction, and
+ * producer W-1 adds its partial to the slot in registers and writes bf16 out_o.  The fp32
+ * summation order is therefore fixed (p = 0, 1, ..., W-1): results are bit-identical across
+ * runs, swizzle modes and grid sizes.
+ * Shapes: 1 <= W <= 8; m % (128*W) == 0; n % 8 == 0; k_r % 8 == 0.
+ */
+size_t tl_gemm_rs_workspace_bytes(int W, int m, int n, int k_r);
+int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* const* b, void* const* out,
+               void* workspace, size_t workspace_bytes, int m, int n, int k_r, tl_stream_t stream);
+
+/* ---------------------------------------------------------------- 2-layer MLP chain
+ * [TL] §2.1 (AG + GEMM -> activation -> GEMM + RS), [RA] CTA-pipelining (the second GEMM's
+ * CTAs start as soon as the first GEMM's CTAs that produce their inputs are done).
+ *
+ *   X = [X_0; ...; X_{W-1}]  (tokens x hidden),   H_r = GELU(X . W1_r)  (exact erf GELU),
+ *   out_o = rows_o( sum_r H_r . W2_r ).
+ *
+ * x_shards: W pointers, X_r bf16 [(tokens/W) x hidden]; w1: W pointers, bf16 [hidden x f_r];
+ * w2: W pointers, bf16 [f_r x hidden]; out: W pointers, bf16 [(tokens/W) x hidden].
+ * workspace: tl_mlp2_workspace_bytes(): per-rank gathered X (W x tokens x hidden bf16), the
+ * intermediate H (W x tokens x f_r bf16), the fp32 reduction slot (tokens x hidden) and signals.
+ * One persistent launch runs, per emulated rank r: the mover (gather X into rank r's copy),
+ * layer-1 tiles (wait on the slab signals, GELU epilogue, notify per H tile) and layer-2 tiles
+ * (wait on the H tiles covering their K range, then the GEMM+RS chain above).
+ * Shapes: 1 <= W <= 8; tokens % (128*W) == 0; hidden % 8 == 0; f_r % 8 == 0.
+ */
+size_t tl_mlp2_workspace_bytes(int W, int tokens, int hidden, int f_r);
+int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const void* const* w1, const void* const* w2,
+            void* const* out, void* workspace, size_t workspace_bytes, int tokens, int hidden, int f_r,
+            tl_stream_t stream);
+
+/* ---------------------------------------------------------------- MoE layer with combine partition
+ * [TL] §4.1 (dynamic mapping tables filled by the routing), §7.2 (Gather + GroupGEMM, then
+ * GroupGEMM + Scatter + TopK reduce), [RA] MoE abstract (persistent expert producer; a
+ * persistent combine consumer on `combine_ctas` dedicated SMs that handles output tiles as
+ * their ready signals arrive).
+ *
+ * x: bf16 [T x H]; logits: fp32 [T x E]; w_gate, w_up: bf16 [E x H x F]; w_down: bf16 [E x F x H].
+ * out: fp32 [T x H] (written, not accumulated into).
+ * perm_out (optional, may be NULL): int32 [T*topk]: perm_out[pos] = t*topk + j, assignments
+ *   ordered by (expert, t, j).  counts_out (optional): int32 [E] assignments per expert.
+ * Routing: experts = the topk largest logits (ties to the lower expert index), gates = softmax
+ * over all E logits taken at those experts (no renormalisation).
+ *   y_(t,j) = (SiLU(x_t . Wg_e) * (x_t . Wu_e)) . Wd_e   (h kept in bf16, y in bf16)
+ *   out_t   = sum_j gate_(t,j) * y_(t,j)                  (fp32)
+ * workspace: tl_moe_workspace_bytes().
+ * Shapes: T >= 1; 1 <= topk <= 8; topk <= E <= 256; H % 256 == 0; F % 128 == 0.
+ */
+size_t tl_moe_workspace_bytes(int T, int H, int E, int F, int topk);
+int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, int topk, const void* w_gate,
+                   const void* w_up, const void* w_down, float* out, int* perm_out, int* counts_out,
+                   void* workspace, size_t workspace_bytes, int T, int H, int E, int F, tl_stream_t stream);
+
+/* ---------------------------------------------------------------- host-side tile maps (no GPU)
+ * The static tile-centric mappings the kernels use ([TL] §4.1), evaluated on the host by the
+ * same code the device runs, for inspection and testing.
+ *
+ * tl_ag_tile_order: for the AllGather + GEMM tile sequence t = 0..count-1 writes the source
+ *   rank, the row block inside that rank's shard and the column block.  Returns the number of
+ *   tiles, or TL_ERR_INVALID.  Arrays may be NULL to query the count; otherwise they must hold
+ *   `cap` entries.
+ * tl_rs_tile_order: the same for GEMM + ReduceScatter: producer, owner, row block within the
+ *   owner's rows, column block.
+ */
+int tl_ag_tile_order(int W, int rank, int m_per_rank, int n, int swizzle, int* src_rank, int* m_block,
+                     int* n_block, int cap);
+int tl_rs_tile_order(int W, int m, int n, int swizzle, int* producer, int* owner, int* m_block, int* n_block,
+                     int cap);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TL_GB300_H */

@@ -1,0 +1,210 @@
+"""GPU parity of AllGather+GEMM, GEMM+ReduceScatter and the MLP chain against the fp64 oracle.
+
+Every call goes through the C ABI (via the ctypes binding).  Tolerance for the
+bf16-in / fp32-accumulate outputs: max|gpu - ref| <= 1e-2 * max|ref| + 1e-3.
+The gather index map is checked bit-exactly; results that the design fixes
+bit-for-bit (tile order, swizzle, mover geometry, grid size) are compared with
+array_equal.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from seeded_inputs import make_inputs, workload_inputs
+from tests.gpu_helpers import assert_close, bf16_bits, bf16_to_f64, to_dev_bf16, workspace
+
+pytestmark = pytest.mark.gpu
+
+tl = pytest.importorskip("communication_overlapped_gemm_gb300")
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import torch
+    assert torch.cuda.is_available()
+    c = tl.Context(0)
+    yield c
+    c.close()
+
+
+def run_ag(ctx, inp, rank=0):
+    import torch
+    a = [to_dev_bf16(x) for x in inp["a_shards"]]
+    b = to_dev_bf16(inp["b"])
+    W = len(a)
+    mpr, k = a[0].shape
+    n = b.shape[1]
+    c = torch.empty((W * mpr, n), dtype=torch.bfloat16, device="cuda")
+    ws = workspace(tl.tl_ag_gemm_workspace_bytes(W, mpr, n, k))
+    tl.tl_ag_gemm(ctx, a, b, c, ws, rank=rank)
+    torch.cuda.synchronize()
+    assert ctx.check() == tl.TL_OK
+    return c, ws
+
+
+# ----------------------------------------------------------------------------- AllGather + GEMM
+def test_ag_gemm_tiny_matches_oracle(ctx):
+    inp = workload_inputs("ag_tiny")
+    c, ws = run_ag(ctx, inp)
+    ref = oracle.ag_gemm(inp["a_shards"], inp["b"])
+    assert_close(bf16_to_f64(c), ref, "ag_tiny")
+    # the gathered operand is the rank-order concatenation, bit for bit
+    gath = oracle.ag_gather_bits(inp["a_shards"])
+    got = bf16_bits(ws[: gath.size * 2].view(__import__("torch").bfloat16).view(gath.shape))
+    assert np.array_equal(got, gath)
+
+
+@pytest.mark.parametrize("W,mpr,n,k", [(1, 128, 256, 64), (3, 256, 200, 136), (4, 128, 520, 328)])
+def test_ag_gemm_ragged_matches_oracle(ctx, W, mpr, n, k):
+    inp = make_inputs("ag_gemm", 11 + W, W=W, m_per_rank=mpr, n=n, k=k)
+    for rank in range(W):
+        c, ws = run_ag(ctx, inp, rank=rank)
+        assert_close(bf16_to_f64(c), oracle.ag_gemm(inp["a_shards"], inp["b"]), f"ag W={W} rank={rank}")
+        gath = oracle.ag_gather_bits(inp["a_shards"])
+        import torch
+        got = bf16_bits(ws[: gath.size * 2].view(torch.bfloat16).view(gath.shape))
+        assert np.array_equal(got, gath)
+
+
+def test_ag_gemm_invariant_to_order_and_geometry():
+    """Tile order, swizzle, mover chunking, mover warps and grid size do not change a bit."""
+    import torch
+    inp = make_inputs("ag_gemm", 21, W=4, m_per_rank=256, n=768, k=512)
+    outs = []
+    for cfg in [dict(swizzle=1), dict(swizzle=0), dict(chunks_per_slab=1, mover_warps=1),
+                dict(chunks_per_slab=8, mover_warps=4), dict(grid_ctas=37)]:
+        with tl.Context(0, **cfg) as c2:
+            for rank in (0, 3):
+                c, _ = run_ag(c2, inp, rank=rank)
+                outs.append(bf16_bits(c))
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    assert_close(bf16_to_f64(torch.from_numpy(outs[0].view(np.int16)).view(torch.bfloat16)),
+                 oracle.ag_gemm(inp["a_shards"], inp["b"]), "ag invariance")
+
+
+def test_ag_gemm_llama70b_sampled(ctx):
+    """Full-size AllGather+GEMM (W=8, 8192x3584x8192) checked on sampled entries."""
+    inp = workload_inputs("ag_70b")
+    c, ws = run_ag(ctx, inp, rank=0)
+    rng = np.random.default_rng(7)
+    rows = np.concatenate([rng.integers(0, 8192, 200), [0, 8191, 1023, 1024, 7 * 1024]])
+    cols = np.concatenate([rng.integers(0, 3584, 200), [0, 3583, 255, 256, 3583]])
+    got = bf16_to_f64(c)[rows, cols]
+    ref = oracle.ag_gemm_entries(inp["a_shards"], inp["b"], rows, cols)
+    assert_close(got, ref, "ag_70b sampled")
+    # and whole rows of every shard region (several tiles, every rank)
+    for r in range(8):
+        row = r * 1024 + 517
+        ref_row = oracle.ag_gemm_entries(inp["a_shards"], inp["b"], [row] * 3584, np.arange(3584))
+        assert_close(bf16_to_f64(c)[row], ref_row, f"ag_70b row {row}")
+    gath = oracle.ag_gather_bits(inp["a_shards"])
+    import torch
+    got = bf16_bits(ws[: gath.size * 2].view(torch.bfloat16).view(gath.shape))
+    assert np.array_equal(got, gath)
+
+
+# ----------------------------------------------------------------------------- GEMM + ReduceScatter
+def run_rs(ctx, inp):
+    import torch
+    a = [to_dev_bf16(x) for x in inp["a"]]
+    b = [to_dev_bf16(x) for x in inp["b"]]
+    W = len(a)
+    m, kr = a[0].shape
+    n = b[0].shape[1]
+    out = [torch.empty((m // W, n), dtype=torch.bfloat16, device="cuda") for _ in range(W)]
+    ws = workspace(tl.tl_gemm_rs_workspace_bytes(W, m, n, kr))
+    tl.tl_gemm_rs(ctx, a, b, out, ws)
+    torch.cuda.synchronize()
+    assert ctx.check() == tl.TL_OK
+    return out
+
+
+@pytest.mark.parametrize("W,m,n,kr", [(1, 128, 256, 64), (2, 256, 256, 128), (4, 512, 328, 200),
+                                      (8, 1024, 264, 72)])
+def test_gemm_rs_matches_oracle(ctx, W, m, n, kr):
+    inp = make_inputs("gemm_rs", 31 + W, W=W, m=m, n=n, k_r=kr)
+    out = run_rs(ctx, inp)
+    ref = oracle.gemm_rs(inp["a"], inp["b"])
+    for o in range(W):
+        assert_close(bf16_to_f64(out[o]), ref[o], f"rs W={W} owner {o}")
+
+
+def test_gemm_rs_deterministic_across_orders():
+    inp = make_inputs("gemm_rs", 41, W=4, m=1024, n=512, k_r=256)
+    outs = []
+    for cfg in [dict(swizzle=1), dict(swizzle=0), dict(grid_ctas=23)]:
+        with tl.Context(0, **cfg) as c2:
+            for _ in range(2):
+                outs.append([bf16_bits(o) for o in run_rs(c2, inp)])
+    for o in outs[1:]:
+        assert all(np.array_equal(x, y) for x, y in zip(o, outs[0]))
+
+
+def test_gemm_rs_full_size_sampled(ctx):
+    """Full-size GEMM+RS (W=8, A_p 8192x3584, B_p 3584x8192) on sampled entries of every owner."""
+    inp = workload_inputs("rs_70b")
+    out = run_rs(ctx, inp)
+    rng = np.random.default_rng(9)
+    for o in range(8):
+        rows = np.concatenate([rng.integers(0, 1024, 24), [0, 1023]])
+        cols = np.concatenate([rng.integers(0, 8192, 24), [0, 8191]])
+        ref = oracle.gemm_rs_entries(inp["a"], inp["b"], o, rows, cols)
+        assert_close(bf16_to_f64(out[o])[rows, cols], ref, f"rs_70b owner {o}")
+
+
+# ----------------------------------------------------------------------------- MLP chain
+def run_mlp2(ctx, inp):
+    import torch
+    x = [to_dev_bf16(v) for v in inp["x_shards"]]
+    w1 = [to_dev_bf16(v) for v in inp["w1"]]
+    w2 = [to_dev_bf16(v) for v in inp["w2"]]
+    W = len(x)
+    tr, h = x[0].shape
+    f = w1[0].shape[1]
+    out = [torch.empty((tr, h), dtype=torch.bfloat16, device="cuda") for _ in range(W)]
+    ws = workspace(tl.tl_mlp2_workspace_bytes(W, tr * W, h, f))
+    tl.tl_mlp2(ctx, x, w1, w2, out, ws)
+    torch.cuda.synchronize()
+    assert ctx.check() == tl.TL_OK
+    return out
+
+
+@pytest.mark.parametrize("W,T,h,f", [(1, 128, 256, 256), (2, 512, 264, 328), (4, 1024, 512, 384)])
+def test_mlp2_matches_oracle(ctx, W, T, h, f):
+    inp = make_inputs("mlp2", 51 + W, W=W, tokens=T, hidden=h, f_r=f)
+    out = run_mlp2(ctx, inp)
+    ref = oracle.mlp2(inp["x_shards"], inp["w1"], inp["w2"])
+    for o in range(W):
+        assert_close(bf16_to_f64(out[o]), ref[o], f"mlp2 W={W} owner {o}")
+
+
+def test_mlp2_full_size_sampled(ctx):
+    inp = workload_inputs("mlp2_8b")
+    out = run_mlp2(ctx, inp)
+    rng = np.random.default_rng(11)
+    for o in range(4):
+        rows = rng.integers(0, 1024, 6)
+        cols = rng.integers(0, 4096, 6)
+        ref = oracle.mlp2_entries(inp["x_shards"], inp["w1"], inp["w2"], o, rows, cols)
+        assert_close(bf16_to_f64(out[o])[rows, cols], ref, f"mlp2_8b owner {o}")
+
+
+# ----------------------------------------------------------------------------- bounded waits
+def test_missing_signal_times_out_and_context_survives():
+    """A mover chunk that is never signalled makes the consumer's bounded wait run out:
+    the call reports TL_ERR_TIMEOUT and the context stays usable."""
+    import torch
+    inp = make_inputs("ag_gemm", 61, W=2, m_per_rank=128, n=256, k=256)
+    with tl.Context(0, debug_skip_chunk=3, timeout_ns=50_000_000) as c2:
+        a = [to_dev_bf16(x) for x in inp["a_shards"]]
+        b = to_dev_bf16(inp["b"])
+        c = torch.empty((256, 256), dtype=torch.bfloat16, device="cuda")
+        ws = workspace(tl.tl_ag_gemm_workspace_bytes(2, 128, 256, 256))
+        tl.tl_ag_gemm(c2, a, b, c, ws, rank=0)
+        torch.cuda.synchronize()
+        assert c2.check() == tl.TL_ERR_TIMEOUT
+        assert c2.check() == tl.TL_OK  # cleared
+    with tl.Context(0) as c3:
+        c, _ = run_ag(c3, inp)
+        assert_close(bf16_to_f64(c), oracle.ag_gemm(inp["a_shards"], inp["b"]), "after timeout")
