@@ -140,6 +140,20 @@ struct Job {
   int x0, x1, x2, x3;  // op-specific (ranks, owners, blocks)
 };
 
+// Defaults for the optional hooks of an op (an op derives from OpBase<its Params>).
+template <class P>
+struct OpBase {
+  // Whether this CTA belongs to the GEMM partition; (gi, gn) = its index / partition size.
+  static __device__ bool gemm_partition(const P&, int&, int&) { return true; }
+  // Work of CTAs outside the GEMM partition (all threads of the CTA).
+  static __device__ void side_role(const P&, int, int, uint8_t*) {}
+  static __device__ void producer_init(const P&) {}
+  static __device__ void prefetch(const P&) {}
+  static __device__ bool publishes(const P&, const Job&) { return false; }
+  static __device__ void publish(const P&, const Job&) {}
+  static __device__ void mover(const P&, int, int) {}
+};
+
 struct Smem {
   uint8_t* stages;
   uint8_t* epi;
@@ -180,14 +194,15 @@ struct EpiStage {
 };
 
 template <class Op>
-__device__ __forceinline__ void role_producer(const typename Op::Params& p, const Smem& sm, int lane) {
+__device__ __forceinline__ void role_producer(const typename Op::Params& p, const Smem& sm, int lane, int gi,
+                                              int gn) {
   const Common& c = p.common;
   const int ntiles = Op::num_tiles(p);
   uint32_t stage = 0, phase = 0;
   uint32_t filled = 0, fill_parity = 0;  // per-stage: fill issued / parity of that fill
   bool ok = true;
   Op::producer_init(p);
-  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+  for (int t = gi; t < ntiles && ok; t += gn) {
     const Job j = Op::job(p, t);
     for (int kb = 0; kb < j.kblocks; ++kb) {
       Op::wait_deps(p, j, kb, lane);
@@ -215,12 +230,12 @@ __device__ __forceinline__ void role_producer(const typename Op::Params& p, cons
 
 template <class Op>
 __device__ __forceinline__ void role_mma(const typename Op::Params& p, const Smem& sm, int lane,
-                                         uint32_t tmem_base) {
+                                         uint32_t tmem_base, int gi, int gn) {
   const Common& c = p.common;
   const int ntiles = Op::num_tiles(p);
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   bool ok = true;
-  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+  for (int t = gi; t < ntiles && ok; t += gn) {
     const Job j = Op::job(p, t);
     if (lane == 0) {
       ok = mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, c, kSiteTmemEmpty);
@@ -232,7 +247,7 @@ __device__ __forceinline__ void role_mma(const typename Op::Params& p, const Sme
         tc_fence_after();
         const uint32_t a0 = smem_u32(sm.a(stage));
         const uint32_t b0 = smem_u32(sm.b(stage));
-        Op::mma_stage(d, a0, b0, kb);
+        Op::mma_stage(j, d, a0, b0, kb);
         umma_commit(&sm.empty[stage]);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
@@ -252,7 +267,7 @@ __device__ __forceinline__ void role_mma(const typename Op::Params& p, const Sme
 
 template <class Op>
 __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, const Smem& sm, int warp,
-                                              int lane, uint32_t tmem_base) {
+                                              int lane, uint32_t tmem_base, int gi, int gn) {
   const Common& c = p.common;
   const int ntiles = Op::num_tiles(p);
   const int q = warp & 3;   // TMEM lane quadrant this warp may access
@@ -263,7 +278,7 @@ __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, cons
   es.idx = 0;
   uint32_t acc = 0, acc_phase = 0;
   bool ok = true;
-  for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+  for (int t = gi; t < ntiles && ok; t += gn) {
     const Job j = Op::job(p, t);
     ok = mbar_wait(&sm.tfull[acc], acc_phase, c, kSiteTmemFull);
     if (!ok) break;
@@ -315,6 +330,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) persistent_kernel(const __grid
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTAs outside the GEMM partition (e.g. a combine partition) run the op's side role.
+  int gi = blockIdx.x, gn = gridDim.x;
+  if (!Op::gemm_partition(p, gi, gn)) {
+    Op::side_role(p, warp, lane, smem_raw);
+    return;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -340,11 +361,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) persistent_kernel(const __grid
   const uint32_t tmem_base = *sm.tmem_slot;
 
   if (warp == 0) {
-    role_producer<Op>(p, sm, lane);
+    role_producer<Op>(p, sm, lane, gi, gn);
   } else if (warp == 1) {
-    role_mma<Op>(p, sm, lane, tmem_base);
+    role_mma<Op>(p, sm, lane, tmem_base, gi, gn);
   } else if (warp < kCoreWarps) {
-    role_epilogue<Op>(p, sm, warp, lane, tmem_base);
+    role_epilogue<Op>(p, sm, warp, lane, tmem_base, gi, gn);
   } else {
     Op::mover(p, warp - kCoreWarps, lane);
   }

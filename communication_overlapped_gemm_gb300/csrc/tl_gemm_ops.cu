@@ -92,7 +92,7 @@ struct AgParams {
   int W, rank, m_per_rank, mps, n, nbk, kblocks, swizzle, chunks, skip_chunk;
 };
 
-struct AgOp {
+struct AgOp : OpBase<AgParams> {
   using Params = AgParams;
   static constexpr uint32_t kTxBytes = kStageBytes;
   static __device__ int num_tiles(const Params& p) { return ag_num_tiles(p.W, p.mps, p.nbk); }
@@ -118,7 +118,6 @@ struct AgOp {
     tma_prefetch_map(&p.b);
     tma_prefetch_map(&p.c);
   }
-  static __device__ void producer_init(const Params&) {}
   // consumer_tile_wait: a remote row block is read only after every chunk of its slab
   // has been released by the mover.
   static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
@@ -131,7 +130,9 @@ struct AgOp {
 #pragma unroll
     for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.b, bar, j.b_col + g * 64, kb * kBK);
   }
-  static __device__ void mma_stage(uint32_t d, uint32_t a0, uint32_t b0, int kb) { mma_stage_256(d, a0, b0, kb); }
+  static __device__ void mma_stage(const Job&, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
+    mma_stage_256(d, a0, b0, kb);
+  }
   static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 64; ++ch) {
@@ -142,8 +143,6 @@ struct AgOp {
       store_bf16_chunk(&p.c, es, lane, v, x, j.x2 + q * 32);
     }
   }
-  static __device__ bool publishes(const Params&, const Job&) { return false; }
-  static __device__ void publish(const Params&, const Job&) {}
   static __device__ void mover(const Params& p, int mw, int lane) {
     const int nthreads = p.common.mover_warps * 32;
     const int tid = mw * 32 + lane;
@@ -176,7 +175,7 @@ struct RsParams {
   int W, m, mo, mbo, n, nbk, kblocks, swizzle;
 };
 
-struct RsOp {
+struct RsOp : OpBase<RsParams> {
   using Params = RsParams;
   static constexpr uint32_t kTxBytes = kStageBytes;
   static __device__ int num_tiles(const Params& p) { return rs_num_tiles(p.W, p.mbo, p.nbk); }
@@ -197,14 +196,15 @@ struct RsOp {
     return j;
   }
   static __device__ void prefetch(const Params& p) { tma_prefetch_map(&p.acc); }
-  static __device__ void producer_init(const Params&) {}
   static __device__ void wait_deps(const Params&, const Job&, int, int) {}
   static __device__ void load(const Params& p, const Job& j, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
     tma_load_2d(sa, &p.a[j.a_sel], bar, kb * kBK, j.a_row);
 #pragma unroll
     for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.b[j.b_sel], bar, j.b_col + g * 64, kb * kBK);
   }
-  static __device__ void mma_stage(uint32_t d, uint32_t a0, uint32_t b0, int kb) { mma_stage_256(d, a0, b0, kb); }
+  static __device__ void mma_stage(const Job&, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
+    mma_stage_256(d, a0, b0, kb);
+  }
   static __device__ int tile_id(const Params& p, const Job& j) { return (j.a_row / kBM) * p.nbk + j.x3; }
   static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
     rs_epilogue(&p.acc, p.acc_ptr, &p.out[j.x1], p.flags + tile_id(p, j), j.x0, p.W, j.a_row, j.x2 * kBM, j.b_col,
@@ -215,7 +215,6 @@ struct RsOp {
   static __device__ void publish(const Params& p, const Job& j) {
     st_release_gpu(p.flags + tile_id(p, j), (p.common.epoch << 4) | static_cast<unsigned long long>(j.x0 + 1));
   }
-  static __device__ void mover(const Params&, int, int) {}
 };
 
 // ============================================================================ 2-layer MLP chain
@@ -239,7 +238,7 @@ struct Mlp2Params {
   int W, T, Tr, h, f, mps, nb1, kb1, nb2, kb2, swizzle, chunks, skip_chunk;
 };
 
-struct Mlp2Op {
+struct Mlp2Op : OpBase<Mlp2Params> {
   using Params = Mlp2Params;
   static constexpr uint32_t kTxBytes = kStageBytes;
   static __device__ int per_rank(const Params& p) { return p.W * p.mps * (p.nb1 + p.nb2); }
@@ -290,7 +289,6 @@ struct Mlp2Op {
     tma_prefetch_map(&p.h_ld);
     tma_prefetch_map(&p.acc);
   }
-  static __device__ void producer_init(const Params&) {}
   static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
     if (kb != 0) return;
     if (j.kind == 1) {
@@ -317,7 +315,9 @@ struct Mlp2Op {
       for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.w2[j.b_sel], bar, j.b_col + g * 64, kb * kBK);
     }
   }
-  static __device__ void mma_stage(uint32_t d, uint32_t a0, uint32_t b0, int kb) { mma_stage_256(d, a0, b0, kb); }
+  static __device__ void mma_stage(const Job&, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
+    mma_stage_256(d, a0, b0, kb);
+  }
   static __device__ int h_row(const Params& p, const Job& j) { return j.x0 * p.T + j.x1 * p.Tr + j.x2 * kBM; }
   static __device__ int rs_tile_id(const Params& p, const Job& j) {
     return ((j.x1 * p.Tr) / kBM + j.x2) * p.nb2 + j.x3;

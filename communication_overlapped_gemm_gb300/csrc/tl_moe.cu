@@ -1,9 +1,464 @@
-// MoE layer (routing, permutation, grouped expert GEMMs, combine partition).
+// MoE layer: routing, stable expert permutation (the dynamic tile-centric mapping
+// tables), token gather, and one persistent launch in which a GEMM partition runs the
+// grouped expert GEMMs while a dedicated combine partition scatter-adds finished
+// output tiles back into token order as their ready signals arrive.
+//
+// "TileLink: Generating Efficient Compute-Communication Overlapping Kernels using
+// Tile-Centric Primitives", §4.1 (dynamic mapping: lookup tables f_S_low/high, f_R
+// filled at run time by the routing) and §7.2 (Gather + GroupGEMM; GroupGEMM + Scatter
+// + TopK reduce as a producer/consumer chain); "Resource-aware Computation-
+// Communication Overlap for multi-GPU ML Workloads", MoE abstract (a persistent
+// producer covering all local experts; a persistent consumer on a small dedicated SM
+// partition that handles output segments as tiles become ready).
+#include <cuda_bf16.h>
+
 #include "tl_host.h"
 
-extern "C" size_t tl_moe_workspace_bytes(int, int, int, int, int) { return 0; }
+namespace tl {
 
-extern "C" int tl_moe_combine(tl_ctx*, const void*, const float*, int, const void*, const void*, const void*, float*,
-                              int*, int*, void*, size_t, int, int, int, int, tl_stream_t) {
-  return TL_ERR_UNSUPPORTED;
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopk = 8;
+
+// ---------------------------------------------------------------------------- routing
+// One warp per token: top-k of the fp32 logits (larger first, equal values to the
+// lower expert index), softmax over all E logits in fp32 taken at the chosen experts.
+// Also zeroes the token's fp32 output row (the combine adds into it).
+__global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E, int topk, int* __restrict__ experts,
+                                 float* __restrict__ gates, float* __restrict__ out, int H) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+  float4* orow = reinterpret_cast<float4*>(out + static_cast<size_t>(t) * H);
+  for (int c = lane; c < H / 4; c += 32) orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  constexpr int kPer = kMaxExperts / 32;
+  float v[kPer];
+  const float* row = logits + static_cast<size_t>(t) * E;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? row[e] : -INFINITY;
+    mx = fmaxf(mx, v[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    if (lane + 32 * i < E) s += expf(v[i] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+
+  uint32_t taken = 0;
+  for (int j = 0; j < topk; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !(taken & (1u << i)) && (v[i] > bv || (v[i] == bv && e < bi))) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == 0) {
+      experts[t * topk + j] = bi;
+      gates[t * topk + j] = expf(bv - mx) / s;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------- permutation
+// One block per expert e.  Every block histograms all assignments (so each knows all
+// offsets without a grid-wide step), then ranks the assignments of its own expert in
+// (t, j) order with a block-wide ballot scan.  Outputs:
+//   perm[off_e + pos] = a                      (unpadded order: expert, t, j)
+//   row_assign[poff_e + pos] = a, -1 on padding rows of the expert's 128-row-aligned segment
+//   tile_expert / tile_rows for each 128-row tile of the padded layout (the f_R / f_S tables)
+__global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict__ experts, int n, int E,
+                                                           int* __restrict__ perm, int* __restrict__ row_assign,
+                                                           int* __restrict__ tile_expert, int* __restrict__ tile_rows,
+                                                           int* __restrict__ num_mtiles, int* __restrict__ counts,
+                                                           int* __restrict__ perm_out, int* __restrict__ counts_out) {
+  __shared__ int hist[kMaxExperts];
+  __shared__ int off[kMaxExperts + 1];
+  __shared__ int poff[kMaxExperts + 1];
+  __shared__ int warp_tot[32];
+  __shared__ int warp_pre[32];
+  const int e = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for (int a = tid; a < n; a += blockDim.x) {
+    const unsigned ex = static_cast<unsigned>(experts[a]);
+    if (ex < static_cast<unsigned>(E)) atomicAdd(&hist[ex], 1);  // never index outside the table
+  }
+  __syncthreads();
+  if (tid == 0) {
+    off[0] = 0;
+    poff[0] = 0;
+    for (int i = 0; i < E; ++i) {
+      off[i + 1] = off[i] + hist[i];
+      poff[i + 1] = poff[i] + (hist[i] + kBM - 1) / kBM * kBM;
+    }
+  }
+  __syncthreads();
+  int running = 0;
+  const int nw = blockDim.x >> 5;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int a = base + tid;
+    const bool mine = a < n && experts[a] == e;
+    const uint32_t ball = __ballot_sync(0xffffffffu, mine);
+    if (lane == 0) warp_tot[warp] = __popc(ball);
+    __syncthreads();
+    if (warp == 0) {
+      const int v = lane < nw ? warp_tot[lane] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      warp_pre[lane] = incl - v;
+      if (lane == 31) warp_tot[0] = incl;  // block total (read after the barrier)
+    }
+    __syncthreads();
+    if (mine) {
+      const int pos = running + warp_pre[warp] + __popc(ball & ((1u << lane) - 1u));
+      perm[off[e] + pos] = a;
+      if (perm_out) perm_out[off[e] + pos] = a;
+      row_assign[poff[e] + pos] = a;
+    }
+    const int tot = warp_tot[0];
+    __syncthreads();
+    running += tot;
+  }
+  const int cnt = hist[e];
+  const int padded = poff[e + 1] - poff[e];
+  for (int i = cnt + tid; i < padded; i += blockDim.x) row_assign[poff[e] + i] = -1;
+  for (int i = tid; i < padded / kBM; i += blockDim.x) {
+    const int tile = poff[e] / kBM + i;
+    tile_expert[tile] = e;
+    tile_rows[tile] = min(kBM, cnt - i * kBM);
+  }
+  if (tid == 0) {
+    counts[e] = cnt;
+    if (counts_out) counts_out[e] = cnt;
+    if (e == 0) *num_mtiles = poff[E] / kBM;
+  }
+}
+
+// ---------------------------------------------------------------------------- gather
+// One warp per padded row: Xp[row] = x[token of row_assign[row]] (zeros on padding rows).
+__global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk,
+                                  const int* __restrict__ row_assign, const int* __restrict__ num_mtiles,
+                                  __nv_bfloat16* __restrict__ xp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (row >= *num_mtiles * kBM) return;
+  const int a = row_assign[row];
+  const uint4* src = a >= 0 ? reinterpret_cast<const uint4*>(x + static_cast<size_t>(a / topk) * H) : nullptr;
+  uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(row) * H);
+  for (int c = lane; c < H / 8; c += 32) dst[c] = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+}
+
+// ---------------------------------------------------------------------------- grouped GEMMs + combine
+struct MoeParams {
+  CUtensorMap xp;    // gathered rows {H, R}, box {64, 128}
+  CUtensorMap wg;    // {F, H, E}, box {64, 64, 1}
+  CUtensorMap wu;    // {F, H, E}, box {64, 64, 1}
+  CUtensorMap wd;    // {H, F, E}, box {64, 64, 1}
+  CUtensorMap h_st;  // h {F, R}, box {64, 32}
+  CUtensorMap h_ld;  // h {F, R}, box {64, 128}
+  CUtensorMap y_st;  // y {H, R}, box {64, 32}
+  Common common;
+  const int* num_mtiles;
+  const int* tile_expert;
+  const int* tile_rows;
+  const int* row_assign;
+  const float* gates;
+  const __nv_bfloat16* y;
+  float* out;
+  uint64_t* up_flags;  // [R/128][n_up]
+  uint64_t* y_flags;   // [R/128][n_down]
+  int T, H, E, F, topk, n_up, n_down, kb_up, kb_down, combine_ctas;
+};
+
+// Up-projection stage: two 128x128 accumulators (gate, up) from one A stage.
+__device__ __forceinline__ void mma_stage_dual128(uint32_t d, uint32_t a0, uint32_t b0, int kb) {
+  constexpr uint32_t idesc = umma_idesc_bf16(kBM, 128, true);
+#pragma unroll
+  for (int k = 0; k < kBK / 16; ++k) {
+    const uint64_t ad = umma_desc_sw128(a0 + k * 32, 16, 1024);
+    const uint64_t bg = umma_desc_sw128(b0 + k * 2048, TL_B_LBO, TL_B_SBO);
+    const uint64_t bu = umma_desc_sw128(b0 + 2 * 8192 + k * 2048, TL_B_LBO, TL_B_SBO);
+    const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+    umma_bf16(d, ad, bg, idesc, acc);
+    umma_bf16(d + 128, ad, bu, idesc, acc);
+  }
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+struct MoeOp : OpBase<MoeParams> {
+  using Params = MoeParams;
+  static constexpr uint32_t kTxBytes = kStageBytes;
+  static __device__ int mtiles(const Params& p) { return *reinterpret_cast<const volatile int*>(p.num_mtiles); }
+  static __device__ int num_tiles(const Params& p) { return mtiles(p) * (p.n_up + p.n_down); }
+  static __device__ bool gemm_partition(const Params& p, int& gi, int& gn) {
+    gn = gridDim.x - p.combine_ctas;
+    gi = blockIdx.x;
+    return static_cast<int>(blockIdx.x) < gn;
+  }
+  // Tile order: all up-projection tiles, then all down-projection tiles; inside each,
+  // the row tile is the fastest index so that the row tiles of one expert (which
+  // share its weight columns) run side by side.
+  static __device__ Job job(const Params& p, int t) {
+    const int m = mtiles(p);
+    const int nu = m * p.n_up;
+    Job j;
+    if (t < nu) {
+      j.kind = 1;
+      j.x0 = t % m;
+      j.x1 = t / m;
+      j.b_col = j.x1 * 128;
+      j.kblocks = p.kb_up;
+    } else {
+      const int u = t - nu;
+      j.kind = 2;
+      j.x0 = u % m;
+      j.x1 = u / m;
+      j.b_col = j.x1 * kBN;
+      j.kblocks = p.kb_down;
+    }
+    j.a_sel = 0;
+    j.b_sel = 0;
+    j.a_row = j.x0 * kBM;
+    j.b_z = p.tile_expert[j.x0];
+    j.x2 = 0;
+    j.x3 = 0;
+    return j;
+  }
+  static __device__ void prefetch(const Params& p) {
+    tma_prefetch_map(&p.xp);
+    tma_prefetch_map(&p.wg);
+    tma_prefetch_map(&p.wu);
+    tma_prefetch_map(&p.wd);
+    tma_prefetch_map(&p.h_ld);
+  }
+  // consumer_tile_wait: a down-projection tile reads its row tile of h only after all
+  // n_up up-projection tiles of that row tile have signalled.
+  static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
+    if (kb != 0 || j.kind != 2) return;
+    warp_wait_signals(p.up_flags + static_cast<size_t>(j.x0) * p.n_up, p.n_up, p.common.epoch, p.common, lane,
+                      kSiteSignal, (3ull << 60) | j.x0);
+  }
+  static __device__ void load(const Params& p, const Job& j, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+    if (j.kind == 1) {
+      tma_load_2d(sa, &p.xp, bar, kb * kBK, j.a_row);
+      tma_load_3d(sb, &p.wg, bar, j.b_col, kb * kBK, j.b_z);
+      tma_load_3d(sb + 8192, &p.wg, bar, j.b_col + 64, kb * kBK, j.b_z);
+      tma_load_3d(sb + 16384, &p.wu, bar, j.b_col, kb * kBK, j.b_z);
+      tma_load_3d(sb + 24576, &p.wu, bar, j.b_col + 64, kb * kBK, j.b_z);
+    } else {
+      tma_load_2d(sa, &p.h_ld, bar, kb * kBK, j.a_row);
+#pragma unroll
+      for (int g = 0; g < kBN / 64; ++g) tma_load_3d(sb + g * 8192, &p.wd, bar, j.b_col + g * 64, kb * kBK, j.b_z);
+    }
+  }
+  static __device__ void mma_stage(const Job& j, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
+    if (j.kind == 1)
+      mma_stage_dual128(d, a0, b0, kb);
+    else
+      mma_stage_256(d, a0, b0, kb);
+  }
+  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
+    const int row = j.a_row + q * 32;
+    if (j.kind == 1) {
+#pragma unroll 1
+      for (int ch = 0; ch < 2; ++ch) {
+        float g[64], u[64];
+        tmem_ld64(taddr, ch * 64, g);
+        tmem_ld64(taddr, 128 + ch * 64, u);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) g[i] = g[i] / (1.0f + expf(-g[i])) * u[i];
+        store_bf16_chunk(&p.h_st, es, lane, g, j.b_col + ch * 64, row);
+      }
+    } else {
+#pragma unroll 1
+      for (int ch = 0; ch < kBN / 64; ++ch) {
+        float v[64];
+        tmem_ld64(taddr, ch * 64, v);
+        store_bf16_chunk(&p.y_st, es, lane, v, j.b_col + ch * 64, row);
+      }
+    }
+  }
+  static __device__ bool publishes(const Params&, const Job&) { return true; }
+  static __device__ void publish(const Params& p, const Job& j) {
+    if (j.kind == 1)
+      st_release_gpu(p.up_flags + static_cast<size_t>(j.x0) * p.n_up + j.x1, p.common.epoch);
+    else
+      st_release_gpu(p.y_flags + static_cast<size_t>(j.x0) * p.n_down + j.x1, p.common.epoch);
+  }
+  // Combine partition: y tiles are taken in the order the GEMM partition produces them;
+  // for each valid row a = (t, j): out[t, cols] += gate_a * y[a, cols] (fp32 vector
+  // reductions; with a zeroed out and top-2, 0 + a + b == 0 + b + a, so the result
+  // does not depend on which contribution lands first).
+  static __device__ void side_role(const Params& p, int warp, int lane, uint8_t*) {
+    const int nwarps = blockDim.x >> 5;
+    const int cc = blockIdx.x - (gridDim.x - p.combine_ctas);
+    const int m = mtiles(p);
+    const int total = m * p.n_down;
+    for (int v = cc; v < total; v += p.combine_ctas) {
+      const int i = v % m;
+      const int nb = v / m;
+      warp_wait_one(p.y_flags + static_cast<size_t>(i) * p.n_down + nb, p.common.epoch, p.common, lane,
+                    kSiteCombine, (4ull << 60) | v);
+      const int rows = p.tile_rows[i];
+      const int col = nb * kBN + lane * 8;
+      for (int r = warp; r < rows; r += nwarps) {
+        const int row = i * kBM + r;
+        const int a = p.row_assign[row];
+        if (a < 0) continue;
+        const int t = a / p.topk;
+        const float g = p.gates[a];
+        const uint4 yv = __ldcg(reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(row) * p.H + col));
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&yv);
+        const float2 f0 = __bfloat1622float2(h2[0]);
+        const float2 f1 = __bfloat1622float2(h2[1]);
+        const float2 f2 = __bfloat1622float2(h2[2]);
+        const float2 f3 = __bfloat1622float2(h2[3]);
+        float* o = p.out + static_cast<size_t>(t) * p.H + col;
+        red_add_v4(o, g * f0.x, g * f0.y, g * f1.x, g * f1.y);
+        red_add_v4(o + 4, g * f2.x, g * f2.y, g * f3.x, g * f3.y);
+      }
+    }
+  }
+};
+
+}  // namespace tl
+
+using namespace tl;
+
+// ============================================================================ C ABI
+static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct MoeLayout {
+  size_t experts, gates, perm, row_assign, tile_expert, tile_rows, num_mtiles, counts, xp, h, y, up_flags, y_flags,
+      total;
+  int rmax;
+};
+
+static MoeLayout moe_layout(int T, int H, int E, int F, int topk) {
+  MoeLayout L;
+  const size_t n = static_cast<size_t>(T) * topk;
+  const long long r = static_cast<long long>(n) + 127LL * E;
+  L.rmax = static_cast<int>((r + kBM - 1) / kBM * kBM);
+  const size_t tiles = L.rmax / kBM;
+  size_t o = 0;
+  L.experts = o; o += al256(n * 4);
+  L.gates = o; o += al256(n * 4);
+  L.perm = o; o += al256(n * 4);
+  L.row_assign = o; o += al256(static_cast<size_t>(L.rmax) * 4);
+  L.tile_expert = o; o += al256(tiles * 4);
+  L.tile_rows = o; o += al256(tiles * 4);
+  L.num_mtiles = o; o += 256;
+  L.counts = o; o += al256(static_cast<size_t>(E) * 4);
+  L.xp = o; o += al256(static_cast<size_t>(L.rmax) * H * 2);
+  L.h = o; o += al256(static_cast<size_t>(L.rmax) * F * 2);
+  L.y = o; o += al256(static_cast<size_t>(L.rmax) * H * 2);
+  L.up_flags = o; o += al256(tiles * (F / 128) * 8);
+  L.y_flags = o; o += al256(tiles * (H / kBN) * 8);
+  L.total = o;
+  return L;
+}
+
+static bool moe_shape_ok(int T, int H, int E, int F, int topk) {
+  return T >= 1 && topk >= 1 && topk <= kMaxTopk && E >= topk && E <= kMaxExperts && H > 0 && F > 0 &&
+         H % kBN == 0 && F % 128 == 0 && static_cast<long long>(T) * topk < (1LL << 30);
+}
+
+extern "C" size_t tl_moe_workspace_bytes(int T, int H, int E, int F, int topk) {
+  if (!moe_shape_ok(T, H, E, F, topk)) return 0;
+  return moe_layout(T, H, E, F, topk).total;
+}
+
+extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, int topk, const void* w_gate,
+                              const void* w_up, const void* w_down, float* out, int* perm_out, int* counts_out,
+                              void* workspace, size_t workspace_bytes, int T, int H, int E, int F,
+                              tl_stream_t stream) {
+  if (!ctx || !moe_shape_ok(T, H, E, F, topk)) return TL_ERR_INVALID;
+  if (!x || !logits || !w_gate || !w_up || !w_down || !out || !workspace) return TL_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(logits) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(out) || !aligned16(workspace) || (perm_out && !aligned16(perm_out)) ||
+      (counts_out && !aligned16(counts_out)))
+    return TL_ERR_INVALID;
+  if (workspace_bytes < tl_moe_workspace_bytes(T, H, E, F, topk)) return TL_ERR_WORKSPACE;
+  if (ctx->ctas <= ctx->cfg.combine_ctas) return TL_ERR_UNSUPPORTED;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const MoeLayout L = moe_layout(T, H, E, F, topk);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* experts = reinterpret_cast<int*>(ws + L.experts);
+  float* gates = reinterpret_cast<float*>(ws + L.gates);
+  int* perm = reinterpret_cast<int*>(ws + L.perm);
+  int* row_assign = reinterpret_cast<int*>(ws + L.row_assign);
+  int* tile_expert = reinterpret_cast<int*>(ws + L.tile_expert);
+  int* tile_rows = reinterpret_cast<int*>(ws + L.tile_rows);
+  int* num_mtiles = reinterpret_cast<int*>(ws + L.num_mtiles);
+  int* counts = reinterpret_cast<int*>(ws + L.counts);
+  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws + L.xp);
+  __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
+  __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
+
+  moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, experts, gates, out, H);
+  moe_permute_kernel<<<E, 1024, 0, st>>>(experts, T * topk, E, perm, row_assign, tile_expert, tile_rows, num_mtiles,
+                                         counts, perm_out, counts_out);
+  moe_gather_kernel<<<(L.rmax + 7) / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), H, topk, row_assign,
+                                                      num_mtiles, xp);
+  if (cudaGetLastError() != cudaSuccess) return TL_ERR_CUDA;
+
+  MoeParams p;
+  std::memset(&p, 0, sizeof(p));
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!tmap_2d(&p.xp, BF, 2, xp, H, L.rmax, 64, 128) || !tmap_3d(&p.wg, BF, 2, w_gate, F, H, E, 64, 64, 1) ||
+      !tmap_3d(&p.wu, BF, 2, w_up, F, H, E, 64, 64, 1) || !tmap_3d(&p.wd, BF, 2, w_down, H, F, E, 64, 64, 1) ||
+      !tmap_2d(&p.h_st, BF, 2, hb, F, L.rmax, 64, 32) || !tmap_2d(&p.h_ld, BF, 2, hb, F, L.rmax, 64, 128) ||
+      !tmap_2d(&p.y_st, BF, 2, yb, H, L.rmax, 64, 32))
+    return TL_ERR_CUDA;
+  p.common = make_common(ctx);
+  p.num_mtiles = num_mtiles;
+  p.tile_expert = tile_expert;
+  p.tile_rows = tile_rows;
+  p.row_assign = row_assign;
+  p.gates = gates;
+  p.y = yb;
+  p.out = out;
+  p.up_flags = reinterpret_cast<uint64_t*>(ws + L.up_flags);
+  p.y_flags = reinterpret_cast<uint64_t*>(ws + L.y_flags);
+  p.T = T;
+  p.H = H;
+  p.E = E;
+  p.F = F;
+  p.topk = topk;
+  p.n_up = F / 128;
+  p.n_down = H / kBN;
+  p.kb_up = H / kBK;
+  p.kb_down = F / kBK;
+  p.combine_ctas = ctx->cfg.combine_ctas;
+  return launch_persistent<MoeOp>(ctx, p, st, 0);
 }
