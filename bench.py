@@ -1,0 +1,550 @@
+#!/usr/bin/env python
+"""Benchmark of the tile-centric communication-overlapped GEMM path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one fused AllGather+GEMM call (the mover, per-chunk signals and the
+rank-swizzled persistent tcgen05 GEMM: every row of the AG+GEMM hot path) on the
+Llama-70B-MLP-like workload: W=8 emulated ranks, A_r 1024x8192, B 8192x3584 bf16
+(481.0 GFLOP).  Inputs are seeded synthetic data resident in HBM; L2 is flushed
+(a 256 MiB write) between timed steps, outside the timed events.  Each step is
+timed with CUDA events on the launching stream; K steps are bracketed by a
+barrier and a device synchronise; the max over ranks is reported.  Under
+torchrun (N > 1) every rank runs an independent replica (the path is one GPU's
+work; there is no data-path collective), so scaling is weak.
+
+The JSON line also carries the other workloads of the path (tiny AG+GEMM,
+GEMM+ReduceScatter, the MLP chain, the MoE layer) measured the same way, the
+overlap efficiency of the AG+GEMM fusion, the roofline of the dominant kernel,
+an end-to-end number through host buffers, SM clocks sampled during the timed
+region, and the CPU oracle timed on a bounded sample of the same workload.
+
+--impl reference times the fp64 CPU oracle itself (the only reference this
+path has) on bounded samples of the same workload and prints the same line
+with "impl": "reference"; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "ag_70b"
+METRIC = "fused AG+GEMM / GEMM+RS TFLOP/s on 1 GB300 (W emulated ranks); % BF16 peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+# DRAM bytes per launch of the dominant kernel from ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by the hash of the CUDA sources they were taken on.
+# A kernel changed since the capture reports traffic null.
+NCU_TRAFFIC = {}
+
+
+def src_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "communication_overlapped_gemm_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float, device=None) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.devnull, "w") if False else None
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["clock sampling unavailable"], samples=0)
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            n += 1
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(smax) if smax else None,
+                    reasons=sorted(reasons), samples=n)
+
+
+def gpu_id_for(device: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[device]
+        return str(device)
+
+
+# ----------------------------------------------------------------------------- helpers
+def dev_bf16(bits, device):
+    import numpy as np
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device)
+
+
+def pinned_bf16(bits):
+    import numpy as np
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.pin_memory()
+
+
+def timed_steps(fn, steps, flush, stream):
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each step (outside the events)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+
+def ag_flops(W, mpr, n, k):
+    return 2.0 * W * mpr * n * k
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as ge
+    ge.build()
+    import communication_overlapped_gemm_gb300 as tl
+    from seeded_inputs import WORKLOADS, workload_inputs
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    ctx = tl.Context(local)
+
+    d = WORKLOADS[WORKLOAD].dims
+    W, mpr, n, k = d["W"], d["m_per_rank"], d["n"], d["k"]
+    inp = workload_inputs(WORKLOAD)
+    a = [dev_bf16(x, device) for x in inp["a_shards"]]
+    b = dev_bf16(inp["b"], device)
+    c = torch.empty((W * mpr, n), dtype=torch.bfloat16, device=device)
+    ws = torch.zeros(tl.tl_ag_gemm_workspace_bytes(W, mpr, n, k), dtype=torch.uint8, device=device)
+    flops = ag_flops(W, mpr, n, k)
+
+    def step():
+        tl.tl_ag_gemm(ctx, a, b, c, ws, rank=0, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if ctx.check() != tl.TL_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    sampler = ClockSampler(gpu_id_for(local))
+    barrier(dist)
+    torch.cuda.synchronize()
+    sampler.start()
+    times = timed_steps(step, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    clocks = sampler.stop()
+    if ctx.check() != tl.TL_OK:
+        raise RuntimeError("device status not OK after the timed steps")
+    total_ms = max_over_ranks(dist, sum(times), device)
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    launch_ms = statistics.mean(times)
+    achieved = flops / (launch_ms * 1e-3) / 1e12
+    h = src_hash()
+    traffic = NCU_TRAFFIC.get(WORKLOAD, {}).get(h)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "W": W, "m_per_rank": mpr, "n": n, "k": k, "rank": 0,
+                   "parallelism": f"replicas x{world} (each GPU runs the W={W} emulated-rank workload)",
+                   "l2": "flushed between timed steps (256 MiB write outside the events)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": round(achieved / pk["bf16"], 4), "traffic": traffic,
+                     "peak_src": f"bf16 burst, {pk['src']} (MEASURED_PEAKS.json)" if pk["src"] == "measured"
+                     else "bf16 burst, fallback 1.9 PFLOP/s",
+                     "kernel": "tl::persistent_kernel<tl::AgOp>", "algorithmic": f"{flops/1e9:.1f} GFLOP per launch",
+                     "src_hash": h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+
+    if not args.quick:
+        line["overlap"] = overlap_ag(tl, ctx, a, b, c, ws, flush, stream, device, times, W, mpr, n, k, pk)
+        line["workloads"] = sub_workloads(tl, ctx, flush, stream, device, pk, args)
+        line["e2e"] = e2e_ag(tl, ctx, inp, device, stream, W, mpr, n, k, args)
+        line["baselines"] = {"cublas_plus_copy_ms": cublas_plus_copy(a, b, flush, stream, device)}
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline_ag(inp, args.cpu_seconds)
+    ctx.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def overlap_ag(tl, ctx, a, b, c, ws, flush, stream, device, fused_times, W, mpr, n, k, pk):
+    """(t_copy_alone + t_gemm_alone - t_fused) / min(t_copy_alone, t_gemm_alone)."""
+    import torch
+    reps = 30
+    # communication alone: the same mover, standalone
+    for _ in range(3):
+        tl.tl_allgather(ctx, a, ws, rank=0, stream=stream)
+    t_copy = statistics.median(timed_steps(lambda: tl.tl_allgather(ctx, a, ws, rank=0, stream=stream), reps,
+                                           flush, stream))
+    # GEMM alone: the same engine on the already-gathered operand (W = 1, no signals)
+    gath = ws[: W * mpr * k * 2].view(torch.bfloat16).view(W * mpr, k)
+    ws1 = torch.zeros(tl.tl_ag_gemm_workspace_bytes(1, W * mpr, n, k), dtype=torch.uint8, device=device)
+    g = lambda: tl.tl_ag_gemm(ctx, [gath], b, c, ws1, rank=0, stream=stream)
+    for _ in range(3):
+        g()
+    t_gemm = statistics.median(timed_steps(g, reps, flush, stream))
+    t_fused = statistics.median(fused_times)
+    moved = 2.0 * (W - 1 + 1) * mpr * k * 2  # bytes read + written by the mover (all W shards)
+    return {
+        "t_copy_alone_us": round(t_copy * 1e3, 2), "t_gemm_alone_us": round(t_gemm * 1e3, 2),
+        "t_fused_us": round(t_fused * 1e3, 2),
+        "efficiency": round((t_copy + t_gemm - t_fused) / min(t_copy, t_gemm), 4),
+        "copy_alone_gbs": round(moved / (t_copy * 1e-3) / 1e9, 1),
+        "gemm_alone_tflops": round(ag_flops(W, mpr, n, k) / (t_gemm * 1e-3) / 1e12, 2),
+        "gemm_alone_frac": round(ag_flops(W, mpr, n, k) / (t_gemm * 1e-3) / 1e12 / pk["bf16"], 4),
+    }
+
+
+def cublas_plus_copy(a, b, flush, stream, device):
+    """Non-overlapped context baseline: serial gather (torch.cat) then cuBLAS (torch.matmul)."""
+    import torch
+    f = lambda: torch.matmul(torch.cat(a, dim=0), b)
+    for _ in range(3):
+        f()
+    return round(statistics.median(timed_steps(f, 20, flush, stream)), 5)
+
+
+def sub_workloads(tl, ctx, flush, stream, device, pk, args):
+    import torch
+    from seeded_inputs import WORKLOADS, workload_inputs
+    out = {}
+    reps = args.sub_steps
+
+    def rec(name, fn, flops, bytes_alg, bound, launches):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        if ctx.check() != tl.TL_OK:
+            raise RuntimeError(f"{name}: device status not OK")
+        t = statistics.median(timed_steps(fn, reps, flush, stream))
+        tf = flops / (t * 1e-3) / 1e12
+        gbs = bytes_alg / (t * 1e-3) / 1e9
+        r = {"us": round(t * 1e3, 2), "tflops": round(tf, 2), "gpu_launches_per_call": launches,
+             "bound": bound}
+        if bound == "tensor":
+            r["frac"] = round(tf / pk["bf16"], 4)
+        else:
+            r["hbm_gbs"] = round(gbs, 1)
+            r["frac"] = round(gbs / pk["hbm"], 4)
+            r["tensor_frac"] = round(tf / pk["bf16"], 4)
+        out[name] = r
+
+    # tiny AG+GEMM
+    d = WORKLOADS["ag_tiny"].dims
+    inp = workload_inputs("ag_tiny")
+    a = [dev_bf16(x, device) for x in inp["a_shards"]]
+    b = dev_bf16(inp["b"], device)
+    c = torch.empty((d["W"] * d["m_per_rank"], d["n"]), dtype=torch.bfloat16, device=device)
+    ws = torch.zeros(tl.tl_ag_gemm_workspace_bytes(d["W"], d["m_per_rank"], d["n"], d["k"]), dtype=torch.uint8,
+                     device=device)
+    rec("ag_tiny", lambda: tl.tl_ag_gemm(ctx, a, b, c, ws, stream=stream),
+        ag_flops(d["W"], d["m_per_rank"], d["n"], d["k"]), 0, "latency", 1)
+    del a, b, c, ws
+
+    # GEMM + ReduceScatter
+    d = WORKLOADS["rs_70b"].dims
+    inp = workload_inputs("rs_70b")
+    a = [dev_bf16(x, device) for x in inp["a"]]
+    b = [dev_bf16(x, device) for x in inp["b"]]
+    W, m, n, kr = d["W"], d["m"], d["n"], d["k_r"]
+    o = [torch.empty((m // W, n), dtype=torch.bfloat16, device=device) for _ in range(W)]
+    ws = torch.zeros(tl.tl_gemm_rs_workspace_bytes(W, m, n, kr), dtype=torch.uint8, device=device)
+    rec("rs_70b", lambda: tl.tl_gemm_rs(ctx, a, b, o, ws, stream=stream), 2.0 * W * m * n * kr, 0, "tensor", 1)
+    del a, b, o, ws
+
+    # MLP chain
+    d = WORKLOADS["mlp2_8b"].dims
+    inp = workload_inputs("mlp2_8b")
+    W, T, hdim, f = d["W"], d["tokens"], d["hidden"], d["f_r"]
+    x = [dev_bf16(v, device) for v in inp["x_shards"]]
+    w1 = [dev_bf16(v, device) for v in inp["w1"]]
+    w2 = [dev_bf16(v, device) for v in inp["w2"]]
+    o = [torch.empty((T // W, hdim), dtype=torch.bfloat16, device=device) for _ in range(W)]
+    ws = torch.zeros(tl.tl_mlp2_workspace_bytes(W, T, hdim, f), dtype=torch.uint8, device=device)
+    rec("mlp2_8b", lambda: tl.tl_mlp2(ctx, x, w1, w2, o, ws, stream=stream), 2.0 * W * T * hdim * f * 2, 0,
+        "tensor", 1)
+    del x, w1, w2, o, ws
+
+    # MoE layer
+    d = WORKLOADS["moe_64e"].dims
+    inp = workload_inputs("moe_64e")
+    T, H, E, F, kk = d["T"], d["H"], d["E"], d["F"], d["topk"]
+    xx = dev_bf16(inp["x"], device)
+    lg = torch.from_numpy(inp["logits"]).to(device)
+    wg, wu, wd = (dev_bf16(inp[q], device) for q in ("w_gate", "w_up", "w_down"))
+    oo = torch.empty((T, H), dtype=torch.float32, device=device)
+    ws = torch.zeros(tl.tl_moe_workspace_bytes(T, H, E, F, kk), dtype=torch.uint8, device=device)
+    moe_flops = 2.0 * T * kk * H * F * 3
+    moe_bytes = 3.0 * E * H * F * 2 + T * H * 2 + T * H * 4 + T * E * 4
+    rec("moe_64e", lambda: tl.tl_moe_combine(ctx, xx, lg, kk, wg, wu, wd, oo, ws, stream=stream), moe_flops,
+        moe_bytes, "hbm", 4)
+    return out
+
+
+def e2e_ag(tl, ctx, inp, device, stream, W, mpr, n, k, args):
+    """Same metric through the public API with host buffers: H2D of the step's inputs from
+    pinned memory, the call, D2H of the result, all inside the timed region."""
+    import torch
+    ha = [pinned_bf16(x) for x in inp["a_shards"]]
+    hb = pinned_bf16(inp["b"])
+    hc = torch.empty((W * mpr, n), dtype=torch.bfloat16).pin_memory()
+    a = [torch.empty_like(x, device=device) for x in ha]
+    b = torch.empty_like(hb, device=device)
+    c = torch.empty((W * mpr, n), dtype=torch.bfloat16, device=device)
+    ws = torch.zeros(tl.tl_ag_gemm_workspace_bytes(W, mpr, n, k), dtype=torch.uint8, device=device)
+
+    def step():
+        for d_, h_ in zip(a, ha):
+            d_.copy_(h_, non_blocking=True)
+        b.copy_(hb, non_blocking=True)
+        tl.tl_ag_gemm(ctx, a, b, c, ws, stream=stream)
+        hc.copy_(c, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    steps = args.e2e_steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = sum(x.numel() * 2 for x in ha) + hb.numel() * 2
+    return {"value": round(ag_flops(W, mpr, n, k) / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hc.numel() * 2,
+            "steps": steps}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_ag_sample(inp, rows_per_shard, cols):
+    """The oracle on a sample of the workload: the first rows of every shard, the first cols of B."""
+    import oracle
+    shards = [x[:rows_per_shard] for x in inp["a_shards"]]
+    bs = inp["b"][:, :cols]
+    t0 = time.perf_counter()
+    oracle.ag_gemm(shards, bs)
+    dt = time.perf_counter() - t0
+    W = len(shards)
+    k = inp["b"].shape[0]
+    return dt, 2.0 * W * rows_per_shard * cols * k
+
+
+def cpu_baseline_ag(inp, seconds):
+    """The fp64 oracle, as it stands, on a bounded sample of the AG+GEMM workload.
+
+    The sample is the first `rows` rows of every shard times all columns of B; rows
+    doubles from 32 until one run takes at least a third of `seconds` or covers the
+    whole workload; the last run is reported.
+    """
+    n_full = inp["b"].shape[1]
+    mpr = inp["a_shards"][0].shape[0]
+    W = len(inp["a_shards"])
+    k = inp["b"].shape[0]
+    rows = 32
+    while True:
+        dt, fl = oracle_ag_sample(inp, rows, n_full)
+        if dt >= seconds / 3 or rows >= mpr:
+            break
+        rows = min(mpr, rows * 2)
+    return {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"C rows 0..{rows - 1} of each of the {W} shards x all {n_full} columns "
+                      f"({fl / 1e9:.1f} GFLOP of {2.0 * W * mpr * n_full * k / 1e9:.1f}), float64 numpy",
+            "seconds": round(dt, 3)}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from seeded_inputs import WORKLOADS, workload_inputs
+    d = WORKLOADS[WORKLOAD].dims
+    W, mpr, n, k = d["W"], d["m_per_rank"], d["n"], d["k"]
+    inp = workload_inputs(WORKLOAD)
+    # Each step is one output block: the first r rows of every shard x the first c columns
+    # (W*r == c), the largest such block whose oracle time fits args.ref_budget / (W + K).
+    per_step = args.ref_budget / (args.warmup + args.steps)
+    c = 64
+    while c < n:
+        dt, _ = oracle_ag_sample(inp, max(1, (2 * c) // W), 2 * c)
+        if dt > per_step:
+            break
+        c *= 2
+    c = min(c, n)
+    r = max(1, c // W)
+    for _ in range(args.warmup):
+        oracle_ag_sample(inp, r, c)
+    ts, fls = [], []
+    for _ in range(args.steps):
+        dt, fl = oracle_ag_sample(inp, r, c)
+        ts.append(dt)
+        fls.append(fl)
+    total_s = sum(ts)
+    value = sum(fls) / total_s / 1e12
+    sample = (f"per step: C rows 0..{r - 1} of each of the {W} shards x columns 0..{c - 1} "
+              f"({fls[0] / 1e9:.3f} GFLOP), float64 numpy")
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "W": W, "m_per_rank": mpr, "n": n, "k": k},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sub-steps", type=int, default=20, help="timed calls per extra workload")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline sample")
+    ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work in --impl reference")
+    ap.add_argument("--quick", action="store_true", help="headline only (no extra workloads / e2e / overlap)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -21,7 +21,7 @@ from . import _build
 __all__ = [
     "TL_OK", "TL_ERR_INVALID", "TL_ERR_UNSUPPORTED", "TL_ERR_CUDA", "TL_ERR_TIMEOUT", "TL_ERR_WORKSPACE",
     "TLError", "Config", "Context", "lib", "library_path", "build",
-    "tl_ag_gemm", "tl_gemm_rs", "tl_mlp2", "tl_moe_combine",
+    "tl_ag_gemm", "tl_allgather", "tl_gemm_rs", "tl_mlp2", "tl_moe_combine",
     "tl_ag_gemm_workspace_bytes", "tl_gemm_rs_workspace_bytes", "tl_mlp2_workspace_bytes",
     "tl_moe_workspace_bytes", "tl_ag_tile_order", "tl_rs_tile_order", "EXPORTED_SYMBOLS",
 ]
@@ -65,6 +65,7 @@ _SIGS = {
     "tl_strerror": (ctypes.c_char_p, [_i]),
     "tl_ag_gemm_workspace_bytes": (_c_size, [_i, _i, _i, _i]),
     "tl_ag_gemm": (_i, [_vp, _i, _i, ctypes.POINTER(_vp), _vp, _vp, _vp, _c_size, _i, _i, _i, _vp]),
+    "tl_allgather": (_i, [_vp, _i, _i, ctypes.POINTER(_vp), _vp, _c_size, _i, _i, _vp]),
     "tl_gemm_rs_workspace_bytes": (_c_size, [_i, _i, _i, _i]),
     "tl_gemm_rs": (_i, [_vp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _c_size,
                         _i, _i, _i, _vp]),
@@ -217,6 +218,18 @@ def tl_ag_gemm(ctx: Context, a_shards, b, c, workspace, rank: int = 0, stream=No
     rc = lib().tl_ag_gemm(ctx.handle, W, rank, _ptrs(a_shards), _ptr(b), _ptr(c), _ptr(workspace),
                           workspace.numel(), m_per_rank, n, k, _stream(stream))
     _check(rc, "tl_ag_gemm")
+
+
+def tl_allgather(ctx: Context, a_shards, workspace, rank: int = 0, stream=None) -> None:
+    """Pull-mode AllGather alone: the gathered [A_0; ...; A_{W-1}] lands at the start of workspace."""
+    W = len(a_shards)
+    for i, a in enumerate(a_shards):
+        _need(a, "bf16", f"a_shards[{i}]")
+    _need(workspace, "u8", "workspace")
+    m_per_rank, k = a_shards[0].shape
+    rc = lib().tl_allgather(ctx.handle, W, rank, _ptrs(a_shards), _ptr(workspace), workspace.numel(),
+                            m_per_rank, k, _stream(stream))
+    _check(rc, "tl_allgather")
 
 
 def tl_gemm_rs(ctx: Context, a, b, out, workspace, stream=None) -> None:

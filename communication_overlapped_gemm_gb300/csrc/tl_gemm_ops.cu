@@ -375,6 +375,15 @@ struct Mlp2Op : OpBase<Mlp2Params> {
   }
 };
 
+// ============================================================================ AllGather alone
+// The pull-mode AllGather as its own kernel (the communication task of "Triton-
+// distributed ...", §3.2 Algorithm 2, without a consumer): the same mover code, chunk
+// geometry, order and signals as the fused AllGather+GEMM, run by mover_warps warps in
+// each of the persistent CTAs.
+__global__ void __launch_bounds__(kMaxMoverWarps * 32) allgather_kernel(const __grid_constant__ AgParams p) {
+  AgOp::mover(p, threadIdx.x >> 5, threadIdx.x & 31);
+}
+
 }  // namespace tl
 
 using namespace tl;
@@ -570,4 +579,33 @@ extern "C" int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const vo
   p.shard_bytes = static_cast<long long>(Tr) * hidden * 2;
   p.slab_bytes = static_cast<long long>(kBM) * hidden * 2;
   return launch_persistent<Mlp2Op>(ctx, p, reinterpret_cast<cudaStream_t>(stream), ctx->cfg.mover_warps);
+}
+
+extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_shards, void* workspace,
+                            size_t workspace_bytes, int m_per_rank, int k, tl_stream_t stream) {
+  if (!ctx || !ag_shape_ok(W, m_per_rank, 8, k) || rank < 0 || rank >= W) return TL_ERR_INVALID;
+  if (m_per_rank == 0 || k == 0) return TL_OK;
+  if (!a_shards || !workspace || !aligned16(workspace)) return TL_ERR_INVALID;
+  for (int r = 0; r < W; ++r)
+    if (!a_shards[r] || !aligned16(a_shards[r])) return TL_ERR_INVALID;
+  if (workspace_bytes < tl_ag_gemm_workspace_bytes(W, m_per_rank, 8, k)) return TL_ERR_WORKSPACE;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
+  AgParams p;
+  std::memset(&p, 0, sizeof(p));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.gath = ws;
+  p.flags = reinterpret_cast<uint64_t*>(ws + align256(static_cast<size_t>(W) * m_per_rank * k * 2));
+  p.common = make_common(ctx);
+  for (int r = 0; r < W; ++r) p.shard[r] = static_cast<const uint8_t*>(a_shards[r]);
+  p.W = W;
+  p.rank = rank;
+  p.m_per_rank = m_per_rank;
+  p.mps = m_per_rank / kBM;
+  p.swizzle = ctx->cfg.swizzle;
+  p.chunks = ctx->cfg.chunks_per_slab;
+  p.skip_chunk = -1;
+  p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
+  p.slab_bytes = static_cast<long long>(kBM) * k * 2;
+  allgather_kernel<<<ctx->ctas, ctx->cfg.mover_warps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? TL_OK : TL_ERR_CUDA;
 }

@@ -130,6 +130,17 @@ size_t tl_ag_gemm_workspace_bytes(int W, int m_per_rank, int n, int k);
 int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b, void* c,
                void* workspace, size_t workspace_bytes, int m_per_rank, int n, int k, tl_stream_t stream);
 
+/* ---------------------------------------------------------------- AllGather alone
+ * [TD] §3.2 Algorithm 2 (pull-mode one-sided AllGather) as its own kernel: the shard mover of
+ * tl_ag_gemm (same chunks, order and signals) without the GEMM, run by cfg.mover_warps warps
+ * in each persistent CTA.  Fills the gathered buffer at the start of `workspace` (sized by
+ * tl_ag_gemm_workspace_bytes(W, m_per_rank, 8, k)) with [A_0; ...; A_{W-1}] and releases every
+ * chunk signal.  Shapes and errors as tl_ag_gemm.  This is the "communication alone" leg of
+ * the overlap measurement.
+ */
+int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_shards, void* workspace, size_t workspace_bytes,
+                 int m_per_rank, int k, tl_stream_t stream);
+
 /* ---------------------------------------------------------------- GEMM + ReduceScatter
  * [TD] §3.3 Algorithm 3 (each producer pushes its partial into the owner's slot, the owner
  * accumulates), [TL] §5 / Figure 4 text (producer tiles notify; peer tiles chain the partial
