@@ -74,6 +74,7 @@ _SIGS = {
                      _vp, _c_size, _i, _i, _i, _vp]),
     "tl_moe_workspace_bytes": (_c_size, [_i, _i, _i, _i, _i]),
     "tl_moe_combine": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_size, _i, _i, _i, _i, _vp]),
+    "tl_ag_gemm_static_scratch": (_i, [_vp, _i, _i, ctypes.POINTER(_vp), _vp, _vp, _i, _i, _i, _vp]),
     "tl_ag_tile_order": (_i, [_i, _i, _i, _i, _i, _vp, _vp, _vp, _i]),
     "tl_rs_tile_order": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _i]),
 }
@@ -311,3 +312,23 @@ def tl_rs_tile_order(W, m, n, swizzle):
     if rc < 0:
         raise TLError(rc, "tl_rs_tile_order")
     return tuple(out)
+
+
+# ---------------------------------------------------------------- AllGather + GEMM without allocation
+TL_AG_GEMM_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def tl_ag_gemm_static_scratch(ctx: Context, a_shards, b, c, rank: int = 0, stream=None) -> None:
+    """tl_ag_gemm for callers that cannot allocate device memory (stream capture, plug-ins
+    without an allocator, allocation-free real-time paths): the scratch is the library's
+    fixed 16 MiB device array, so problems needing more raise TLError(TL_ERR_WORKSPACE),
+    and calls whose GPU work overlaps race on that array."""
+    W = len(a_shards)
+    for i, a in enumerate(a_shards):
+        _need(a, "bf16", f"a_shards[{i}]")
+    _need(b, "bf16", "b"); _need(c, "bf16", "c")
+    m_per_rank, k = a_shards[0].shape
+    n = b.shape[1]
+    rc = lib().tl_ag_gemm_static_scratch(ctx.handle, W, rank, _ptrs(a_shards), _ptr(b), _ptr(c), m_per_rank, n, k,
+                                         _stream(stream))
+    _check(rc, "tl_ag_gemm_static_scratch")

@@ -207,6 +207,27 @@ int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, int topk, co
                    const void* w_up, const void* w_down, float* out, int* perm_out, int* counts_out,
                    void* workspace, size_t workspace_bytes, int T, int H, int E, int F, tl_stream_t stream);
 
+/* ---------------------------------------------------------------- AllGather + GEMM without allocation
+ * The pages have no counterpart of this entry point.  It exists for callers that cannot
+ * allocate device memory when they call in: code being recorded into a CUDA graph by stream
+ * capture (cudaMalloc cannot be recorded), plug-ins whose host framework owns the allocator
+ * and gives out no scratch, and real-time paths that forbid allocation after start-up.
+ *
+ * Same operation, arguments, shapes and result as tl_ag_gemm, minus the workspace: the
+ * gathered operand and the chunk signals live in a fixed device array of
+ * TL_AG_GEMM_STATIC_SCRATCH_BYTES inside the library, which every GPU that loads the library
+ * keeps until the process exits.  A problem whose tl_ag_gemm_workspace_bytes() exceeds that
+ * size is rejected with TL_ERR_WORKSPACE before anything is enqueued.  The entry point
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library call).  Its first call on a
+ * device looks up the array's device address with that device current; make that first call
+ * before any stream capture begins.  All calls share the one array (each call clears the
+ * signals and overwrites the gathered operand), so calls whose GPU work overlaps in time race
+ * and give undefined results: order them on one stream or with events.
+ */
+#define TL_AG_GEMM_STATIC_SCRATCH_BYTES (16u << 20)
+int tl_ag_gemm_static_scratch(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b, void* c,
+                              int m_per_rank, int n, int k, tl_stream_t stream);
+
 /* ---------------------------------------------------------------- host-side tile maps (no GPU)
  * The static tile-centric mappings the kernels use ([TL] §4.1), evaluated on the host by the
  * same code the device runs, for inspection and testing.
