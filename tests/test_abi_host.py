@@ -1,0 +1,130 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+The library builds for sm_103a with nvcc, loads, and exports every function that
+include/tl.h declares; host-only entry points (config defaults, status strings,
+workspace sizes, argument validation, the tile-order maps) behave as documented.
+The tile orders are tied to the static tile-centric mapping formulas of
+"TileLink: Generating Efficient Compute-Communication Overlapping Kernels using
+Tile-Centric Primitives", §4.1 (as restated in the oracle), and to the swizzles of
+"Triton-distributed ...", §3.7.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tl():
+    import communication_overlapped_gemm_gb300 as tl
+    tl.build()
+    tl.lib()
+    return tl
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "tl.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tl_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(tl):
+    declared = header_functions()
+    assert len(declared) >= 19
+    L = tl.lib()
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in include/tl.h but not exported"
+    assert sorted(tl.EXPORTED_SYMBOLS) == declared
+
+
+def test_built_for_sm103a_only():
+    from communication_overlapped_gemm_gb300 import _build
+    assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_config_defaults_and_strerror(tl):
+    c = tl.Config()
+    assert tl.lib().tl_config_default(ctypes.byref(c)) == tl.TL_OK
+    assert (c.mover_warps, c.chunks_per_slab, c.swizzle, c.grid_ctas, c.combine_ctas) == (2, 32, 1, 0, 8)
+    assert c.debug_skip_chunk == -1 and c.timeout_ns == 2_000_000_000
+    assert tl.lib().tl_config_default(None) == tl.TL_ERR_INVALID
+    for code in (tl.TL_OK, tl.TL_ERR_INVALID, tl.TL_ERR_UNSUPPORTED, tl.TL_ERR_CUDA, tl.TL_ERR_TIMEOUT,
+                 tl.TL_ERR_WORKSPACE):
+        assert tl.lib().tl_strerror(code)
+    assert tl.lib().tl_version() >= 100
+
+
+def test_workspace_sizes(tl):
+    # gathered A (W*m*k*2) + 32 signals of 8 bytes per 128-row slab, each 256-aligned
+    assert tl.tl_ag_gemm_workspace_bytes(8, 1024, 3584, 8192) == 8 * 1024 * 8192 * 2 + 8 * 8 * 32 * 8
+    assert tl.tl_ag_gemm_workspace_bytes(2, 100, 256, 256) == 0       # m_per_rank not a 128 multiple
+    assert tl.tl_ag_gemm_workspace_bytes(9, 128, 256, 256) == 0       # W > 8
+    assert tl.tl_gemm_rs_workspace_bytes(8, 8192, 8192, 3584) == 8192 * 8192 * 4 + 64 * 32 * 8
+    assert tl.tl_gemm_rs_workspace_bytes(8, 1000, 256, 64) == 0
+    assert tl.tl_mlp2_workspace_bytes(4, 4096, 4096, 3584) > 4 * 4096 * 4096 * 2 + 4 * 4096 * 3584 * 2
+    assert tl.tl_moe_workspace_bytes(4096, 2048, 64, 1408, 2) > 0
+    assert tl.tl_moe_workspace_bytes(4096, 2000, 64, 1408, 2) == 0    # H not a 256 multiple
+    assert tl.tl_moe_workspace_bytes(4096, 2048, 300, 1408, 2) == 0   # E > 256
+
+
+def test_argument_validation_needs_no_gpu(tl):
+    L = tl.lib()
+    ptrs = (ctypes.c_void_p * 2)(16, 32)
+    # null context / bad shapes are rejected before any CUDA call
+    assert L.tl_ag_gemm(None, 2, 0, ptrs, 16, 16, 16, 1 << 20, 128, 256, 256, None) == tl.TL_ERR_INVALID
+    assert L.tl_gemm_rs(None, 2, ptrs, ptrs, ptrs, 16, 1 << 20, 256, 256, 64, None) == tl.TL_ERR_INVALID
+    assert L.tl_mlp2(None, 2, ptrs, ptrs, ptrs, ptrs, 16, 1 << 20, 256, 256, 256, None) == tl.TL_ERR_INVALID
+    assert L.tl_moe_combine(None, 16, 16, 2, 16, 16, 16, 16, None, None, 16, 1 << 20, 64, 256, 4, 128,
+                            None) == tl.TL_ERR_INVALID
+    assert L.tl_ag_gemm_static_scratch(None, 2, 0, ptrs, 16, 16, 128, 256, 256, None) == tl.TL_ERR_INVALID
+    assert L.tl_allgather(None, 2, 0, ptrs, 16, 1 << 20, 128, 256, None) == tl.TL_ERR_INVALID
+    assert L.tl_ctx_check(None) == tl.TL_ERR_INVALID
+
+
+@pytest.mark.parametrize("W,rank,mpr,n", [(8, 0, 1024, 3584), (8, 5, 1024, 3584), (2, 1, 128, 256), (3, 2, 256, 520)])
+def test_ag_tile_order_is_rank_swizzled_and_matches_static_map(tl, W, rank, mpr, n):
+    src, mb, nb = tl.tl_ag_tile_order(W, rank, mpr, n, 1)
+    mps, nbk = mpr // 128, -(-n // 256)
+    assert len(src) == W * mps * nbk
+    # every tile exactly once
+    keys = set(zip(src.tolist(), mb.tolist(), nb.tolist()))
+    assert len(keys) == len(src) == len({(s, m, b) for s in range(W) for m in range(mps) for b in range(nbk)})
+    # step s computes with the shard of rank (rank + s) mod W: the local shard first
+    per = mps * nbk
+    for s in range(W):
+        assert set(src[s * per:(s + 1) * per].tolist()) == {(rank + s) % W}
+    # the source rank agrees with the pages' static mapping f_R for the tile's global rows
+    for t in range(0, len(src), max(1, len(src) // 97)):
+        row_tile = (src[t] * mpr) // 128 + mb[t]
+        lo, hi, r, _ = oracle.static_tile_map(int(row_tile), W * mpr, W, 1, 128)
+        assert r == src[t] and lo == src[t] * mpr + mb[t] * 128
+    s0, _, _ = tl.tl_ag_tile_order(W, rank, mpr, n, 0)
+    assert s0[:per].tolist() == [0] * per  # identity order starts at rank 0
+
+
+@pytest.mark.parametrize("W,m,n", [(8, 8192, 8192), (4, 1024, 520), (1, 128, 256)])
+def test_rs_tile_order_producer_major_owner_swizzled(tl, W, m, n):
+    p, o, mb, nb = tl.tl_rs_tile_order(W, m, n, 1)
+    mbo, nbk = m // W // 128, -(-n // 256)
+    assert len(p) == W * W * mbo * nbk
+    assert len(set(zip(p.tolist(), o.tolist(), mb.tolist(), nb.tolist()))) == len(p)
+    assert np.all(np.diff(p) >= 0)  # producers visited 0..W-1 (fixed fp32 summation order)
+    per_owner = mbo * nbk
+    for q in range(W):
+        seq = o[p == q][::per_owner].tolist()
+        assert seq == [(q + 1 + s) % W for s in range(W)]  # next rank's rows first, own rows last
+    p0, o0, _, _ = tl.tl_rs_tile_order(W, m, n, 0)
+    assert o0[p0 == 0][::per_owner].tolist() == list(range(W))
+
+
+def test_tile_order_rejects_bad_shapes(tl):
+    with pytest.raises(tl.TLError):
+        tl.tl_ag_tile_order(2, 2, 128, 256, 1)
+    with pytest.raises(tl.TLError):
+        tl.tl_rs_tile_order(3, 1000, 256, 1)
