@@ -85,9 +85,13 @@ __global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E,
 // (t, j) order with a block-wide ballot scan.  Outputs:
 //   perm[off_e + pos] = a                      (unpadded order: expert, t, j)
 //   row_assign[poff_e + pos] = a, -1 on padding rows of the expert's 128-row-aligned segment
+//   row_meta[row] = {token, gate bits} of the row's assignment ({-1, 0} on padding rows), so
+//     the combine reads one 8-byte record per row instead of two dependent loads
 //   tile_expert / tile_rows for each 128-row tile of the padded layout (the f_R / f_S tables)
-__global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict__ experts, int n, int E,
+__global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict__ experts, int n, int E, int topk,
+                                                           const float* __restrict__ gates,
                                                            int* __restrict__ perm, int* __restrict__ row_assign,
+                                                           int2* __restrict__ row_meta,
                                                            int* __restrict__ tile_expert, int* __restrict__ tile_rows,
                                                            int* __restrict__ num_mtiles, int* __restrict__ counts,
                                                            int* __restrict__ perm_out, int* __restrict__ counts_out) {
@@ -139,6 +143,7 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
       perm[off[e] + pos] = a;
       if (perm_out) perm_out[off[e] + pos] = a;
       row_assign[poff[e] + pos] = a;
+      row_meta[poff[e] + pos] = make_int2(a / topk, __float_as_int(gates[a]));
     }
     const int tot = warp_tot[0];
     __syncthreads();
@@ -146,7 +151,10 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
   }
   const int cnt = hist[e];
   const int padded = poff[e + 1] - poff[e];
-  for (int i = cnt + tid; i < padded; i += blockDim.x) row_assign[poff[e] + i] = -1;
+  for (int i = cnt + tid; i < padded; i += blockDim.x) {
+    row_assign[poff[e] + i] = -1;
+    row_meta[poff[e] + i] = make_int2(-1, 0);
+  }
   for (int i = tid; i < padded / kBM; i += blockDim.x) {
     const int tile = poff[e] / kBM + i;
     tile_expert[tile] = e;
@@ -182,17 +190,23 @@ struct MoeParams {
   CUtensorMap h_st;  // h {F, R}, box {64, 32}
   CUtensorMap h_ld;  // h {F, R}, box {64, 128}
   CUtensorMap y_st;  // y {H, R}, box {64, 32}
+  CUtensorMap y_ld;  // y {H, R}, box {64, 128} (combine partition loads)
   Common common;
   const int* num_mtiles;
   const int* tile_expert;
   const int* tile_rows;
-  const int* row_assign;
-  const float* gates;
+  const int2* row_meta;
   const __nv_bfloat16* y;
   float* out;
   uint64_t* up_flags;  // [R/128][n_up]
   uint64_t* y_flags;   // [R/128][n_down]
-  int T, H, E, F, topk, n_up, n_down, kb_up, kb_down, combine_ctas;
+  int T, H, E, F, topk, n_up, n_down, kb_up, kb_down, combine_ctas, chunk;
+};
+
+struct MoeSlot {
+  int kind;  // 1 up-projection, 2 down-projection
+  int i;     // row tile
+  int nb;    // column block
 };
 
 // Up-projection stage: two 128x128 accumulators (gate, up) from one A stage.
@@ -224,25 +238,60 @@ struct MoeOp : OpBase<MoeParams> {
     gi = blockIdx.x;
     return static_cast<int>(blockIdx.x) < gn;
   }
-  // Tile order: all up-projection tiles, then all down-projection tiles; inside each,
-  // the row tile is the fastest index so that the row tiles of one expert (which
-  // share its weight columns) run side by side.
+  // Tile order.  Row tiles (128 padded rows, expert-major) are grouped in chunks of
+  // p.chunk; the sequence is U0, U1, D0, U2, D1, ..., U_last, D_last-1, D_last where U_c
+  // are chunk c's up-projection tiles and D_c its down-projection tiles.  A down tile
+  // therefore comes after every up tile it waits on (no deadlock in a co-resident grid),
+  // one chunk of up work separates them, and down tiles (hence the combine partition's
+  // work) start early instead of after the whole up phase.  Inside a chunk the row tile
+  // is the fastest index, so the row tiles of one expert, which share its weight
+  // columns, run side by side.
+  static __device__ MoeSlot slot(const Params& p, int m, int t) {
+    const int G = p.chunk;
+    const int nc = (m + G - 1) / G;
+    int pos = 0;
+    for (int sg = 0; sg <= nc; ++sg) {
+      if (sg < nc) {
+        const int gc = min(G, m - sg * G);
+        const int sz = gc * p.n_up;
+        if (t < pos + sz) {
+          const int w = t - pos;
+          return MoeSlot{1, sg * G + w % gc, w / gc};
+        }
+        pos += sz;
+      }
+      if (sg >= 1) {
+        const int c = sg - 1;
+        const int gc = min(G, m - c * G);
+        const int sz = gc * p.n_down;
+        if (t < pos + sz) {
+          const int w = t - pos;
+          return MoeSlot{2, c * G + w % gc, w / gc};
+        }
+        pos += sz;
+      }
+    }
+    return MoeSlot{2, 0, 0};  // t beyond the sequence: never requested
+  }
+  // The v-th down-projection tile in production order (the combine partition's order).
+  static __device__ MoeSlot down_slot(const Params& p, int m, int v) {
+    const int G = p.chunk;
+    const int c = v / (G * p.n_down);
+    const int gc = min(G, m - c * G);
+    const int w = v - c * G * p.n_down;
+    return MoeSlot{2, c * G + w % gc, w / gc};
+  }
   static __device__ Job job(const Params& p, int t) {
-    const int m = mtiles(p);
-    const int nu = m * p.n_up;
+    const MoeSlot sl = slot(p, mtiles(p), t);
     Job j;
-    if (t < nu) {
-      j.kind = 1;
-      j.x0 = t % m;
-      j.x1 = t / m;
-      j.b_col = j.x1 * 128;
+    j.kind = sl.kind;
+    j.x0 = sl.i;
+    j.x1 = sl.nb;
+    if (sl.kind == 1) {
+      j.b_col = sl.nb * 128;
       j.kblocks = p.kb_up;
     } else {
-      const int u = t - nu;
-      j.kind = 2;
-      j.x0 = u % m;
-      j.x1 = u / m;
-      j.b_col = j.x1 * kBN;
+      j.b_col = sl.nb * kBN;
       j.kblocks = p.kb_down;
     }
     j.a_sel = 0;
@@ -318,34 +367,73 @@ struct MoeOp : OpBase<MoeParams> {
   // for each valid row a = (t, j): out[t, cols] += gate_a * y[a, cols] (fp32 vector
   // reductions; with a zeroed out and top-2, 0 + a + b == 0 + b + a, so the result
   // does not depend on which contribution lands first).
-  static __device__ void side_role(const Params& p, int warp, int lane, uint8_t*) {
-    const int nwarps = blockDim.x >> 5;
+  //
+  // Each combine CTA runs two independent halves (warps 0-3 and 4-7), each with its own
+  // 64 KB shared-memory tile buffer: the half's first warp waits on the tile's signal, one
+  // lane TMA-loads the 128 x 256 y tile, and the half stages the 128 rows' (token, gate)
+  // records.  Each warp then takes 32 rows: for every row, lane l scales columns
+  // [4l, 4l+4) and [128+4l, 128+4l+4) by the gate and adds them into out[token] with two
+  // fp32 vector reductions, so each warp instruction covers 512 contiguous bytes of the
+  // output row.  While one half waits for its load the other reduces.
+  static __device__ void side_role(const Params& p, int warp, int lane, uint8_t* smem_raw) {
+    uint8_t* base =
+        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int kTileBytes = kBM * kBN * 2;  // 64 KB of bf16 y
+    const int half = warp >> 2;
+    if (half > 1) return;
+    const int hw = warp & 3;  // warp inside the half
+    uint8_t* buf = base + half * kTileBytes;
+    int2* meta = reinterpret_cast<int2*>(base + 2 * kTileBytes) + half * kBM;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + 2 * kTileBytes + 2 * kBM * sizeof(int2)) + half;
+    if (hw == 0 && lane == 0) {
+      mbar_init(bar, 1);
+      fence_mbar_init();
+    }
+    named_bar_sync(1 + half, 128);
     const int cc = blockIdx.x - (gridDim.x - p.combine_ctas);
     const int m = mtiles(p);
     const int total = m * p.n_down;
-    for (int v = cc; v < total; v += p.combine_ctas) {
-      const int i = v % m;
-      const int nb = v / m;
-      warp_wait_one(p.y_flags + static_cast<size_t>(i) * p.n_down + nb, p.common.epoch, p.common, lane,
-                    kSiteCombine, (4ull << 60) | v);
-      const int rows = p.tile_rows[i];
-      const int col = nb * kBN + lane * 8;
-      for (int r = warp; r < rows; r += nwarps) {
-        const int row = i * kBM + r;
-        const int a = p.row_assign[row];
-        if (a < 0) continue;
-        const int t = a / p.topk;
-        const float g = p.gates[a];
-        const uint4 yv = __ldcg(reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(row) * p.H + col));
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&yv);
-        const float2 f0 = __bfloat1622float2(h2[0]);
-        const float2 f1 = __bfloat1622float2(h2[1]);
-        const float2 f2 = __bfloat1622float2(h2[2]);
-        const float2 f3 = __bfloat1622float2(h2[3]);
-        float* o = p.out + static_cast<size_t>(t) * p.H + col;
-        red_add_v4(o, g * f0.x, g * f0.y, g * f1.x, g * f1.y);
-        red_add_v4(o + 4, g * f2.x, g * f2.y, g * f3.x, g * f3.y);
+    // This lane's two 4-column groups: box g (64 columns each), byte offset inside the 128-B row.
+    const int g0 = lane >> 4, g1 = 2 + (lane >> 4);
+    const int piece = (lane & 15) >> 1, sub = (lane & 1) * 8;
+    uint32_t phase = 0;
+    for (int v = 2 * cc + half; v < total; v += 2 * p.combine_ctas) {
+      const MoeSlot sl = down_slot(p, m, v);
+      if (hw == 0) {
+        warp_wait_one(p.y_flags + static_cast<size_t>(sl.i) * p.n_down + sl.nb, p.common.epoch, p.common, lane,
+                      kSiteCombine, (4ull << 60) | v);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, kTileBytes);
+#pragma unroll
+          for (int g = 0; g < kBN / 64; ++g)
+            tma_load_2d(buf + g * (kBM * 128), &p.y_ld, bar, sl.nb * kBN + g * 64, sl.i * kBM);
+        }
       }
+      const int tid = hw * 32 + lane;  // one row record per thread of the half
+      meta[tid] = __ldcg(p.row_meta + sl.i * kBM + tid);
+      mbar_wait(bar, phase, p.common, kSiteCombine);
+      phase ^= 1u;
+      named_bar_sync(1 + half, 128);
+      const uint32_t b0 = smem_u32(buf);
+#pragma unroll 4
+      for (int r = hw * 32; r < hw * 32 + 32; ++r) {
+        const int2 md = meta[r];
+        if (md.x < 0) continue;
+        // 128-byte swizzle of the TMA box: 16-byte piece j of row r sits at j ^ (r & 7)
+        const uint32_t off = r * 128 + (((piece ^ (r & 7))) << 4) + sub;
+        uint32_t a0, a1, c0, c1;
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(a0), "=r"(a1) : "r"(b0 + g0 * (kBM * 128) + off));
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(c0), "=r"(c1) : "r"(b0 + g1 * (kBM * 128) + off));
+        const float gt = __int_as_float(md.y);
+        const float2 fa = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&a0));
+        const float2 fb = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&a1));
+        const float2 fc = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&c0));
+        const float2 fd = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&c1));
+        float* o = p.out + static_cast<size_t>(md.x) * p.H + sl.nb * kBN + lane * 4;
+        red_add_v4(o, gt * fa.x, gt * fa.y, gt * fb.x, gt * fb.y);
+        red_add_v4(o + 128, gt * fc.x, gt * fc.y, gt * fd.x, gt * fd.y);
+      }
+      named_bar_sync(1 + half, 128);  // the tile buffer and records are free for the next tile
     }
   }
 };
@@ -358,7 +446,7 @@ using namespace tl;
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct MoeLayout {
-  size_t experts, gates, perm, row_assign, tile_expert, tile_rows, num_mtiles, counts, xp, h, y, up_flags, y_flags,
+  size_t experts, gates, perm, row_assign, row_meta, tile_expert, tile_rows, num_mtiles, counts, xp, h, y, up_flags, y_flags,
       total;
   int rmax;
 };
@@ -374,6 +462,7 @@ static MoeLayout moe_layout(int T, int H, int E, int F, int topk) {
   L.gates = o; o += al256(n * 4);
   L.perm = o; o += al256(n * 4);
   L.row_assign = o; o += al256(static_cast<size_t>(L.rmax) * 4);
+  L.row_meta = o; o += al256(static_cast<size_t>(L.rmax) * 8);
   L.tile_expert = o; o += al256(tiles * 4);
   L.tile_rows = o; o += al256(tiles * 4);
   L.num_mtiles = o; o += 256;
@@ -417,6 +506,7 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   float* gates = reinterpret_cast<float*>(ws + L.gates);
   int* perm = reinterpret_cast<int*>(ws + L.perm);
   int* row_assign = reinterpret_cast<int*>(ws + L.row_assign);
+  int2* row_meta = reinterpret_cast<int2*>(ws + L.row_meta);
   int* tile_expert = reinterpret_cast<int*>(ws + L.tile_expert);
   int* tile_rows = reinterpret_cast<int*>(ws + L.tile_rows);
   int* num_mtiles = reinterpret_cast<int*>(ws + L.num_mtiles);
@@ -426,7 +516,7 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
 
   moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, experts, gates, out, H);
-  moe_permute_kernel<<<E, 1024, 0, st>>>(experts, T * topk, E, perm, row_assign, tile_expert, tile_rows, num_mtiles,
+  moe_permute_kernel<<<E, 1024, 0, st>>>(experts, T * topk, E, topk, gates, perm, row_assign, row_meta, tile_expert, tile_rows, num_mtiles,
                                          counts, perm_out, counts_out);
   moe_gather_kernel<<<(L.rmax + 7) / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), H, topk, row_assign,
                                                       num_mtiles, xp);
@@ -438,14 +528,13 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   if (!tmap_2d(&p.xp, BF, 2, xp, H, L.rmax, 64, 128) || !tmap_3d(&p.wg, BF, 2, w_gate, F, H, E, 64, 64, 1) ||
       !tmap_3d(&p.wu, BF, 2, w_up, F, H, E, 64, 64, 1) || !tmap_3d(&p.wd, BF, 2, w_down, H, F, E, 64, 64, 1) ||
       !tmap_2d(&p.h_st, BF, 2, hb, F, L.rmax, 64, 32) || !tmap_2d(&p.h_ld, BF, 2, hb, F, L.rmax, 64, 128) ||
-      !tmap_2d(&p.y_st, BF, 2, yb, H, L.rmax, 64, 32))
+      !tmap_2d(&p.y_st, BF, 2, yb, H, L.rmax, 64, 32) || !tmap_2d(&p.y_ld, BF, 2, yb, H, L.rmax, 64, 128))
     return TL_ERR_CUDA;
   p.common = make_common(ctx);
   p.num_mtiles = num_mtiles;
   p.tile_expert = tile_expert;
   p.tile_rows = tile_rows;
-  p.row_assign = row_assign;
-  p.gates = gates;
+  p.row_meta = row_meta;
   p.y = yb;
   p.out = out;
   p.up_flags = reinterpret_cast<uint64_t*>(ws + L.up_flags);
@@ -460,5 +549,7 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   p.kb_up = H / kBK;
   p.kb_down = F / kBK;
   p.combine_ctas = ctx->cfg.combine_ctas;
-  return launch_persistent<MoeOp>(ctx, p, st, 0);
+  p.chunk = 16;
+  // Two extra warps per CTA: idle in the GEMM partition, combine workers in the combine CTAs.
+  return launch_persistent<MoeOp>(ctx, p, st, 2);
 }
