@@ -180,14 +180,15 @@ int tl_ag_tile_order(int W, int rank, int m_per_rank, int n, int swizzle, int* s
   if (W < 1 || W > 8 || rank < 0 || rank >= W || m_per_rank <= 0 || m_per_rank % tl::kBM || n <= 0 ||
       (swizzle != 0 && swizzle != 1))
     return TL_ERR_INVALID;
-  const int mps = m_per_rank / tl::kBM, nbk = tl::ceil_div(n, tl::kBN);
+  const int bm = m_per_rank % 256 == 0 ? 256 : 128;  // the tile rows tl_ag_gemm uses
+  const int mps = m_per_rank / bm, nbk = tl::ceil_div(n, tl::kBN);
   const int total = tl::ag_num_tiles(W, mps, nbk);
   if (!src_rank && !m_block && !n_block) return total;
   if (!src_rank || !m_block || !n_block || cap < total) return TL_ERR_INVALID;
   for (int t = 0; t < total; ++t) {
     tl::AgTile a = tl::ag_tile(t, W, rank, mps, nbk, swizzle);
     src_rank[t] = a.src;
-    m_block[t] = a.mb;
+    m_block[t] = a.mb * (bm / tl::kBM);
     n_block[t] = a.nb;
   }
   return total;
@@ -197,7 +198,8 @@ int tl_rs_tile_order(int W, int m, int n, int swizzle, int* producer, int* owner
                      int cap) {
   if (W < 1 || W > 8 || m <= 0 || m % (tl::kBM * W) || n <= 0 || (swizzle != 0 && swizzle != 1))
     return TL_ERR_INVALID;
-  const int mbo = m / W / tl::kBM, nbk = tl::ceil_div(n, tl::kBN);
+  const int bm = (m / W) % 256 == 0 ? 256 : 128;  // the tile rows tl_gemm_rs uses
+  const int mbo = m / W / bm, nbk = tl::ceil_div(n, tl::kBN);
   const int total = tl::rs_num_tiles(W, mbo, nbk);
   if (!producer && !owner && !m_block && !n_block) return total;
   if (!producer || !owner || !m_block || !n_block || cap < total) return TL_ERR_INVALID;
@@ -205,7 +207,7 @@ int tl_rs_tile_order(int W, int m, int n, int swizzle, int* producer, int* owner
     tl::RsTile r = tl::rs_tile(t, W, mbo, nbk, swizzle);
     producer[t] = r.p;
     owner[t] = r.o;
-    m_block[t] = r.mb;
+    m_block[t] = r.mb * (bm / tl::kBM);
     n_block[t] = r.nb;
   }
   return total;

@@ -31,15 +31,31 @@
 
 namespace tl {
 
-constexpr int kStages = 4;
-constexpr int kAStageBytes = kBM * kBK * 2;               // 16 KB
-constexpr int kBStageBytes = kBN * kBK * 2;               // 32 KB
-constexpr int kStageBytes = kAStageBytes + kBStageBytes;  // 48 KB
-constexpr int kEpiBufBytes = 32 * 128;                    // 32 rows x 128 B
-constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;           // 4 warps x 2 buffers
+constexpr int kMaxStages = 4;
+constexpr int kBStageBytes = kBN * kBK * 2;  // 32 KB of B per stage
+constexpr int kEpiBufBytes = 32 * 128;       // 32 rows x 128 B
+constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;  // 4 warps x 2 buffers
 constexpr int kBarBytes = 256;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
+constexpr int kRingBytes = 196608;  // the A/B stage ring: 4 x 48 KB (BM = 128) or 3 x 64 KB (BM = 256)
+constexpr int kSmemBytes = 1024 + kRingBytes + kEpiBytes + kBarBytes;
 constexpr int kTmemCols = 512;
+
+// Tile geometry.  BM = 128: one 128x256 accumulator per tile, 4 stages of 48 KB, two
+// TMEM accumulators so the epilogue of one tile overlaps the next tile's MMAs.
+// BM = 256: two 128x256 accumulators per tile (rows 0-127 and 128-255) fed by the same
+// B slice, 3 stages of 64 KB, one TMEM buffer.  The 256-row tile reads each B slice from
+// shared memory once per two MMAs, cutting shared-memory traffic per MMA from ~24 KB to
+// ~20 KB (operand reads + TMA fill), which is what bounds the 128-row tile.
+template <int BM>
+struct Geo {
+  static_assert(BM == 128 || BM == 256, "tile rows");
+  static constexpr int kStages = BM == 256 ? 3 : 4;
+  static constexpr int kABytes = BM * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBStageBytes;
+  static constexpr int kAccBufs = BM == 256 ? 1 : 2;
+  static constexpr int kAccStride = BM == 256 ? 512 : 256;  // TMEM columns per accumulator buffer
+  static_assert(kStages * kStageBytes == kRingBytes, "stage ring");
+};
 constexpr int kCoreWarps = 6;  // producer, MMA, 4 epilogue
 constexpr int kMaxMoverWarps = 4;
 constexpr int kMaxThreads = (kCoreWarps + kMaxMoverWarps) * 32;
@@ -156,6 +172,8 @@ struct OpBase {
 
 struct Smem {
   uint8_t* stages;
+  int stage_bytes;
+  int a_bytes;
   uint8_t* epi;
   uint64_t* full;
   uint64_t* empty;
@@ -164,8 +182,8 @@ struct Smem {
   uint64_t* drain;
   uint32_t* tmem_slot;
   uint32_t* epi_cnt;  // [2] publish-round counters, one per TMEM accumulator
-  __device__ uint8_t* a(int s) const { return stages + s * kStageBytes; }
-  __device__ uint8_t* b(int s) const { return stages + s * kStageBytes + kAStageBytes; }
+  __device__ uint8_t* a(int s) const { return stages + s * stage_bytes; }
+  __device__ uint8_t* b(int s) const { return stages + s * stage_bytes + a_bytes; }
   __device__ uint8_t* epi_buf(int ew, int i) const { return epi + (ew * 2 + i) * kEpiBufBytes; }
 };
 
@@ -198,6 +216,7 @@ __device__ __forceinline__ void role_producer(const typename Op::Params& p, cons
                                               int gn) {
   const Common& c = p.common;
   const int ntiles = Op::num_tiles(p);
+  constexpr int kStages = Geo<Op::kBM>::kStages;
   uint32_t stage = 0, phase = 0;
   uint32_t filled = 0, fill_parity = 0;  // per-stage: fill issued / parity of that fill
   bool ok = true;
@@ -231,6 +250,8 @@ __device__ __forceinline__ void role_producer(const typename Op::Params& p, cons
 template <class Op>
 __device__ __forceinline__ void role_mma(const typename Op::Params& p, const Smem& sm, int lane,
                                          uint32_t tmem_base, int gi, int gn) {
+  using G = Geo<Op::kBM>;
+  constexpr int kStages = G::kStages;
   const Common& c = p.common;
   const int ntiles = Op::num_tiles(p);
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -240,7 +261,7 @@ __device__ __forceinline__ void role_mma(const typename Op::Params& p, const Sme
     if (lane == 0) {
       ok = mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, c, kSiteTmemEmpty);
       tc_fence_after();
-      const uint32_t d = tmem_base + acc * kBN;
+      const uint32_t d = tmem_base + acc * G::kAccStride;
       for (int kb = 0; kb < j.kblocks && ok; ++kb) {
         ok = mbar_wait(&sm.full[stage], phase, c, kSiteFull);
         if (!ok) break;
@@ -254,8 +275,10 @@ __device__ __forceinline__ void role_mma(const typename Op::Params& p, const Sme
       if (ok) umma_commit(&sm.tfull[acc]);
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    acc ^= 1u;
-    if (acc == 0) acc_phase ^= 1u;
+    if (++acc == G::kAccBufs) {
+      acc = 0;
+      acc_phase ^= 1u;
+    }
   }
   // Drain: all MMAs this thread issued complete before TMEM is freed.
   if (lane == 0) {
@@ -268,6 +291,7 @@ __device__ __forceinline__ void role_mma(const typename Op::Params& p, const Sme
 template <class Op>
 __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, const Smem& sm, int warp,
                                               int lane, uint32_t tmem_base, int gi, int gn) {
+  using G = Geo<Op::kBM>;
   const Common& c = p.common;
   const int ntiles = Op::num_tiles(p);
   const int q = warp & 3;   // TMEM lane quadrant this warp may access
@@ -283,7 +307,7 @@ __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, cons
     ok = mbar_wait(&sm.tfull[acc], acc_phase, c, kSiteTmemFull);
     if (!ok) break;
     tc_fence_after();
-    const uint32_t taddr = tmem_base + acc * kBN + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t taddr = tmem_base + acc * G::kAccStride + (static_cast<uint32_t>(q * 32) << 16);
     Op::epilogue(p, j, taddr, q, lane, es);
     if (Op::publishes(p, j)) {
       // producer_tile_notify: the last of the four warps to see its own stores of this
@@ -305,8 +329,10 @@ __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, cons
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.tempty[acc]);
-    acc ^= 1u;
-    if (acc == 0) acc_phase ^= 1u;
+    if (++acc == G::kAccBufs) {
+      acc = 0;
+      acc_phase ^= 1u;
+    }
   }
   if (lane == 0) bulk_wait<0>();
   __syncwarp();
@@ -316,16 +342,19 @@ template <class Op>
 __global__ void __launch_bounds__(kMaxThreads, 1) persistent_kernel(const __grid_constant__ typename Op::Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using G = Geo<Op::kBM>;
   Smem sm;
   sm.stages = base;
-  sm.epi = base + kStages * kStageBytes;
+  sm.stage_bytes = G::kStageBytes;
+  sm.a_bytes = G::kABytes;
+  sm.epi = base + kRingBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm.epi + kEpiBytes);
   sm.full = bars;
-  sm.empty = bars + kStages;
-  sm.tfull = bars + 2 * kStages;
-  sm.tempty = bars + 2 * kStages + 2;
-  sm.drain = bars + 2 * kStages + 4;
-  sm.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  sm.empty = bars + kMaxStages;
+  sm.tfull = bars + 2 * kMaxStages;
+  sm.tempty = bars + 2 * kMaxStages + 2;
+  sm.drain = bars + 2 * kMaxStages + 4;
+  sm.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
   sm.epi_cnt = sm.tmem_slot + 2;
 
   const int warp = threadIdx.x >> 5;
@@ -337,7 +366,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) persistent_kernel(const __grid
     return;
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < G::kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
@@ -455,6 +484,30 @@ __device__ __forceinline__ void mma_stage_256(uint32_t d, uint32_t a0, uint32_t 
     const uint64_t bd = umma_desc_sw128(b0 + k * 2048, TL_B_LBO, TL_B_SBO);
     umma_bf16(d, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
   }
+}
+
+// The 256-row MMA stage: per K step of 16, rows 0-127 of A into d and rows 128-255 into
+// d + 256, both against the same B slice (4 x 2 x (128x256x16)).
+__device__ __forceinline__ void mma_stage_256x256(uint32_t d, uint32_t a0, uint32_t b0, int kb) {
+  constexpr uint32_t idesc = umma_idesc_bf16(kBM, kBN, true);
+#pragma unroll
+  for (int k = 0; k < kBK / 16; ++k) {
+    const uint64_t ad0 = umma_desc_sw128(a0 + k * 32, 16, 1024);
+    const uint64_t ad1 = umma_desc_sw128(a0 + 128 * 128 + k * 32, 16, 1024);
+    const uint64_t bd = umma_desc_sw128(b0 + k * 2048, TL_B_LBO, TL_B_SBO);
+    const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
+    umma_bf16(d, ad0, bd, idesc, accum);
+    umma_bf16(d + 256, ad1, bd, idesc, accum);
+  }
+}
+
+// MMA stage for a tile of BM rows.
+template <int BM>
+__device__ __forceinline__ void mma_stage_bm(uint32_t d, uint32_t a0, uint32_t b0, int kb) {
+  if constexpr (BM == 256)
+    mma_stage_256x256(d, a0, b0, kb);
+  else
+    mma_stage_256(d, a0, b0, kb);
 }
 
 // Mover copy of `bytes` (multiple of 16) from src to dst by `nthreads` threads.

@@ -25,9 +25,11 @@ __device__ __forceinline__ void mover_chunk(const uint8_t* src, uint8_t* dst, si
   if (tid == 0 && signal) st_release_gpu(flag, c.epoch);
 }
 
-// GEMM+RS epilogue on one 128x256 partial tile of producer `prod` (of W), reduced into
+// GEMM+RS epilogue on one BM x 256 partial tile of producer `prod` (of W), reduced into
 // the fp32 slot tile at (grow, n0); the last producer writes bf16 rows of `out` at orow.
 // Order of the fp32 sums is fixed: slot = P_0; slot += P_1; ...; out = slot + P_{W-1}.
+// Rows 128h..128h+127 of the tile are TMEM columns [256h, 256h+256).
+template <int BM>
 __device__ __forceinline__ void rs_epilogue(const CUtensorMap* acc_map, const float* acc_ptr,
                                             const CUtensorMap* out_map, const uint64_t* flag, int prod, int W,
                                             int grow, int orow, int n0, int n, const Common& c, uint32_t taddr,
@@ -39,76 +41,104 @@ __device__ __forceinline__ void rs_epilogue(const CUtensorMap* acc_map, const fl
     warp_wait_one(flag, (c.epoch << 4) | static_cast<unsigned long long>(prod), c, lane, kSitePeer,
                   static_cast<unsigned long long>(grow) << 20 | static_cast<unsigned>(n0));
   }
-  if (!last) {
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
-      const int x = n0 + ch * 32;
-      if (x >= n) break;
-      float v[32];
-      tmem_ld32(taddr + ch * 32, v);
-      store_f32_chunk(acc_map, es, lane, v, x, grow + q * 32, !first);
-    }
-  } else {
-    const int row = grow + q * 32 + lane;
+  for (int h = 0; h < BM / 128; ++h) {
+    const uint32_t th = taddr + h * 256;
+    const int gr = grow + h * 128 + q * 32;
+    if (!last) {
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 64; ++ch) {
-      const int x = n0 + ch * 64;
-      if (x >= n) break;
-      float v[64];
-      tmem_ld64(taddr, ch * 64, v);
-      if (!first) {
-        const float* src = acc_ptr + static_cast<size_t>(row) * n + x;
-        if (x + 64 <= n) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float4 s = __ldcg(reinterpret_cast<const float4*>(src) + i);
-            v[4 * i] += s.x;
-            v[4 * i + 1] += s.y;
-            v[4 * i + 2] += s.z;
-            v[4 * i + 3] += s.w;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (x + i < n) v[i] += __ldcg(src + i);
-        }
+      for (int ch = 0; ch < kBN / 32; ++ch) {
+        const int x = n0 + ch * 32;
+        if (x >= n) break;
+        float v[32];
+        tmem_ld32(th + ch * 32, v);
+        store_f32_chunk(acc_map, es, lane, v, x, gr, !first);
       }
-      store_bf16_chunk(out_map, es, lane, v, x, orow + q * 32);
+    } else {
+      const int row = gr + lane;
+#pragma unroll 1
+      for (int ch = 0; ch < kBN / 64; ++ch) {
+        const int x = n0 + ch * 64;
+        if (x >= n) break;
+        float v[64];
+        tmem_ld64(th, ch * 64, v);
+        if (!first) {
+          const float* src = acc_ptr + static_cast<size_t>(row) * n + x;
+          if (x + 64 <= n) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float4 s = __ldcg(reinterpret_cast<const float4*>(src) + i);
+              v[4 * i] += s.x;
+              v[4 * i + 1] += s.y;
+              v[4 * i + 2] += s.z;
+              v[4 * i + 3] += s.w;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              if (x + i < n) v[i] += __ldcg(src + i);
+          }
+        }
+        store_bf16_chunk(out_map, es, lane, v, x, orow + h * 128 + q * 32);
+      }
     }
   }
 }
 
 // ============================================================================ AllGather + GEMM
 struct AgParams {
-  CUtensorMap a_local;  // shard `rank` read in place: {k, m_per_rank}, box {64, 128}
-  CUtensorMap a_gath;   // gathered buffer T: {k, W*m_per_rank}, box {64, 128}
+  CUtensorMap a_local;  // shard `rank` read in place: {k, m_per_rank}, box {64, BM}
+  CUtensorMap a_gath;   // gathered buffer T: {k, W*m_per_rank}, box {64, BM}
   CUtensorMap b;        // {n, k}, box {64, 64}
   CUtensorMap c;        // {n, W*m_per_rank}, box {64, 32}
   Common common;
   const uint8_t* shard[8];
   uint8_t* gath;
-  uint64_t* flags;  // [W][mps][chunks]
+  uint64_t* flags;  // [W][spr][chunks]
   long long shard_bytes, slab_bytes;
-  int W, rank, m_per_rank, mps, n, nbk, kblocks, swizzle, chunks, skip_chunk;
+  int W, rank, m_per_rank, mps, spr, n, nbk, kblocks, swizzle, chunks, skip_chunk;
 };
 
+// The shard mover: pull every shard (the self rank's last) into the gathered buffer in
+// 128-row slabs of `chunks` chunks, one release signal per chunk.
+__device__ __forceinline__ void ag_mover(const AgParams& p, int mw, int lane) {
+  const int nthreads = p.common.mover_warps * 32;
+  const int tid = mw * 32 + lane;
+  const int per_shard = p.spr * p.chunks;
+  const int total = p.W * per_shard;
+  const size_t chunk_bytes = static_cast<size_t>(p.slab_bytes / p.chunks);
+  for (int g = blockIdx.x; g < total; g += gridDim.x) {
+    const int i = g / per_shard;
+    const int rem = g - i * per_shard;
+    const int slab = rem / p.chunks;
+    const int ch = rem - slab * p.chunks;
+    const int r = ag_mover_rank(p.W, p.rank, p.swizzle, i);
+    const size_t off = static_cast<size_t>(slab) * p.slab_bytes + static_cast<size_t>(ch) * chunk_bytes;
+    mover_chunk(p.shard[r] + off, p.gath + static_cast<size_t>(r) * p.shard_bytes + off, chunk_bytes,
+                p.flags + (static_cast<size_t>(r) * p.spr + slab) * p.chunks + ch, g != p.skip_chunk, p.common, tid,
+                nthreads);
+  }
+}
+
+template <int BM>
 struct AgOp : OpBase<AgParams> {
   using Params = AgParams;
-  static constexpr uint32_t kTxBytes = kStageBytes;
+  static constexpr int kBM = BM;
+  static constexpr uint32_t kTxBytes = Geo<BM>::kStageBytes;
   static __device__ int num_tiles(const Params& p) { return ag_num_tiles(p.W, p.mps, p.nbk); }
   static __device__ Job job(const Params& p, int t) {
     const AgTile a = ag_tile(t, p.W, p.rank, p.mps, p.nbk, p.swizzle);
     Job j;
     j.kind = 0;
     j.a_sel = a.src == p.rank ? 0 : 1;
-    j.a_row = (a.src == p.rank ? 0 : a.src * p.m_per_rank) + a.mb * kBM;
+    j.a_row = (a.src == p.rank ? 0 : a.src * p.m_per_rank) + a.mb * BM;
     j.b_sel = 0;
     j.b_col = a.nb * kBN;
     j.b_z = 0;
     j.kblocks = p.kblocks;
     j.x0 = a.src;
     j.x1 = a.mb;
-    j.x2 = a.src * p.m_per_rank + a.mb * kBM;  // row of C
+    j.x2 = a.src * p.m_per_rank + a.mb * BM;  // row of C
     j.x3 = 0;
     return j;
   }
@@ -118,12 +148,12 @@ struct AgOp : OpBase<AgParams> {
     tma_prefetch_map(&p.b);
     tma_prefetch_map(&p.c);
   }
-  // consumer_tile_wait: a remote row block is read only after every chunk of its slab
-  // has been released by the mover.
+  // consumer_tile_wait: a remote row block is read only after every chunk of its
+  // BM/128 slabs has been released by the mover.
   static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
     if (kb != 0 || j.a_sel == 0) return;
-    const uint64_t* f = p.flags + (static_cast<size_t>(j.x0) * p.mps + j.x1) * p.chunks;
-    wait_slab(f, p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x0) << 32) | j.x1);
+    const uint64_t* f = p.flags + (static_cast<size_t>(j.x0) * p.spr + j.x1 * (BM / 128)) * p.chunks;
+    wait_slab(f, (BM / 128) * p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x0) << 32) | j.x1);
   }
   static __device__ void load(const Params& p, const Job& j, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
     tma_load_2d(sa, j.a_sel ? &p.a_gath : &p.a_local, bar, kb * kBK, j.a_row);
@@ -131,60 +161,48 @@ struct AgOp : OpBase<AgParams> {
     for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.b, bar, j.b_col + g * 64, kb * kBK);
   }
   static __device__ void mma_stage(const Job&, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
-    mma_stage_256(d, a0, b0, kb);
+    mma_stage_bm<BM>(d, a0, b0, kb);
   }
   static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 64; ++ch) {
-      const int x = j.b_col + ch * 64;
-      if (x >= p.n) break;
-      float v[64];
-      tmem_ld64(taddr, ch * 64, v);
-      store_bf16_chunk(&p.c, es, lane, v, x, j.x2 + q * 32);
+    for (int h = 0; h < BM / 128; ++h) {
+#pragma unroll 1
+      for (int ch = 0; ch < kBN / 64; ++ch) {
+        const int x = j.b_col + ch * 64;
+        if (x >= p.n) break;
+        float v[64];
+        tmem_ld64(taddr + h * 256, ch * 64, v);
+        store_bf16_chunk(&p.c, es, lane, v, x, j.x2 + h * 128 + q * 32);
+      }
     }
   }
-  static __device__ void mover(const Params& p, int mw, int lane) {
-    const int nthreads = p.common.mover_warps * 32;
-    const int tid = mw * 32 + lane;
-    const int per_shard = p.mps * p.chunks;
-    const int total = p.W * per_shard;
-    const size_t chunk_bytes = static_cast<size_t>(p.slab_bytes / p.chunks);
-    for (int g = blockIdx.x; g < total; g += gridDim.x) {
-      const int i = g / per_shard;
-      const int rem = g - i * per_shard;
-      const int slab = rem / p.chunks;
-      const int ch = rem - slab * p.chunks;
-      const int r = ag_mover_rank(p.W, p.rank, p.swizzle, i);
-      const size_t off = static_cast<size_t>(slab) * p.slab_bytes + static_cast<size_t>(ch) * chunk_bytes;
-      mover_chunk(p.shard[r] + off, p.gath + static_cast<size_t>(r) * p.shard_bytes + off, chunk_bytes,
-                  p.flags + (static_cast<size_t>(r) * p.mps + slab) * p.chunks + ch, g != p.skip_chunk, p.common,
-                  tid, nthreads);
-    }
-  }
+  static __device__ void mover(const Params& p, int mw, int lane) { ag_mover(p, mw, lane); }
 };
 
 // ============================================================================ GEMM + ReduceScatter
 struct RsParams {
-  CUtensorMap a[8];    // A_p: {k_r, m}, box {64, 128}
+  CUtensorMap a[8];    // A_p: {k_r, m}, box {64, BM}
   CUtensorMap b[8];    // B_p: {n, k_r}, box {64, 64}
   CUtensorMap out[8];  // out_o: {n, m/W}, box {64, 32}
   CUtensorMap acc;     // fp32 slot: {n, m}, box {32, 32}
   Common common;
   const float* acc_ptr;
-  uint64_t* flags;  // [m/128][nbk]
+  uint64_t* flags;  // [m/128][nbk] (a tile uses the signal of its first 128-row block)
   int W, m, mo, mbo, n, nbk, kblocks, swizzle;
 };
 
+template <int BM>
 struct RsOp : OpBase<RsParams> {
   using Params = RsParams;
-  static constexpr uint32_t kTxBytes = kStageBytes;
+  static constexpr int kBM = BM;
+  static constexpr uint32_t kTxBytes = Geo<BM>::kStageBytes;
   static __device__ int num_tiles(const Params& p) { return rs_num_tiles(p.W, p.mbo, p.nbk); }
   static __device__ Job job(const Params& p, int t) {
     const RsTile r = rs_tile(t, p.W, p.mbo, p.nbk, p.swizzle);
     Job j;
     j.kind = 0;
     j.a_sel = r.p;
-    j.a_row = r.o * p.mo + r.mb * kBM;
+    j.a_row = r.o * p.mo + r.mb * BM;
     j.b_sel = r.p;
     j.b_col = r.nb * kBN;
     j.b_z = 0;
@@ -203,12 +221,12 @@ struct RsOp : OpBase<RsParams> {
     for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.b[j.b_sel], bar, j.b_col + g * 64, kb * kBK);
   }
   static __device__ void mma_stage(const Job&, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
-    mma_stage_256(d, a0, b0, kb);
+    mma_stage_bm<BM>(d, a0, b0, kb);
   }
-  static __device__ int tile_id(const Params& p, const Job& j) { return (j.a_row / kBM) * p.nbk + j.x3; }
+  static __device__ int tile_id(const Params& p, const Job& j) { return (j.a_row / 128) * p.nbk + j.x3; }
   static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
-    rs_epilogue(&p.acc, p.acc_ptr, &p.out[j.x1], p.flags + tile_id(p, j), j.x0, p.W, j.a_row, j.x2 * kBM, j.b_col,
-                p.n, p.common, taddr, q, lane, es);
+    rs_epilogue<BM>(&p.acc, p.acc_ptr, &p.out[j.x1], p.flags + tile_id(p, j), j.x0, p.W, j.a_row, j.x2 * BM,
+                    j.b_col, p.n, p.common, taddr, q, lane, es);
   }
   // peer_tile_notify: producer p's contribution to this slot tile is complete.
   static __device__ bool publishes(const Params& p, const Job& j) { return j.x0 != p.W - 1; }
@@ -219,31 +237,34 @@ struct RsOp : OpBase<RsParams> {
 
 // ============================================================================ 2-layer MLP chain
 struct Mlp2Params {
-  CUtensorMap x_local[8];  // X_r in place: {h, Tr}, box {64, 128}
+  CUtensorMap x_local[8];  // X_r in place: {h, Tr}, box {64, BM}
   CUtensorMap w1[8];       // {f, h}, box {64, 64}
   CUtensorMap w2[8];       // {h, f}, box {64, 64}
   CUtensorMap out[8];      // {h, Tr}, box {64, 32}
-  CUtensorMap x_gath;      // per-rank gathered X: {h, W*T}, box {64, 128}
+  CUtensorMap x_gath;      // per-rank gathered X: {h, W*T}, box {64, BM}
   CUtensorMap h_st;        // H: {f, W*T}, box {64, 32}
-  CUtensorMap h_ld;        // H: {f, W*T}, box {64, 128}
+  CUtensorMap h_ld;        // H: {f, W*T}, box {64, BM}
   CUtensorMap acc;         // fp32 slot {h, T}, box {32, 32}
   Common common;
   const uint8_t* x[8];
   uint8_t* xg;
   const float* acc_ptr;
-  uint64_t* ag_flags;  // [W gathering rank][W src][mps][chunks]
+  uint64_t* ag_flags;  // [W gathering rank][W src][spr][chunks]
   uint64_t* h_flags;   // [W][T/128][nb1]
   uint64_t* rs_flags;  // [T/128][nb2]
   long long shard_bytes, slab_bytes;
-  int W, T, Tr, h, f, mps, nb1, kb1, nb2, kb2, swizzle, chunks, skip_chunk;
+  int W, T, Tr, h, f, mps, spr, nb1, kb1, nb2, kb2, swizzle, chunks, skip_chunk;
 };
 
+template <int BM>
 struct Mlp2Op : OpBase<Mlp2Params> {
   using Params = Mlp2Params;
-  static constexpr uint32_t kTxBytes = kStageBytes;
+  static constexpr int kBM = BM;
+  static constexpr int kSub = BM / 128;  // 128-row blocks per tile
+  static constexpr uint32_t kTxBytes = Geo<BM>::kStageBytes;
   static __device__ int per_rank(const Params& p) { return p.W * p.mps * (p.nb1 + p.nb2); }
   static __device__ int num_tiles(const Params& p) { return p.W * per_rank(p); }
-  // kind 1: layer-1 tile of rank x0 on shard x1, row block x2, column block (b_col)
+  // kind 1: layer-1 tile of rank x0 on shard x1, row block x2, column block x3
   // kind 2: layer-2 tile of producer x0 for owner x1, row block x2, column block x3
   static __device__ Job job(const Params& p, int t) {
     const int pr = per_rank(p);
@@ -256,7 +277,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
       const AgTile a = ag_tile(u, p.W, r, p.mps, p.nb1, p.swizzle);
       j.kind = 1;
       j.a_sel = a.src == r ? 0 : 1;
-      j.a_row = a.src == r ? a.mb * kBM : r * p.T + a.src * p.Tr + a.mb * kBM;
+      j.a_row = a.src == r ? a.mb * BM : r * p.T + a.src * p.Tr + a.mb * BM;
       j.b_sel = r;
       j.b_col = a.nb * kBN;
       j.kblocks = p.kb1;
@@ -276,7 +297,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
       j.x2 = w / p.nb2;
       j.x3 = w - j.x2 * p.nb2;
       j.a_sel = 0;
-      j.a_row = r * p.T + j.x1 * p.Tr + j.x2 * kBM;
+      j.a_row = r * p.T + j.x1 * p.Tr + j.x2 * BM;
       j.b_sel = r;
       j.b_col = j.x3 * kBN;
       j.kblocks = p.kb2;
@@ -289,18 +310,20 @@ struct Mlp2Op : OpBase<Mlp2Params> {
     tma_prefetch_map(&p.h_ld);
     tma_prefetch_map(&p.acc);
   }
+  // first 128-row block (of T) covered by the tile
+  static __device__ int row_block(const Params& p, const Job& j) { return (j.x1 * p.Tr) / 128 + j.x2 * kSub; }
   static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
     if (kb != 0) return;
     if (j.kind == 1) {
       if (j.a_sel == 0) return;
       const uint64_t* f =
-          p.ag_flags + ((static_cast<size_t>(j.x0) * p.W + j.x1) * p.mps + j.x2) * p.chunks;
-      wait_slab(f, p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x1) << 32) | j.x2);
+          p.ag_flags + ((static_cast<size_t>(j.x0) * p.W + j.x1) * p.spr + j.x2 * kSub) * p.chunks;
+      wait_slab(f, kSub * p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x1) << 32) | j.x2);
     } else {
       // CTA-level chain: the layer-1 tiles that produce this row block of H_r are done.
-      const int rb = (j.x1 * p.Tr) / kBM + j.x2;
-      const uint64_t* f = p.h_flags + (static_cast<size_t>(j.x0) * (p.T / kBM) + rb) * p.nb1;
-      warp_wait_signals(f, p.nb1, p.common.epoch, p.common, lane, kSiteSignal,
+      const int rb = row_block(p, j);
+      const uint64_t* f = p.h_flags + (static_cast<size_t>(j.x0) * (p.T / 128) + rb) * p.nb1;
+      warp_wait_signals(f, kSub * p.nb1, p.common.epoch, p.common, lane, kSiteSignal,
                         (2ull << 60) | (static_cast<unsigned long long>(j.x0) << 32) | rb);
     }
   }
@@ -316,35 +339,38 @@ struct Mlp2Op : OpBase<Mlp2Params> {
     }
   }
   static __device__ void mma_stage(const Job&, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
-    mma_stage_256(d, a0, b0, kb);
+    mma_stage_bm<BM>(d, a0, b0, kb);
   }
-  static __device__ int h_row(const Params& p, const Job& j) { return j.x0 * p.T + j.x1 * p.Tr + j.x2 * kBM; }
-  static __device__ int rs_tile_id(const Params& p, const Job& j) {
-    return ((j.x1 * p.Tr) / kBM + j.x2) * p.nb2 + j.x3;
-  }
+  static __device__ int h_row(const Params& p, const Job& j) { return j.x0 * p.T + j.x1 * p.Tr + j.x2 * BM; }
+  static __device__ int rs_tile_id(const Params& p, const Job& j) { return row_block(p, j) * p.nb2 + j.x3; }
   static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
     if (j.kind == 1) {
-      const int row = h_row(p, j) + q * 32;
 #pragma unroll 1
-      for (int ch = 0; ch < kBN / 64; ++ch) {
-        const int x = j.b_col + ch * 64;
-        if (x >= p.f) break;
-        float v[64];
-        tmem_ld64(taddr, ch * 64, v);
+      for (int hh = 0; hh < kSub; ++hh) {
+        const int row = h_row(p, j) + hh * 128 + q * 32;
+#pragma unroll 1
+        for (int ch = 0; ch < kBN / 64; ++ch) {
+          const int x = j.b_col + ch * 64;
+          if (x >= p.f) break;
+          float v[64];
+          tmem_ld64(taddr + hh * 256, ch * 64, v);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.70710678118654752f));
-        store_bf16_chunk(&p.h_st, es, lane, v, x, row);
+          for (int i = 0; i < 64; ++i) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.70710678118654752f));
+          store_bf16_chunk(&p.h_st, es, lane, v, x, row);
+        }
       }
     } else {
-      rs_epilogue(&p.acc, p.acc_ptr, &p.out[j.x1], p.rs_flags + rs_tile_id(p, j), j.x0, p.W,
-                  j.x1 * p.Tr + j.x2 * kBM, j.x2 * kBM, j.b_col, p.h, p.common, taddr, q, lane, es);
+      rs_epilogue<BM>(&p.acc, p.acc_ptr, &p.out[j.x1], p.rs_flags + rs_tile_id(p, j), j.x0, p.W,
+                      j.x1 * p.Tr + j.x2 * BM, j.x2 * BM, j.b_col, p.h, p.common, taddr, q, lane, es);
     }
   }
   static __device__ bool publishes(const Params& p, const Job& j) { return j.kind == 1 || j.x0 != p.W - 1; }
   static __device__ void publish(const Params& p, const Job& j) {
     if (j.kind == 1) {
-      const int rb = (j.x1 * p.Tr) / kBM + j.x2;
-      st_release_gpu(p.h_flags + (static_cast<size_t>(j.x0) * (p.T / kBM) + rb) * p.nb1 + j.x3, p.common.epoch);
+      const int rb = row_block(p, j);
+#pragma unroll
+      for (int s = 0; s < kSub; ++s)
+        st_release_gpu(p.h_flags + (static_cast<size_t>(j.x0) * (p.T / 128) + rb + s) * p.nb1 + j.x3, p.common.epoch);
     } else {
       st_release_gpu(p.rs_flags + rs_tile_id(p, j), (p.common.epoch << 4) | static_cast<unsigned long long>(j.x0 + 1));
     }
@@ -354,7 +380,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
   static __device__ void mover(const Params& p, int mw, int lane) {
     const int nthreads = p.common.mover_warps * 32;
     const int tid = mw * 32 + lane;
-    const int per_shard = p.mps * p.chunks;
+    const int per_shard = p.spr * p.chunks;
     const int per_rank = p.W * per_shard;
     const int total = p.W * per_rank;
     const size_t chunk_bytes = static_cast<size_t>(p.slab_bytes / p.chunks);
@@ -369,7 +395,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
       const size_t off = static_cast<size_t>(slab) * p.slab_bytes + static_cast<size_t>(ch) * chunk_bytes;
       uint8_t* dst = p.xg + (static_cast<size_t>(r) * p.T + static_cast<size_t>(src) * p.Tr) * p.h * 2 + off;
       mover_chunk(p.x[src] + off, dst, chunk_bytes,
-                  p.ag_flags + ((static_cast<size_t>(r) * p.W + src) * p.mps + slab) * p.chunks + ch,
+                  p.ag_flags + ((static_cast<size_t>(r) * p.W + src) * p.spr + slab) * p.chunks + ch,
                   g != p.skip_chunk, p.common, tid, nthreads);
     }
   }
@@ -381,7 +407,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
 // geometry, order and signals as the fused AllGather+GEMM, run by mover_warps warps in
 // each of the persistent CTAs.
 __global__ void __launch_bounds__(kMaxMoverWarps * 32) allgather_kernel(const __grid_constant__ AgParams p) {
-  AgOp::mover(p, threadIdx.x >> 5, threadIdx.x & 31);
+  ag_mover(p, threadIdx.x >> 5, threadIdx.x & 31);
 }
 
 }  // namespace tl
@@ -394,6 +420,9 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static bool ag_shape_ok(int W, int mpr, int n, int k) {
   return W >= 1 && W <= 8 && mpr >= 0 && n >= 0 && k >= 0 && mpr % kBM == 0 && n % 8 == 0 && k % 8 == 0;
 }
+
+// Tile rows used for a row extent: 256 when every block of the extent is a 256 multiple.
+static int pick_bm(int rows) { return rows % 256 == 0 ? 256 : 128; }
 
 extern "C" size_t tl_ag_gemm_workspace_bytes(int W, int m_per_rank, int n, int k) {
   if (!ag_shape_ok(W, m_per_rank, n, k)) return 0;
@@ -422,8 +451,9 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   p.gath = ws;
   p.flags = reinterpret_cast<uint64_t*>(ws + align256(gath_bytes));
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!tmap_2d(&p.a_local, BF, 2, a_shards[rank], k, m_per_rank, 64, 128) ||
-      !tmap_2d(&p.a_gath, BF, 2, p.gath, k, M, 64, 128) || !tmap_2d(&p.b, BF, 2, b, n, k, 64, 64) ||
+  const int bm = pick_bm(m_per_rank);
+  if (!tmap_2d(&p.a_local, BF, 2, a_shards[rank], k, m_per_rank, 64, bm) ||
+      !tmap_2d(&p.a_gath, BF, 2, p.gath, k, M, 64, bm) || !tmap_2d(&p.b, BF, 2, b, n, k, 64, 64) ||
       !tmap_2d(&p.c, BF, 2, c, n, M, 64, 32))
     return TL_ERR_CUDA;
   p.common = make_common(ctx);
@@ -431,7 +461,8 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   p.W = W;
   p.rank = rank;
   p.m_per_rank = m_per_rank;
-  p.mps = m_per_rank / kBM;
+  p.mps = m_per_rank / bm;
+  p.spr = m_per_rank / kBM;
   p.n = n;
   p.nbk = ceil_div(n, kBN);
   p.kblocks = ceil_div(k, kBK);
@@ -440,7 +471,9 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   p.skip_chunk = ctx->cfg.debug_skip_chunk;
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
-  return launch_persistent<AgOp>(ctx, p, reinterpret_cast<cudaStream_t>(stream), ctx->cfg.mover_warps);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return bm == 256 ? launch_persistent<AgOp<256>>(ctx, p, st, ctx->cfg.mover_warps)
+                   : launch_persistent<AgOp<128>>(ctx, p, st, ctx->cfg.mover_warps);
 }
 
 static bool rs_shape_ok(int W, int m, int n, int kr) {
@@ -474,8 +507,9 @@ extern "C" int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* 
   p.flags = reinterpret_cast<uint64_t*>(ws + align256(static_cast<size_t>(m) * n * 4));
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int mo = m / W;
+  const int bm = pick_bm(mo);
   for (int r = 0; r < W; ++r) {
-    if (!tmap_2d(&p.a[r], BF, 2, a[r], k_r, m, 64, 128) || !tmap_2d(&p.b[r], BF, 2, b[r], n, k_r, 64, 64) ||
+    if (!tmap_2d(&p.a[r], BF, 2, a[r], k_r, m, 64, bm) || !tmap_2d(&p.b[r], BF, 2, b[r], n, k_r, 64, 64) ||
         !tmap_2d(&p.out[r], BF, 2, out[r], n, mo, 64, 32))
       return TL_ERR_CUDA;
   }
@@ -484,12 +518,13 @@ extern "C" int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* 
   p.W = W;
   p.m = m;
   p.mo = mo;
-  p.mbo = mo / kBM;
+  p.mbo = mo / bm;
   p.n = n;
   p.nbk = ceil_div(n, kBN);
   p.kblocks = ceil_div(k_r, kBK);
   p.swizzle = ctx->cfg.swizzle;
-  return launch_persistent<RsOp>(ctx, p, reinterpret_cast<cudaStream_t>(stream), 0);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return bm == 256 ? launch_persistent<RsOp<256>>(ctx, p, st, 0) : launch_persistent<RsOp<128>>(ctx, p, st, 0);
 }
 
 static bool mlp2_shape_ok(int W, int T, int h, int f) {
@@ -549,17 +584,18 @@ extern "C" int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const vo
   p.h_flags = reinterpret_cast<uint64_t*>(ws + L.hf);
   p.rs_flags = reinterpret_cast<uint64_t*>(ws + L.rsf);
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int bm = pick_bm(Tr);
   for (int r = 0; r < W; ++r) {
-    if (!tmap_2d(&p.x_local[r], BF, 2, x_shards[r], hidden, Tr, 64, 128) ||
+    if (!tmap_2d(&p.x_local[r], BF, 2, x_shards[r], hidden, Tr, 64, bm) ||
         !tmap_2d(&p.w1[r], BF, 2, w1[r], f_r, hidden, 64, 64) ||
         !tmap_2d(&p.w2[r], BF, 2, w2[r], hidden, f_r, 64, 64) ||
         !tmap_2d(&p.out[r], BF, 2, out[r], hidden, Tr, 64, 32))
       return TL_ERR_CUDA;
     p.x[r] = static_cast<const uint8_t*>(x_shards[r]);
   }
-  if (!tmap_2d(&p.x_gath, BF, 2, p.xg, hidden, static_cast<uint64_t>(W) * tokens, 64, 128) ||
+  if (!tmap_2d(&p.x_gath, BF, 2, p.xg, hidden, static_cast<uint64_t>(W) * tokens, 64, bm) ||
       !tmap_2d(&p.h_st, BF, 2, hb, f_r, static_cast<uint64_t>(W) * tokens, 64, 32) ||
-      !tmap_2d(&p.h_ld, BF, 2, hb, f_r, static_cast<uint64_t>(W) * tokens, 64, 128) ||
+      !tmap_2d(&p.h_ld, BF, 2, hb, f_r, static_cast<uint64_t>(W) * tokens, 64, bm) ||
       !tmap_2d(&p.acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, hidden, tokens, 32, 32))
     return TL_ERR_CUDA;
   p.common = make_common(ctx);
@@ -568,7 +604,8 @@ extern "C" int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const vo
   p.Tr = Tr;
   p.h = hidden;
   p.f = f_r;
-  p.mps = Tr / kBM;
+  p.mps = Tr / bm;
+  p.spr = Tr / kBM;
   p.nb1 = ceil_div(f_r, kBN);
   p.kb1 = ceil_div(hidden, kBK);
   p.nb2 = ceil_div(hidden, kBN);
@@ -578,7 +615,9 @@ extern "C" int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const vo
   p.skip_chunk = ctx->cfg.debug_skip_chunk;
   p.shard_bytes = static_cast<long long>(Tr) * hidden * 2;
   p.slab_bytes = static_cast<long long>(kBM) * hidden * 2;
-  return launch_persistent<Mlp2Op>(ctx, p, reinterpret_cast<cudaStream_t>(stream), ctx->cfg.mover_warps);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return bm == 256 ? launch_persistent<Mlp2Op<256>>(ctx, p, st, ctx->cfg.mover_warps)
+                   : launch_persistent<Mlp2Op<128>>(ctx, p, st, ctx->cfg.mover_warps);
 }
 
 extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_shards, void* workspace,
@@ -601,6 +640,7 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   p.rank = rank;
   p.m_per_rank = m_per_rank;
   p.mps = m_per_rank / kBM;
+  p.spr = m_per_rank / kBM;
   p.swizzle = ctx->cfg.swizzle;
   p.chunks = ctx->cfg.chunks_per_slab;
   p.skip_chunk = -1;

@@ -230,7 +230,8 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 
 struct MoeOp : OpBase<MoeParams> {
   using Params = MoeParams;
-  static constexpr uint32_t kTxBytes = kStageBytes;
+  static constexpr int kBM = 128;
+  static constexpr uint32_t kTxBytes = Geo<128>::kStageBytes;
   static __device__ int mtiles(const Params& p) { return *reinterpret_cast<const volatile int*>(p.num_mtiles); }
   static __device__ int num_tiles(const Params& p) { return mtiles(p) * (p.n_up + p.n_down); }
   static __device__ bool gemm_partition(const Params& p, int& gi, int& gn) {

@@ -232,6 +232,9 @@ int tl_ag_gemm_static_scratch(tl_ctx* ctx, int W, int rank, const void* const* a
  * The static tile-centric mappings the kernels use ([TL] §4.1), evaluated on the host by the
  * same code the device runs, for inspection and testing.
  *
+ * Tiles are 256 x 256 when every shard (AG) or owner block (RS) is a multiple of 256 rows,
+ * else 128 x 256; row blocks are reported in units of 128 rows (the first 128-row block a
+ * tile covers), column blocks in units of 256 columns.
  * tl_ag_tile_order: for the AllGather + GEMM tile sequence t = 0..count-1 writes the source
  *   rank, the row block inside that rank's shard and the column block.  Returns the number of
  *   tiles, or TL_ERR_INVALID.  Arrays may be NULL to query the count; otherwise they must hold

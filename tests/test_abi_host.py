@@ -90,11 +90,12 @@ def test_argument_validation_needs_no_gpu(tl):
 @pytest.mark.parametrize("W,rank,mpr,n", [(8, 0, 1024, 3584), (8, 5, 1024, 3584), (2, 1, 128, 256), (3, 2, 256, 520)])
 def test_ag_tile_order_is_rank_swizzled_and_matches_static_map(tl, W, rank, mpr, n):
     src, mb, nb = tl.tl_ag_tile_order(W, rank, mpr, n, 1)
-    mps, nbk = mpr // 128, -(-n // 256)
+    bm = 256 if mpr % 256 == 0 else 128  # tile rows the kernel uses; m_block is in 128-row units
+    mps, nbk = mpr // bm, -(-n // 256)
     assert len(src) == W * mps * nbk
     # every tile exactly once
     keys = set(zip(src.tolist(), mb.tolist(), nb.tolist()))
-    assert len(keys) == len(src) == len({(s, m, b) for s in range(W) for m in range(mps) for b in range(nbk)})
+    assert keys == {(s, m * (bm // 128), b) for s in range(W) for m in range(mps) for b in range(nbk)}
     # step s computes with the shard of rank (rank + s) mod W: the local shard first
     per = mps * nbk
     for s in range(W):
@@ -111,7 +112,8 @@ def test_ag_tile_order_is_rank_swizzled_and_matches_static_map(tl, W, rank, mpr,
 @pytest.mark.parametrize("W,m,n", [(8, 8192, 8192), (4, 1024, 520), (1, 128, 256)])
 def test_rs_tile_order_producer_major_owner_swizzled(tl, W, m, n):
     p, o, mb, nb = tl.tl_rs_tile_order(W, m, n, 1)
-    mbo, nbk = m // W // 128, -(-n // 256)
+    bm = 256 if (m // W) % 256 == 0 else 128
+    mbo, nbk = m // W // bm, -(-n // 256)
     assert len(p) == W * W * mbo * nbk
     assert len(set(zip(p.tolist(), o.tolist(), mb.tolist(), nb.tolist()))) == len(p)
     assert np.all(np.diff(p) >= 0)  # producers visited 0..W-1 (fixed fp32 summation order)
