@@ -10,7 +10,8 @@
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and issues
 //               tcgen05.mma from one lane; tcgen05.commit frees smem stages and hands
 //               finished accumulators to the epilogue.
-//   warps 2-5   epilogue: tcgen05.ld -> registers -> per-op math -> swizzled smem
+//   warps 2..   epilogue (4 warps, or 8 = one warpgroup per 128-row half of a 256-row
+//               tile): tcgen05.ld -> registers -> per-op math -> swizzled smem
 //               staging -> TMA store / TMA bulk reduction; then the producer side of the
 //               signal primitives (producer_tile_notify) for tiles others wait on.
 //   warps 6..   shard mover (tile_pull_data of §3.2.2, pull mode): copies shard chunks
@@ -56,9 +57,7 @@ struct Geo {
   static constexpr int kAccStride = BM == 256 ? 512 : 256;  // TMEM columns per accumulator buffer
   static_assert(kStages * kStageBytes == kRingBytes, "stage ring");
 };
-constexpr int kCoreWarps = 6;  // producer, MMA, 4 epilogue
 constexpr int kMaxMoverWarps = 4;
-constexpr int kMaxThreads = (kCoreWarps + kMaxMoverWarps) * 32;
 
 // Status codes written to the device status word (host maps them to TL_ERR_*).
 constexpr unsigned kStatusTimeout = 4;
@@ -168,7 +167,15 @@ struct OpBase {
   static __device__ bool publishes(const P&, const Job&) { return false; }
   static __device__ void publish(const P&, const Job&) {}
   static __device__ void mover(const P&, int, int) {}
+  static constexpr int kEpiWarps = 4;   // epilogue warps (4, or 8 = one warpgroup per 128-row half)
+  static constexpr int kMaxMovers = 4;  // mover warps the launch bounds allow
 };
+
+// Threads per CTA the launch bounds of an op's kernel allow.
+template <class Op>
+constexpr int op_max_threads() {
+  return (2 + Op::kEpiWarps + Op::kMaxMovers) * 32;
+}
 
 struct Smem {
   uint8_t* stages;
@@ -184,7 +191,6 @@ struct Smem {
   uint32_t* epi_cnt;  // [2] publish-round counters, one per TMEM accumulator
   __device__ uint8_t* a(int s) const { return stages + s * stage_bytes; }
   __device__ uint8_t* b(int s) const { return stages + s * stage_bytes + a_bytes; }
-  __device__ uint8_t* epi_buf(int ew, int i) const { return epi + (ew * 2 + i) * kEpiBufBytes; }
 };
 
 // Write one 32-row x 128-byte chunk (lane = row) into a staging buffer laid out in the
@@ -198,17 +204,25 @@ __device__ __forceinline__ void stage_row128(uint8_t* buf, int lane, const uint3
   }
 }
 
-// Epilogue staging state of one warp: double-buffered smem chunk + TMA bulk groups.
+// Epilogue staging state of one warp: one or two 4 KB smem chunks + TMA bulk groups.
 struct EpiStage {
   uint8_t* buf[2];
   int idx;
-  // Get a free buffer: at most one bulk group of this warp may still be reading smem.
+  int nbuf;
+  // Get a free buffer: the bulk group that last read it has finished reading smem.
   __device__ __forceinline__ uint8_t* acquire(int lane) {
-    if (lane == 0) bulk_wait_read<1>();
+    if (lane == 0) {
+      if (nbuf == 2)
+        bulk_wait_read<1>();
+      else
+        bulk_wait_read<0>();
+    }
     __syncwarp();
     return buf[idx];
   }
-  __device__ __forceinline__ void flip() { idx ^= 1; }
+  __device__ __forceinline__ void flip() {
+    if (nbuf == 2) idx ^= 1;
+  }
 };
 
 template <class Op>
@@ -294,12 +308,17 @@ __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, cons
   using G = Geo<Op::kBM>;
   const Common& c = p.common;
   const int ntiles = Op::num_tiles(p);
+  constexpr int E = Op::kEpiWarps;
   const int q = warp & 3;   // TMEM lane quadrant this warp may access
-  const int ew = warp - 2;  // epilogue warp index 0..3
+  const int ew = warp - 2;  // epilogue warp index 0..E-1
   EpiStage es;
-  es.buf[0] = sm.epi_buf(ew, 0);
-  es.buf[1] = sm.epi_buf(ew, 1);
+  es.nbuf = 8 / E;
+  es.buf[0] = sm.epi + (ew * es.nbuf) * kEpiBufBytes;
+  es.buf[1] = sm.epi + (ew * es.nbuf + es.nbuf - 1) * kEpiBufBytes;
   es.idx = 0;
+  // With 8 warps, warps ew and ew+4 share a lane quadrant and take one 128-row half each.
+  const int h0 = E == 8 ? ew / 4 : 0;
+  const int h1 = E == 8 ? h0 + 1 : Op::kBM / 128;
   uint32_t acc = 0, acc_phase = 0;
   bool ok = true;
   for (int t = gi; t < ntiles && ok; t += gn) {
@@ -308,7 +327,7 @@ __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, cons
     if (!ok) break;
     tc_fence_after();
     const uint32_t taddr = tmem_base + acc * G::kAccStride + (static_cast<uint32_t>(q * 32) << 16);
-    Op::epilogue(p, j, taddr, q, lane, es);
+    Op::epilogue(p, j, taddr, q, lane, es, h0, h1);
     if (Op::publishes(p, j)) {
       // producer_tile_notify: the last of the four warps to see its own stores of this
       // tile complete publishes the tile's signal (release).  Each warp arrives here
@@ -319,7 +338,7 @@ __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, cons
         fence_proxy_async_global();
         __threadfence();
         const uint32_t old = atomicAdd(&sm.epi_cnt[acc], 1u);
-        if ((old & 3u) == 3u) {
+        if ((old & (E - 1u)) == E - 1u) {
           __threadfence();
           Op::publish(p, j);
         }
@@ -339,7 +358,8 @@ __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, cons
 }
 
 template <class Op>
-__global__ void __launch_bounds__(kMaxThreads, 1) persistent_kernel(const __grid_constant__ typename Op::Params p) {
+__global__ void __launch_bounds__(op_max_threads<Op>(), 1)
+    persistent_kernel(const __grid_constant__ typename Op::Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using G = Geo<Op::kBM>;
@@ -372,7 +392,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) persistent_kernel(const __grid
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.tfull[b], 1);
-      mbar_init(&sm.tempty[b], 4);
+      mbar_init(&sm.tempty[b], Op::kEpiWarps);
     }
     mbar_init(sm.drain, 1);
     sm.epi_cnt[0] = 0;
@@ -393,10 +413,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) persistent_kernel(const __grid
     role_producer<Op>(p, sm, lane, gi, gn);
   } else if (warp == 1) {
     role_mma<Op>(p, sm, lane, tmem_base, gi, gn);
-  } else if (warp < kCoreWarps) {
+  } else if (warp < 2 + Op::kEpiWarps) {
     role_epilogue<Op>(p, sm, warp, lane, tmem_base, gi, gn);
   } else {
-    Op::mover(p, warp - kCoreWarps, lane);
+    Op::mover(p, warp - 2 - Op::kEpiWarps, lane);
   }
 
   tc_fence_before();

@@ -33,7 +33,7 @@ template <int BM>
 __device__ __forceinline__ void rs_epilogue(const CUtensorMap* acc_map, const float* acc_ptr,
                                             const CUtensorMap* out_map, const uint64_t* flag, int prod, int W,
                                             int grow, int orow, int n0, int n, const Common& c, uint32_t taddr,
-                                            int q, int lane, EpiStage& es) {
+                                            int q, int lane, EpiStage& es, int h0, int h1) {
   const bool first = prod == 0;
   const bool last = prod == W - 1;
   if (!first) {
@@ -42,7 +42,7 @@ __device__ __forceinline__ void rs_epilogue(const CUtensorMap* acc_map, const fl
                   static_cast<unsigned long long>(grow) << 20 | static_cast<unsigned>(n0));
   }
 #pragma unroll 1
-  for (int h = 0; h < BM / 128; ++h) {
+  for (int h = h0; h < h1; ++h) {
     const uint32_t th = taddr + h * 256;
     const int gr = grow + h * 128 + q * 32;
     if (!last) {
@@ -124,6 +124,8 @@ template <int BM>
 struct AgOp : OpBase<AgParams> {
   using Params = AgParams;
   static constexpr int kBM = BM;
+  static constexpr int kEpiWarps = 4;  // light bf16 epilogue
+  static constexpr int kMaxMovers = 4;
   static constexpr uint32_t kTxBytes = Geo<BM>::kStageBytes;
   static __device__ int num_tiles(const Params& p) { return ag_num_tiles(p.W, p.mps, p.nbk); }
   static __device__ Job job(const Params& p, int t) {
@@ -163,9 +165,10 @@ struct AgOp : OpBase<AgParams> {
   static __device__ void mma_stage(const Job&, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
     mma_stage_bm<BM>(d, a0, b0, kb);
   }
-  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
+  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es,
+                                 int h0, int h1) {
 #pragma unroll 1
-    for (int h = 0; h < BM / 128; ++h) {
+    for (int h = h0; h < h1; ++h) {
 #pragma unroll 1
       for (int ch = 0; ch < kBN / 64; ++ch) {
         const int x = j.b_col + ch * 64;
@@ -195,6 +198,8 @@ template <int BM>
 struct RsOp : OpBase<RsParams> {
   using Params = RsParams;
   static constexpr int kBM = BM;
+  static constexpr int kEpiWarps = BM == 256 ? 8 : 4;  // fp32 reduction epilogue of a whole tile
+  static constexpr int kMaxMovers = 0;
   static constexpr uint32_t kTxBytes = Geo<BM>::kStageBytes;
   static __device__ int num_tiles(const Params& p) { return rs_num_tiles(p.W, p.mbo, p.nbk); }
   static __device__ Job job(const Params& p, int t) {
@@ -224,9 +229,10 @@ struct RsOp : OpBase<RsParams> {
     mma_stage_bm<BM>(d, a0, b0, kb);
   }
   static __device__ int tile_id(const Params& p, const Job& j) { return (j.a_row / 128) * p.nbk + j.x3; }
-  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
+  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es,
+                                 int h0, int h1) {
     rs_epilogue<BM>(&p.acc, p.acc_ptr, &p.out[j.x1], p.flags + tile_id(p, j), j.x0, p.W, j.a_row, j.x2 * BM,
-                    j.b_col, p.n, p.common, taddr, q, lane, es);
+                    j.b_col, p.n, p.common, taddr, q, lane, es, h0, h1);
   }
   // peer_tile_notify: producer p's contribution to this slot tile is complete.
   static __device__ bool publishes(const Params& p, const Job& j) { return j.x0 != p.W - 1; }
@@ -260,6 +266,8 @@ template <int BM>
 struct Mlp2Op : OpBase<Mlp2Params> {
   using Params = Mlp2Params;
   static constexpr int kBM = BM;
+  static constexpr int kEpiWarps = BM == 256 ? 8 : 4;  // erf-GELU and fp32 reduction epilogues
+  static constexpr int kMaxMovers = BM == 256 ? 2 : 4;
   static constexpr int kSub = BM / 128;  // 128-row blocks per tile
   static constexpr uint32_t kTxBytes = Geo<BM>::kStageBytes;
   static __device__ int per_rank(const Params& p) { return p.W * p.mps * (p.nb1 + p.nb2); }
@@ -343,10 +351,11 @@ struct Mlp2Op : OpBase<Mlp2Params> {
   }
   static __device__ int h_row(const Params& p, const Job& j) { return j.x0 * p.T + j.x1 * p.Tr + j.x2 * BM; }
   static __device__ int rs_tile_id(const Params& p, const Job& j) { return row_block(p, j) * p.nb2 + j.x3; }
-  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
+  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es,
+                                 int h0, int h1) {
     if (j.kind == 1) {
 #pragma unroll 1
-      for (int hh = 0; hh < kSub; ++hh) {
+      for (int hh = h0; hh < h1; ++hh) {
         const int row = h_row(p, j) + hh * 128 + q * 32;
 #pragma unroll 1
         for (int ch = 0; ch < kBN / 64; ++ch) {
@@ -361,7 +370,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
       }
     } else {
       rs_epilogue<BM>(&p.acc, p.acc_ptr, &p.out[j.x1], p.rs_flags + rs_tile_id(p, j), j.x0, p.W,
-                      j.x1 * p.Tr + j.x2 * BM, j.x2 * BM, j.b_col, p.h, p.common, taddr, q, lane, es);
+                      j.x1 * p.Tr + j.x2 * BM, j.x2 * BM, j.b_col, p.h, p.common, taddr, q, lane, es, h0, h1);
     }
   }
   static __device__ bool publishes(const Params& p, const Job& j) { return j.kind == 1 || j.x0 != p.W - 1; }

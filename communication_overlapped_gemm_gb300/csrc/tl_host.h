@@ -37,7 +37,7 @@ inline Common make_common(tl_ctx* ctx) {
   c.status = ctx->status;
   c.epoch = next_epoch(ctx);
   c.timeout_ns = ctx->cfg.timeout_ns;
-  c.mover_warps = ctx->cfg.mover_warps;
+  c.mover_warps = ctx->cfg.mover_warps;  // clamped per op at launch (see launch_persistent)
   return c;
 }
 
@@ -53,7 +53,10 @@ int launch_persistent(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t st
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(ctx->ctas, 1, 1);
-  cfg.blockDim = dim3((kCoreWarps + mover_warps) * 32, 1, 1);
+  if (mover_warps > Op::kMaxMovers) mover_warps = Op::kMaxMovers;
+  cfg.blockDim = dim3((2 + Op::kEpiWarps + mover_warps) * 32, 1, 1);
+  typename Op::Params q = p;  // the device movers size their loops by the launched warp count
+  q.common.mover_warps = mover_warps;
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -61,7 +64,7 @@ int launch_persistent(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t st
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, q);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
     (void)cudaGetLastError();
     return TL_ERR_UNSUPPORTED;

@@ -231,6 +231,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 struct MoeOp : OpBase<MoeParams> {
   using Params = MoeParams;
   static constexpr int kBM = 128;
+  static constexpr int kMaxMovers = 2;  // the combine partition's CTAs use these two warps
   static constexpr uint32_t kTxBytes = Geo<128>::kStageBytes;
   static __device__ int mtiles(const Params& p) { return *reinterpret_cast<const volatile int*>(p.num_mtiles); }
   static __device__ int num_tiles(const Params& p) { return mtiles(p) * (p.n_up + p.n_down); }
@@ -336,7 +337,8 @@ struct MoeOp : OpBase<MoeParams> {
     else
       mma_stage_256(d, a0, b0, kb);
   }
-  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es) {
+  static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es,
+                                 int, int) {
     const int row = j.a_row + q * 32;
     if (j.kind == 1) {
 #pragma unroll 1
