@@ -69,7 +69,7 @@ int tl_version(void) { return 100; }
 
 int tl_config_default(tl_config* cfg) {
   if (!cfg) return TL_ERR_INVALID;
-  cfg->mover_warps = 2;
+  cfg->mover_warps = 4;
   cfg->chunks_per_slab = 32;
   cfg->swizzle = 1;
   cfg->grid_ctas = 0;

@@ -73,7 +73,7 @@ typedef struct CUstream_st* tl_stream_t;
  * bound on every device-side wait.
  */
 typedef struct tl_config {
-  int mover_warps;            /* warps per persistent CTA that move shards (1..4; default 2)          */
+  int mover_warps;            /* warps per persistent CTA that move shards (1..4; default 4)          */
   int chunks_per_slab;        /* mover chunks, hence signals, per 128-row slab (1..32; default 32)     */
   int swizzle;                /* 0: identity tile order; 1: rank-swizzled ([TD] §3.7; default)          */
   int grid_ctas;              /* persistent CTAs; 0 = one per SM (default)                              */

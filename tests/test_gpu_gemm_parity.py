@@ -121,7 +121,7 @@ def run_rs(ctx, inp):
 
 
 @pytest.mark.parametrize("W,m,n,kr", [(1, 128, 256, 64), (2, 256, 256, 128), (4, 512, 328, 200),
-                                      (8, 1024, 264, 72)])
+                                      (8, 1024, 264, 72), (2, 512, 264, 136), (3, 768, 520, 3584)])
 def test_gemm_rs_matches_oracle(ctx, W, m, n, kr):
     inp = make_inputs("gemm_rs", 31 + W, W=W, m=m, n=n, k_r=kr)
     out = run_rs(ctx, inp)
