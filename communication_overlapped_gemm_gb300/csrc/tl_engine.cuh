@@ -167,6 +167,8 @@ struct OpBase {
   static __device__ bool publishes(const P&, const Job&) { return false; }
   static __device__ void publish(const P&, const Job&) {}
   static __device__ void mover(const P&, int, int) {}
+  // Work the epilogue warps may do before their first tile (they idle until then).
+  static __device__ void epilogue_prologue(const P&, int, int) {}
   static constexpr int kEpiWarps = 4;   // epilogue warps (4, or 8 = one warpgroup per 128-row half)
   static constexpr int kMaxMovers = 4;  // mover warps the launch bounds allow
 };
@@ -204,7 +206,9 @@ __device__ __forceinline__ void stage_row128(uint8_t* buf, int lane, const uint3
   }
 }
 
-// Epilogue staging state of one warp: one or two 4 KB smem chunks + TMA bulk groups.
+// Epilogue staging state of one warp: one or two 4 KB chunk buffers (32 rows x 128 B).
+// With two, filling one overlaps the TMA engine reading the other; with 8 epilogue warps
+// the 32 KB staging area leaves one buffer per warp.
 struct EpiStage {
   uint8_t* buf[2];
   int idx;
@@ -316,6 +320,7 @@ __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, cons
   es.buf[0] = sm.epi + (ew * es.nbuf) * kEpiBufBytes;
   es.buf[1] = sm.epi + (ew * es.nbuf + es.nbuf - 1) * kEpiBufBytes;
   es.idx = 0;
+  Op::epilogue_prologue(p, ew, lane);
   // With 8 warps, warps ew and ew+4 share a lane quadrant and take one 128-row half each.
   const int h0 = E == 8 ? ew / 4 : 0;
   const int h1 = E == 8 ? h0 + 1 : Op::kBM / 128;
@@ -446,7 +451,7 @@ __device__ __forceinline__ void pack64_bf16(const float (&v)[64], uint32_t (&w)[
   for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
 }
 
-// Stage 64 bf16 columns of 32 rows and TMA-store them at (x, y) of `map`.
+// Stage 64 bf16 columns of 32 rows and TMA-store them at (x, y) of `map` (box {64, 32}).
 __device__ __forceinline__ void store_bf16_chunk(const CUtensorMap* map, EpiStage& es, int lane,
                                                  const float (&v)[64], int x, int y) {
   uint32_t w[32];
@@ -462,7 +467,8 @@ __device__ __forceinline__ void store_bf16_chunk(const CUtensorMap* map, EpiStag
   es.flip();
 }
 
-// Stage 32 fp32 columns of 32 rows and TMA-store (reduce = false) or TMA-add (reduce = true).
+// Stage 32 fp32 columns of 32 rows and TMA-store (reduce = false) or TMA-add (reduce = true)
+// them at (x, y) of `map` (box {32, 32}).
 __device__ __forceinline__ void store_f32_chunk(const CUtensorMap* map, EpiStage& es, int lane,
                                                 const float (&v)[32], int x, int y, bool reduce) {
   uint32_t w[32];
@@ -483,8 +489,8 @@ __device__ __forceinline__ void store_f32_chunk(const CUtensorMap* map, EpiStage
 }
 
 // Operand layouts in shared memory (both written by TMA with the 128-byte swizzle):
-//   A (K-major): 128 rows x 128 B; 8-row core groups 1024 B apart (SBO); a K step of
-//     16 elements advances the start address by 32 B inside the swizzle atom.
+//   A (K-major): 128-row groups of 128 B rows; 8-row core groups 1024 B apart (SBO); a K
+//     step of 16 elements advances the start address by 32 B inside the swizzle atom.
 //   B (MN-major, B is K x N row-major): BN/64 column groups of [64 k-rows x 128 B]
 //     (8 KB each) -> LBO = 8192 B between 64-column groups, SBO = 1024 B between
 //     8-row K groups; a K step of 16 rows advances the start by 2048 B.

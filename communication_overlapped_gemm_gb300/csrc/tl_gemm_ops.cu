@@ -17,13 +17,17 @@ __device__ __forceinline__ void wait_slab(const uint64_t* flags, int chunks, con
 // Pull one chunk of a shard into the gathered buffer and release its signal
 // (tile_pull_data + producer notify of "TileLink ...", §3.2; pull-mode AllGather of
 // "Triton-distributed ...", §3.2 Algorithm 2, with the chunk as the communication tile).
+// `bar` is the named barrier of the `nthreads` threads that copy together.
 __device__ __forceinline__ void mover_chunk(const uint8_t* src, uint8_t* dst, size_t bytes, uint64_t* flag,
-                                            bool signal, const Common& c, int tid, int nthreads) {
+                                            bool signal, const Common& c, int tid, int nthreads, int bar = 2) {
   copy_chunk(reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), bytes / 16, tid, nthreads);
   __threadfence();
-  named_bar_sync(2, nthreads);
+  named_bar_sync(bar, nthreads);
   if (tid == 0 && signal) st_release_gpu(flag, c.epoch);
 }
+
+// Exact GELU, 0.5 x (1 + erf(x / sqrt 2)).
+__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
 
 // GEMM+RS epilogue on one BM x 256 partial tile of producer `prod` (of W), reduced into
 // the fp32 slot tile at (grow, n0); the last producer writes bf16 rows of `out` at orow.
@@ -97,17 +101,21 @@ struct AgParams {
   uint64_t* flags;  // [W][spr][chunks]
   long long shard_bytes, slab_bytes;
   int W, rank, m_per_rank, mps, spr, n, nbk, kblocks, swizzle, chunks, skip_chunk;
+  int boost;  // chunks [0, boost) are split with the epilogue warps (see ag_mover)
 };
 
 // The shard mover: pull every shard (the self rank's last) into the gathered buffer in
-// 128-row slabs of `chunks` chunks, one release signal per chunk.
-__device__ __forceinline__ void ag_mover(const AgParams& p, int mw, int lane) {
-  const int nthreads = p.common.mover_warps * 32;
-  const int tid = mw * 32 + lane;
+// 128-row slabs of `chunks` chunks, one release signal per chunk.  Chunk g belongs to CTA
+// g mod grid.  The first `boost` chunks (the shards the first wave of tiles waits for) are
+// shared with the epilogue warps, which are idle until their first tile: in every other
+// round of the head (g / grid odd) the mover warps copy, in the others the epilogue warps
+// (group = 1), so the head arrives up to twice as fast.
+__device__ __forceinline__ void ag_copy(const AgParams& p, int tid, int nthreads, int group, int bar) {
   const int per_shard = p.spr * p.chunks;
-  const int total = p.W * per_shard;
+  const int total = group == 1 ? p.boost : p.W * per_shard;
   const size_t chunk_bytes = static_cast<size_t>(p.slab_bytes / p.chunks);
   for (int g = blockIdx.x; g < total; g += gridDim.x) {
+    if (g < p.boost && ((g / static_cast<int>(gridDim.x)) & 1) == (group == 1 ? 1 : 0)) continue;
     const int i = g / per_shard;
     const int rem = g - i * per_shard;
     const int slab = rem / p.chunks;
@@ -116,8 +124,12 @@ __device__ __forceinline__ void ag_mover(const AgParams& p, int mw, int lane) {
     const size_t off = static_cast<size_t>(slab) * p.slab_bytes + static_cast<size_t>(ch) * chunk_bytes;
     mover_chunk(p.shard[r] + off, p.gath + static_cast<size_t>(r) * p.shard_bytes + off, chunk_bytes,
                 p.flags + (static_cast<size_t>(r) * p.spr + slab) * p.chunks + ch, g != p.skip_chunk, p.common, tid,
-                nthreads);
+                nthreads, bar);
   }
+}
+
+__device__ __forceinline__ void ag_mover(const AgParams& p, int mw, int lane) {
+  ag_copy(p, mw * 32 + lane, p.common.mover_warps * 32, 0, 2);
 }
 
 template <int BM>
@@ -180,6 +192,9 @@ struct AgOp : OpBase<AgParams> {
     }
   }
   static __device__ void mover(const Params& p, int mw, int lane) { ag_mover(p, mw, lane); }
+  static __device__ void epilogue_prologue(const Params& p, int ew, int lane) {
+    if (p.boost > 0) ag_copy(p, ew * 32 + lane, kEpiWarps * 32, 1, 3);
+  }
 };
 
 // ============================================================================ GEMM + ReduceScatter
@@ -364,7 +379,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
           float v[64];
           tmem_ld64(taddr + hh * 256, ch * 64, v);
 #pragma unroll
-          for (int i = 0; i < 64; ++i) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.70710678118654752f));
+          for (int i = 0; i < 64; ++i) v[i] = gelu_erf(v[i]);
           store_bf16_chunk(&p.h_st, es, lane, v, x, row);
         }
       }
@@ -480,6 +495,7 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   p.skip_chunk = ctx->cfg.debug_skip_chunk;
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
+  p.boost = (W > 1 ? (W - 1 < 2 ? W - 1 : 2) : 0) * p.spr * p.chunks;  // the next two shards
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return bm == 256 ? launch_persistent<AgOp<256>>(ctx, p, st, ctx->cfg.mover_warps)
                    : launch_persistent<AgOp<128>>(ctx, p, st, ctx->cfg.mover_warps);
