@@ -525,6 +525,60 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """Run one workload's call (3 warm-up + 1) and exit: the target of an ncu capture."""
+    import torch
+
+    import __graft_entry__ as ge
+    ge.build()
+    import communication_overlapped_gemm_gb300 as tl
+    from seeded_inputs import WORKLOADS, workload_inputs
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    ctx = tl.Context(0)
+    name = args.profile
+    d = WORKLOADS[name].dims
+    inp = workload_inputs(name)
+    if WORKLOADS[name].kind == "ag_gemm":
+        a = [dev_bf16(x, device) for x in inp["a_shards"]]
+        b = dev_bf16(inp["b"], device)
+        c = torch.empty((d["W"] * d["m_per_rank"], d["n"]), dtype=torch.bfloat16, device=device)
+        ws = torch.zeros(tl.tl_ag_gemm_workspace_bytes(d["W"], d["m_per_rank"], d["n"], d["k"]), dtype=torch.uint8,
+                         device=device)
+        call = lambda: tl.tl_ag_gemm(ctx, a, b, c, ws)
+    elif WORKLOADS[name].kind == "gemm_rs":
+        a = [dev_bf16(x, device) for x in inp["a"]]
+        b = [dev_bf16(x, device) for x in inp["b"]]
+        o = [torch.empty((d["m"] // d["W"], d["n"]), dtype=torch.bfloat16, device=device) for _ in range(d["W"])]
+        ws = torch.zeros(tl.tl_gemm_rs_workspace_bytes(d["W"], d["m"], d["n"], d["k_r"]), dtype=torch.uint8,
+                         device=device)
+        call = lambda: tl.tl_gemm_rs(ctx, a, b, o, ws)
+    elif WORKLOADS[name].kind == "mlp2":
+        x = [dev_bf16(v, device) for v in inp["x_shards"]]
+        w1 = [dev_bf16(v, device) for v in inp["w1"]]
+        w2 = [dev_bf16(v, device) for v in inp["w2"]]
+        W, T = d["W"], d["tokens"]
+        o = [torch.empty((T // W, d["hidden"]), dtype=torch.bfloat16, device=device) for _ in range(W)]
+        ws = torch.zeros(tl.tl_mlp2_workspace_bytes(W, T, d["hidden"], d["f_r"]), dtype=torch.uint8, device=device)
+        call = lambda: tl.tl_mlp2(ctx, x, w1, w2, o, ws)
+    else:
+        xx = dev_bf16(inp["x"], device)
+        lg = torch.from_numpy(inp["logits"]).to(device)
+        wg, wu, wd = (dev_bf16(inp[q], device) for q in ("w_gate", "w_up", "w_down"))
+        oo = torch.empty((d["T"], d["H"]), dtype=torch.float32, device=device)
+        ws = torch.zeros(tl.tl_moe_workspace_bytes(d["T"], d["H"], d["E"], d["F"], d["topk"]), dtype=torch.uint8,
+                         device=device)
+        call = lambda: tl.tl_moe_combine(ctx, xx, lg, d["topk"], wg, wu, wd, oo, ws)
+    for _ in range(4):
+        call()
+    torch.cuda.synchronize()
+    rc = ctx.check()
+    ctx.close()
+    if rc != tl.TL_OK:
+        raise RuntimeError(f"device status {rc}")
+    print(json.dumps({"profiled": name, "calls": 4}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -537,10 +591,14 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work in --impl reference")
     ap.add_argument("--quick", action="store_true", help="headline only (no extra workloads / e2e / overlap)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--profile", choices=["ag_tiny", "ag_70b", "rs_70b", "mlp2_8b", "moe_64e"],
+                    help="only run this workload's call 4 times (target of an ncu capture), no timing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -51,6 +51,7 @@ class Config(ctypes.Structure):
         ("combine_ctas", _i),
         ("debug_skip_chunk", _i),
         ("timeout_ns", ctypes.c_ulonglong),
+        ("pair_ctas", _i),
     ]
 
 

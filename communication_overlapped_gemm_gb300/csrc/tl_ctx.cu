@@ -76,6 +76,7 @@ int tl_config_default(tl_config* cfg) {
   cfg->combine_ctas = 8;
   cfg->debug_skip_chunk = -1;
   cfg->timeout_ns = 2000000000ull;
+  cfg->pair_ctas = 2;
   return TL_OK;
 }
 
@@ -90,7 +91,8 @@ int tl_ctx_create(tl_ctx** out, int device, const tl_config* cfg) {
   else
     tl_config_default(&c);
   if (c.mover_warps < 1 || c.mover_warps > tl::kMaxMoverWarps || !pow2_le32(c.chunks_per_slab) ||
-      (c.swizzle != 0 && c.swizzle != 1) || c.grid_ctas < 0 || c.combine_ctas < 1 || c.timeout_ns == 0)
+      (c.swizzle != 0 && c.swizzle != 1) || c.grid_ctas < 0 || c.combine_ctas < 1 || c.timeout_ns == 0 ||
+      c.pair_ctas < 0 || c.pair_ctas > 2)
     return TL_ERR_INVALID;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) {

@@ -153,6 +153,7 @@ struct Job {
   int b_z;      // third B coordinate (expert), 0 if unused
   int kblocks;  // K / 64, rounded up
   int x0, x1, x2, x3;  // op-specific (ranks, owners, blocks)
+  int rank = 0;        // CTA of a pair (pair engine): which 128-row / 128-column half it owns
 };
 
 // Defaults for the optional hooks of an op (an op derives from OpBase<its Params>).

@@ -2,11 +2,22 @@
 // persistent tcgen05 engine, plus their C-ABI entry points.
 #include <cuda_bf16.h>
 
+#include "tl_engine2.cuh"
 #include "tl_host.h"
 
 namespace tl {
 
 // ============================================================================ shared op pieces
+
+// A 2-D TMA tile load: plain (single CTA) or, in a CTA pair, completing on the leader's
+// barrier at the same shared offset as `bar`.
+template <bool Pair>
+__device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y) {
+  if constexpr (Pair)
+    tma_load_2d_pair(dst, m, mapa_shared(smem_u32(bar), 0), x, y);
+  else
+    tma_load_2d(dst, m, bar, x, y);
+}
 
 // Wait for the `chunks` mover signals of one slab.
 __device__ __forceinline__ void wait_slab(const uint64_t* flags, int chunks, const Common& c, int lane,
@@ -132,13 +143,15 @@ __device__ __forceinline__ void ag_mover(const AgParams& p, int mw, int lane) {
   ag_copy(p, mw * 32 + lane, p.common.mover_warps * 32, 0, 2);
 }
 
-template <int BM>
+// Pair = true: 256-row tiles on a CTA pair (tl_engine2.cuh); this CTA owns rows and B
+// columns [128 rank, 128 rank + 128) of the tile.
+template <int BM, bool Pair = false>
 struct AgOp : OpBase<AgParams> {
   using Params = AgParams;
   static constexpr int kBM = BM;
   static constexpr int kEpiWarps = 4;  // light bf16 epilogue
   static constexpr int kMaxMovers = 4;
-  static constexpr uint32_t kTxBytes = Geo<BM>::kStageBytes;
+  static constexpr uint32_t kTxBytes = Pair ? Geo2::kStageBytes : Geo<BM>::kStageBytes;
   static __device__ int num_tiles(const Params& p) { return ag_num_tiles(p.W, p.mps, p.nbk); }
   static __device__ Job job(const Params& p, int t) {
     const AgTile a = ag_tile(t, p.W, p.rank, p.mps, p.nbk, p.swizzle);
@@ -166,13 +179,17 @@ struct AgOp : OpBase<AgParams> {
   // BM/128 slabs has been released by the mover.
   static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
     if (kb != 0 || j.a_sel == 0) return;
-    const uint64_t* f = p.flags + (static_cast<size_t>(j.x0) * p.spr + j.x1 * (BM / 128)) * p.chunks;
-    wait_slab(f, (BM / 128) * p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x0) << 32) | j.x1);
+    constexpr int kSlabs = Pair ? 1 : BM / 128;  // 128-row slabs this CTA reads
+    const int slab0 = j.x1 * (BM / 128) + (Pair ? j.rank : 0);
+    const uint64_t* f = p.flags + (static_cast<size_t>(j.x0) * p.spr + slab0) * p.chunks;
+    wait_slab(f, kSlabs * p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x0) << 32) | j.x1);
   }
   static __device__ void load(const Params& p, const Job& j, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
-    tma_load_2d(sa, j.a_sel ? &p.a_gath : &p.a_local, bar, kb * kBK, j.a_row);
+    const int r0 = Pair ? 128 * j.rank : 0;
+    load_tile<Pair>(sa, j.a_sel ? &p.a_gath : &p.a_local, bar, kb * kBK, j.a_row + r0);
 #pragma unroll
-    for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.b, bar, j.b_col + g * 64, kb * kBK);
+    for (int g = 0; g < (Pair ? 2 : kBN / 64); ++g)
+      load_tile<Pair>(sb + g * 8192, &p.b, bar, j.b_col + r0 + g * 64, kb * kBK);
   }
   static __device__ void mma_stage(const Job&, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
     mma_stage_bm<BM>(d, a0, b0, kb);
@@ -209,13 +226,15 @@ struct RsParams {
   int W, m, mo, mbo, n, nbk, kblocks, swizzle;
 };
 
-template <int BM>
+template <int BM, bool Pair = false>
 struct RsOp : OpBase<RsParams> {
   using Params = RsParams;
   static constexpr int kBM = BM;
-  static constexpr int kEpiWarps = BM == 256 ? 8 : 4;  // fp32 reduction epilogue of a whole tile
+  // fp32 reduction epilogue of a whole tile: 8 warps when the single-CTA 256-row tile has
+  // one TMEM accumulator; the pair keeps two, so 4 suffice.
+  static constexpr int kEpiWarps = (BM == 256 && !Pair) ? 8 : 4;
   static constexpr int kMaxMovers = 0;
-  static constexpr uint32_t kTxBytes = Geo<BM>::kStageBytes;
+  static constexpr uint32_t kTxBytes = Pair ? Geo2::kStageBytes : Geo<BM>::kStageBytes;
   static __device__ int num_tiles(const Params& p) { return rs_num_tiles(p.W, p.mbo, p.nbk); }
   static __device__ Job job(const Params& p, int t) {
     const RsTile r = rs_tile(t, p.W, p.mbo, p.nbk, p.swizzle);
@@ -236,14 +255,19 @@ struct RsOp : OpBase<RsParams> {
   static __device__ void prefetch(const Params& p) { tma_prefetch_map(&p.acc); }
   static __device__ void wait_deps(const Params&, const Job&, int, int) {}
   static __device__ void load(const Params& p, const Job& j, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
-    tma_load_2d(sa, &p.a[j.a_sel], bar, kb * kBK, j.a_row);
+    const int r0 = Pair ? 128 * j.rank : 0;
+    load_tile<Pair>(sa, &p.a[j.a_sel], bar, kb * kBK, j.a_row + r0);
 #pragma unroll
-    for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.b[j.b_sel], bar, j.b_col + g * 64, kb * kBK);
+    for (int g = 0; g < (Pair ? 2 : kBN / 64); ++g)
+      load_tile<Pair>(sb + g * 8192, &p.b[j.b_sel], bar, j.b_col + r0 + g * 64, kb * kBK);
   }
   static __device__ void mma_stage(const Job&, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
     mma_stage_bm<BM>(d, a0, b0, kb);
   }
-  static __device__ int tile_id(const Params& p, const Job& j) { return (j.a_row / 128) * p.nbk + j.x3; }
+  // signal of the first 128-row block this CTA writes (each CTA of a pair owns one block)
+  static __device__ int tile_id(const Params& p, const Job& j) {
+    return (j.a_row / 128 + (Pair ? j.rank : 0)) * p.nbk + j.x3;
+  }
   static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es,
                                  int h0, int h1) {
     rs_epilogue<BM>(&p.acc, p.acc_ptr, &p.out[j.x1], p.flags + tile_id(p, j), j.x0, p.W, j.a_row, j.x2 * BM,
@@ -277,14 +301,15 @@ struct Mlp2Params {
   int W, T, Tr, h, f, mps, spr, nb1, kb1, nb2, kb2, swizzle, chunks, skip_chunk;
 };
 
-template <int BM>
+template <int BM, bool Pair = false>
 struct Mlp2Op : OpBase<Mlp2Params> {
   using Params = Mlp2Params;
   static constexpr int kBM = BM;
-  static constexpr int kEpiWarps = BM == 256 ? 8 : 4;  // erf-GELU and fp32 reduction epilogues
-  static constexpr int kMaxMovers = BM == 256 ? 2 : 4;
-  static constexpr int kSub = BM / 128;  // 128-row blocks per tile
-  static constexpr uint32_t kTxBytes = Geo<BM>::kStageBytes;
+  static constexpr int kSub = BM / 128;             // 128-row blocks per tile
+  static constexpr int kOwn = Pair ? 1 : BM / 128;  // 128-row blocks this CTA reads / writes
+  static constexpr int kEpiWarps = (BM == 256 && !Pair) ? 8 : 4;  // erf-GELU and fp32 reduction epilogues
+  static constexpr int kMaxMovers = (BM == 256 && !Pair) ? 2 : 4;
+  static constexpr uint32_t kTxBytes = Pair ? Geo2::kStageBytes : Geo<BM>::kStageBytes;
   static __device__ int per_rank(const Params& p) { return p.W * p.mps * (p.nb1 + p.nb2); }
   static __device__ int num_tiles(const Params& p) { return p.W * per_rank(p); }
   // kind 1: layer-1 tile of rank x0 on shard x1, row block x2, column block x3
@@ -333,32 +358,38 @@ struct Mlp2Op : OpBase<Mlp2Params> {
     tma_prefetch_map(&p.h_ld);
     tma_prefetch_map(&p.acc);
   }
-  // first 128-row block (of T) covered by the tile
-  static __device__ int row_block(const Params& p, const Job& j) { return (j.x1 * p.Tr) / 128 + j.x2 * kSub; }
+  // first 128-row block (of T) this CTA covers
+  static __device__ int row_block(const Params& p, const Job& j) {
+    return (j.x1 * p.Tr) / 128 + j.x2 * kSub + (Pair ? j.rank : 0);
+  }
   static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
     if (kb != 0) return;
     if (j.kind == 1) {
       if (j.a_sel == 0) return;
-      const uint64_t* f =
-          p.ag_flags + ((static_cast<size_t>(j.x0) * p.W + j.x1) * p.spr + j.x2 * kSub) * p.chunks;
-      wait_slab(f, kSub * p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x1) << 32) | j.x2);
+      const uint64_t* f = p.ag_flags +
+                          ((static_cast<size_t>(j.x0) * p.W + j.x1) * p.spr + j.x2 * kSub + (Pair ? j.rank : 0)) *
+                              p.chunks;
+      wait_slab(f, kOwn * p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x1) << 32) | j.x2);
     } else {
       // CTA-level chain: the layer-1 tiles that produce this row block of H_r are done.
       const int rb = row_block(p, j);
       const uint64_t* f = p.h_flags + (static_cast<size_t>(j.x0) * (p.T / 128) + rb) * p.nb1;
-      warp_wait_signals(f, kSub * p.nb1, p.common.epoch, p.common, lane, kSiteSignal,
+      warp_wait_signals(f, kOwn * p.nb1, p.common.epoch, p.common, lane, kSiteSignal,
                         (2ull << 60) | (static_cast<unsigned long long>(j.x0) << 32) | rb);
     }
   }
   static __device__ void load(const Params& p, const Job& j, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+    const int r0 = Pair ? 128 * j.rank : 0;
     if (j.kind == 1) {
-      tma_load_2d(sa, j.a_sel ? &p.x_gath : &p.x_local[j.x0], bar, kb * kBK, j.a_row);
+      load_tile<Pair>(sa, j.a_sel ? &p.x_gath : &p.x_local[j.x0], bar, kb * kBK, j.a_row + r0);
 #pragma unroll
-      for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.w1[j.b_sel], bar, j.b_col + g * 64, kb * kBK);
+      for (int g = 0; g < (Pair ? 2 : kBN / 64); ++g)
+        load_tile<Pair>(sb + g * 8192, &p.w1[j.b_sel], bar, j.b_col + r0 + g * 64, kb * kBK);
     } else {
-      tma_load_2d(sa, &p.h_ld, bar, kb * kBK, j.a_row);
+      load_tile<Pair>(sa, &p.h_ld, bar, kb * kBK, j.a_row + r0);
 #pragma unroll
-      for (int g = 0; g < kBN / 64; ++g) tma_load_2d(sb + g * 8192, &p.w2[j.b_sel], bar, j.b_col + g * 64, kb * kBK);
+      for (int g = 0; g < (Pair ? 2 : kBN / 64); ++g)
+        load_tile<Pair>(sb + g * 8192, &p.w2[j.b_sel], bar, j.b_col + r0 + g * 64, kb * kBK);
     }
   }
   static __device__ void mma_stage(const Job&, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
@@ -393,7 +424,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
     if (j.kind == 1) {
       const int rb = row_block(p, j);
 #pragma unroll
-      for (int s = 0; s < kSub; ++s)
+      for (int s = 0; s < kOwn; ++s)
         st_release_gpu(p.h_flags + (static_cast<size_t>(j.x0) * (p.T / 128) + rb + s) * p.nb1 + j.x3, p.common.epoch);
     } else {
       st_release_gpu(p.rs_flags + rs_tile_id(p, j), (p.common.epoch << 4) | static_cast<unsigned long long>(j.x0 + 1));
@@ -476,8 +507,10 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   p.flags = reinterpret_cast<uint64_t*>(ws + align256(gath_bytes));
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int bm = pick_bm(m_per_rank);
-  if (!tmap_2d(&p.a_local, BF, 2, a_shards[rank], k, m_per_rank, 64, bm) ||
-      !tmap_2d(&p.a_gath, BF, 2, p.gath, k, M, 64, bm) || !tmap_2d(&p.b, BF, 2, b, n, k, 64, 64) ||
+  const bool pair = bm == 256 && ctx->cfg.pair_ctas == 1;
+  const int abox = pair ? 128 : bm;  // a CTA of a pair loads 128 of the tile's 256 rows
+  if (!tmap_2d(&p.a_local, BF, 2, a_shards[rank], k, m_per_rank, 64, abox) ||
+      !tmap_2d(&p.a_gath, BF, 2, p.gath, k, M, 64, abox) || !tmap_2d(&p.b, BF, 2, b, n, k, 64, 64) ||
       !tmap_2d(&p.c, BF, 2, c, n, M, 64, 32))
     return TL_ERR_CUDA;
   p.common = make_common(ctx);
@@ -497,6 +530,7 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
   p.boost = (W > 1 ? (W - 1 < 2 ? W - 1 : 2) : 0) * p.spr * p.chunks;  // the next two shards
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (pair) return launch_persistent_pair<AgOp<256, true>>(ctx, p, st, ctx->cfg.mover_warps);
   return bm == 256 ? launch_persistent<AgOp<256>>(ctx, p, st, ctx->cfg.mover_warps)
                    : launch_persistent<AgOp<128>>(ctx, p, st, ctx->cfg.mover_warps);
 }
@@ -533,8 +567,9 @@ extern "C" int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* 
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int mo = m / W;
   const int bm = pick_bm(mo);
+  const bool pair = bm == 256 && ctx->cfg.pair_ctas != 0;
   for (int r = 0; r < W; ++r) {
-    if (!tmap_2d(&p.a[r], BF, 2, a[r], k_r, m, 64, bm) || !tmap_2d(&p.b[r], BF, 2, b[r], n, k_r, 64, 64) ||
+    if (!tmap_2d(&p.a[r], BF, 2, a[r], k_r, m, 64, pair ? 128 : bm) || !tmap_2d(&p.b[r], BF, 2, b[r], n, k_r, 64, 64) ||
         !tmap_2d(&p.out[r], BF, 2, out[r], n, mo, 64, 32))
       return TL_ERR_CUDA;
   }
@@ -549,6 +584,7 @@ extern "C" int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* 
   p.kblocks = ceil_div(k_r, kBK);
   p.swizzle = ctx->cfg.swizzle;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (pair) return launch_persistent_pair<RsOp<256, true>>(ctx, p, st, 0);
   return bm == 256 ? launch_persistent<RsOp<256>>(ctx, p, st, 0) : launch_persistent<RsOp<128>>(ctx, p, st, 0);
 }
 
@@ -610,17 +646,19 @@ extern "C" int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const vo
   p.rs_flags = reinterpret_cast<uint64_t*>(ws + L.rsf);
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int bm = pick_bm(Tr);
+  const bool pair = bm == 256 && ctx->cfg.pair_ctas != 0;
+  const int abox = pair ? 128 : bm;
   for (int r = 0; r < W; ++r) {
-    if (!tmap_2d(&p.x_local[r], BF, 2, x_shards[r], hidden, Tr, 64, bm) ||
+    if (!tmap_2d(&p.x_local[r], BF, 2, x_shards[r], hidden, Tr, 64, abox) ||
         !tmap_2d(&p.w1[r], BF, 2, w1[r], f_r, hidden, 64, 64) ||
         !tmap_2d(&p.w2[r], BF, 2, w2[r], hidden, f_r, 64, 64) ||
         !tmap_2d(&p.out[r], BF, 2, out[r], hidden, Tr, 64, 32))
       return TL_ERR_CUDA;
     p.x[r] = static_cast<const uint8_t*>(x_shards[r]);
   }
-  if (!tmap_2d(&p.x_gath, BF, 2, p.xg, hidden, static_cast<uint64_t>(W) * tokens, 64, bm) ||
+  if (!tmap_2d(&p.x_gath, BF, 2, p.xg, hidden, static_cast<uint64_t>(W) * tokens, 64, abox) ||
       !tmap_2d(&p.h_st, BF, 2, hb, f_r, static_cast<uint64_t>(W) * tokens, 64, 32) ||
-      !tmap_2d(&p.h_ld, BF, 2, hb, f_r, static_cast<uint64_t>(W) * tokens, 64, bm) ||
+      !tmap_2d(&p.h_ld, BF, 2, hb, f_r, static_cast<uint64_t>(W) * tokens, 64, abox) ||
       !tmap_2d(&p.acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, hidden, tokens, 32, 32))
     return TL_ERR_CUDA;
   p.common = make_common(ctx);
@@ -641,6 +679,7 @@ extern "C" int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const vo
   p.shard_bytes = static_cast<long long>(Tr) * hidden * 2;
   p.slab_bytes = static_cast<long long>(kBM) * hidden * 2;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (pair) return launch_persistent_pair<Mlp2Op<256, true>>(ctx, p, st, ctx->cfg.mover_warps);
   return bm == 256 ? launch_persistent<Mlp2Op<256>>(ctx, p, st, ctx->cfg.mover_warps)
                    : launch_persistent<Mlp2Op<128>>(ctx, p, st, ctx->cfg.mover_warps);
 }

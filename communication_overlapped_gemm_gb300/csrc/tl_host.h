@@ -10,6 +10,7 @@
 
 #include "../../include/tl.h"
 #include "tl_engine.cuh"
+#include "tl_engine2.cuh"
 
 struct tl_ctx {
   int device;
@@ -68,6 +69,60 @@ int launch_persistent(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t st
   if (e == cudaErrorCooperativeLaunchTooLarge) {
     (void)cudaGetLastError();
     return TL_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TL_ERR_CUDA;
+  }
+  return TL_OK;
+}
+
+// Launch of the CTA-pair engine: clusters of 2 CTAs, as many as can be co-resident (at most
+// one CTA per SM).  The launch is cooperative when the runtime accepts it together with the
+// cluster shape; otherwise co-residency rests on the grid not exceeding the number of
+// clusters the device reports it can hold at once (every wait stays bounded either way).
+template <class Op>
+int launch_persistent_pair(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t stream, int mover_warps) {
+  auto kern = persistent_kernel_pair<Op>;
+  int rc = set_smem_attr(reinterpret_cast<const void*>(kern));
+  if (rc != TL_OK) return rc;
+  if (mover_warps > Op::kMaxMovers) mover_warps = Op::kMaxMovers;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.blockDim = dim3((2 + Op::kEpiWarps + mover_warps) * 32, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters = -1;  // per kernel instantiation
+  if (max_clusters < 0) {
+    cfg.gridDim = dim3(ctx->ctas & ~1, 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      return TL_ERR_UNSUPPORTED;
+    }
+    max_clusters = n;
+  }
+  int nclusters = ctx->ctas / 2;
+  if (nclusters > max_clusters) nclusters = max_clusters;
+  if (nclusters < 1) return TL_ERR_UNSUPPORTED;
+  cfg.gridDim = dim3(2 * nclusters, 1, 1);
+  typename Op::Params q = p;
+  q.common.mover_warps = mover_warps;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, q);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    cfg.numAttrs = 1;  // cluster shape only
+    e = cudaLaunchKernelEx(&cfg, kern, q);
   }
   if (e != cudaSuccess) {
     (void)cudaGetLastError();

@@ -80,6 +80,11 @@ typedef struct tl_config {
   int combine_ctas;           /* MoE combine partition, CTAs = SMs ([RA]; default 8)                    */
   int debug_skip_chunk;       /* fault injection: this mover chunk is copied but never signalled (-1 off) */
   unsigned long long timeout_ns; /* bound of every device wait (default 2e9 ns)                       */
+  int pair_ctas;              /* where shards / owner blocks are 256-row multiples, 256 x 256 tiles run
+                                 on: 0 single CTAs; 1 CTA pairs (two SMs, tcgen05 cta_group::2) for
+                                 every op; 2 (default) CTA pairs for tl_gemm_rs and tl_mlp2, whose
+                                 heavier epilogues gain from the pair's double-buffered
+                                 accumulators, single CTAs for tl_ag_gemm                           */
 } tl_config;
 
 typedef struct tl_ctx tl_ctx;

@@ -72,7 +72,7 @@ def test_ag_gemm_invariant_to_order_and_geometry():
     inp = make_inputs("ag_gemm", 21, W=4, m_per_rank=256, n=768, k=512)
     outs = []
     for cfg in [dict(swizzle=1), dict(swizzle=0), dict(chunks_per_slab=1, mover_warps=1),
-                dict(chunks_per_slab=8, mover_warps=4), dict(grid_ctas=37)]:
+                dict(chunks_per_slab=8, mover_warps=4), dict(grid_ctas=37), dict(pair_ctas=1, grid_ctas=38)]:
         with tl.Context(0, **cfg) as c2:
             for rank in (0, 3):
                 c, _ = run_ag(c2, inp, rank=rank)
@@ -133,7 +133,7 @@ def test_gemm_rs_matches_oracle(ctx, W, m, n, kr):
 def test_gemm_rs_deterministic_across_orders():
     inp = make_inputs("gemm_rs", 41, W=4, m=1024, n=512, k_r=256)
     outs = []
-    for cfg in [dict(swizzle=1), dict(swizzle=0), dict(grid_ctas=23)]:
+    for cfg in [dict(swizzle=1), dict(swizzle=0), dict(grid_ctas=23), dict(pair_ctas=0), dict(pair_ctas=1, grid_ctas=46)]:
         with tl.Context(0, **cfg) as c2:
             for _ in range(2):
                 outs.append([bf16_bits(o) for o in run_rs(c2, inp)])
@@ -208,3 +208,28 @@ def test_missing_signal_times_out_and_context_survives():
     with tl.Context(0) as c3:
         c, _ = run_ag(c3, inp)
         assert_close(bf16_to_f64(c), oracle.ag_gemm(inp["a_shards"], inp["b"]), "after timeout")
+
+
+@pytest.mark.parametrize("op", ["ag", "rs", "mlp2"])
+def test_cta_pair_and_single_cta_paths_agree(op):
+    """256-row tiles on CTA pairs (cta_group::2) and on single CTAs give the same result
+    within tolerance (both checked against the oracle)."""
+    import torch
+    outs = []
+    for pair in (1, 0):  # 1 forces CTA pairs for every op
+        with tl.Context(0, pair_ctas=pair) as c2:
+            if op == "ag":
+                inp = make_inputs("ag_gemm", 71, W=2, m_per_rank=512, n=520, k=328)
+                c, _ = run_ag(c2, inp, rank=1)
+                outs.append(bf16_to_f64(c))
+                ref = oracle.ag_gemm(inp["a_shards"], inp["b"])
+            elif op == "rs":
+                inp = make_inputs("gemm_rs", 72, W=2, m=1024, n=520, k_r=200)
+                outs.append(np.concatenate([bf16_to_f64(o) for o in run_rs(c2, inp)]))
+                ref = np.concatenate(oracle.gemm_rs(inp["a"], inp["b"]))
+            else:
+                inp = make_inputs("mlp2", 73, W=2, tokens=1024, hidden=264, f_r=520)
+                outs.append(np.concatenate([bf16_to_f64(o) for o in run_mlp2(c2, inp)]))
+                ref = np.concatenate(oracle.mlp2(inp["x_shards"], inp["w1"], inp["w2"]))
+            assert_close(outs[-1], ref, f"{op} pair_ctas={pair}")
+    assert_close(outs[0], outs[1], f"{op} pair vs single")
