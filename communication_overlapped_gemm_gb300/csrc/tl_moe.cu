@@ -552,7 +552,7 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   p.kb_up = H / kBK;
   p.kb_down = F / kBK;
   p.combine_ctas = ctx->cfg.combine_ctas;
-  p.chunk = 16;
+  p.chunk = 8;
   // Two extra warps per CTA: idle in the GEMM partition, combine workers in the combine CTAs.
   return launch_persistent<MoeOp>(ctx, p, st, 2);
 }
