@@ -77,10 +77,10 @@ int launch_persistent(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t st
   return TL_OK;
 }
 
-// Launch of the CTA-pair engine: clusters of 2 CTAs, as many as can be co-resident (at most
-// one CTA per SM).  The launch is cooperative when the runtime accepts it together with the
-// cluster shape; otherwise co-residency rests on the grid not exceeding the number of
-// clusters the device reports it can hold at once (every wait stays bounded either way).
+// Launch of the CTA-pair engine: clusters of 2 CTAs, as many as the device reports it can
+// hold at once (at most one CTA per SM), so every CTA that waits on a signal is resident
+// together with the CTAs that set it.  The cluster shape is the only launch attribute (the
+// cooperative attribute is not combined with clusters); every wait stays bounded.
 template <class Op>
 int launch_persistent_pair(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t stream, int mover_warps) {
   auto kern = persistent_kernel_pair<Op>;
@@ -92,18 +92,16 @@ int launch_persistent_pair(tl_ctx* ctx, const typename Op::Params& p, cudaStream
   cfg.blockDim = dim3((2 + Op::kEpiWarps + mover_warps) * 32, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   static int max_clusters = -1;  // per kernel instantiation
   if (max_clusters < 0) {
-    cfg.gridDim = dim3(ctx->ctas & ~1, 1, 1);
+    cfg.gridDim = dim3(ctx->sms & ~1, 1, 1);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
       (void)cudaGetLastError();
@@ -117,14 +115,7 @@ int launch_persistent_pair(tl_ctx* ctx, const typename Op::Params& p, cudaStream
   cfg.gridDim = dim3(2 * nclusters, 1, 1);
   typename Op::Params q = p;
   q.common.mover_warps = mover_warps;
-  cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, q);
-  if (e != cudaSuccess) {
-    (void)cudaGetLastError();
-    cfg.numAttrs = 1;  // cluster shape only
-    e = cudaLaunchKernelEx(&cfg, kern, q);
-  }
-  if (e != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, q) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_CUDA;
   }
