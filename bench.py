@@ -569,14 +569,41 @@ def run_profile(args):
         ws = torch.zeros(tl.tl_moe_workspace_bytes(d["T"], d["H"], d["E"], d["F"], d["topk"]), dtype=torch.uint8,
                          device=device)
         call = lambda: tl.tl_moe_combine(ctx, xx, lg, d["topk"], wg, wu, wd, oo, ws)
-    for _ in range(4):
+    if not args.trace:
+        for _ in range(4):
+            call()
+        torch.cuda.synchronize()
+        rc = ctx.check()
+        ctx.close()
+        if rc != tl.TL_OK:
+            raise RuntimeError(f"device status {rc}")
+        print(json.dumps({"profiled": name, "calls": 4}))
+        return
+    # Traced run: 3 warm-up calls, an L2 flush, then one call with the trace buffer on.
+    import numpy as np
+
+    from communication_overlapped_gemm_gb300 import trace
+    for _ in range(3):
         call()
+    cap = args.trace_spans
+    buf = torch.zeros(tl.tl_trace_bytes(ctx.num_ctas, cap), dtype=torch.uint8, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush.fill_(1)
+    ctx.set_trace(buf, cap)
+    call()
     torch.cuda.synchronize()
+    ctx.set_trace(None, cap)
     rc = ctx.check()
     ctx.close()
     if rc != tl.TL_OK:
         raise RuntimeError(f"device status {rc}")
-    print(json.dumps({"profiled": name, "calls": 4}))
+    tr = trace.parse(buf.cpu().numpy().tobytes())
+    if args.trace.endswith(".npz"):
+        np.savez_compressed(args.trace, spans=tr["spans"], counts=tr["counts"], grid=tr["grid"])
+    else:
+        trace.to_chrome(tr, args.trace)
+    print(json.dumps({"traced": name, "grid": tr["grid"], "spans": int(tr["spans"].size), "dropped": tr["dropped"],
+                      "chrome_json": args.trace, "summary": trace.summary(tr)}))
 
 
 def main():
@@ -593,9 +620,15 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile", choices=["ag_tiny", "ag_70b", "rs_70b", "mlp2_8b", "moe_64e"],
                     help="only run this workload's call 4 times (target of an ncu capture), no timing")
+    ap.add_argument("--trace", metavar="PATH", help="with --profile: trace one call (after 3 warm-up calls and an "
+                    "L2 flush) and write its per-CTA timeline to PATH: Chrome trace JSON, or the decoded spans "
+                    "(numpy .npz) when PATH ends in .npz")
+    ap.add_argument("--trace-spans", type=int, default=2048, help="trace buffer spans per warp")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.trace and not args.profile:
+        ap.error("--trace needs --profile WORKLOAD")
     if args.profile:
         run_profile(args)
     elif args.impl == "reference":

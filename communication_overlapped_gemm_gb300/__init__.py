@@ -8,8 +8,9 @@ not sm_103, the calls raise.
 
 Entry points (same names as the C ABI): ``tl_ag_gemm``, ``tl_gemm_rs``,
 ``tl_mlp2``, ``tl_moe_combine`` and their ``*_workspace_bytes`` sizes, plus
-``Context`` (tl_ctx_create / tl_ctx_check / tl_ctx_destroy) and the host-side
-tile maps ``tl_ag_tile_order`` / ``tl_rs_tile_order``.
+``Context`` (tl_ctx_create / tl_ctx_check / tl_ctx_destroy / tl_ctx_set_trace),
+the host-side tile maps ``tl_ag_tile_order`` / ``tl_rs_tile_order`` and
+``tl_trace_bytes`` (the trace buffer is read by ``.trace``).
 """
 from __future__ import annotations
 
@@ -23,7 +24,7 @@ __all__ = [
     "TLError", "Config", "Context", "lib", "library_path", "build",
     "tl_ag_gemm", "tl_allgather", "tl_gemm_rs", "tl_mlp2", "tl_moe_combine",
     "tl_ag_gemm_workspace_bytes", "tl_gemm_rs_workspace_bytes", "tl_mlp2_workspace_bytes",
-    "tl_moe_workspace_bytes", "tl_ag_tile_order", "tl_rs_tile_order", "EXPORTED_SYMBOLS",
+    "tl_moe_workspace_bytes", "tl_ag_tile_order", "tl_rs_tile_order", "tl_trace_bytes", "EXPORTED_SYMBOLS",
 ]
 
 TL_OK = 0
@@ -63,6 +64,8 @@ _SIGS = {
     "tl_ctx_destroy": (None, [_vp]),
     "tl_ctx_check": (_i, [_vp]),
     "tl_ctx_num_ctas": (_i, [_vp]),
+    "tl_trace_bytes": (_c_size, [_i, _i]),
+    "tl_ctx_set_trace": (_i, [_vp, _vp, _c_size, _i]),
     "tl_strerror": (ctypes.c_char_p, [_i]),
     "tl_ag_gemm_workspace_bytes": (_c_size, [_i, _i, _i, _i]),
     "tl_ag_gemm": (_i, [_vp, _i, _i, ctypes.POINTER(_vp), _vp, _vp, _vp, _c_size, _i, _i, _i, _vp]),
@@ -167,6 +170,17 @@ class Context:
     def num_ctas(self) -> int:
         return lib().tl_ctx_num_ctas(self.handle)
 
+    def set_trace(self, buf, spans_per_warp: int) -> None:
+        """tl_ctx_set_trace: record the persistent kernels' spans into ``buf`` (a CUDA uint8
+        tensor of at least ``tl_trace_bytes(1, spans_per_warp)`` bytes), or stop with None."""
+        if buf is None:
+            _check(lib().tl_ctx_set_trace(self.handle, None, 0, spans_per_warp), "tl_ctx_set_trace")
+            self._trace_buf = None
+            return
+        _need(buf, "u8", "trace buffer")
+        _check(lib().tl_ctx_set_trace(self.handle, _ptr(buf), buf.numel(), spans_per_warp), "tl_ctx_set_trace")
+        self._trace_buf = buf  # the library keeps the pointer: keep the memory alive
+
     def check(self) -> int:
         """tl_ctx_check: synchronise, read and clear the device status word (returns the code)."""
         return lib().tl_ctx_check(self.handle)
@@ -204,6 +218,10 @@ def tl_mlp2_workspace_bytes(W, tokens, hidden, f_r) -> int:
 
 def tl_moe_workspace_bytes(T, H, E, F, topk) -> int:
     return lib().tl_moe_workspace_bytes(T, H, E, F, topk)
+
+
+def tl_trace_bytes(ctas, spans_per_warp) -> int:
+    return lib().tl_trace_bytes(ctas, spans_per_warp)
 
 
 # ---------------------------------------------------------------- operators

@@ -165,6 +165,32 @@ int tl_ctx_check(tl_ctx* ctx) {
 
 int tl_ctx_num_ctas(const tl_ctx* ctx) { return ctx ? ctx->ctas : 0; }
 
+// Trace buffer: header (8 words), per-warp counts (16 words per CTA), then the spans.  The
+// header and counts take 32 + 64 * ctas bytes, a multiple of 16, so the spans stay aligned.
+size_t tl_trace_bytes(int ctas, int spans_per_warp) {
+  if (ctas < 1 || spans_per_warp < 1) return 0;
+  return 4 * tl::kTraceHdrWords +
+         static_cast<size_t>(ctas) * (4 * tl::kTraceWarps + sizeof(tl::TraceRec) * tl::kTraceWarps *
+                                                                static_cast<size_t>(spans_per_warp));
+}
+
+int tl_ctx_set_trace(tl_ctx* ctx, void* buf, size_t bytes, int spans_per_warp) {
+  if (!ctx) return TL_ERR_INVALID;
+  if (!buf) {
+    ctx->trace_buf = nullptr;
+    ctx->trace_cap = 0;
+    ctx->trace_ctas = 0;
+    return TL_OK;
+  }
+  if (spans_per_warp < 1 || !tl::aligned16(buf) || bytes < tl_trace_bytes(1, spans_per_warp)) return TL_ERR_INVALID;
+  const size_t per_cta = tl_trace_bytes(2, spans_per_warp) - tl_trace_bytes(1, spans_per_warp);
+  const size_t held = (bytes - 4 * tl::kTraceHdrWords) / per_cta;
+  ctx->trace_buf = buf;
+  ctx->trace_cap = spans_per_warp;
+  ctx->trace_ctas = held > 4096 ? 4096 : static_cast<int>(held);
+  return TL_OK;
+}
+
 const char* tl_strerror(int code) {
   switch (code) {
     case TL_OK: return "ok";

@@ -75,12 +75,109 @@ struct DevStatus {
   unsigned long long info;
 };
 
+// One trace span: a warp role's activity [t0, t0 + dur) in %globaltimer nanoseconds.
+struct TraceRec {
+  unsigned long long t0;
+  unsigned int dur;
+  unsigned int tag;  // kind << 24 | (tile or chunk index & 0xffffff)
+};
+
 struct Common {
   DevStatus* status;
   unsigned long long epoch;       // this call's signal value (never 0)
   unsigned long long timeout_ns;  // bound of every wait
   int mover_warps;
+  int trace_cap;                  // spans per warp the trace buffer holds
+  int trace_ctas;                 // CTAs the trace buffer holds
+  unsigned int* trace_hdr;        // trace buffer (null: tracing off): header, counts, spans
+  TraceRec* trace;
 };
+
+// ------------------------------------------------------------------ trace spans
+// Span kinds (the trace buffer's tag field carries kind << 24 | index).
+enum TraceKind : unsigned {
+  kTrProdTile = 1,     // producer: the tile's first wait .. its last load issued
+  kTrProdWait = 2,     // producer: one dependency-signal wait
+  kTrProdStall = 3,    // producer: total wait for free ring stages in the tile (t0 = tile start)
+  kTrMmaTile = 4,      // MMA: accumulator acquired .. the tile's last commit issued
+  kTrMmaStarve = 5,    // MMA: total wait for filled stages in the tile (t0 = tile start)
+  kTrMmaAccWait = 6,   // MMA: wait for a free accumulator
+  kTrEpiTile = 7,      // epilogue: accumulator full .. accumulator released
+  kTrEpiWait = 8,      // epilogue: wait for a full accumulator
+  kTrMoverChunk = 9,   // mover: one chunk copied and signalled
+  kTrSideTile = 10,    // side partition: one unit of work from the start of its wait (e.g. one y tile)
+  kTrSideWait = 11,    // side partition: its signal wait
+};
+constexpr int kTraceWarps = 16;           // warps per CTA with a span list
+constexpr unsigned kTraceMinWaitNs = 200;  // shorter waits are not recorded
+constexpr unsigned kTraceMagic = 0x544c5452u;
+constexpr int kTraceHdrWords = 8;
+
+// Per-warp span counters: 16 words at a fixed place in the barrier area of dynamic
+// shared memory, which neither engine's barriers nor any side role use.
+__device__ __forceinline__ uint32_t* trace_slots() {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  return reinterpret_cast<uint32_t*>(base + kRingBytes + kEpiBytes + kBarBytes - 4 * kTraceWarps);
+}
+
+__device__ __forceinline__ bool tracing(const Common& c) { return c.trace_hdr != nullptr; }
+
+// Record one span of the calling warp (call from one lane).
+__device__ __forceinline__ void trace_span(const Common& c, unsigned kind, int index, uint64_t t0, uint64_t t1) {
+  if (!tracing(c) || static_cast<int>(blockIdx.x) >= c.trace_ctas) return;
+  const int w = static_cast<int>(threadIdx.x >> 5);
+  if (w >= kTraceWarps) return;
+  uint32_t* cnt = trace_slots() + w;
+  const uint32_t i = *cnt;
+  *cnt = i + 1;
+  if (i < static_cast<uint32_t>(c.trace_cap)) {
+    TraceRec r;
+    r.t0 = t0;
+    const uint64_t d = t1 > t0 ? t1 - t0 : 0;
+    r.dur = d > 0xffffffffull ? 0xffffffffu : static_cast<unsigned>(d);
+    r.tag = (kind << 24) | (static_cast<unsigned>(index) & 0xffffffu);
+    c.trace[(static_cast<size_t>(blockIdx.x) * kTraceWarps + w) * c.trace_cap + i] = r;
+  }
+}
+
+// Open a span of the calling warp at t0 (call from one lane); trace_close sets its duration.
+// Nothing stays live in registers in between, which keeps the epilogue's register budget.
+__device__ __forceinline__ void trace_open(const Common& c, unsigned kind, int index, uint64_t t0) {
+  trace_span(c, kind, index, t0, t0);
+}
+__device__ __forceinline__ void trace_close(const Common& c, uint64_t t1) {
+  if (!tracing(c) || static_cast<int>(blockIdx.x) >= c.trace_ctas) return;
+  const int w = static_cast<int>(threadIdx.x >> 5);
+  if (w >= kTraceWarps) return;
+  const uint32_t i = trace_slots()[w] - 1;
+  if (i < static_cast<uint32_t>(c.trace_cap)) {
+    TraceRec* r = c.trace + (static_cast<size_t>(blockIdx.x) * kTraceWarps + w) * c.trace_cap + i;
+    const uint64_t d = t1 > r->t0 ? t1 - r->t0 : 0;
+    r->dur = d > 0xffffffffull ? 0xffffffffu : static_cast<unsigned>(d);
+  }
+}
+
+// Kernel start (all threads, before the CTA's first barrier): zero the span counters.
+__device__ __forceinline__ void trace_begin() {
+  if (threadIdx.x < kTraceWarps) trace_slots()[threadIdx.x] = 0;
+}
+
+// Kernel end (all threads, after the CTA's last barrier): publish the span counts, and
+// from CTA 0 the header {magic, version 1, grid, warps per CTA, spans per warp, CTAs held}.
+__device__ __forceinline__ void trace_end(const Common& c) {
+  if (!tracing(c) || static_cast<int>(blockIdx.x) >= c.trace_ctas) return;
+  if (threadIdx.x < kTraceWarps)
+    c.trace_hdr[kTraceHdrWords + blockIdx.x * kTraceWarps + threadIdx.x] = trace_slots()[threadIdx.x];
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    c.trace_hdr[0] = kTraceMagic;
+    c.trace_hdr[1] = 1u;
+    c.trace_hdr[2] = gridDim.x;
+    c.trace_hdr[3] = kTraceWarps;
+    c.trace_hdr[4] = static_cast<unsigned>(c.trace_cap);
+    c.trace_hdr[5] = static_cast<unsigned>(c.trace_ctas);
+  }
+}
 
 __device__ __forceinline__ void report_timeout(DevStatus* st, unsigned where, unsigned long long info) {
   if (atomicCAS(&st->code, 0u, kStatusTimeout) == 0u) {
@@ -161,14 +258,18 @@ template <class P>
 struct OpBase {
   // Whether this CTA belongs to the GEMM partition; (gi, gn) = its index / partition size.
   static __device__ bool gemm_partition(const P&, int&, int&) { return true; }
-  // Work of CTAs outside the GEMM partition (all threads of the CTA).
+  // Work of CTAs outside the GEMM partition (all threads of the CTA).  The hooks that run
+  // outside the GEMM roles take the kernel's Trace flag (true: they may record spans).
+  template <bool Trace>
   static __device__ void side_role(const P&, int, int, uint8_t*) {}
   static __device__ void producer_init(const P&) {}
   static __device__ void prefetch(const P&) {}
   static __device__ bool publishes(const P&, const Job&) { return false; }
   static __device__ void publish(const P&, const Job&) {}
+  template <bool Trace>
   static __device__ void mover(const P&, int, int) {}
   // Work the epilogue warps may do before their first tile (they idle until then).
+  template <bool Trace>
   static __device__ void epilogue_prologue(const P&, int, int) {}
   static constexpr int kEpiWarps = 4;   // epilogue warps (4, or 8 = one warpgroup per 128-row half)
   static constexpr int kMaxMovers = 4;  // mover warps the launch bounds allow
@@ -230,7 +331,7 @@ struct EpiStage {
   }
 };
 
-template <class Op>
+template <class Op, bool Trace>
 __device__ __forceinline__ void role_producer(const typename Op::Params& p, const Smem& sm, int lane, int gi,
                                               int gn) {
   const Common& c = p.common;
@@ -239,13 +340,23 @@ __device__ __forceinline__ void role_producer(const typename Op::Params& p, cons
   uint32_t stage = 0, phase = 0;
   uint32_t filled = 0, fill_parity = 0;  // per-stage: fill issued / parity of that fill
   bool ok = true;
+  constexpr bool tr = Trace;
   Op::producer_init(p);
   for (int t = gi; t < ntiles && ok; t += gn) {
     const Job j = Op::job(p, t);
+    const uint64_t tt0 = tr ? globaltimer() : 0;
+    uint64_t stall = 0;
     for (int kb = 0; kb < j.kblocks; ++kb) {
+      const uint64_t w0 = tr ? globaltimer() : 0;
       Op::wait_deps(p, j, kb, lane);
+      if (tr && lane == 0) {
+        const uint64_t w1 = globaltimer();
+        if (w1 - w0 > kTraceMinWaitNs) trace_span(c, kTrProdWait, t, w0, w1);
+      }
       if (lane == 0) {
+        const uint64_t e0 = tr ? globaltimer() : 0;
         ok = mbar_wait(&sm.empty[stage], phase ^ 1u, c, kSiteEmpty);
+        if (tr) stall += globaltimer() - e0;
         if (ok) {
           mbar_arrive_expect_tx(&sm.full[stage], Op::kTxBytes);
           Op::load(p, j, kb, sm.a(stage), sm.b(stage), &sm.full[stage]);
@@ -257,6 +368,10 @@ __device__ __forceinline__ void role_producer(const typename Op::Params& p, cons
       if (!ok) break;
       if (++stage == kStages) { stage = 0; phase ^= 1u; }
     }
+    if (tr && lane == 0) {
+      trace_span(c, kTrProdTile, t, tt0, globaltimer());
+      trace_span(c, kTrProdStall, t, tt0, tt0 + stall);
+    }
   }
   // Drain: every TMA fill this warp issued must have landed before the CTA exits.
   if (lane == 0) {
@@ -266,7 +381,7 @@ __device__ __forceinline__ void role_producer(const typename Op::Params& p, cons
   __syncwarp();
 }
 
-template <class Op>
+template <class Op, bool Trace>
 __device__ __forceinline__ void role_mma(const typename Op::Params& p, const Smem& sm, int lane,
                                          uint32_t tmem_base, int gi, int gn) {
   using G = Geo<Op::kBM>;
@@ -275,14 +390,21 @@ __device__ __forceinline__ void role_mma(const typename Op::Params& p, const Sme
   const int ntiles = Op::num_tiles(p);
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   bool ok = true;
+  constexpr bool tr = Trace;
   for (int t = gi; t < ntiles && ok; t += gn) {
     const Job j = Op::job(p, t);
     if (lane == 0) {
+      const uint64_t a0t = tr ? globaltimer() : 0;
       ok = mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, c, kSiteTmemEmpty);
       tc_fence_after();
+      const uint64_t tt0 = tr ? globaltimer() : 0;
+      if (tr && tt0 - a0t > kTraceMinWaitNs) trace_span(c, kTrMmaAccWait, t, a0t, tt0);
+      uint64_t starve = 0;
       const uint32_t d = tmem_base + acc * G::kAccStride;
       for (int kb = 0; kb < j.kblocks && ok; ++kb) {
+        const uint64_t f0 = tr ? globaltimer() : 0;
         ok = mbar_wait(&sm.full[stage], phase, c, kSiteFull);
+        if (tr) starve += globaltimer() - f0;
         if (!ok) break;
         tc_fence_after();
         const uint32_t a0 = smem_u32(sm.a(stage));
@@ -292,6 +414,10 @@ __device__ __forceinline__ void role_mma(const typename Op::Params& p, const Sme
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       if (ok) umma_commit(&sm.tfull[acc]);
+      if (tr) {
+        trace_span(c, kTrMmaTile, t, tt0, globaltimer());
+        trace_span(c, kTrMmaStarve, t, tt0, tt0 + starve);
+      }
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (++acc == G::kAccBufs) {
@@ -307,7 +433,7 @@ __device__ __forceinline__ void role_mma(const typename Op::Params& p, const Sme
   __syncwarp();
 }
 
-template <class Op>
+template <class Op, bool Trace>
 __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, const Smem& sm, int warp,
                                               int lane, uint32_t tmem_base, int gi, int gn) {
   using G = Geo<Op::kBM>;
@@ -321,17 +447,24 @@ __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, cons
   es.buf[0] = sm.epi + (ew * es.nbuf) * kEpiBufBytes;
   es.buf[1] = sm.epi + (ew * es.nbuf + es.nbuf - 1) * kEpiBufBytes;
   es.idx = 0;
-  Op::epilogue_prologue(p, ew, lane);
+  Op::template epilogue_prologue<Trace>(p, ew, lane);
   // With 8 warps, warps ew and ew+4 share a lane quadrant and take one 128-row half each.
   const int h0 = E == 8 ? ew / 4 : 0;
   const int h1 = E == 8 ? h0 + 1 : Op::kBM / 128;
   uint32_t acc = 0, acc_phase = 0;
   bool ok = true;
+  constexpr bool tr = Trace;
   for (int t = gi; t < ntiles && ok; t += gn) {
     const Job j = Op::job(p, t);
+    const uint64_t w0 = tr ? globaltimer() : 0;
     ok = mbar_wait(&sm.tfull[acc], acc_phase, c, kSiteTmemFull);
     if (!ok) break;
     tc_fence_after();
+    if (tr && lane == 0) {
+      const uint64_t tt0 = globaltimer();
+      if (tt0 - w0 > kTraceMinWaitNs) trace_span(c, kTrEpiWait, t, w0, tt0);
+      trace_open(c, kTrEpiTile, t, tt0);
+    }
     const uint32_t taddr = tmem_base + acc * G::kAccStride + (static_cast<uint32_t>(q * 32) << 16);
     Op::epilogue(p, j, taddr, q, lane, es, h0, h1);
     if (Op::publishes(p, j)) {
@@ -354,6 +487,7 @@ __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, cons
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+    if (tr && lane == 0) trace_close(c, globaltimer());
     if (++acc == G::kAccBufs) {
       acc = 0;
       acc_phase ^= 1u;
@@ -363,7 +497,9 @@ __device__ __forceinline__ void role_epilogue(const typename Op::Params& p, cons
   __syncwarp();
 }
 
-template <class Op>
+// Trace: the instantiation that records spans (launched while the context has a trace
+// buffer); the other one carries no trace code at all.
+template <class Op, bool Trace>
 __global__ void __launch_bounds__(op_max_threads<Op>(), 1)
     persistent_kernel(const __grid_constant__ typename Op::Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -382,13 +518,22 @@ __global__ void __launch_bounds__(op_max_threads<Op>(), 1)
   sm.drain = bars + 2 * kMaxStages + 4;
   sm.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
   sm.epi_cnt = sm.tmem_slot + 2;
+  static_assert((2 * kMaxStages + 5) * 8 + 16 <= kBarBytes - 4 * kTraceWarps, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if constexpr (Trace) {
+    trace_begin();
+    __syncthreads();
+  }
   // CTAs outside the GEMM partition (e.g. a combine partition) run the op's side role.
   int gi = blockIdx.x, gn = gridDim.x;
   if (!Op::gemm_partition(p, gi, gn)) {
-    Op::side_role(p, warp, lane, smem_raw);
+    Op::template side_role<Trace>(p, warp, lane, smem_raw);
+    if constexpr (Trace) {
+      __syncthreads();
+      trace_end(p.common);
+    }
     return;
   }
   if (threadIdx.x == 0) {
@@ -416,17 +561,18 @@ __global__ void __launch_bounds__(op_max_threads<Op>(), 1)
   const uint32_t tmem_base = *sm.tmem_slot;
 
   if (warp == 0) {
-    role_producer<Op>(p, sm, lane, gi, gn);
+    role_producer<Op, Trace>(p, sm, lane, gi, gn);
   } else if (warp == 1) {
-    role_mma<Op>(p, sm, lane, tmem_base, gi, gn);
+    role_mma<Op, Trace>(p, sm, lane, tmem_base, gi, gn);
   } else if (warp < 2 + Op::kEpiWarps) {
-    role_epilogue<Op>(p, sm, warp, lane, tmem_base, gi, gn);
+    role_epilogue<Op, Trace>(p, sm, warp, lane, tmem_base, gi, gn);
   } else {
-    Op::mover(p, warp - 2 - Op::kEpiWarps, lane);
+    Op::template mover<Trace>(p, warp - 2 - Op::kEpiWarps, lane);
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (Trace) trace_end(p.common);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);

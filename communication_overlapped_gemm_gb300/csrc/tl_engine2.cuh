@@ -56,7 +56,7 @@ __device__ __forceinline__ void mma_stage_pair(uint32_t d, uint32_t a0, uint32_t
   }
 }
 
-template <class Op>
+template <class Op, bool Trace>
 __device__ __forceinline__ void pair_producer(const typename Op::Params& p, const Smem& sm, int lane, int gi,
                                               int gn, uint32_t rank) {
   const Common& c = p.common;
@@ -64,14 +64,24 @@ __device__ __forceinline__ void pair_producer(const typename Op::Params& p, cons
   uint32_t stage = 0, phase = 0;
   uint32_t filled = 0, fill_parity = 0;
   bool ok = true;
+  constexpr bool tr = Trace;
   for (int t = gi; t < ntiles && ok; t += gn) {
     Job j = Op::job(p, t);
     j.rank = static_cast<int>(rank);
+    const uint64_t tt0 = tr ? globaltimer() : 0;
+    uint64_t stall = 0;
     for (int kb = 0; kb < j.kblocks; ++kb) {
+      const uint64_t w0 = tr ? globaltimer() : 0;
       Op::wait_deps(p, j, kb, lane);
+      if (tr && lane == 0) {
+        const uint64_t w1 = globaltimer();
+        if (w1 - w0 > kTraceMinWaitNs) trace_span(c, kTrProdWait, t, w0, w1);
+      }
       if (lane == 0) {
+        const uint64_t e0 = tr ? globaltimer() : 0;
         ok = rank == 0 ? mbar_wait(&sm.empty[stage], phase ^ 1u, c, kSiteEmpty)
                        : mbar_wait_cl(&sm.empty[stage], phase ^ 1u, c, kSiteEmpty);
+        if (tr) stall += globaltimer() - e0;
         if (ok) {
           // the leader's full[stage] counts both CTAs' bytes; the loads below complete on it
           if (rank == 0) mbar_arrive_expect_tx(&sm.full[stage], 2 * Op::kTxBytes);
@@ -87,6 +97,10 @@ __device__ __forceinline__ void pair_producer(const typename Op::Params& p, cons
         phase ^= 1u;
       }
     }
+    if (tr && lane == 0) {
+      trace_span(c, kTrProdTile, t, tt0, globaltimer());
+      trace_span(c, kTrProdStall, t, tt0, tt0 + stall);
+    }
   }
   // Drain (leader): its full[s] completes when both CTAs' loads of that fill have landed.
   if (lane == 0 && rank == 0) {
@@ -98,7 +112,7 @@ __device__ __forceinline__ void pair_producer(const typename Op::Params& p, cons
 
 // Leader: issue the pair MMAs and commit their completion to both CTAs' barriers.  The
 // peer's MMA warp has nothing to do.
-template <class Op>
+template <class Op, bool Trace>
 __device__ __forceinline__ void pair_mma(const typename Op::Params& p, const Smem& sm, int lane, uint32_t tmem_base,
                                          int gi, int gn, uint32_t rank) {
   if (rank != 0) return;
@@ -108,14 +122,21 @@ __device__ __forceinline__ void pair_mma(const typename Op::Params& p, const Sme
   const uint32_t peer_tfull0 = mapa_shared(smem_u32(&sm.tfull[0]), 1);
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   bool ok = true;
+  constexpr bool tr = Trace;
   for (int t = gi; t < ntiles && ok; t += gn) {
     const Job j = Op::job(p, t);
     if (lane == 0) {
+      const uint64_t a0t = tr ? globaltimer() : 0;
       ok = mbar_wait_cl(&sm.tempty[acc], acc_phase ^ 1u, c, kSiteTmemEmpty);
       tc_fence_after();
+      const uint64_t tt0 = tr ? globaltimer() : 0;
+      if (tr && tt0 - a0t > kTraceMinWaitNs) trace_span(c, kTrMmaAccWait, t, a0t, tt0);
+      uint64_t starve = 0;
       const uint32_t d = tmem_base + acc * Geo2::kAccStride;
       for (int kb = 0; kb < j.kblocks && ok; ++kb) {
+        const uint64_t f0 = tr ? globaltimer() : 0;
         ok = mbar_wait_cl(&sm.full[stage], phase, c, kSiteFull);
+        if (tr) starve += globaltimer() - f0;
         if (!ok) break;
         tc_fence_after();
         mma_stage_pair(d, smem_u32(sm.a(stage)), smem_u32(sm.b(stage)), kb);
@@ -129,6 +150,10 @@ __device__ __forceinline__ void pair_mma(const typename Op::Params& p, const Sme
       if (ok) {
         umma_commit_pair(&sm.tfull[acc]);
         umma_commit_pair_at(peer_tfull0 + acc * 8u);
+      }
+      if (tr) {
+        trace_span(c, kTrMmaTile, t, tt0, globaltimer());
+        trace_span(c, kTrMmaStarve, t, tt0, tt0 + starve);
       }
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -145,7 +170,7 @@ __device__ __forceinline__ void pair_mma(const typename Op::Params& p, const Sme
   __syncwarp();
 }
 
-template <class Op>
+template <class Op, bool Trace>
 __device__ __forceinline__ void pair_epilogue(const typename Op::Params& p, const Smem& sm, int warp, int lane,
                                               uint32_t tmem_base, int gi, int gn, uint32_t rank) {
   constexpr int E = Op::kEpiWarps;
@@ -159,17 +184,24 @@ __device__ __forceinline__ void pair_epilogue(const typename Op::Params& p, cons
   es.buf[0] = sm.epi + (ew * 2) * kEpiBufBytes;
   es.buf[1] = sm.epi + (ew * 2 + 1) * kEpiBufBytes;
   es.idx = 0;
-  Op::epilogue_prologue(p, ew, lane);
+  Op::template epilogue_prologue<Trace>(p, ew, lane);
   const uint32_t tempty_leader0 = mapa_shared(smem_u32(&sm.tempty[0]), 0);
   uint32_t acc = 0, acc_phase = 0;
   bool ok = true;
+  constexpr bool tr = Trace;
   for (int t = gi; t < ntiles && ok; t += gn) {
     Job j = Op::job(p, t);
     j.rank = static_cast<int>(rank);
+    const uint64_t w0 = tr ? globaltimer() : 0;
     ok = rank == 0 ? mbar_wait(&sm.tfull[acc], acc_phase, c, kSiteTmemFull)
                    : mbar_wait_cl(&sm.tfull[acc], acc_phase, c, kSiteTmemFull);
     if (!ok) break;
     tc_fence_after();
+    if (tr && lane == 0) {
+      const uint64_t tt0 = globaltimer();
+      if (tt0 - w0 > kTraceMinWaitNs) trace_span(c, kTrEpiWait, t, w0, tt0);
+      trace_open(c, kTrEpiTile, t, tt0);
+    }
     // This CTA's 128 rows are rows [128 rank, 128 rank + 128) of the pair tile; the ops'
     // epilogues address row half h at taddr + 256 h, so offset the base by -256 rank.
     const uint32_t taddr = tmem_base + acc * Geo2::kAccStride + (static_cast<uint32_t>(q * 32) << 16) - rank * 256u;
@@ -195,6 +227,7 @@ __device__ __forceinline__ void pair_epilogue(const typename Op::Params& p, cons
       else
         mbar_arrive_cluster(tempty_leader0 + acc * 8u);
     }
+    if (tr && lane == 0) trace_close(c, globaltimer());
     if (++acc == Geo2::kAccBufs) {
       acc = 0;
       acc_phase ^= 1u;
@@ -204,7 +237,7 @@ __device__ __forceinline__ void pair_epilogue(const typename Op::Params& p, cons
   __syncwarp();
 }
 
-template <class Op>
+template <class Op, bool Trace>
 __global__ void __launch_bounds__(op_max_threads<Op>(), 1)
     persistent_kernel_pair(const __grid_constant__ typename Op::Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -222,12 +255,14 @@ __global__ void __launch_bounds__(op_max_threads<Op>(), 1)
   sm.drain = bars + 2 * Geo2::kStages + 4;
   sm.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * Geo2::kStages + 5);
   sm.epi_cnt = sm.tmem_slot + 2;
+  static_assert((2 * Geo2::kStages + 5) * 8 + 16 <= kBarBytes - 4 * kTraceWarps, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const int gi = static_cast<int>(blockIdx.x >> 1);
   const int gn = static_cast<int>(gridDim.x >> 1);
+  if constexpr (Trace) trace_begin();
   if (threadIdx.x == 0) {
     for (int s = 0; s < Geo2::kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -254,18 +289,19 @@ __global__ void __launch_bounds__(op_max_threads<Op>(), 1)
   const uint32_t tmem_base = *sm.tmem_slot;
 
   if (warp == 0) {
-    pair_producer<Op>(p, sm, lane, gi, gn, rank);
+    pair_producer<Op, Trace>(p, sm, lane, gi, gn, rank);
   } else if (warp == 1) {
-    pair_mma<Op>(p, sm, lane, tmem_base, gi, gn, rank);
+    pair_mma<Op, Trace>(p, sm, lane, tmem_base, gi, gn, rank);
   } else if (warp < 2 + Op::kEpiWarps) {
-    pair_epilogue<Op>(p, sm, warp, lane, tmem_base, gi, gn, rank);
+    pair_epilogue<Op, Trace>(p, sm, warp, lane, tmem_base, gi, gn, rank);
   } else {
-    Op::mover(p, warp - 2 - Op::kEpiWarps, lane);
+    Op::template mover<Trace>(p, warp - 2 - Op::kEpiWarps, lane);
   }
 
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the leader's MMAs are drained and both epilogues are done with TMEM
+  if constexpr (Trace) trace_end(p.common);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, kTmemCols);

@@ -121,6 +121,7 @@ struct AgParams {
 // shared with the epilogue warps, which are idle until their first tile: in every other
 // round of the head (g / grid odd) the mover warps copy, in the others the epilogue warps
 // (group = 1), so the head arrives up to twice as fast.
+template <bool Trace>
 __device__ __forceinline__ void ag_copy(const AgParams& p, int tid, int nthreads, int group, int bar) {
   const int per_shard = p.spr * p.chunks;
   const int total = group == 1 ? p.boost : p.W * per_shard;
@@ -133,14 +134,17 @@ __device__ __forceinline__ void ag_copy(const AgParams& p, int tid, int nthreads
     const int ch = rem - slab * p.chunks;
     const int r = ag_mover_rank(p.W, p.rank, p.swizzle, i);
     const size_t off = static_cast<size_t>(slab) * p.slab_bytes + static_cast<size_t>(ch) * chunk_bytes;
+    const uint64_t t0 = Trace ? globaltimer() : 0;
     mover_chunk(p.shard[r] + off, p.gath + static_cast<size_t>(r) * p.shard_bytes + off, chunk_bytes,
                 p.flags + (static_cast<size_t>(r) * p.spr + slab) * p.chunks + ch, g != p.skip_chunk, p.common, tid,
                 nthreads, bar);
+    if (Trace && tid == 0) trace_span(p.common, kTrMoverChunk, g, t0, globaltimer());
   }
 }
 
+template <bool Trace>
 __device__ __forceinline__ void ag_mover(const AgParams& p, int mw, int lane) {
-  ag_copy(p, mw * 32 + lane, p.common.mover_warps * 32, 0, 2);
+  ag_copy<Trace>(p, mw * 32 + lane, p.common.mover_warps * 32, 0, 2);
 }
 
 // Pair = true: 256-row tiles on a CTA pair (tl_engine2.cuh); this CTA owns rows and B
@@ -208,9 +212,13 @@ struct AgOp : OpBase<AgParams> {
       }
     }
   }
-  static __device__ void mover(const Params& p, int mw, int lane) { ag_mover(p, mw, lane); }
+  template <bool Trace>
+  static __device__ void mover(const Params& p, int mw, int lane) {
+    ag_mover<Trace>(p, mw, lane);
+  }
+  template <bool Trace>
   static __device__ void epilogue_prologue(const Params& p, int ew, int lane) {
-    if (p.boost > 0) ag_copy(p, ew * 32 + lane, kEpiWarps * 32, 1, 3);
+    if (p.boost > 0) ag_copy<Trace>(p, ew * 32 + lane, kEpiWarps * 32, 1, 3);
   }
 };
 
@@ -432,6 +440,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
   }
   // Every emulated rank r gathers the other ranks' X shards into its own copy of X
   // (rows r*T ..), in its swizzled order; rank 0's gather first.
+  template <bool Trace>
   static __device__ void mover(const Params& p, int mw, int lane) {
     const int nthreads = p.common.mover_warps * 32;
     const int tid = mw * 32 + lane;
@@ -462,7 +471,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
 // geometry, order and signals as the fused AllGather+GEMM, run by mover_warps warps in
 // each of the persistent CTAs.
 __global__ void __launch_bounds__(kMaxMoverWarps * 32) allgather_kernel(const __grid_constant__ AgParams p) {
-  ag_mover(p, threadIdx.x >> 5, threadIdx.x & 31);
+  ag_mover<false>(p, threadIdx.x >> 5, threadIdx.x & 31);
 }
 
 }  // namespace tl
@@ -699,6 +708,9 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   p.gath = ws;
   p.flags = reinterpret_cast<uint64_t*>(ws + align256(static_cast<size_t>(W) * m_per_rank * k * 2));
   p.common = make_common(ctx);
+  // The standalone mover kernel has no dynamic shared memory for span counters: no trace.
+  p.common.trace_hdr = nullptr;
+  p.common.trace = nullptr;
   for (int r = 0; r < W; ++r) p.shard[r] = static_cast<const uint8_t*>(a_shards[r]);
   p.W = W;
   p.rank = rank;

@@ -19,6 +19,9 @@ struct tl_ctx {
   tl_config cfg;
   tl::DevStatus* status;      // device status word (the only memory the library owns)
   unsigned long long epoch;   // last signal value handed out
+  void* trace_buf;            // caller-owned trace buffer (null: tracing off)
+  int trace_cap;              // spans per warp
+  int trace_ctas;             // CTAs the buffer holds
 };
 
 namespace tl {
@@ -39,16 +42,23 @@ inline Common make_common(tl_ctx* ctx) {
   c.epoch = next_epoch(ctx);
   c.timeout_ns = ctx->cfg.timeout_ns;
   c.mover_warps = ctx->cfg.mover_warps;  // clamped per op at launch (see launch_persistent)
+  c.trace_cap = ctx->trace_cap;
+  c.trace_ctas = ctx->trace_ctas;
+  c.trace_hdr = static_cast<unsigned int*>(ctx->trace_buf);
+  c.trace = ctx->trace_buf ? reinterpret_cast<TraceRec*>(static_cast<uint8_t*>(ctx->trace_buf) + 4 * kTraceHdrWords +
+                                                         4 * kTraceWarps * static_cast<size_t>(ctx->trace_ctas))
+                           : nullptr;
   return c;
 }
 
 int set_smem_attr(const void* kern);
 
 // Cooperative launch of one persistent CTA per SM (or cfg.grid_ctas), so that every CTA
-// that waits on a signal is co-resident with the CTAs that will set it.
+// that waits on a signal is co-resident with the CTAs that will set it.  While the context
+// has a trace buffer the span-recording instantiation runs.
 template <class Op>
 int launch_persistent(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t stream, int mover_warps) {
-  auto kern = persistent_kernel<Op>;
+  auto kern = ctx->trace_buf ? persistent_kernel<Op, true> : persistent_kernel<Op, false>;
   int rc = set_smem_attr(reinterpret_cast<const void*>(kern));
   if (rc != TL_OK) return rc;
   cudaLaunchConfig_t cfg;
@@ -83,7 +93,8 @@ int launch_persistent(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t st
 // cooperative attribute is not combined with clusters); every wait stays bounded.
 template <class Op>
 int launch_persistent_pair(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t stream, int mover_warps) {
-  auto kern = persistent_kernel_pair<Op>;
+  const int traced = ctx->trace_buf ? 1 : 0;
+  auto kern = traced ? persistent_kernel_pair<Op, true> : persistent_kernel_pair<Op, false>;
   int rc = set_smem_attr(reinterpret_cast<const void*>(kern));
   if (rc != TL_OK) return rc;
   if (mover_warps > Op::kMaxMovers) mover_warps = Op::kMaxMovers;
@@ -99,18 +110,18 @@ int launch_persistent_pair(tl_ctx* ctx, const typename Op::Params& p, cudaStream
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  static int max_clusters = -1;  // per kernel instantiation
-  if (max_clusters < 0) {
+  static int max_clusters[2] = {-1, -1};  // per kernel instantiation
+  if (max_clusters[traced] < 0) {
     cfg.gridDim = dim3(ctx->sms & ~1, 1, 1);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
       (void)cudaGetLastError();
       return TL_ERR_UNSUPPORTED;
     }
-    max_clusters = n;
+    max_clusters[traced] = n;
   }
   int nclusters = ctx->ctas / 2;
-  if (nclusters > max_clusters) nclusters = max_clusters;
+  if (nclusters > max_clusters[traced]) nclusters = max_clusters[traced];
   if (nclusters < 1) return TL_ERR_UNSUPPORTED;
   cfg.gridDim = dim3(2 * nclusters, 1, 1);
   typename Op::Params q = p;

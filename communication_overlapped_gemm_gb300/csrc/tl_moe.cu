@@ -200,7 +200,7 @@ struct MoeParams {
   float* out;
   uint64_t* up_flags;  // [R/128][n_up]
   uint64_t* y_flags;   // [R/128][n_down]
-  int T, H, E, F, topk, n_up, n_down, kb_up, kb_down, combine_ctas, chunk;
+  int T, H, E, F, topk, n_up, n_down, kb_up, kb_down, combine_ctas, chunk, lag;
 };
 
 struct MoeSlot {
@@ -241,18 +241,19 @@ struct MoeOp : OpBase<MoeParams> {
     return static_cast<int>(blockIdx.x) < gn;
   }
   // Tile order.  Row tiles (128 padded rows, expert-major) are grouped in chunks of
-  // p.chunk; the sequence is U0, U1, D0, U2, D1, ..., U_last, D_last-1, D_last where U_c
-  // are chunk c's up-projection tiles and D_c its down-projection tiles.  A down tile
-  // therefore comes after every up tile it waits on (no deadlock in a co-resident grid),
-  // one chunk of up work separates them, and down tiles (hence the combine partition's
-  // work) start early instead of after the whole up phase.  Inside a chunk the row tile
-  // is the fastest index, so the row tiles of one expert, which share its weight
-  // columns, run side by side.
+  // p.chunk; U_c are chunk c's up-projection tiles and D_c its down-projection tiles.  The
+  // sequence runs groups g = 0, 1, ...: group g is U_g (while g < chunks) followed by
+  // D_{g - lag} (once g >= lag), so U_0 .. U_{lag-1} lead and D_{last-lag+1} .. D_last trail.
+  // A down tile therefore comes after every up tile it waits on (no deadlock in a
+  // co-resident grid), `lag` chunks of up work separate a down chunk from the up tiles it
+  // reads, and down tiles (hence the combine partition's work) start early instead of
+  // after the whole up phase.  Inside a chunk the row tile is the fastest index, so the
+  // row tiles of one expert, which share its weight columns, run side by side.
   static __device__ MoeSlot slot(const Params& p, int m, int t) {
     const int G = p.chunk;
     const int nc = (m + G - 1) / G;
     int pos = 0;
-    for (int sg = 0; sg <= nc; ++sg) {
+    for (int sg = 0; sg < nc + p.lag; ++sg) {
       if (sg < nc) {
         const int gc = min(G, m - sg * G);
         const int sz = gc * p.n_up;
@@ -262,8 +263,8 @@ struct MoeOp : OpBase<MoeParams> {
         }
         pos += sz;
       }
-      if (sg >= 1) {
-        const int c = sg - 1;
+      if (sg >= p.lag) {
+        const int c = sg - p.lag;
         const int gc = min(G, m - c * G);
         const int sz = gc * p.n_down;
         if (t < pos + sz) {
@@ -378,6 +379,7 @@ struct MoeOp : OpBase<MoeParams> {
   // [4l, 4l+4) and [128+4l, 128+4l+4) by the gate and adds them into out[token] with two
   // fp32 vector reductions, so each warp instruction covers 512 contiguous bytes of the
   // output row.  While one half waits for its load the other reduces.
+  template <bool Trace>
   static __device__ void side_role(const Params& p, int warp, int lane, uint8_t* smem_raw) {
     uint8_t* base =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -403,8 +405,14 @@ struct MoeOp : OpBase<MoeParams> {
     for (int v = 2 * cc + half; v < total; v += 2 * p.combine_ctas) {
       const MoeSlot sl = down_slot(p, m, v);
       if (hw == 0) {
+        const uint64_t w0 = Trace ? globaltimer() : 0;
         warp_wait_one(p.y_flags + static_cast<size_t>(sl.i) * p.n_down + sl.nb, p.common.epoch, p.common, lane,
                       kSiteCombine, (4ull << 60) | v);
+        if (Trace && lane == 0) {
+          const uint64_t w1 = globaltimer();
+          if (w1 - w0 > kTraceMinWaitNs) trace_span(p.common, kTrSideWait, v, w0, w1);
+          trace_open(p.common, kTrSideTile, v, w0);
+        }
         if (lane == 0) {
           mbar_arrive_expect_tx(bar, kTileBytes);
 #pragma unroll
@@ -437,6 +445,7 @@ struct MoeOp : OpBase<MoeParams> {
         red_add_v4(o + 128, gt * fc.x, gt * fc.y, gt * fd.x, gt * fd.y);
       }
       named_bar_sync(1 + half, 128);  // the tile buffer and records are free for the next tile
+      if (Trace && hw == 0 && lane == 0) trace_close(p.common, globaltimer());
     }
   }
 };
@@ -552,7 +561,8 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   p.kb_up = H / kBK;
   p.kb_down = F / kBK;
   p.combine_ctas = ctx->cfg.combine_ctas;
-  p.chunk = 8;
+  p.chunk = 4;  // row tiles per chunk
+  p.lag = 4;    // chunks of up work ahead of the down chunk that reads them
   // Two extra warps per CTA: idle in the GEMM partition, combine workers in the combine CTAs.
   return launch_persistent<MoeOp>(ctx, p, st, 2);
 }

@@ -113,6 +113,39 @@ int tl_version(void);
 /* Number of SMs / persistent CTAs the context launches with. */
 int tl_ctx_num_ctas(const tl_ctx* ctx);
 
+/* ---------------------------------------------------------------- trace buffer
+ * A per-CTA timeline of the persistent kernels.  Every warp role records spans into a
+ * caller-owned device buffer.  A span is a %globaltimer start, a duration in ns, and a kind
+ * plus a tile or chunk index.  The pages name no such facility.  It shows where a fused kernel
+ * waits: a mover chunk landing, a tile waiting on its signal, the MMA warp starved of data.
+ *
+ * tl_trace_bytes(ctas, spans_per_warp): bytes a buffer needs to hold `ctas` CTAs.
+ * tl_ctx_set_trace(ctx, buf, bytes, spans_per_warp): every later persistent-kernel launch on
+ *   ctx records into buf.  buf is device memory, 16-byte aligned and caller-owned; it must stay
+ *   valid while such launches run.  buf NULL turns tracing off.  Each launch overwrites the
+ *   previous trace.  CTAs beyond what `bytes` holds are not recorded.  Spans beyond
+ *   spans_per_warp are dropped, but the per-warp count still counts them.
+ *   Returns TL_ERR_INVALID for a null ctx, a misaligned buf, a size below
+ *   tl_trace_bytes(1, spans_per_warp), or spans_per_warp < 1.
+ * Layout (little-endian), written by the kernels:
+ *   uint32 header[8]: magic 0x544c5452, version 1, grid of the last launch, warps per CTA (16),
+ *                     spans per warp, CTAs held, 0, 0
+ *   uint32 count[CTAs held][16]: spans each warp recorded (may exceed spans per warp)
+ *   span[CTAs held][16][spans per warp], 16 bytes each: uint64 t0_ns, uint32 dur_ns,
+ *                     uint32 tag = kind << 24 | index
+ * Kinds:
+ *   1 producer tile; 2 producer signal wait; 3 producer ring-stall total (t0 = tile start);
+ *   4 MMA tile; 5 MMA starve total (t0 = tile start); 6 MMA accumulator wait;
+ *   7 epilogue tile; 8 epilogue accumulator wait;
+ *   9 mover chunk; 10 side-partition unit (from the start of its wait); 11 side-partition wait.
+ * Waits shorter than 200 ns are not recorded.
+ * Warp w of a GEMM CTA: 0 producer, 1 MMA, 2.. epilogue, then the movers.  In a side partition
+ * (the MoE combine CTAs) warps 0 and 4 record.  Only the persistent kernels trace.  While on,
+ * tracing costs a few timer reads per tile and k-block.
+ */
+size_t tl_trace_bytes(int ctas, int spans_per_warp);
+int tl_ctx_set_trace(tl_ctx* ctx, void* buf, size_t bytes, int spans_per_warp);
+
 /* ---------------------------------------------------------------- AllGather + GEMM
  * [TL] §2.1, [TD] §3.2 Algorithm 2 (pull mode) and §3.7 (AG+GEMM swizzle).
  *
