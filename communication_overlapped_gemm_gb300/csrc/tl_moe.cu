@@ -233,7 +233,10 @@ struct MoeOp : OpBase<MoeParams> {
   static constexpr int kBM = 128;
   static constexpr int kMaxMovers = 2;  // the combine partition's CTAs use these two warps
   static constexpr uint32_t kTxBytes = Geo<128>::kStageBytes;
-  static __device__ int mtiles(const Params& p) { return *reinterpret_cast<const volatile int*>(p.num_mtiles); }
+  // The tile count and tile table come from the permutation kernel, which completed
+  // before this kernel started: read-only for this kernel, so they go through the
+  // non-coherent cache (one L2 trip per SM, then L1 hits).
+  static __device__ int mtiles(const Params& p) { return __ldg(p.num_mtiles); }
   static __device__ int num_tiles(const Params& p) { return mtiles(p) * (p.n_up + p.n_down); }
   static __device__ bool gemm_partition(const Params& p, int& gi, int& gn) {
     gn = gridDim.x - p.combine_ctas;
@@ -249,32 +252,36 @@ struct MoeOp : OpBase<MoeParams> {
   // reads, and down tiles (hence the combine partition's work) start early instead of
   // after the whole up phase.  Inside a chunk the row tile is the fastest index, so the
   // row tiles of one expert, which share its weight columns, run side by side.
+  // Tiles before group g: the up tiles of chunks 0 .. min(g, nc) - 1 and the down tiles of
+  // chunks 0 .. g - lag - 1 (every chunk holds G row tiles but the last, which holds
+  // m - (nc - 1) G).
+  static __device__ __forceinline__ int rows_before(int c, int m, int G) { return min(c * G, m); }
+  static __device__ __forceinline__ int group_start(const Params& p, int m, int nc, int g) {
+    const int cu = min(g, nc), cd = max(0, min(g - p.lag, nc));
+    return rows_before(cu, m, p.chunk) * p.n_up + rows_before(cd, m, p.chunk) * p.n_down;
+  }
   static __device__ MoeSlot slot(const Params& p, int m, int t) {
     const int G = p.chunk;
     const int nc = (m + G - 1) / G;
-    int pos = 0;
-    for (int sg = 0; sg < nc + p.lag; ++sg) {
-      if (sg < nc) {
-        const int gc = min(G, m - sg * G);
-        const int sz = gc * p.n_up;
-        if (t < pos + sz) {
-          const int w = t - pos;
-          return MoeSlot{1, sg * G + w % gc, w / gc};
-        }
-        pos += sz;
-      }
-      if (sg >= p.lag) {
-        const int c = sg - p.lag;
-        const int gc = min(G, m - c * G);
-        const int sz = gc * p.n_down;
-        if (t < pos + sz) {
-          const int w = t - pos;
-          return MoeSlot{2, c * G + w % gc, w / gc};
-        }
-        pos += sz;
-      }
+    // the last group g with group_start(g) <= t (binary search over g in [0, nc + lag))
+    int lo = 0, hi = nc + p.lag - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (group_start(p, m, nc, mid) <= t)
+        lo = mid;
+      else
+        hi = mid - 1;
     }
-    return MoeSlot{2, 0, 0};  // t beyond the sequence: never requested
+    const int g = lo;
+    int w = t - group_start(p, m, nc, g);
+    if (g < nc) {
+      const int gc = min(G, m - g * G);
+      if (w < gc * p.n_up) return MoeSlot{1, g * G + w % gc, w / gc};
+      w -= gc * p.n_up;
+    }
+    const int c = g - p.lag;
+    const int gc = min(G, m - c * G);
+    return MoeSlot{2, c * G + w % gc, w / gc};
   }
   // The v-th down-projection tile in production order (the combine partition's order).
   static __device__ MoeSlot down_slot(const Params& p, int m, int v) {
@@ -300,7 +307,7 @@ struct MoeOp : OpBase<MoeParams> {
     j.a_sel = 0;
     j.b_sel = 0;
     j.a_row = j.x0 * kBM;
-    j.b_z = p.tile_expert[j.x0];
+    j.b_z = __ldg(p.tile_expert + j.x0);
     j.x2 = 0;
     j.x3 = 0;
     return j;

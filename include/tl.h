@@ -77,7 +77,7 @@ typedef struct tl_config {
   int chunks_per_slab;        /* mover chunks, hence signals, per 128-row slab (1..32; default 32)     */
   int swizzle;                /* 0: identity tile order; 1: rank-swizzled ([TD] §3.7; default)          */
   int grid_ctas;              /* persistent CTAs; 0 = one per SM (default)                              */
-  int combine_ctas;           /* MoE combine partition, CTAs = SMs ([RA]; default 8)                    */
+  int combine_ctas;           /* MoE combine partition, CTAs = SMs ([RA]; default 16)                   */
   int debug_skip_chunk;       /* fault injection: this mover chunk is copied but never signalled (-1 off) */
   unsigned long long timeout_ns; /* bound of every device wait (default 2e9 ns)                       */
   int pair_ctas;              /* where shards / owner blocks are 256-row multiples, 256 x 256 tiles run
