@@ -65,21 +65,31 @@ struct RsTile {
   int nb;  // column block
 };
 
-// GEMM + ReduceScatter: producers in order p = 0..W-1; each walks W owners of
-// (mbo row blocks x nbk column blocks).
+// GEMM + ReduceScatter: producers in order p = 0..W-1 (the fixed fp32 summation order).
+// Producer p walks its W owners in the order (p + 1 + s) mod W, s = 0..W-1, taken in groups
+// of kRsOwnerGroup consecutive owners.  Inside a group the column block is the slowest
+// index and the owner's row block the fastest, so the tiles that run at the same time
+// share a few column slabs of B_p and the group's rows of A_p: B_p is read once per owner
+// group rather than once per wave of tiles.  Owners still come first in the rotated order,
+// the producer's own rows in the last group.
+constexpr int kRsOwnerGroup = 4;
 TL_HD int rs_num_tiles(int W, int mbo, int nbk) { return W * W * mbo * nbk; }
 TL_HD int rs_owner(int W, int p, int s, int swizzle) { return swizzle ? (p + 1 + s) % W : s; }
 TL_HD RsTile rs_tile(int t, int W, int mbo, int nbk, int swizzle) {
-  const int per_owner = mbo * nbk;
-  const int per_prod = W * per_owner;
+  const int per_prod = W * mbo * nbk;
   RsTile r;
   r.p = t / per_prod;
   int rem = t - r.p * per_prod;
-  const int s = rem / per_owner;
-  rem -= s * per_owner;
+  const int full_group = kRsOwnerGroup * mbo * nbk;  // tiles of a group of kRsOwnerGroup owners
+  const int g = rem / full_group;                     // every group but the last is full
+  rem -= g * full_group;
+  const int s0 = g * kRsOwnerGroup;
+  const int gsz = W - s0 < kRsOwnerGroup ? W - s0 : kRsOwnerGroup;  // owners in this group
+  r.nb = rem / (gsz * mbo);
+  rem -= r.nb * gsz * mbo;
+  const int s = s0 + rem / mbo;
+  r.mb = rem - (s - s0) * mbo;
   r.o = rs_owner(W, r.p, s, swizzle);
-  r.mb = rem / nbk;
-  r.nb = rem - r.mb * nbk;
   return r;
 }
 

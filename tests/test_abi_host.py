@@ -109,7 +109,7 @@ def test_ag_tile_order_is_rank_swizzled_and_matches_static_map(tl, W, rank, mpr,
     assert s0[:per].tolist() == [0] * per  # identity order starts at rank 0
 
 
-@pytest.mark.parametrize("W,m,n", [(8, 8192, 8192), (4, 1024, 520), (1, 128, 256)])
+@pytest.mark.parametrize("W,m,n", [(8, 8192, 8192), (4, 1024, 520), (1, 128, 256), (6, 1536, 768), (5, 640, 300)])
 def test_rs_tile_order_producer_major_owner_swizzled(tl, W, m, n):
     p, o, mb, nb = tl.tl_rs_tile_order(W, m, n, 1)
     bm = 256 if (m // W) % 256 == 0 else 128
@@ -117,12 +117,24 @@ def test_rs_tile_order_producer_major_owner_swizzled(tl, W, m, n):
     assert len(p) == W * W * mbo * nbk
     assert len(set(zip(p.tolist(), o.tolist(), mb.tolist(), nb.tolist()))) == len(p)
     assert np.all(np.diff(p) >= 0)  # producers visited 0..W-1 (fixed fp32 summation order)
-    per_owner = mbo * nbk
+    G = 4  # owners per group
     for q in range(W):
-        seq = o[p == q][::per_owner].tolist()
-        assert seq == [(q + 1 + s) % W for s in range(W)]  # next rank's rows first, own rows last
+        oq, nq, mq = o[p == q], nb[p == q], mb[p == q]
+        rot = [(q + 1 + s) % W for s in range(W)]
+        first = list(dict.fromkeys(oq.tolist()))
+        assert first == rot  # next rank's rows first, own rows last
+        # groups of G owners in rotated order; inside a group the column block is the slowest
+        # index and the row block the fastest
+        pos = 0
+        for g0 in range(0, W, G):
+            grp = rot[g0:g0 + G]
+            size = len(grp) * mbo * nbk
+            exp = [(grp[s], r * (bm // 128), c) for c in range(nbk) for s in range(len(grp)) for r in range(mbo)]
+            got = list(zip(oq[pos:pos + size].tolist(), mq[pos:pos + size].tolist(), nq[pos:pos + size].tolist()))
+            assert got == exp
+            pos += size
     p0, o0, _, _ = tl.tl_rs_tile_order(W, m, n, 0)
-    assert o0[p0 == 0][::per_owner].tolist() == list(range(W))
+    assert list(dict.fromkeys(o0[p0 == 0].tolist())) == list(range(W))
 
 
 def test_tile_order_rejects_bad_shapes(tl):
