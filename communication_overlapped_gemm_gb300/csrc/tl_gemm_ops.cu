@@ -153,7 +153,9 @@ template <int BM, bool Pair = false>
 struct AgOp : OpBase<AgParams> {
   using Params = AgParams;
   static constexpr int kBM = BM;
-  static constexpr int kEpiWarps = 4;  // light bf16 epilogue
+  // bf16 epilogue; the single-CTA 256-row tile has one accumulator, so its epilogue stalls the
+  // next tile's MMAs: 8 warps (one warpgroup per 128-row half) drain it twice as fast.
+  static constexpr int kEpiWarps = (BM == 256 && !Pair) ? 8 : 4;
   static constexpr int kMaxMovers = 4;
   static constexpr uint32_t kTxBytes = Pair ? Geo2::kStageBytes : Geo<BM>::kStageBytes;
   static __device__ int num_tiles(const Params& p) { return ag_num_tiles(p.W, p.mps, p.nbk); }

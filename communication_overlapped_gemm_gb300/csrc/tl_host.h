@@ -61,8 +61,7 @@ int launch_persistent(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t st
   auto kern = ctx->trace_buf ? persistent_kernel<Op, true> : persistent_kernel<Op, false>;
   int rc = set_smem_attr(reinterpret_cast<const void*>(kern));
   if (rc != TL_OK) return rc;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctx->ctas, 1, 1);
   if (mover_warps > Op::kMaxMovers) mover_warps = Op::kMaxMovers;
   cfg.blockDim = dim3((2 + Op::kEpiWarps + mover_warps) * 32, 1, 1);
@@ -98,8 +97,7 @@ int launch_persistent_pair(tl_ctx* ctx, const typename Op::Params& p, cudaStream
   int rc = set_smem_attr(reinterpret_cast<const void*>(kern));
   if (rc != TL_OK) return rc;
   if (mover_warps > Op::kMaxMovers) mover_warps = Op::kMaxMovers;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3((2 + Op::kEpiWarps + mover_warps) * 32, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;

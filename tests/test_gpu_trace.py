@@ -64,7 +64,7 @@ def test_trace_ag_gemm_tiles_and_chunks():
         ntiles = 4 * 1 * 3  # W x 256-row blocks per shard x 256-column blocks
         once_each(sp, 4, ntiles)          # MMA tile
         once_each(sp, 1, ntiles)          # producer tile
-        once_each(sp, 7, ntiles, per=4)   # epilogue tile, 4 epilogue warps
+        once_each(sp, 7, ntiles, per=8)   # epilogue tile, 8 epilogue warps (one warpgroup per row half)
         once_each(sp, 9, 4 * 2 * 32)      # mover chunk: W x 128-row slabs x chunks
         assert set(sp["warp"][sp["kind"] == 4].tolist()) == {1}
         assert set(sp["warp"][sp["kind"] == 1].tolist()) == {0}
