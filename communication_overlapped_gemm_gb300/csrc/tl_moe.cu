@@ -84,14 +84,12 @@ __global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E,
 // offsets without a grid-wide step), then ranks the assignments of its own expert in
 // (t, j) order with a block-wide ballot scan.  Outputs:
 //   perm[off_e + pos] = a                      (unpadded order: expert, t, j)
-//   row_assign[poff_e + pos] = a, -1 on padding rows of the expert's 128-row-aligned segment
 //   row_meta[row] = {token, gate bits} of the row's assignment ({-1, 0} on padding rows), so
 //     the combine reads one 8-byte record per row instead of two dependent loads
 //   tile_expert / tile_rows for each 128-row tile of the padded layout (the f_R / f_S tables)
 __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict__ experts, int n, int E, int topk,
                                                            const float* __restrict__ gates,
-                                                           int* __restrict__ perm, int* __restrict__ row_assign,
-                                                           int2* __restrict__ row_meta,
+                                                           int* __restrict__ perm, int2* __restrict__ row_meta,
                                                            int* __restrict__ tile_expert, int* __restrict__ tile_rows,
                                                            int* __restrict__ num_mtiles, int* __restrict__ counts,
                                                            int* __restrict__ perm_out, int* __restrict__ counts_out) {
@@ -142,7 +140,6 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
       const int pos = running + warp_pre[warp] + __popc(ball & ((1u << lane) - 1u));
       perm[off[e] + pos] = a;
       if (perm_out) perm_out[off[e] + pos] = a;
-      row_assign[poff[e] + pos] = a;
       row_meta[poff[e] + pos] = make_int2(a / topk, __float_as_int(gates[a]));
     }
     const int tot = warp_tot[0];
@@ -152,7 +149,6 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
   const int cnt = hist[e];
   const int padded = poff[e + 1] - poff[e];
   for (int i = cnt + tid; i < padded; i += blockDim.x) {
-    row_assign[poff[e] + i] = -1;
     row_meta[poff[e] + i] = make_int2(-1, 0);
   }
   for (int i = tid; i < padded / kBM; i += blockDim.x) {
@@ -165,20 +161,6 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
     if (counts_out) counts_out[e] = cnt;
     if (e == 0) *num_mtiles = poff[E] / kBM;
   }
-}
-
-// ---------------------------------------------------------------------------- gather
-// One warp per padded row: Xp[row] = x[token of row_assign[row]] (zeros on padding rows).
-__global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, int H, int topk,
-                                  const int* __restrict__ row_assign, const int* __restrict__ num_mtiles,
-                                  __nv_bfloat16* __restrict__ xp) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (row >= *num_mtiles * kBM) return;
-  const int a = row_assign[row];
-  const uint4* src = a >= 0 ? reinterpret_cast<const uint4*>(x + static_cast<size_t>(a / topk) * H) : nullptr;
-  uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(row) * H);
-  for (int c = lane; c < H / 8; c += 32) dst[c] = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
 }
 
 // ---------------------------------------------------------------------------- grouped GEMMs + combine
@@ -196,12 +178,18 @@ struct MoeParams {
   const int* tile_expert;
   const int* tile_rows;
   const int2* row_meta;
+  const __nv_bfloat16* x;  // tokens, gathered into xp by the mover warps
+  __nv_bfloat16* xp_rows;  // the gathered rows (xp's memory)
+  uint64_t* x_flags;       // [R/128][kGatherPieces]: piece of a row tile gathered
   const __nv_bfloat16* y;
   float* out;
   uint64_t* up_flags;  // [R/128][n_up]
   uint64_t* y_flags;   // [R/128][n_down]
   int T, H, E, F, topk, n_up, n_down, kb_up, kb_down, combine_ctas, chunk, lag;
 };
+
+constexpr int kGatherRows = 4;                  // rows one mover warp gathers per signal
+constexpr int kGatherPieces = kBM / kGatherRows;  // signals per 128-row tile
 
 struct MoeSlot {
   int kind;  // 1 up-projection, 2 down-projection
@@ -231,7 +219,9 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 struct MoeOp : OpBase<MoeParams> {
   using Params = MoeParams;
   static constexpr int kBM = 128;
-  static constexpr int kMaxMovers = 2;  // the combine partition's CTAs use these two warps
+  // Two extra warps per CTA: the token gather (mover) in GEMM CTAs, combine workers in the
+  // combine partition's CTAs.
+  static constexpr int kMaxMovers = 2;
   static constexpr uint32_t kTxBytes = Geo<128>::kStageBytes;
   // The tile count and tile table come from the permutation kernel, which completed
   // before this kernel started: read-only for this kernel, so they go through the
@@ -319,12 +309,60 @@ struct MoeOp : OpBase<MoeParams> {
     tma_prefetch_map(&p.wd);
     tma_prefetch_map(&p.h_ld);
   }
-  // consumer_tile_wait: a down-projection tile reads its row tile of h only after all
-  // n_up up-projection tiles of that row tile have signalled.
+  // consumer_tile_wait: an up-projection tile reads its 128 gathered rows only after the
+  // mover has released all of the row tile's pieces; a down-projection tile reads its row
+  // tile of h only after all n_up up-projection tiles of that row tile have signalled.
   static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
-    if (kb != 0 || j.kind != 2) return;
-    warp_wait_signals(p.up_flags + static_cast<size_t>(j.x0) * p.n_up, p.n_up, p.common.epoch, p.common, lane,
-                      kSiteSignal, (3ull << 60) | j.x0);
+    if (kb != 0) return;
+    if (j.kind == 1)
+      warp_wait_signals(p.x_flags + static_cast<size_t>(j.x0) * kGatherPieces, kGatherPieces, p.common.epoch,
+                        p.common, lane, kSiteSignal, (5ull << 60) | j.x0);
+    else
+      warp_wait_signals(p.up_flags + static_cast<size_t>(j.x0) * p.n_up, p.n_up, p.common.epoch, p.common, lane,
+                        kSiteSignal, (3ull << 60) | j.x0);
+  }
+  // The token gather (the "Gather" before the grouped GEMM, overlapped with it): padded row
+  // r of xp receives x[token of r] (zeros on padding rows).  Pieces of kGatherRows rows are
+  // dealt to the GEMM CTAs' mover warps in row order, so the first chunks' rows come first;
+  // each piece is published with its own release signal.
+  template <bool Trace>
+  static __device__ void mover(const Params& p, int mw, int lane) {
+    const int nw = (static_cast<int>(gridDim.x) - p.combine_ctas) * p.common.mover_warps;
+    const int total = mtiles(p) * kGatherPieces;
+    const int vec_row = p.H / 8;  // 16-byte vectors per row
+    for (int q = blockIdx.x * p.common.mover_warps + mw; q < total; q += nw) {
+      const uint64_t t0 = Trace ? globaltimer() : 0;
+#pragma unroll 1
+      for (int r = q * kGatherRows; r < (q + 1) * kGatherRows; ++r) {
+        const int tok = __ldg(&p.row_meta[r].x);
+        uint4* dst = reinterpret_cast<uint4*>(p.xp_rows + static_cast<size_t>(r) * p.H);
+        if (tok >= 0) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(tok) * p.H);
+#pragma unroll 1
+          for (int c0 = 0; c0 < vec_row; c0 += 8 * 32) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int c = c0 + u * 32 + lane;
+              if (c < vec_row) v[u] = __ldg(src + c);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int c = c0 + u * 32 + lane;
+              if (c < vec_row) dst[c] = v[u];
+            }
+          }
+        } else {
+          for (int c = lane; c < vec_row; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) {
+        st_release_gpu(p.x_flags + q, p.common.epoch);
+        if (Trace) trace_span(p.common, kTrMoverChunk, q, t0, globaltimer());
+      }
+    }
   }
   static __device__ void load(const Params& p, const Job& j, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
     if (j.kind == 1) {
@@ -355,7 +393,10 @@ struct MoeOp : OpBase<MoeParams> {
         tmem_ld64(taddr, ch * 64, g);
         tmem_ld64(taddr, 128 + ch * 64, u);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) g[i] = g[i] / (1.0f + expf(-g[i])) * u[i];
+        // SiLU(g) * u with the fast exp and divide intrinsics (a few ulp in fp32, far below
+        // the bf16 rounding of h): the IEEE expf and division made this epilogue as long as
+        // the tile's MMAs.  Very negative g gives an infinite or > 2^126 divisor and 0.
+        for (int i = 0; i < 64; ++i) g[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
         store_bf16_chunk(&p.h_st, es, lane, g, j.b_col + ch * 64, row);
       }
     } else {
@@ -465,8 +506,8 @@ using namespace tl;
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct MoeLayout {
-  size_t experts, gates, perm, row_assign, row_meta, tile_expert, tile_rows, num_mtiles, counts, xp, h, y, up_flags, y_flags,
-      total;
+  size_t experts, gates, perm, row_meta, tile_expert, tile_rows, num_mtiles, counts, xp, h, y, up_flags, y_flags,
+      x_flags, total;
   int rmax;
 };
 
@@ -480,7 +521,6 @@ static MoeLayout moe_layout(int T, int H, int E, int F, int topk) {
   L.experts = o; o += al256(n * 4);
   L.gates = o; o += al256(n * 4);
   L.perm = o; o += al256(n * 4);
-  L.row_assign = o; o += al256(static_cast<size_t>(L.rmax) * 4);
   L.row_meta = o; o += al256(static_cast<size_t>(L.rmax) * 8);
   L.tile_expert = o; o += al256(tiles * 4);
   L.tile_rows = o; o += al256(tiles * 4);
@@ -491,6 +531,7 @@ static MoeLayout moe_layout(int T, int H, int E, int F, int topk) {
   L.y = o; o += al256(static_cast<size_t>(L.rmax) * H * 2);
   L.up_flags = o; o += al256(tiles * (F / 128) * 8);
   L.y_flags = o; o += al256(tiles * (H / kBN) * 8);
+  L.x_flags = o; o += al256(tiles * kGatherPieces * 8);
   L.total = o;
   return L;
 }
@@ -524,7 +565,6 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   int* experts = reinterpret_cast<int*>(ws + L.experts);
   float* gates = reinterpret_cast<float*>(ws + L.gates);
   int* perm = reinterpret_cast<int*>(ws + L.perm);
-  int* row_assign = reinterpret_cast<int*>(ws + L.row_assign);
   int2* row_meta = reinterpret_cast<int2*>(ws + L.row_meta);
   int* tile_expert = reinterpret_cast<int*>(ws + L.tile_expert);
   int* tile_rows = reinterpret_cast<int*>(ws + L.tile_rows);
@@ -535,10 +575,8 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
 
   moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, experts, gates, out, H);
-  moe_permute_kernel<<<E, 1024, 0, st>>>(experts, T * topk, E, topk, gates, perm, row_assign, row_meta, tile_expert, tile_rows, num_mtiles,
+  moe_permute_kernel<<<E, 1024, 0, st>>>(experts, T * topk, E, topk, gates, perm, row_meta, tile_expert, tile_rows, num_mtiles,
                                          counts, perm_out, counts_out);
-  moe_gather_kernel<<<(L.rmax + 7) / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), H, topk, row_assign,
-                                                      num_mtiles, xp);
   if (cudaGetLastError() != cudaSuccess) return TL_ERR_CUDA;
 
   MoeParams p;
@@ -554,6 +592,9 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   p.tile_expert = tile_expert;
   p.tile_rows = tile_rows;
   p.row_meta = row_meta;
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.xp_rows = xp;
+  p.x_flags = reinterpret_cast<uint64_t*>(ws + L.x_flags);
   p.y = yb;
   p.out = out;
   p.up_flags = reinterpret_cast<uint64_t*>(ws + L.up_flags);
@@ -568,8 +609,9 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   p.kb_up = H / kBK;
   p.kb_down = F / kBK;
   p.combine_ctas = ctx->cfg.combine_ctas;
-  p.chunk = 4;  // row tiles per chunk
-  p.lag = 4;    // chunks of up work ahead of the down chunk that reads them
-  // Two extra warps per CTA: idle in the GEMM partition, combine workers in the combine CTAs.
+  p.chunk = 2;  // row tiles per chunk
+  p.lag = 6;    // chunks of up work ahead of the down chunk that reads them
+  // Two extra warps per CTA: the token gather in the GEMM partition, combine workers in the
+  // combine CTAs.
   return launch_persistent<MoeOp>(ctx, p, st, 2);
 }
