@@ -85,6 +85,12 @@ typedef struct tl_config {
                                  every op; 2 (default) CTA pairs for tl_gemm_rs and tl_mlp2, whose
                                  heavier epilogues gain from the pair's double-buffered
                                  accumulators, single CTAs for tl_ag_gemm                           */
+  int copy_engine;            /* AllGather transport of tl_ag_gemm / tl_allgather: 0 (default) mover
+                                 warps inside the persistent CTAs; 1 the copy engine: one
+                                 cudaMemcpyAsync per shard on a context-owned side stream, then a
+                                 stream write of each of the shard's 128-row slab signals ([TL] §7.2
+                                 maps the AllGather to DMA).  The caller's stream waits for the side
+                                 stream before the call's work completes.                            */
 } tl_config;
 
 typedef struct tl_ctx tl_ctx;
@@ -160,6 +166,8 @@ int tl_ctx_set_trace(tl_ctx* ctx, void* buf, size_t bytes, int spans_per_warp);
  * shards (rank+1) mod W, (rank+2) mod W, ... into T in that order (its own shard last), and the
  * GEMM visits row blocks of shard rank first, then (rank+1) mod W, ... waiting on each slab's
  * signals before its first load.  The result does not depend on `rank` or the swizzle.
+ * W = 1 has nothing to gather: the call is the plain GEMM on shard 0, read in place, and the
+ * gathered region of the workspace is not written.
  * Shapes: 1 <= W <= 8; m_per_rank % 128 == 0; n % 8 == 0; k % 8 == 0 (n, k need not be
  * tile multiples: ragged edges are zero-filled by TMA on load and clipped on store).
  * Any zero dimension is a no-op returning TL_OK.
@@ -173,8 +181,8 @@ int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const 
  * tl_ag_gemm (same chunks, order and signals) without the GEMM, run by cfg.mover_warps warps
  * in each persistent CTA.  Fills the gathered buffer at the start of `workspace` (sized by
  * tl_ag_gemm_workspace_bytes(W, m_per_rank, 8, k)) with [A_0; ...; A_{W-1}] and releases every
- * chunk signal.  Shapes and errors as tl_ag_gemm.  This is the "communication alone" leg of
- * the overlap measurement.
+ * chunk signal.  Shapes and errors as tl_ag_gemm; W = 1 is a no-op.  This is the
+ * "communication alone" leg of the overlap measurement.
  */
 int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_shards, void* workspace, size_t workspace_bytes,
                  int m_per_rank, int k, tl_stream_t stream);
