@@ -116,35 +116,43 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
     }
   }
   __syncthreads();
-  int running = 0;
+  // Stable ranks of this expert's assignments in one pass: warp w takes the contiguous
+  // slice [w * seg, (w + 1) * seg) of the assignments, counts its matches, an exclusive scan
+  // over the warps' counts gives each warp its first position, and each warp then writes its
+  // matches in order (two block barriers in all).
   const int nw = blockDim.x >> 5;
-  for (int base = 0; base < n; base += blockDim.x) {
-    const int a = base + tid;
-    const bool mine = a < n && experts[a] == e;
-    const uint32_t ball = __ballot_sync(0xffffffffu, mine);
-    if (lane == 0) warp_tot[warp] = __popc(ball);
-    __syncthreads();
-    if (warp == 0) {
-      const int v = lane < nw ? warp_tot[lane] : 0;
-      int incl = v;
+  const int seg = ((n + nw - 1) / nw + 31) & ~31;
+  const int s0 = warp * seg, s1 = min(n, s0 + seg);
+  int mine_cnt = 0;
+  for (int a0 = s0; a0 < s1; a0 += 32) {
+    const int a = a0 + lane;
+    mine_cnt += __popc(__ballot_sync(0xffffffffu, a < s1 && experts[a] == e));
+  }
+  if (lane == 0) warp_tot[warp] = mine_cnt;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < nw ? warp_tot[lane] : 0;
+    int incl = v;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      warp_pre[lane] = incl - v;
-      if (lane == 31) warp_tot[0] = incl;  // block total (read after the barrier)
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
     }
-    __syncthreads();
+    warp_pre[lane] = incl - v;
+  }
+  __syncthreads();
+  int running = warp_pre[warp];
+  for (int a0 = s0; a0 < s1; a0 += 32) {
+    const int a = a0 + lane;
+    const bool mine = a < s1 && experts[a] == e;
+    const uint32_t ball = __ballot_sync(0xffffffffu, mine);
     if (mine) {
-      const int pos = running + warp_pre[warp] + __popc(ball & ((1u << lane) - 1u));
+      const int pos = running + __popc(ball & ((1u << lane) - 1u));
       perm[off[e] + pos] = a;
       if (perm_out) perm_out[off[e] + pos] = a;
       row_meta[poff[e] + pos] = make_int2(a / topk, __float_as_int(gates[a]));
     }
-    const int tot = warp_tot[0];
-    __syncthreads();
-    running += tot;
+    running += __popc(ball);
   }
   const int cnt = hist[e];
   const int padded = poff[e + 1] - poff[e];
