@@ -37,8 +37,17 @@ __device__ __forceinline__ void mover_chunk(const uint8_t* src, uint8_t* dst, si
   if (tid == 0 && signal) st_release_gpu(flag, c.epoch);
 }
 
-// Exact GELU, 0.5 x (1 + erf(x / sqrt 2)).
-__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+// Exact-form GELU, 0.5 x (1 + erf(x / sqrt 2)), with erf from Abramowitz & Stegun,
+// "Handbook of Mathematical Functions", formula 7.1.26 (|error| <= 1.5e-7 for x >= 0, odd
+// extension for x < 0), evaluated with the fast exp and divide intrinsics: far below the
+// bf16 rounding of H and cheaper than the IEEE erff in the layer-1 epilogue.
+__device__ __forceinline__ float gelu_erf(float x) {
+  const float z = fabsf(x) * 0.70710678118654752f;
+  const float t = __fdividef(1.0f, 1.0f + 0.3275911f * z);
+  const float poly = t * (0.254829592f + t * (-0.284496736f + t * (1.421413741f + t * (-1.453152027f + t * 1.061405429f))));
+  const float e = 1.0f - poly * __expf(-z * z);
+  return 0.5f * x * (1.0f + copysignf(e, x));
+}
 
 // GEMM+RS epilogue on one BM x 256 partial tile of producer `prod` (of W), reduced into
 // the fp32 slot tile at (grow, n0); the last producer writes bf16 rows of `out` at orow.
