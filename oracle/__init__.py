@@ -38,7 +38,7 @@ except Exception:  # pragma: no cover - fallback keeps the oracle usable without
 __all__ = [
     "widen_bf16", "ag_gather_bits", "ag_gemm", "ag_gemm_entries", "gemm_rs",
     "gemm_rs_entries", "gelu", "silu", "mlp2", "mlp2_entries", "moe_route", "moe_permute",
-    "moe", "moe_rows", "static_tile_map", "round_bf16",
+    "moe", "moe_rows", "static_tile_map", "round_bf16", "attn_gather", "ag_attention", "ag_attention_rows",
 ]
 
 
@@ -315,3 +315,38 @@ def static_tile_map(tile_id: int, M: int, R: int, C: int, Tm: int):
     src_rank = tile_id // (m_per_rank // Tm)
     channel = tile_id // (m_per_channel // Tm)
     return lo, hi, src_rank, channel
+
+
+# ----------------------------------------------------------------------------- AG KV + self-attention
+def attn_gather(shards) -> np.ndarray:
+    """Sequence-parallel context gather: K (or V) shards [heads, L_r, d] of ranks 0..W-1
+    concatenated along the sequence in rank order, per head ([TL] §5, AllGather KV +
+    self-attention: the KV cache sequence S split into W equal parts, one per rank).
+    Returns the bf16 bit patterns [heads, W * L_r, d]."""
+    return np.concatenate([np.ascontiguousarray(x, dtype=np.uint16) for x in shards], axis=1)
+
+
+def ag_attention(q, k_shards, v_shards) -> np.ndarray:
+    """Self-attention of one rank's queries over the gathered context ([TL] §2 and §7.2,
+    sequence-parallel self-attention; the pages give no mask, read as non-causal):
+        O[h] = softmax(Q[h] K[h]^T / sqrt(d)) V[h],  K, V = attn_gather(shards).
+    q: bf16 bits [heads, L_q, d]; shards: bf16 bits [heads, L_r, d].  float64, softmax
+    with the row maximum subtracted."""
+    Q = widen_bf16(q)
+    K = widen_bf16(attn_gather(k_shards))
+    V = widen_bf16(attn_gather(v_shards))
+    d = Q.shape[-1]
+    S = np.matmul(Q, np.swapaxes(K, 1, 2)) / math.sqrt(d)
+    S -= S.max(axis=-1, keepdims=True)
+    P = np.exp(S)
+    P /= P.sum(axis=-1, keepdims=True)
+    return np.matmul(P, V)
+
+
+def ag_attention_rows(q, k_shards, v_shards, heads, rows) -> np.ndarray:
+    """ag_attention at the query rows `rows` of the heads `heads` only (same arithmetic);
+    returns [len(heads), len(rows), d]."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    hs = list(heads)
+    sub = lambda x: np.ascontiguousarray(x, dtype=np.uint16)[hs]
+    return ag_attention(sub(q)[:, list(rows)], [sub(k) for k in k_shards], [sub(v) for v in v_shards])

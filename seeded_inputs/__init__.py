@@ -17,6 +17,9 @@ Compiler", Table 4 (AG+MoE rows with hidden 2048 / ffn 1408)):
   mlp2_8b   MLP2,     W=4, X 4096x4096 N(0,1); W1_r 4096x3584, W2_r 3584x4096 N(0,0.02^2)
   moe_64e   MoE,      T=4096, H=2048, E=64, F=1408, top-2; X N(0,1); logits N(0,1) fp32;
                       Wg, Wu (E,H,F) and Wd (E,F,H) N(0,0.02^2)
+  attn_16k  AG KV + self-attention, W=8, 32 heads, head dim 128, sequence 16k (2048 per rank):
+                      Q [32, 2048, 128], K_r and V_r [32, 2048, 128] per rank, all N(0,1)
+                      ("TileLink ...", Table 4, Attn-1 at 16k)
 
 Each tensor is drawn from its own stream, seed*1000 + tensor_index, with numpy's
 PCG64 generator (standard normal, float32), scaled by the standard deviation in
@@ -82,6 +85,7 @@ WORKLOADS = {
     "rs_70b": Workload("rs_70b", "gemm_rs", 3, dict(W=8, m=8192, n=8192, k_r=3584)),
     "mlp2_8b": Workload("mlp2_8b", "mlp2", 4, dict(W=4, tokens=4096, hidden=4096, f_r=3584)),
     "moe_64e": Workload("moe_64e", "moe", 5, dict(T=4096, H=2048, E=64, F=1408, topk=2)),
+    "attn_16k": Workload("attn_16k", "ag_attn", 6, dict(W=8, heads=32, l_r=2048, d=128)),
 }
 
 
@@ -94,6 +98,7 @@ def make_inputs(kind: str, seed: int, **d) -> dict:
       gemm_rs: a [W] (m, k_r); b [W] (k_r, n)
       mlp2:    x_shards [W] (tokens/W, hidden); w1 [W] (hidden, f_r); w2 [W] (f_r, hidden)
       moe:     x (T, H); logits (T, E) fp32; w_gate, w_up (E, H, F); w_down (E, F, H)
+      ag_attn: q (heads, l_r, d); k_shards, v_shards [W] (heads, l_r, d)
     """
     base = seed * 1000
     if kind == "ag_gemm":
@@ -122,6 +127,13 @@ def make_inputs(kind: str, seed: int, **d) -> dict:
             w_gate=normal_bf16(base + 2, (E, H, F), 0.02),
             w_up=normal_bf16(base + 3, (E, H, F), 0.02),
             w_down=normal_bf16(base + 4, (E, F, H), 0.02),
+        )
+    if kind == "ag_attn":
+        W, Hh, L, hd = d["W"], d["heads"], d["l_r"], d["d"]
+        return dict(
+            q=normal_bf16(base + 0, (Hh, L, hd), 1.0),
+            k_shards=[normal_bf16(base + 100 + r, (Hh, L, hd), 1.0) for r in range(W)],
+            v_shards=[normal_bf16(base + 200 + r, (Hh, L, hd), 1.0) for r in range(W)],
         )
     raise ValueError(f"unknown workload kind {kind!r}")
 

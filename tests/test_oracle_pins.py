@@ -285,3 +285,75 @@ def test_seeded_inputs_deterministic_and_scaled():
     assert not np.array_equal(a1["a_shards"][0], a1["a_shards"][1])
     v = oracle.widen_bf16(a1["b"])
     assert abs(v.std() - 1.0 / 16.0) < 0.002 and abs(v.mean()) < 0.002
+
+
+# ----------------------------------------------------------------------------- AG KV + self-attention
+def _attn_brute(q, ks, vs):
+    """Per-query loops with math.exp: softmax(q k^T / sqrt(d)) v over the rank-order gather."""
+    Q = oracle.widen_bf16(q)
+    K = np.concatenate([oracle.widen_bf16(k) for k in ks], axis=1)
+    V = np.concatenate([oracle.widen_bf16(v) for v in vs], axis=1)
+    H, L, d = Q.shape
+    out = np.zeros_like(Q)
+    for h in range(H):
+        for i in range(L):
+            s = [sum(Q[h, i, c] * K[h, j, c] for c in range(d)) / math.sqrt(d) for j in range(K.shape[1])]
+            m = max(s)
+            w = [math.exp(x - m) for x in s]
+            z = sum(w)
+            for c in range(d):
+                out[h, i, c] = sum(w[j] * V[h, j, c] for j in range(K.shape[1])) / z
+    return out
+
+
+def test_attention_matches_brute_force():
+    inp = make_inputs("ag_attn", 41, W=3, heads=2, l_r=3, d=4)
+    got = oracle.ag_attention(inp["q"], inp["k_shards"], inp["v_shards"])
+    ref = _attn_brute(inp["q"], inp["k_shards"], inp["v_shards"])
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_gather_is_rank_order_concatenation():
+    inp = make_inputs("ag_attn", 42, W=4, heads=3, l_r=5, d=8)
+    g = oracle.attn_gather(inp["k_shards"])
+    assert g.shape == (3, 20, 8)
+    for r in range(4):
+        assert np.array_equal(g[:, 5 * r:5 * (r + 1)], inp["k_shards"][r])
+
+
+def test_attention_zero_query_is_mean_of_values():
+    inp = make_inputs("ag_attn", 43, W=2, heads=2, l_r=6, d=8)
+    q = np.zeros_like(inp["q"])
+    got = oracle.ag_attention(q, inp["k_shards"], inp["v_shards"])
+    V = oracle.widen_bf16(oracle.attn_gather(inp["v_shards"]))
+    assert np.allclose(got, np.broadcast_to(V.mean(axis=1, keepdims=True), got.shape), rtol=0, atol=1e-14)
+
+
+def test_attention_dominant_key_selects_its_value():
+    # one key is 64 times the query direction: its score exceeds every other by > 100,
+    # so the output is that key's value row to within exp(-100)
+    from seeded_inputs import f32_to_bf16_bits
+    inp = make_inputs("ag_attn", 44, W=2, heads=1, l_r=4, d=16)
+    qf = oracle.widen_bf16(inp["q"])
+    ks = [oracle.widen_bf16(k).copy() for k in inp["k_shards"]]
+    ks[1][0, 2] = 64.0 * qf[0, 1]
+    kb = [f32_to_bf16_bits(k.astype(np.float32)) for k in ks]
+    got = oracle.ag_attention(inp["q"], kb, inp["v_shards"])
+    assert np.allclose(got[0, 1], oracle.widen_bf16(inp["v_shards"][1])[0, 2], atol=1e-12)
+
+
+def test_attention_invariant_to_duplicated_context_and_shard_order():
+    inp = make_inputs("ag_attn", 45, W=3, heads=2, l_r=4, d=8)
+    q, ks, vs = inp["q"], inp["k_shards"], inp["v_shards"]
+    base = oracle.ag_attention(q, ks, vs)
+    assert np.allclose(oracle.ag_attention(q, ks + ks, vs + vs), base, rtol=1e-12, atol=1e-13)
+    order = [2, 0, 1]
+    assert np.allclose(oracle.ag_attention(q, [ks[i] for i in order], [vs[i] for i in order]), base,
+                       rtol=1e-12, atol=1e-13)
+
+
+def test_attention_rows_match_full():
+    inp = make_inputs("ag_attn", 46, W=2, heads=3, l_r=8, d=8)
+    full = oracle.ag_attention(inp["q"], inp["k_shards"], inp["v_shards"])
+    part = oracle.ag_attention_rows(inp["q"], inp["k_shards"], inp["v_shards"], [2, 0], [5, 1])
+    assert np.allclose(part, full[[2, 0]][:, [5, 1]], rtol=1e-13, atol=1e-14)
