@@ -24,7 +24,8 @@ __all__ = [
     "TLError", "Config", "Context", "lib", "library_path", "build",
     "tl_ag_gemm", "tl_allgather", "tl_gemm_rs", "tl_mlp2", "tl_moe_combine",
     "tl_ag_gemm_workspace_bytes", "tl_gemm_rs_workspace_bytes", "tl_mlp2_workspace_bytes",
-    "tl_moe_workspace_bytes", "tl_ag_tile_order", "tl_rs_tile_order", "tl_trace_bytes", "EXPORTED_SYMBOLS",
+    "tl_moe_workspace_bytes", "tl_ag_tile_order", "tl_rs_tile_order", "tl_trace_bytes", "tl_ag_attention",
+    "tl_ag_attention_workspace_bytes", "EXPORTED_SYMBOLS",
 ]
 
 TL_OK = 0
@@ -80,6 +81,9 @@ _SIGS = {
     "tl_moe_workspace_bytes": (_c_size, [_i, _i, _i, _i, _i]),
     "tl_moe_combine": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_size, _i, _i, _i, _i, _vp]),
     "tl_ag_gemm_static_scratch": (_i, [_vp, _i, _i, ctypes.POINTER(_vp), _vp, _vp, _i, _i, _i, _vp]),
+    "tl_ag_attention_workspace_bytes": (_c_size, [_i, _i, _i, _i]),
+    "tl_ag_attention": (_i, [_vp, _i, _i, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _vp, _c_size, _i, _i,
+                             _i, _vp]),
     "tl_ag_tile_order": (_i, [_i, _i, _i, _i, _i, _vp, _vp, _vp, _i]),
     "tl_rs_tile_order": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _i]),
 }
@@ -219,6 +223,25 @@ def tl_mlp2_workspace_bytes(W, tokens, hidden, f_r) -> int:
 
 def tl_moe_workspace_bytes(T, H, E, F, topk) -> int:
     return lib().tl_moe_workspace_bytes(T, H, E, F, topk)
+
+
+def tl_ag_attention_workspace_bytes(W, heads, l_r, d) -> int:
+    return lib().tl_ag_attention_workspace_bytes(W, heads, l_r, d)
+
+
+def tl_ag_attention(ctx: Context, q, k_shards, v_shards, out, workspace, rank: int = 0, stream=None) -> None:
+    """out[h] = softmax(q[h] K[h]^T / sqrt(d)) V[h] over the rank-order gather of the K/V
+    shards (bf16 [heads, l_r, d] each); the copy engine gathers them, overlapped."""
+    W = len(k_shards)
+    _need(q, "bf16", "q"); _need(out, "bf16", "out"); _need(workspace, "u8", "workspace")
+    for i in range(W):
+        _need(k_shards[i], "bf16", f"k_shards[{i}]"); _need(v_shards[i], "bf16", f"v_shards[{i}]")
+    heads, l_r, d = q.shape
+    if len(v_shards) != W or any(tuple(t.shape) != (heads, l_r, d) for t in list(k_shards) + list(v_shards) + [out]):
+        raise ValueError("inconsistent shapes")
+    rc = lib().tl_ag_attention(ctx.handle, W, rank, _ptr(q), _ptrs(k_shards), _ptrs(v_shards), _ptr(out),
+                               _ptr(workspace), workspace.numel(), heads, l_r, d, _stream(stream))
+    _check(rc, "tl_ag_attention")
 
 
 def tl_trace_bytes(ctas, spans_per_warp) -> int:

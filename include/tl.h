@@ -253,6 +253,30 @@ int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, int topk, co
                    const void* w_up, const void* w_down, float* out, int* perm_out, int* counts_out,
                    void* workspace, size_t workspace_bytes, int T, int H, int E, int F, tl_stream_t stream);
 
+/* ---------------------------------------------------------------- AllGather KV + self-attention
+ * [TL] §5 (AllGather KV + self-attention: the KV cache sequence split into W equal shards)
+ * and §7.2 (sequence-parallel self-attention; Table 4 Attn-1/Attn-2: head dim 128); [TD] §3.7
+ * (the local shard first).  Non-causal (the pages give no mask):
+ *   out[h] = softmax(q[h] K[h]^T / sqrt(d)) V[h],  K = [K_0 | K_1 | ... | K_{W-1}] along the
+ *   sequence (rank order), V likewise.
+ * q: bf16 [heads x l_r x d] (this rank's queries).  k_shards, v_shards: host arrays of W device
+ * pointers, shard r bf16 [heads x l_r x d].  out: bf16 [heads x l_r x d].
+ * workspace: tl_ag_attention_workspace_bytes(): the gathered K and V, shard-major
+ * [W x heads x l_r x d] (shard r at r, filled completely, the local shard last), and one
+ * signal per (shard, head, 128-key block).
+ * One persistent cooperative launch: mover warps pull the remote shards' K/V blocks into the
+ * gathered buffers and release each block's signal; the attention of each (head, 128-query
+ * tile) reads its own shard in place first and a remote shard's blocks once all of them are
+ * signalled.  The pages run this gather on the copy engine from a second stream; that makes
+ * the kernel wait on work outside its own launch, which nothing guarantees to run alongside
+ * it, so the gather runs inside the kernel, as for tl_ag_gemm.
+ * Shapes: 1 <= W <= 8; d == 128; l_r % 128 == 0.  heads == 0 or l_r == 0 is a no-op.
+ */
+size_t tl_ag_attention_workspace_bytes(int W, int heads, int l_r, int d);
+int tl_ag_attention(tl_ctx* ctx, int W, int rank, const void* q, const void* const* k_shards,
+                    const void* const* v_shards, void* out, void* workspace, size_t workspace_bytes,
+                    int heads, int l_r, int d, tl_stream_t stream);
+
 /* ---------------------------------------------------------------- AllGather + GEMM without allocation
  * The pages have no counterpart of this entry point.  It exists for callers that cannot
  * allocate device memory when they call in: code being recorded into a CUDA graph by stream
