@@ -267,8 +267,6 @@ def run_ours(args):
 
     if not args.quick:
         line["overlap"] = overlap_ag(tl, ctx, a, b, c, ws, flush, stream, device, times, W, mpr, n, k, pk)
-        line["overlap_copy_engine"] = overlap_ag_copy_engine(tl, a, b, c, ws, flush, stream, W, mpr, n, k, pk,
-                                                             line["overlap"]["t_gemm_alone_us"])
         line["workloads"] = sub_workloads(tl, ctx, flush, stream, device, pk, args)
         line["e2e"] = e2e_ag(tl, ctx, inp, device, stream, W, mpr, n, k, args)
         line["baselines"] = {"cublas_plus_copy_ms": cublas_plus_copy(a, b, flush, stream, device)}
@@ -307,36 +305,6 @@ def overlap_ag(tl, ctx, a, b, c, ws, flush, stream, device, fused_times, W, mpr,
         "copy_alone_gbs": round(moved / (t_copy * 1e-3) / 1e9, 1),
         "gemm_alone_tflops": round(ag_flops(W, mpr, n, k) / (t_gemm * 1e-3) / 1e12, 2),
         "gemm_alone_frac": round(ag_flops(W, mpr, n, k) / (t_gemm * 1e-3) / 1e12 / pk["bf16"], 4),
-    }
-
-
-def overlap_ag_copy_engine(tl, a, b, c, ws, flush, stream, W, mpr, n, k, pk, t_gemm_us):
-    """The same AllGather+GEMM with the copy engine as the AllGather transport
-    (tl_config.copy_engine = 1): the AllGather alone, the fused call, and the overlap
-    efficiency against the same GEMM-alone time."""
-    import torch
-    reps = 30
-    with tl.Context(0, copy_engine=1) as ce:
-        cp = lambda: tl.tl_allgather(ce, a, ws, rank=0, stream=stream)
-        fu = lambda: tl.tl_ag_gemm(ce, a, b, c, ws, rank=0, stream=stream)
-        for f in (cp, fu):
-            for _ in range(3):
-                f()
-        torch.cuda.synchronize()
-        if ce.check() != tl.TL_OK:
-            raise RuntimeError("copy-engine AllGather+GEMM: device status not OK")
-        t_copy = statistics.median(timed_steps(cp, reps, flush, stream))
-        t_fused = statistics.median(timed_steps(fu, reps, flush, stream))
-        if ce.check() != tl.TL_OK:
-            raise RuntimeError("copy-engine AllGather+GEMM: device status not OK")
-    t_gemm = t_gemm_us * 1e-3
-    moved = 2.0 * W * mpr * k * 2
-    return {
-        "t_copy_alone_us": round(t_copy * 1e3, 2), "t_fused_us": round(t_fused * 1e3, 2),
-        "efficiency": round((t_copy + t_gemm - t_fused) / min(t_copy, t_gemm), 4),
-        "copy_alone_gbs": round(moved / (t_copy * 1e-3) / 1e9, 1),
-        "fused_tflops": round(ag_flops(W, mpr, n, k) / (t_fused * 1e-3) / 1e12, 2),
-        "fused_frac": round(ag_flops(W, mpr, n, k) / (t_fused * 1e-3) / 1e12 / pk["bf16"], 4),
     }
 
 

@@ -54,7 +54,6 @@ class Config(ctypes.Structure):
         ("debug_skip_chunk", _i),
         ("timeout_ns", ctypes.c_ulonglong),
         ("pair_ctas", _i),
-        ("copy_engine", _i),
     ]
 
 

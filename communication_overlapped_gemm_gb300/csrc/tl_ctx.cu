@@ -13,16 +13,6 @@ namespace tl {
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
-PFN_cuStreamBatchMemOp_v11070 g_batch_memop = nullptr;
-std::once_flag g_batch_once;
-
-void load_batch_memop() {
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuStreamBatchMemOp", &fn, 11070, cudaEnableDefault, &q) == cudaSuccess &&
-      q == cudaDriverEntryPointSuccess)
-    g_batch_memop = reinterpret_cast<PFN_cuStreamBatchMemOp_v11070>(fn);
-}
 
 void load_encode() {
   void* fn = nullptr;
@@ -63,38 +53,6 @@ bool tmap_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base
   return encode(m, dt, 3, base, dims, strides, box);
 }
 
-// Stream writes of `value` to n 64-bit signals (stream-ordered after the stream's earlier
-// work, each write preceded by a memory barrier), in one batch.
-int stream_write_signals(cudaStream_t st, uint64_t* const* addr, int n, unsigned long long value) {
-  std::call_once(g_batch_once, load_batch_memop);
-  if (!g_batch_memop) return TL_ERR_UNSUPPORTED;
-  CUstreamBatchMemOpParams ops[64];
-  for (int i0 = 0; i0 < n; i0 += 64) {
-    const int cnt = n - i0 < 64 ? n - i0 : 64;
-    for (int i = 0; i < cnt; ++i) {
-      std::memset(&ops[i], 0, sizeof(ops[i]));
-      ops[i].writeValue.operation = CU_STREAM_MEM_OP_WRITE_VALUE_64;
-      ops[i].writeValue.address = reinterpret_cast<CUdeviceptr>(addr[i0 + i]);
-      ops[i].writeValue.value64 = value;
-      ops[i].writeValue.flags = CU_STREAM_WRITE_VALUE_DEFAULT;
-    }
-    if (g_batch_memop(reinterpret_cast<CUstream>(st), cnt, ops, 0) != CUDA_SUCCESS) return TL_ERR_CUDA;
-  }
-  return TL_OK;
-}
-
-// The context's side stream and its two events, created on first use.
-int ce_resources(tl_ctx* ctx) {
-  if (ctx->ce_stream) return TL_OK;
-  if (cudaStreamCreateWithFlags(&ctx->ce_stream, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&ctx->ce_start, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&ctx->ce_done, cudaEventDisableTiming) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return TL_ERR_CUDA;
-  }
-  return TL_OK;
-}
-
 int set_smem_attr(const void* kern) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -119,7 +77,6 @@ int tl_config_default(tl_config* cfg) {
   cfg->debug_skip_chunk = -1;
   cfg->timeout_ns = 2000000000ull;
   cfg->pair_ctas = 2;
-  cfg->copy_engine = 0;
   return TL_OK;
 }
 
@@ -135,7 +92,7 @@ int tl_ctx_create(tl_ctx** out, int device, const tl_config* cfg) {
     tl_config_default(&c);
   if (c.mover_warps < 1 || c.mover_warps > tl::kMaxMoverWarps || !pow2_le32(c.chunks_per_slab) ||
       (c.swizzle != 0 && c.swizzle != 1) || c.grid_ctas < 0 || c.combine_ctas < 1 || c.timeout_ns == 0 ||
-      c.pair_ctas < 0 || c.pair_ctas > 2 || (c.copy_engine != 0 && c.copy_engine != 1))
+      c.pair_ctas < 0 || c.pair_ctas > 2)
     return TL_ERR_INVALID;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
@@ -181,9 +138,6 @@ void tl_ctx_destroy(tl_ctx* ctx) {
   cudaGetDevice(&prev);
   cudaSetDevice(ctx->device);
   cudaDeviceSynchronize();
-  if (ctx->ce_stream) cudaStreamDestroy(ctx->ce_stream);
-  if (ctx->ce_start) cudaEventDestroy(ctx->ce_start);
-  if (ctx->ce_done) cudaEventDestroy(ctx->ce_done);
   cudaFree(ctx->status);
   cudaSetDevice(prev);
   delete ctx;

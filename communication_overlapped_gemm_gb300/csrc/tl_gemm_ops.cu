@@ -492,29 +492,6 @@ using namespace tl;
 // ============================================================================ C ABI
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Copy-engine AllGather ([TL] §7.2 maps the AllGather to DMA): on stream `cs`, shard by
-// shard in the mover's order (the self rank's shard last), one cudaMemcpyAsync into the
-// gathered buffer, then a stream write of the epoch to each of the shard's 128-row slab
-// signals (one signal per slab: p.chunks == 1).
-static int ce_gather(const AgParams& p, const void* const* a_shards, cudaStream_t cs) {
-  uint64_t* sig[64];
-  for (int i = 0; i < p.W; ++i) {
-    const int r = ag_mover_rank(p.W, p.rank, p.swizzle, i);
-    if (cudaMemcpyAsync(p.gath + static_cast<size_t>(r) * p.shard_bytes, a_shards[r], p.shard_bytes,
-                        cudaMemcpyDeviceToDevice, cs) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TL_ERR_CUDA;
-    }
-    for (int s0 = 0; s0 < p.spr; s0 += 64) {
-      const int n = p.spr - s0 < 64 ? p.spr - s0 : 64;
-      for (int s = 0; s < n; ++s) sig[s] = p.flags + static_cast<size_t>(r) * p.spr + s0 + s;
-      const int rc = stream_write_signals(cs, sig, n, p.common.epoch);
-      if (rc != TL_OK) return rc;
-    }
-  }
-  return TL_OK;
-}
-
 static bool ag_shape_ok(int W, int mpr, int n, int k) {
   return W >= 1 && W <= 8 && mpr >= 0 && n >= 0 && k >= 0 && mpr % kBM == 0 && n % 8 == 0 && k % 8 == 0;
 }
@@ -577,37 +554,12 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   if (W == 1) {  // nothing to gather: the plain GEMM on shard 0 in place, no mover, no signals
     p.boost = 0;
     movers = 0;
-  } else if (ctx->cfg.copy_engine) {
-    // The copy engine moves the shards on the side stream, which starts after the caller's
-    // earlier work; the kernel runs without mover warps and waits on one signal per slab.
-    int rc = ce_resources(ctx);
-    if (rc != TL_OK) return rc;
-    p.chunks = 1;
-    p.boost = 0;
-    p.skip_chunk = -1;
-    movers = 0;
-    if (cudaEventRecord(ctx->ce_start, st) != cudaSuccess ||
-        cudaStreamWaitEvent(ctx->ce_stream, ctx->ce_start, 0) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TL_ERR_CUDA;
-    }
-    rc = ce_gather(p, a_shards, ctx->ce_stream);
-    if (rc != TL_OK) return rc;
-    if (cudaEventRecord(ctx->ce_done, ctx->ce_stream) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TL_ERR_CUDA;
-    }
   }
   int rc;
   if (pair)
     rc = launch_persistent_pair<AgOp<256, true>>(ctx, p, st, movers);
   else
     rc = bm == 256 ? launch_persistent<AgOp<256>>(ctx, p, st, movers) : launch_persistent<AgOp<128>>(ctx, p, st, movers);
-  // The call's work (gathered buffer included) completes on the caller's stream.
-  if (W > 1 && ctx->cfg.copy_engine && cudaStreamWaitEvent(st, ctx->ce_done, 0) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return TL_ERR_CUDA;
-  }
   return rc;
 }
 
@@ -790,10 +742,6 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   p.skip_chunk = -1;
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
-  if (ctx->cfg.copy_engine) {  // the copy engine on the caller's stream, one signal per slab
-    p.chunks = 1;
-    return ce_gather(p, a_shards, reinterpret_cast<cudaStream_t>(stream));
-  }
   allgather_kernel<<<ctx->ctas, ctx->cfg.mover_warps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? TL_OK : TL_ERR_CUDA;
 }

@@ -19,8 +19,6 @@ struct tl_ctx {
   tl_config cfg;
   tl::DevStatus* status;      // device status word (the only memory the library owns)
   unsigned long long epoch;   // last signal value handed out
-  cudaStream_t ce_stream;     // side stream of the copy-engine AllGather (created on first use)
-  cudaEvent_t ce_start, ce_done;
   void* trace_buf;            // caller-owned trace buffer (null: tracing off)
   int trace_cap;              // spans per warp
   int trace_ctas;             // CTAs the buffer holds
@@ -54,8 +52,7 @@ inline Common make_common(tl_ctx* ctx) {
 }
 
 int set_smem_attr(const void* kern);
-int stream_write_signals(cudaStream_t st, uint64_t* const* addr, int n, unsigned long long value);
-int ce_resources(tl_ctx* ctx);
+
 
 // Cooperative launch of one persistent CTA per SM (or cfg.grid_ctas), so that every CTA
 // that waits on a signal is co-resident with the CTAs that will set it.  While the context

@@ -85,12 +85,6 @@ typedef struct tl_config {
                                  every op; 2 (default) CTA pairs for tl_gemm_rs and tl_mlp2, whose
                                  heavier epilogues gain from the pair's double-buffered
                                  accumulators, single CTAs for tl_ag_gemm                           */
-  int copy_engine;            /* AllGather transport of tl_ag_gemm / tl_allgather: 0 (default) mover
-                                 warps inside the persistent CTAs; 1 the copy engine: one
-                                 cudaMemcpyAsync per shard on a context-owned side stream, then a
-                                 stream write of each of the shard's 128-row slab signals ([TL] §7.2
-                                 maps the AllGather to DMA).  The caller's stream waits for the side
-                                 stream before the call's work completes.                            */
 } tl_config;
 
 typedef struct tl_ctx tl_ctx;

@@ -236,37 +236,3 @@ def test_cta_pair_and_single_cta_paths_agree(op):
                 ref = np.concatenate(oracle.mlp2(inp["x_shards"], inp["w1"], inp["w2"]))
             assert_close(outs[-1], ref, f"{op} pair_ctas={pair}")
     assert_close(outs[0], outs[1], f"{op} pair vs single")
-
-
-# ----------------------------------------------------------------------------- copy-engine AllGather
-@pytest.mark.parametrize("W,mpr,n,k", [(2, 128, 256, 256), (3, 256, 200, 136), (4, 256, 768, 512), (8, 1024, 512, 1024)])
-def test_ag_gemm_copy_engine_matches_mover_warps(W, mpr, n, k):
-    """The copy-engine transport gives the same C and the same gathered buffer, bit for bit,
-    as the mover warps (whose results the oracle pins), for the first and the last rank."""
-    import torch
-    inp = make_inputs("ag_gemm", 61 + W, W=W, m_per_rank=mpr, n=n, k=k)
-    for rank in (0, W - 1):
-        outs = []
-        for ce in (0, 1):
-            with tl.Context(0, copy_engine=ce, timeout_ns=200_000_000) as c2:
-                c, ws = run_ag(c2, inp, rank=rank)
-                gath = bf16_bits(ws[: W * mpr * k * 2].view(torch.bfloat16).view(W * mpr, k))
-                outs.append((bf16_bits(c), gath))
-        assert np.array_equal(outs[0][0], outs[1][0]), f"C differs W={W} rank={rank}"
-        assert np.array_equal(outs[0][1], outs[1][1]), f"gathered buffer differs W={W} rank={rank}"
-    if W == 2:
-        assert_close(bf16_to_f64(c), oracle.ag_gemm(inp["a_shards"], inp["b"]), "ag copy engine")
-
-
-def test_allgather_copy_engine_gathers_in_rank_order():
-    import torch
-    W, mpr, k = 4, 256, 320
-    inp = make_inputs("ag_gemm", 71, W=W, m_per_rank=mpr, n=8, k=k)
-    a = [to_dev_bf16(x) for x in inp["a_shards"]]
-    with tl.Context(0, copy_engine=1, timeout_ns=200_000_000) as c2:
-        ws = workspace(tl.tl_ag_gemm_workspace_bytes(W, mpr, 8, k))
-        tl.tl_allgather(c2, a, ws, rank=1)
-        torch.cuda.synchronize()
-        assert c2.check() == tl.TL_OK
-    got = bf16_bits(ws[: W * mpr * k * 2].view(torch.bfloat16).view(W * mpr, k))
-    assert np.array_equal(got, oracle.ag_gather_bits(inp["a_shards"]))
