@@ -391,6 +391,19 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     moe_bytes = 3.0 * E * H * F * 2 + T * H * 2 + T * H * 4 + T * E * 4
     rec("moe_64e", lambda: tl.tl_moe_combine(ctx, xx, lg, kk, wg, wu, wd, oo, ws, stream=stream), moe_flops,
         moe_bytes, "hbm", 4)
+    del xx, lg, wg, wu, wd, oo, ws
+
+    # AllGather KV + self-attention (Attn-1 at 16k on 8 ranks)
+    d = WORKLOADS["attn_16k"].dims
+    inp = workload_inputs("attn_16k")
+    W, Hh, L, hd = d["W"], d["heads"], d["l_r"], d["d"]
+    q = dev_bf16(inp["q"], device)
+    ks = [dev_bf16(x, device) for x in inp["k_shards"]]
+    vs = [dev_bf16(x, device) for x in inp["v_shards"]]
+    ao = torch.empty((Hh, L, hd), dtype=torch.bfloat16, device=device)
+    ws = torch.zeros(tl.tl_ag_attention_workspace_bytes(W, Hh, L, hd), dtype=torch.uint8, device=device)
+    rec("attn_16k", lambda: tl.tl_ag_attention(ctx, q, ks, vs, ao, ws, stream=stream), 4.0 * L * W * L * hd * Hh, 0,
+        "tensor", 1)
     return out
 
 
