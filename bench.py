@@ -574,6 +574,14 @@ def run_profile(args):
         o = [torch.empty((T // W, d["hidden"]), dtype=torch.bfloat16, device=device) for _ in range(W)]
         ws = torch.zeros(tl.tl_mlp2_workspace_bytes(W, T, d["hidden"], d["f_r"]), dtype=torch.uint8, device=device)
         call = lambda: tl.tl_mlp2(ctx, x, w1, w2, o, ws)
+    elif WORKLOADS[name].kind == "ag_attn":
+        q = dev_bf16(inp["q"], device)
+        ks = [dev_bf16(x, device) for x in inp["k_shards"]]
+        vs = [dev_bf16(x, device) for x in inp["v_shards"]]
+        ao = torch.empty((d["heads"], d["l_r"], d["d"]), dtype=torch.bfloat16, device=device)
+        ws = torch.zeros(tl.tl_ag_attention_workspace_bytes(d["W"], d["heads"], d["l_r"], d["d"]), dtype=torch.uint8,
+                         device=device)
+        call = lambda: tl.tl_ag_attention(ctx, q, ks, vs, ao, ws)
     else:
         xx = dev_bf16(inp["x"], device)
         lg = torch.from_numpy(inp["logits"]).to(device)
@@ -631,7 +639,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work in --impl reference")
     ap.add_argument("--quick", action="store_true", help="headline only (no extra workloads / e2e / overlap)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--profile", choices=["ag_tiny", "ag_70b", "rs_70b", "mlp2_8b", "moe_64e"],
+    ap.add_argument("--profile", choices=["ag_tiny", "ag_70b", "rs_70b", "mlp2_8b", "moe_64e", "attn_16k"],
                     help="only run this workload's call 4 times (target of an ncu capture), no timing")
     ap.add_argument("--trace", metavar="PATH", help="with --profile: trace one call (after 3 warm-up calls and an "
                     "L2 flush) and write its per-CTA timeline to PATH: Chrome trace JSON, or the decoded spans "

@@ -11,10 +11,14 @@
 //             slice's 16 block signals (one warp-wide poll).
 //   warp 1    TMEM allocation and the MMAs: S_j = Q K_j^T into one of two S buffers, then
 //             O += P_{j-1} V_{j-1} once the softmax warps have published P_{j-1}.
-//   warps 2-5 softmax, one query row per thread: S row from TMEM, running max and sum, P
-//             (bf16) into shared memory in the MMA's K-major 128-byte-swizzled layout, and
-//             the rescale of the O row in TMEM when the running max grows (after the
-//             previous P V has completed).  Finally O / l as bf16.
+//   warps 2-5 softmax, one query row per thread: S row from TMEM, running max and sum in
+//             base 2 (the 1/sqrt(d) scale folded into one multiply-add per score), P (bf16)
+//             into one of two shared-memory buffers in the MMA's K-major 128-byte-swizzled
+//             layout.  The running max of a row moves only when the block's max exceeds it
+//             by more than 2^8 (kRescaleLog2): until then P <= 256 and O, l keep the stale
+//             max, which cancels in O / l.  A move rescales the warp's O rows in TMEM after
+//             the previous P V has completed; writing P waits only for the P V two blocks
+//             back.  Finally O / l as bf16.
 //   warps 6-7 movers: remote K/V blocks (32 KB each) into the shard-major gathered buffers,
 //             one release signal per block, the local shard last.
 // The pipeline counters run on across items.  TMEM columns: S0 [0, 128), S1 [128, 256),
@@ -33,7 +37,9 @@ constexpr int kKBytes = 2 * kBlk;   // K block: 2 boxes of 64 head-dim columns
 constexpr int kVBytes = 2 * kBlk;   // V block: 4 boxes of 64 keys x 64 head-dim columns
 constexpr int kPBytes = 2 * kBlk;
 constexpr int kStages = 2;
-constexpr int kSmem = 1024 + kQBytes + kStages * (kKBytes + kVBytes) + kPBytes + 256;
+constexpr int kSmem = 1024 + kQBytes + kStages * (kKBytes + kVBytes) + 2 * kPBytes + 256;
+constexpr float kRescaleLog2 = 8.0f;  // move the running max once it grows by more than this
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMovers = 2;
 constexpr int kThreads = (6 + kMovers) * 32;
 constexpr size_t kBlockBytes = static_cast<size_t>(kBKV) * kD * 2;  // one K or V block
@@ -88,7 +94,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
   uint8_t* sk = sq + kQBytes;
   uint8_t* sv = sk + kStages * kKBytes;
   uint8_t* sp = sv + kStages * kVBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sp + kPBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sp + 2 * kPBytes);
   uint64_t* qfull = bars;
   uint64_t* kfull = bars + 1;   // [2]
   uint64_t* kempty = bars + 3;  // [2]
@@ -96,11 +102,11 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
   uint64_t* vempty = bars + 7;  // [2]
   uint64_t* sfull = bars + 9;   // [2] S of block J in TMEM buffer J % 2
   uint64_t* sfree = bars + 11;  // [2] softmax has read the S buffer
-  uint64_t* pready = bars + 13; // P of block J written and O rescaled
-  uint64_t* ofree = bars + 14;  // P V of block J complete
-  uint64_t* drain = bars + 15;
-  uint64_t* qempty = bars + 16; // the item's last S MMA has read Q
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 17);
+  uint64_t* pready = bars + 13; // [2] P of block J in buffer J % 2 written, O rescaled
+  uint64_t* pfree = bars + 15;  // [2] P V of block J (P buffer J % 2) complete
+  uint64_t* drain = bars + 17;
+  uint64_t* qempty = bars + 18; // the item's last S MMA has read Q
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 19);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Common& c = p.common;
@@ -120,9 +126,9 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sfull[s], 1);
       mbar_init(&sfree[s], 4);
+      mbar_init(&pready[s], 4);
+      mbar_init(&pfree[s], 1);
     }
-    mbar_init(pready, 4);
-    mbar_init(ofree, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
     tma_prefetch_map(&p.q);
@@ -228,12 +234,13 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           }
           if (j >= 1) {  // O += P V of block J0 + j - 1
             const int I = J0 + j - 1, s = I & 1;
-            ok = mbar_wait(pready, I & 1, c, kSiteFull) && mbar_wait(&vfull[s], (I >> 1) & 1, c, kSiteFull);
+            const uint32_t ph = (I >> 1) & 1;
+            ok = mbar_wait(&pready[s], ph, c, kSiteFull) && mbar_wait(&vfull[s], ph, c, kSiteFull);
             if (!ok) break;
             tc_fence_after();
-            attn_mma_pv(to, p0, smem_u32(sv + s * kVBytes), j > 1);
+            attn_mma_pv(to, p0 + s * kPBytes, smem_u32(sv + s * kVBytes), j > 1);
             umma_commit(&vempty[s]);
-            umma_commit(ofree);
+            umma_commit(&pfree[s]);
           }
         }
       }
@@ -246,74 +253,101 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
     const int qd = warp & 3;               // TMEM lane quadrant of this warp
     const int row = qd * 32 + lane;        // query row inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
-    const float sl2 = p.scale;
+    const float sl2 = p.scale * kLog2e;  // raw score -> base-2 exponent
     bool ok = true;
     int J0 = 0;
     for (int it = blockIdx.x; it < nwork && ok; it += gridDim.x, J0 += nblk) {
       const int h = it / nqt, qt = it - h * nqt;
-      float m = -INFINITY, l = 0.f;
+      float m2 = -INFINITY, l = 0.f;  // running max (base-2 units) and sum of the row
       for (int j = 0; j < nblk && ok; ++j) {
         const int J = J0 + j, s = J & 1;
-        ok = mbar_wait(&sfull[s], (J >> 1) & 1, c, kSiteTmemFull);
+        const uint32_t ph = (J >> 1) & 1;
+        ok = mbar_wait(&sfull[s], ph, c, kSiteTmemFull);
         if (!ok) break;
         tc_fence_after();
         float x[128];
+        {
+          uint32_t r[4][32];
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          float t[32];
-          tmem_ld32(tmem + s * 128 + cb * 32 + lane_off, t);
+          for (int cb = 0; cb < 4; ++cb) tmem_ld32_issue(tmem + s * 128 + cb * 32 + lane_off, r[cb]);
+          tmem_ld_wait(r[0]);
+          tmem_ld_after(r[1]);
+          tmem_ld_after(r[2]);
+          tmem_ld_after(r[3]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x[cb * 32 + i] = t[i] * sl2;
+          for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(r[i >> 5][i & 31]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfree[s]);
-        float mx = x[0];
+        float mx[8];
 #pragma unroll
-        for (int i = 1; i < 128; ++i) mx = fmaxf(mx, x[i]);
-        const float mn = fmaxf(m, mx);
-        const float corr = __expf(m - mn);  // 0 on the first block (m = -inf)
-        float sum = 0.f;
+        for (int i = 0; i < 8; ++i) mx[i] = x[i];
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          x[i] = __expf(x[i] - mn);
-          sum += x[i];
-        }
-        l = l * corr + sum;
-        m = mn;
-        if (j >= 1) {
-          // P V of the previous block has completed: the P buffer is free and O is stable.
-          ok = mbar_wait(ofree, (J - 1) & 1, c, kSiteTmemFull);
+        for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) mx[i] = fmaxf(mx[i], mx[i + w]);
+        const float bm2 = mx[0] * sl2;  // the scale is positive: max commutes with it
+        if (j == 0) {
+          m2 = bm2;  // the item's first P V overwrites O
+        } else if (__any_sync(0xffffffffu, bm2 > m2 + kRescaleLog2)) {
+          const float mn = fmaxf(m2, bm2);
+          const float corr = ex2_approx(m2 - mn);
+          // O is stable once the P V of the previous block has completed
+          ok = mbar_wait(&pfree[(J - 1) & 1], ((J - 1) >> 1) & 1, c, kSiteTmemFull);
           if (!ok) break;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, corr != 1.0f)) {
 #pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-              float o[32];
-              tmem_ld32(tmem + 256 + cb * 32 + lane_off, o);
+          for (int cb = 0; cb < 4; ++cb) {
+            float o[32];
+            tmem_ld32(tmem + 256 + cb * 32 + lane_off, o);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= corr;
-              tmem_st32(tmem + 256 + cb * 32 + lane_off, o);
-            }
+            for (int i = 0; i < 32; ++i) o[i] *= corr;
+            tmem_st32(tmem + 256 + cb * 32 + lane_off, o);
           }
+          l *= corr;
+          m2 = mn;
         }
+        const float nm = -m2;
+        float sum[8];
+        uint32_t pk[64];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum[i] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float e0 = ex2_approx(fmaf(x[2 * i], sl2, nm));
+          const float e1 = ex2_approx(fmaf(x[2 * i + 1], sl2, nm));
+          sum[(2 * i) & 7] += e0;
+          sum[(2 * i + 1) & 7] += e1;
+          pk[i] = pack_bf16x2(e0, e1);
+        }
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) sum[i] += sum[i + w];
+        l += sum[0];
+        // P buffer s was last read by the P V of block J - 2
+        ok = mbar_wait(&pfree[s], ph ^ 1u, c, kSiteTmemEmpty);
+        if (!ok) break;
         // P (bf16) as the K-major, 128-byte-swizzled A operand: keys [64 kb, 64 kb + 64) of
         // this row are 128 bytes of box kb; 16-byte piece u sits at piece u ^ (row & 7).
-        const uint32_t prow = smem_u32(sp) + row * 128;
+        const uint32_t prow = smem_u32(sp) + s * kPBytes + row * 128;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const float* v = x + kb * 64 + u * 8;
-            st_shared_v4(prow + kb * kBlk + ((u ^ (row & 7)) << 4), pack_bf16x2(v[0], v[1]),
-                         pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+            const uint32_t* v = pk + kb * 32 + u * 4;
+            st_shared_v4(prow + kb * kBlk + ((u ^ (row & 7)) << 4), v[0], v[1], v[2], v[3]);
           }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(pready);
+        if (lane == 0) mbar_arrive(&pready[s]);
       }
-      if (ok) ok = mbar_wait(ofree, (J0 + nblk - 1) & 1, c, kSiteTmemFull);
+      const int Jl = J0 + nblk - 1;  // the item's last P V
+      if (ok) ok = mbar_wait(&pfree[Jl & 1], (Jl >> 1) & 1, c, kSiteTmemFull);
       tc_fence_after();
       if (ok) {
         const float inv = 1.0f / l;

@@ -1,7 +1,7 @@
 """GPU parity of the AllGather KV + self-attention kernel against the fp64 oracle.
 
-Through the C ABI: the copy engine gathers the K/V shards (rank order, bit for bit) while
-the tcgen05 flash-attention kernel of the rank's queries runs over them.  Tolerance for
+Through the C ABI: the kernel's mover warps gather the K/V shards (rank order, bit for
+bit) while its tcgen05 flash-attention warps run the rank's queries over them.  Tolerance for
 the bf16-in / fp32-accumulate outputs: max|gpu - ref| <= 1e-2 * max|ref| + 1e-3.
 """
 import numpy as np
@@ -53,6 +53,30 @@ def test_ag_attention_peaked_scores():
     out, _ = run_attn(inp, rank=1)
     ref = oracle.ag_attention(inp["q"], inp["k_shards"], inp["v_shards"])
     assert_close(bf16_to_f64(out), ref, "attention peaked")
+
+
+def test_ag_attention_growing_scores():
+    """Keys scaled up block by block in the order the kernel visits them (the local shard,
+    then rank + 1, ...), so that the running maximum of most rows grows by more than 2^8 (in
+    base 2) at every block and O is rescaled each time; the odd query rows are zero, so
+    their scores stay 0 and, in the same warps, they never rescale."""
+    from seeded_inputs import f32_to_bf16_bits
+    W, H, L, rank = 3, 1, 256, 1
+    inp = make_inputs("ag_attn", 93, W=W, heads=H, l_r=L, d=128)
+    q = oracle.widen_bf16(inp["q"]).astype(np.float32)
+    q[:, 1::2] = 0.0
+    inp["q"] = f32_to_bf16_bits(q)
+    ks = []
+    for r, k in enumerate(inp["k_shards"]):
+        kf = oracle.widen_bf16(k).astype(np.float32)
+        step = (r - rank) % W  # the kernel visits shard r at this step
+        for b in range(L // 128):
+            kf[:, b * 128:(b + 1) * 128] *= 1.0 + 3.0 * (step * (L // 128) + b)
+        ks.append(f32_to_bf16_bits(kf))
+    inp["k_shards"] = ks
+    out, _ = run_attn(inp, rank=rank)
+    ref = oracle.ag_attention(inp["q"], inp["k_shards"], inp["v_shards"])
+    assert_close(bf16_to_f64(out), ref, "attention growing scores")
 
 
 def test_ag_attention_16k_sampled():
