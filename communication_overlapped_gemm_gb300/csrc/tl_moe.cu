@@ -205,20 +205,6 @@ struct MoeSlot {
   int nb;    // column block
 };
 
-// Up-projection stage: two 128x128 accumulators (gate, up) from one A stage.
-__device__ __forceinline__ void mma_stage_dual128(uint32_t d, uint32_t a0, uint32_t b0, int kb) {
-  constexpr uint32_t idesc = umma_idesc_bf16(kBM, 128, true);
-#pragma unroll
-  for (int k = 0; k < kBK / 16; ++k) {
-    const uint64_t ad = umma_desc_sw128(a0 + k * 32, 16, 1024);
-    const uint64_t bg = umma_desc_sw128(b0 + k * 2048, TL_B_LBO, TL_B_SBO);
-    const uint64_t bu = umma_desc_sw128(b0 + 2 * 8192 + k * 2048, TL_B_LBO, TL_B_SBO);
-    const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
-    umma_bf16(d, ad, bg, idesc, acc);
-    umma_bf16(d + 128, ad, bu, idesc, acc);
-  }
-}
-
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
@@ -385,11 +371,12 @@ struct MoeOp : OpBase<MoeParams> {
       for (int g = 0; g < kBN / 64; ++g) tma_load_3d(sb + g * 8192, &p.wd, bar, j.b_col + g * 64, kb * kBK, j.b_z);
     }
   }
-  static __device__ void mma_stage(const Job& j, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
-    if (j.kind == 1)
-      mma_stage_dual128(d, a0, b0, kb);
-    else
-      mma_stage_256(d, a0, b0, kb);
+  // Up tiles load the gate and up weight columns as the four 64-column groups of one
+  // 256-column B slice (gate 0-127, up 128-255), so both kinds are one 128x256 MMA per K
+  // step: the gate accumulator in TMEM columns [0, 128), the up accumulator in [128, 256).
+  // (Two 128-column MMAs per step ran at about half the tensor rate.)
+  static __device__ void mma_stage(const Job&, uint32_t d, uint32_t a0, uint32_t b0, int kb) {
+    mma_stage_256(d, a0, b0, kb);
   }
   static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es,
                                  int, int) {
