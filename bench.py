@@ -272,6 +272,7 @@ def run_ours(args):
         line["baselines"] = {"cublas_plus_copy_ms": cublas_plus_copy(a, b, flush, stream, device)}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline_ag(inp, args.cpu_seconds)
+        line["cpu_baseline"]["single_thread"] = cpu_single_thread_ag(args.cpu_seconds / 2)
     ctx.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -323,6 +324,17 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     out = {}
     reps = args.sub_steps
 
+    def gemm_alone(r, fn, flops):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        if ctx.check() != tl.TL_OK:
+            raise RuntimeError("plain GEMMs: device status not OK")
+        t = statistics.median(timed_steps(fn, max(3, reps // 2), flush, stream))
+        r["gemm_alone_us"] = round(t * 1e3, 2)
+        r["gemm_alone_tflops"] = round(flops / (t * 1e-3) / 1e12, 2)
+        r["fused_over_gemm_alone"] = round(r["us"] / (t * 1e3), 4)
+
     def rec(name, fn, flops, bytes_alg, bound, launches):
         for _ in range(3):
             fn()
@@ -363,7 +375,13 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     o = [torch.empty((m // W, n), dtype=torch.bfloat16, device=device) for _ in range(W)]
     ws = torch.zeros(tl.tl_gemm_rs_workspace_bytes(W, m, n, kr), dtype=torch.uint8, device=device)
     rec("rs_70b", lambda: tl.tl_gemm_rs(ctx, a, b, o, ws, stream=stream), 2.0 * W * m * n * kr, 0, "tensor", 1)
-    del a, b, o, ws
+    # the same W products with a plain bf16 store (the AG engine with nothing to gather)
+    cp = torch.empty((m, n), dtype=torch.bfloat16, device=device)
+    ws1 = torch.zeros(tl.tl_ag_gemm_workspace_bytes(1, m, n, kr), dtype=torch.uint8, device=device)
+    gemm_alone(out["rs_70b"], lambda: [tl.tl_ag_gemm(ctx, [a[p]], b[p], cp, ws1, stream=stream) for p in range(W)],
+               2.0 * W * m * n * kr)
+    oracle_time(out["rs_70b"], "rs_70b", inp, args)
+    del a, b, o, ws, cp, ws1
 
     # MLP chain
     d = WORKLOADS["mlp2_8b"].dims
@@ -376,7 +394,20 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     ws = torch.zeros(tl.tl_mlp2_workspace_bytes(W, T, hdim, f), dtype=torch.uint8, device=device)
     rec("mlp2_8b", lambda: tl.tl_mlp2(ctx, x, w1, w2, o, ws, stream=stream), 2.0 * W * T * hdim * f * 2, 0,
         "tensor", 1)
-    del x, w1, w2, o, ws
+    # the same 2 W products as plain GEMMs (no gather, GELU, chaining or reduction)
+    xg = torch.cat(x, dim=0)
+    hbuf = torch.empty((T, f), dtype=torch.bfloat16, device=device)
+    ybuf = torch.empty((T, hdim), dtype=torch.bfloat16, device=device)
+    ws1 = torch.zeros(max(tl.tl_ag_gemm_workspace_bytes(1, T, f, hdim), tl.tl_ag_gemm_workspace_bytes(1, T, hdim, f)),
+                      dtype=torch.uint8, device=device)
+
+    def mlp_plain():
+        for r in range(W):
+            tl.tl_ag_gemm(ctx, [xg], w1[r], hbuf, ws1, stream=stream)
+            tl.tl_ag_gemm(ctx, [hbuf], w2[r], ybuf, ws1, stream=stream)
+    gemm_alone(out["mlp2_8b"], mlp_plain, 2.0 * W * T * hdim * f * 2)
+    oracle_time(out["mlp2_8b"], "mlp2_8b", inp, args)
+    del x, w1, w2, o, ws, xg, hbuf, ybuf, ws1
 
     # MoE layer
     d = WORKLOADS["moe_64e"].dims
@@ -391,6 +422,7 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     moe_bytes = 3.0 * E * H * F * 2 + T * H * 2 + T * H * 4 + T * E * 4
     rec("moe_64e", lambda: tl.tl_moe_combine(ctx, xx, lg, kk, wg, wu, wd, oo, ws, stream=stream), moe_flops,
         moe_bytes, "hbm", 4)
+    oracle_time(out["moe_64e"], "moe_64e", inp, args)
     del xx, lg, wg, wu, wd, oo, ws
 
     # AllGather KV + self-attention (Attn-1 at 16k on 8 ranks)
@@ -404,6 +436,7 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     ws = torch.zeros(tl.tl_ag_attention_workspace_bytes(W, Hh, L, hd), dtype=torch.uint8, device=device)
     rec("attn_16k", lambda: tl.tl_ag_attention(ctx, q, ks, vs, ao, ws, stream=stream), 4.0 * L * W * L * hd * Hh, 0,
         "tensor", 1)
+    oracle_time(out["attn_16k"], "attn_16k", inp, args)
     return out
 
 
@@ -492,6 +525,83 @@ def cpu_baseline_ag(inp, seconds):
             "sample": f"C rows 0..{rows - 1} of each of the {W} shards x all {n_full} columns "
                       f"({fl / 1e9:.1f} GFLOP of {2.0 * W * mpr * n_full * k / 1e9:.1f}), float64 numpy",
             "seconds": round(dt, 3)}
+
+
+def oracle_time(r, name, inp, args):
+    """The fp64 oracle, as it stands, on a bounded sample of one workload: the sample
+    doubles until one run takes a third of the budget (or covers the workload); the
+    rate is scaled to the full workload's FLOPs."""
+    if args.no_cpu or dist_env()[0] != 0:
+        return
+    import oracle
+    from seeded_inputs import WORKLOADS
+    d = WORKLOADS[name].dims
+    budget = args.cpu_seconds / 5
+
+    def run(n):  # -> (seconds, sample FLOPs, description, full FLOPs, n at the full workload)
+        if name == "rs_70b":
+            W, m, nn, kr = d["W"], d["m"], d["n"], d["k_r"]
+            t0 = time.perf_counter()
+            oracle.gemm_rs([x[:n] for x in inp["a"]], inp["b"])
+            return (time.perf_counter() - t0, 2.0 * W * n * nn * kr, f"rows 0..{n - 1} of S (all {W} producers)",
+                    2.0 * W * m * nn * kr, m)
+        if name == "mlp2_8b":
+            W, T, hdim, f = d["W"], d["tokens"], d["hidden"], d["f_r"]
+            r = n // W
+            t0 = time.perf_counter()
+            oracle.mlp2([x[:r] for x in inp["x_shards"]], inp["w1"], inp["w2"])
+            return (time.perf_counter() - t0, 2.0 * W * (W * r) * hdim * f * 2, f"the first {r} tokens of each shard",
+                    2.0 * W * T * hdim * f * 2, T)
+        if name == "moe_64e":
+            T, H, F, kk = d["T"], d["H"], d["F"], d["topk"]
+            t0 = time.perf_counter()
+            oracle.moe(inp["x"][:n], inp["logits"][:n], inp["w_gate"], inp["w_up"], inp["w_down"], kk)
+            return (time.perf_counter() - t0, 2.0 * n * kk * H * F * 3, f"tokens 0..{n - 1}", 2.0 * T * kk * H * F * 3, T)
+        W, Hh, L, hd = d["W"], d["heads"], d["l_r"], d["d"]
+        heads, rows = ([0], range(n)) if n <= L else (range(n // L), range(L))  # n (head, row) pairs
+        t0 = time.perf_counter()
+        oracle.ag_attention_rows(inp["q"], inp["k_shards"], inp["v_shards"], heads, rows)
+        desc = f"head 0, query rows 0..{n - 1}" if n <= L else f"heads 0..{n // L - 1}, all {L} query rows"
+        return (time.perf_counter() - t0, 4.0 * len(heads) * len(rows) * W * L * hd, desc,
+                4.0 * L * W * L * hd * Hh, L * Hh)
+
+    # Sizes double until one run takes a third of the budget; the full-workload time is
+    # extrapolated from the last two runs (the per-call widening of the weights is a fixed
+    # cost, the rest grows with the sample).
+    n, runs = 32, []
+    while True:
+        dt, fl, desc, full, n_full = run(n)
+        runs.append((n, dt, fl, desc))
+        if (dt >= budget / 3 and len(runs) >= 2) or n >= n_full:
+            break
+        n = min(n_full, n * 2)
+    n1, t1, fl1, desc1 = runs[-1]
+    if n1 >= n_full or len(runs) < 2:
+        est = t1
+    else:
+        n0, t0 = runs[-2][0], runs[-2][1]
+        est = t1 + max(0.0, (t1 - t0) / (n1 - n0)) * (n_full - n1)
+    r["cpu_oracle"] = {"tflops": round(full / est / 1e12, 6), "est_full_s": round(est, 2), "seconds": round(t1, 3),
+                       "sample": f"{desc1} ({fl1 / 1e9:.2f} GFLOP of {full / 1e9:.1f}) and the run at half that size, "
+                                 f"extrapolated to the full workload; float64 numpy",
+                       "cores": oracle_threads()}
+
+
+def cpu_single_thread_ag(seconds):
+    """The headline oracle sample again, in a child process limited to one BLAS thread."""
+    import subprocess
+    code = ("import json, bench; from seeded_inputs import workload_inputs; inp = workload_inputs(bench.WORKLOAD); "
+            f"r = bench.cpu_baseline_ag(inp, {seconds!r}); print(json.dumps(r))")
+    env = dict(os.environ)
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = "1"
+    try:
+        p = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                           timeout=max(120, 10 * seconds))
+        r = json.loads(p.stdout.strip().splitlines()[-1])
+        return {"value": r["value"], "unit": r["unit"], "cores": 1, "sample": r["sample"], "seconds": r["seconds"]}
+    except Exception as e:  # reported, not fatal: the all-core figure stands
+        return {"error": str(e)[:200]}
 
 
 # ----------------------------------------------------------------------------- reference arm
