@@ -419,7 +419,9 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     oo = torch.empty((T, H), dtype=torch.float32, device=device)
     ws = torch.zeros(tl.tl_moe_workspace_bytes(T, H, E, F, kk), dtype=torch.uint8, device=device)
     moe_flops = 2.0 * T * kk * H * F * 3
-    moe_bytes = 3.0 * E * H * F * 2 + T * H * 2 + T * H * 4 + T * E * 4
+    # algorithmic bytes: the expert weights, x, logits and out once; the intermediates the
+    # layer materialises (the gathered rows Xp, h and y, all bf16) written once and read once
+    moe_bytes = 3.0 * E * H * F * 2 + T * H * 2 + T * E * 4 + T * H * 4 + 2.0 * T * kk * (H * 2 + F * 2 + H * 2)
     rec("moe_64e", lambda: tl.tl_moe_combine(ctx, xx, lg, kk, wg, wu, wd, oo, ws, stream=stream), moe_flops,
         moe_bytes, "hbm", 4)
     oracle_time(out["moe_64e"], "moe_64e", inp, args)
