@@ -24,12 +24,10 @@ constexpr int kMaxTopk = 8;
 // lower expert index), softmax over all E logits in fp32 taken at the chosen experts.
 // Also zeroes the token's fp32 output row (the combine adds into it).
 __global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E, int topk, int* __restrict__ experts,
-                                 float* __restrict__ gates, float* __restrict__ out, int H) {
+                                 float* __restrict__ gates) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
-  float4* orow = reinterpret_cast<float4*>(out + static_cast<size_t>(t) * H);
-  for (int c = lane; c < H / 4; c += 32) orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 
   constexpr int kPer = kMaxExperts / 32;
   float v[kPer];
@@ -92,7 +90,8 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
                                                            int* __restrict__ perm, int2* __restrict__ row_meta,
                                                            int* __restrict__ tile_expert, int* __restrict__ tile_rows,
                                                            int* __restrict__ num_mtiles, int* __restrict__ counts,
-                                                           int* __restrict__ perm_out, int* __restrict__ counts_out) {
+                                                           int* __restrict__ perm_out, int* __restrict__ counts_out,
+                                                           float4* __restrict__ out, size_t out_vec) {
   __shared__ int hist[kMaxExperts];
   __shared__ int off[kMaxExperts + 1];
   __shared__ int poff[kMaxExperts + 1];
@@ -100,6 +99,14 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
   __shared__ int warp_pre[32];
   const int e = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (e >= E) {
+    // CTAs past the experts zero the fp32 output the combine partition adds into, on the
+    // SMs the per-expert CTAs leave idle.
+    const size_t nz = gridDim.x - E;
+    for (size_t i = (e - E) * static_cast<size_t>(blockDim.x) + tid; i < out_vec; i += nz * blockDim.x)
+      out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
   for (int i = tid; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   for (int a = tid; a < n; a += blockDim.x) {
@@ -569,9 +576,12 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
   __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
 
-  moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, experts, gates, out, H);
-  moe_permute_kernel<<<E, 1024, 0, st>>>(experts, T * topk, E, topk, gates, perm, row_meta, tile_expert, tile_rows, num_mtiles,
-                                         counts, perm_out, counts_out);
+  moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, experts, gates);
+  const int zero_ctas = ctx->sms > E ? ctx->sms - E : 1;
+  moe_permute_kernel<<<E + zero_ctas, 1024, 0, st>>>(experts, T * topk, E, topk, gates, perm, row_meta, tile_expert,
+                                                     tile_rows, num_mtiles, counts, perm_out, counts_out,
+                                                     reinterpret_cast<float4*>(out),
+                                                     static_cast<size_t>(T) * H / 4);
   if (cudaGetLastError() != cudaSuccess) return TL_ERR_CUDA;
 
   MoeParams p;
