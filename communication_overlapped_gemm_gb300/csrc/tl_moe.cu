@@ -114,12 +114,40 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
     if (ex < static_cast<unsigned>(E)) atomicAdd(&hist[ex], 1);  // never index outside the table
   }
   __syncthreads();
-  if (tid == 0) {
-    off[0] = 0;
-    poff[0] = 0;
-    for (int i = 0; i < E; ++i) {
-      off[i + 1] = off[i] + hist[i];
-      poff[i + 1] = poff[i] + (hist[i] + kBM - 1) / kBM * kBM;
+  if (warp == 0) {  // exclusive prefix sums of the counts and the 128-padded counts (E <= 256)
+    int c[kMaxExperts / 32], pc[kMaxExperts / 32];
+    int sc = 0, sp = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxExperts / 32; ++k) {  // lane holds experts [lane * per, lane * per + per)
+      const int i = lane * (kMaxExperts / 32) + k;
+      c[k] = i < E ? hist[i] : 0;
+      pc[k] = (c[k] + kBM - 1) / kBM * kBM;
+      sc += c[k];
+      sp += pc[k];
+    }
+    int ic = sc, ip = sp;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int uc = __shfl_up_sync(0xffffffffu, ic, o), up = __shfl_up_sync(0xffffffffu, ip, o);
+      if (lane >= o) {
+        ic += uc;
+        ip += up;
+      }
+    }
+    int rc = ic - sc, rp = ip - sp;
+#pragma unroll
+    for (int k = 0; k < kMaxExperts / 32; ++k) {
+      const int i = lane * (kMaxExperts / 32) + k;
+      if (i < E) {
+        off[i] = rc;
+        poff[i] = rp;
+      }
+      rc += c[k];
+      rp += pc[k];
+    }
+    if (lane == 31) {  // the totals
+      off[E] = ic;
+      poff[E] = ip;
     }
   }
   __syncthreads();
@@ -131,9 +159,15 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
   const int seg = ((n + nw - 1) / nw + 31) & ~31;
   const int s0 = warp * seg, s1 = min(n, s0 + seg);
   int mine_cnt = 0;
-  for (int a0 = s0; a0 < s1; a0 += 32) {
-    const int a = a0 + lane;
-    mine_cnt += __popc(__ballot_sync(0xffffffffu, a < s1 && experts[a] == e));
+  for (int a0 = s0; a0 < s1; a0 += 32 * 8) {  // eight independent loads per lane in flight
+    int ex[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int a = a0 + 32 * u + lane;
+      ex[u] = a < s1 ? experts[a] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) mine_cnt += __popc(__ballot_sync(0xffffffffu, ex[u] == e));
   }
   if (lane == 0) warp_tot[warp] = mine_cnt;
   __syncthreads();
@@ -149,17 +183,26 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
   }
   __syncthreads();
   int running = warp_pre[warp];
-  for (int a0 = s0; a0 < s1; a0 += 32) {
-    const int a = a0 + lane;
-    const bool mine = a < s1 && experts[a] == e;
-    const uint32_t ball = __ballot_sync(0xffffffffu, mine);
-    if (mine) {
-      const int pos = running + __popc(ball & ((1u << lane) - 1u));
-      perm[off[e] + pos] = a;
-      if (perm_out) perm_out[off[e] + pos] = a;
-      row_meta[poff[e] + pos] = make_int2(a / topk, __float_as_int(gates[a]));
+  for (int a0 = s0; a0 < s1; a0 += 32 * 8) {
+    int ex[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int a = a0 + 32 * u + lane;
+      ex[u] = a < s1 ? experts[a] : -1;
     }
-    running += __popc(ball);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int a = a0 + 32 * u + lane;
+      const bool mine = ex[u] == e;
+      const uint32_t ball = __ballot_sync(0xffffffffu, mine);
+      if (mine) {
+        const int pos = running + __popc(ball & ((1u << lane) - 1u));
+        perm[off[e] + pos] = a;
+        if (perm_out) perm_out[off[e] + pos] = a;
+        row_meta[poff[e] + pos] = make_int2(a / topk, __float_as_int(gates[a]));
+      }
+      running += __popc(ball);
+    }
   }
   const int cnt = hist[e];
   const int padded = poff[e + 1] - poff[e];
