@@ -44,14 +44,32 @@ UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
 # DRAM bytes per launch of the dominant kernel from ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by the hash of the CUDA sources they were taken on.
+# dram__bytes_write.sum), keyed by the hash of the kernel's sources (AG_KERNEL_SOURCES) they
+# were taken on.
 # A kernel changed since the capture reports traffic null.
-NCU_TRAFFIC = {"ag_70b": {"c5ef0221add98294": 618765824}}  # profiles/ag_70b_persistent_kernel_ncu.md
+NCU_TRAFFIC = {"ag_70b": {"62ba51ac7f0cea8e": 618765824}}  # profiles/ag_70b_persistent_kernel_ncu.md
 
 
-def src_hash() -> str:
+# The sources the AllGather+GEMM kernel is compiled from: its translation unit and every
+# header it includes (the ABI header too).
+AG_KERNEL_SOURCES = ["communication_overlapped_gemm_gb300/csrc/tl_gemm_ops.cu",
+                     "communication_overlapped_gemm_gb300/csrc/tl_engine.cuh",
+                     "communication_overlapped_gemm_gb300/csrc/tl_engine2.cuh",
+                     "communication_overlapped_gemm_gb300/csrc/tl_ptx.cuh",
+                     "communication_overlapped_gemm_gb300/csrc/tl_sched.h",
+                     "communication_overlapped_gemm_gb300/csrc/tl_host.h",
+                     "include/tl.h"]
+
+
+def src_hash(files=None) -> str:
+    """Hash of the given source files (paths from the repository root), by default of every
+    file of the CUDA sources."""
+    if files is None:
+        paths = sorted(glob.glob(os.path.join(ROOT, "communication_overlapped_gemm_gb300", "csrc", "*")))
+    else:
+        paths = [os.path.join(ROOT, f) for f in sorted(files)]
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "communication_overlapped_gemm_gb300", "csrc", "*"))):
+    for f in paths:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
             h.update(fh.read())
@@ -245,7 +263,7 @@ def run_ours(args):
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
     launch_ms = statistics.mean(times)
     achieved = flops / (launch_ms * 1e-3) / 1e12
-    h = src_hash()
+    h = src_hash(AG_KERNEL_SOURCES)
     traffic = NCU_TRAFFIC.get(WORKLOAD, {}).get(h)
 
     line = {
