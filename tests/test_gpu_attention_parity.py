@@ -34,7 +34,8 @@ def run_attn(inp, rank=0, **cfg):
     return out, kg
 
 
-@pytest.mark.parametrize("W,H,L,rank", [(2, 2, 128, 0), (1, 1, 128, 0), (3, 2, 256, 2), (4, 1, 384, 1), (3, 3, 128, 1)])
+@pytest.mark.parametrize("W,H,L,rank", [(2, 2, 128, 0), (1, 1, 128, 0), (3, 2, 256, 2), (4, 1, 384, 1), (3, 3, 128, 1),
+                                        (8, 1, 128, 7)])
 def test_ag_attention_matches_oracle(W, H, L, rank):
     inp = make_inputs("ag_attn", 80 + W, W=W, heads=H, l_r=L, d=128)
     out, kg = run_attn(inp, rank=rank)
