@@ -230,7 +230,7 @@ def tl_ag_attention_workspace_bytes(W, heads, l_r, d) -> int:
 
 def tl_ag_attention(ctx: Context, q, k_shards, v_shards, out, workspace, rank: int = 0, stream=None) -> None:
     """out[h] = softmax(q[h] K[h]^T / sqrt(d)) V[h] over the rank-order gather of the K/V
-    shards (bf16 [heads, l_r, d] each); the copy engine gathers them, overlapped."""
+    shards (bf16 [heads, l_r, d] each); the kernel's mover warps gather them, overlapped."""
     W = len(k_shards)
     _need(q, "bf16", "q"); _need(out, "bf16", "out"); _need(workspace, "u8", "workspace")
     for i in range(W):

@@ -42,7 +42,6 @@ constexpr float kRescaleLog2 = 8.0f;  // move the running max once it grows by m
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMovers = 2;
 constexpr int kThreads = (6 + kMovers) * 32;
-constexpr size_t kBlockBytes = static_cast<size_t>(kBKV) * kD * 2;  // one K or V block
 }  // namespace attn
 
 struct AttnParams {
@@ -86,6 +85,9 @@ __device__ __forceinline__ void attn_mma_pv(uint32_t d, uint32_t p0, uint32_t v0
                 (acc || kb || k) ? 1u : 0u);
 }
 
+// Ragged: some shard length l_r is not a multiple of 128 (a partial last key block of every
+// shard and a partial last query tile); the common case is compiled without those checks.
+template <bool Ragged>
 __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   using namespace attn;
   extern __shared__ uint8_t smem_raw[];
@@ -110,9 +112,9 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Common& c = p.common;
-  const int bps = p.Lr / kBKV;        // key blocks per shard
-  const int nblk = p.W * bps;         // key blocks per item
-  const int nqt = p.Lq / kBQ;
+  const int bps = (p.Lr + kBKV - 1) / kBKV;  // key blocks per shard (the last may be partial)
+  const int nblk = p.W * bps;                 // key blocks per item
+  const int nqt = (p.Lq + kBQ - 1) / kBQ;     // query tiles (the last may be partial)
   const int nwork = p.heads * nqt;
   if (threadIdx.x == 0) {
     mbar_init(qfull, 1);
@@ -259,9 +261,13 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
     for (int it = blockIdx.x; it < nwork && ok; it += gridDim.x, J0 += nblk) {
       const int h = it / nqt, qt = it - h * nqt;
       float m2 = -INFINITY, l = 0.f;  // running max (base-2 units) and sum of the row
+      int blk = -1;                   // block index inside the current shard
       for (int j = 0; j < nblk && ok; ++j) {
         const int J = J0 + j, s = J & 1;
+        if (++blk == bps) blk = 0;
         const uint32_t ph = (J >> 1) & 1;
+        // The wait results are warp-uniform, as the warp-collective TMEM accesses below need:
+        // the converged warp runs each try_wait and timer read as one instruction.
         ok = mbar_wait(&sfull[s], ph, c, kSiteTmemFull);
         if (!ok) break;
         tc_fence_after();
@@ -280,6 +286,15 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfree[s]);
+        if constexpr (Ragged) {
+          // keys past the end of a shard (its partial last block, zero-filled by TMA) get no
+          // weight: their scores become -inf before the maximum
+          const int valid = p.Lr - blk * kBKV;
+          if (valid < kBKV) {
+#pragma unroll
+            for (int i = 0; i < 128; ++i) x[i] = i < valid ? x[i] : -INFINITY;
+          }
+        }
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = x[i];
@@ -350,18 +365,23 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
       if (ok) ok = mbar_wait(&pfree[Jl & 1], (Jl >> 1) & 1, c, kSiteTmemFull);
       tc_fence_after();
       if (ok) {
+        // Every lane takes part in the (warp-collective) TMEM loads; rows past the end of
+        // the queries (a partial last tile) are only not stored.
+        const bool live = !Ragged || qt * kBQ + row < p.Lq;
         const float inv = 1.0f / l;
         uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(h) * p.Lq + qt * kBQ + row) * kD);
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           float o[32];
           tmem_ld32(tmem + 256 + cb * 32 + lane_off, o);
+          if (live) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            dst[cb * 4 + u] = make_uint4(pack_bf16x2(o[8 * u] * inv, o[8 * u + 1] * inv),
-                                         pack_bf16x2(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
-                                         pack_bf16x2(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
-                                         pack_bf16x2(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
+            for (int u = 0; u < 4; ++u)
+              dst[cb * 4 + u] = make_uint4(pack_bf16x2(o[8 * u] * inv, o[8 * u + 1] * inv),
+                                           pack_bf16x2(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
+                                           pack_bf16x2(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
+                                           pack_bf16x2(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
+          }
         }
       }
       tc_fence_before();
@@ -378,12 +398,22 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
       const int i = g / per_step, rem = g - i * per_step;
       const int hh = rem / bps, b = rem - hh * bps;
       const int r = (p.rank + 1 + i) % p.W;
-      const size_t src = (static_cast<size_t>(hh) * bps + b) * kBlockBytes;
-      const size_t dst = ((static_cast<size_t>(r) * p.heads + hh) * bps + b) * kBlockBytes;
-      copy_chunk(reinterpret_cast<const uint4*>(p.kshard[r] + src), reinterpret_cast<uint4*>(p.kg + dst),
-                 kBlockBytes / 16, lane, 32);
-      copy_chunk(reinterpret_cast<const uint4*>(p.vshard[r] + src), reinterpret_cast<uint4*>(p.vg + dst),
-                 kBlockBytes / 16, lane, 32);
+      const size_t rows = static_cast<size_t>(min(kBKV, p.Lr - b * kBKV));  // the last block may be partial
+      const size_t row_bytes = static_cast<size_t>(kD) * 2;
+      const size_t src = (static_cast<size_t>(hh) * p.Lr + static_cast<size_t>(b) * kBKV) * row_bytes;
+      const size_t dst = ((static_cast<size_t>(r) * p.heads + hh) * p.Lr + static_cast<size_t>(b) * kBKV) * row_bytes;
+      constexpr size_t kFullVec = static_cast<size_t>(kBKV) * kD * 2 / 16;  // a full block in 16-byte vectors
+      if (!Ragged || rows == static_cast<size_t>(kBKV)) {  // full blocks: a compile-time trip count
+        copy_chunk(reinterpret_cast<const uint4*>(p.kshard[r] + src), reinterpret_cast<uint4*>(p.kg + dst), kFullVec,
+                   lane, 32);
+        copy_chunk(reinterpret_cast<const uint4*>(p.vshard[r] + src), reinterpret_cast<uint4*>(p.vg + dst), kFullVec,
+                   lane, 32);
+      } else {
+        copy_chunk(reinterpret_cast<const uint4*>(p.kshard[r] + src), reinterpret_cast<uint4*>(p.kg + dst),
+                   rows * row_bytes / 16, lane, 32);
+        copy_chunk(reinterpret_cast<const uint4*>(p.vshard[r] + src), reinterpret_cast<uint4*>(p.vg + dst),
+                   rows * row_bytes / 16, lane, 32);
+      }
       __threadfence();
       __syncwarp();
       if (lane == 0) st_release_gpu(p.flags + (static_cast<size_t>(r) * p.heads + hh) * bps + b, c.epoch);
@@ -405,14 +435,14 @@ using namespace tl;
 static size_t attn_al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static bool attn_shape_ok(int W, int heads, int l_r, int d) {
-  return W >= 1 && W <= 8 && heads >= 0 && l_r >= 0 && d == attn::kD && l_r % attn::kBKV == 0 &&
+  return W >= 1 && W <= 8 && heads >= 0 && l_r >= 0 && d == attn::kD &&
          static_cast<long long>(W) * l_r < (1LL << 30);
 }
 
 extern "C" size_t tl_ag_attention_workspace_bytes(int W, int heads, int l_r, int d) {
   if (!attn_shape_ok(W, heads, l_r, d)) return 0;
   const size_t kv = static_cast<size_t>(heads) * W * l_r * d * 2;
-  const size_t flags = static_cast<size_t>(W) * heads * (l_r / attn::kBKV) * 8;
+  const size_t flags = static_cast<size_t>(W) * heads * ((l_r + attn::kBKV - 1) / attn::kBKV) * 8;
   return 2 * attn_al256(kv) + attn_al256(flags);
 }
 
@@ -460,7 +490,7 @@ extern "C" int tl_ag_attention(tl_ctx* ctx, int W, int rank, const void* q, cons
 
   // One cooperative CTA per SM: a CTA waiting on a block's signal is co-resident with the
   // mover warps that will set it.
-  auto kern = attn_kernel;
+  auto kern = l_r % attn::kBKV == 0 ? attn_kernel<false> : attn_kernel<true>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmem) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_CUDA;

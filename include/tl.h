@@ -264,7 +264,8 @@ int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, int topk, co
  * signalled.  The pages run this gather on the copy engine from a second stream; that makes
  * the kernel wait on work outside its own launch, which nothing guarantees to run alongside
  * it, so the gather runs inside the kernel, as for tl_ag_gemm.
- * Shapes: 1 <= W <= 8; d == 128; l_r % 128 == 0.  heads == 0 or l_r == 0 is a no-op.
+ * Shapes: 1 <= W <= 8; d == 128; any l_r (a shard's last 128-key block and the last 128-query
+ * tile may be partial).  heads == 0 or l_r == 0 is a no-op.
  */
 size_t tl_ag_attention_workspace_bytes(int W, int heads, int l_r, int d);
 int tl_ag_attention(tl_ctx* ctx, int W, int rank, const void* q, const void* const* k_shards,

@@ -45,6 +45,17 @@ def test_ag_attention_matches_oracle(W, H, L, rank):
     assert np.array_equal(np.concatenate(list(kg), axis=1), oracle.attn_gather(inp["k_shards"]))
 
 
+@pytest.mark.parametrize("W,H,L,rank", [(3, 2, 200, 1), (2, 1, 100, 0), (1, 1, 72, 0), (4, 2, 130, 3)])
+def test_ag_attention_ragged_lengths(W, H, L, rank):
+    """Shard lengths that are not a multiple of 128: each shard's last key block and the last
+    query tile are partial (the absent keys get no weight, the absent rows are not stored)."""
+    inp = make_inputs("ag_attn", 97 + L, W=W, heads=H, l_r=L, d=128)
+    out, kg = run_attn(inp, rank=rank)
+    ref = oracle.ag_attention(inp["q"], inp["k_shards"], inp["v_shards"])
+    assert_close(bf16_to_f64(out), ref, f"attention W={W} H={H} L={L} rank={rank}")
+    assert np.array_equal(np.concatenate(list(kg), axis=1), oracle.attn_gather(inp["k_shards"]))
+
+
 def test_ag_attention_peaked_scores():
     """Large-magnitude queries make the softmax peaked and its running maximum move a lot
     from block to block (the rescale of O in TMEM)."""
