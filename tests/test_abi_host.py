@@ -71,6 +71,13 @@ def test_workspace_sizes(tl):
     assert tl.tl_moe_workspace_bytes(4096, 2048, 64, 1408, 2) > 0
     assert tl.tl_moe_workspace_bytes(4096, 2000, 64, 1408, 2) == 0    # H not a 256 multiple
     assert tl.tl_moe_workspace_bytes(4096, 2048, 300, 1408, 2) == 0   # E > 256
+    al = lambda x: (x + 255) // 256 * 256
+    # attention: gathered K and V, then one signal per (shard, head, 128-key block), the last
+    # block of a shard partial when l_r is not a multiple of 128
+    assert tl.tl_ag_attention_workspace_bytes(8, 32, 2048, 128) == 2 * al(8 * 32 * 2048 * 128 * 2) + al(8 * 32 * 16 * 8)
+    assert tl.tl_ag_attention_workspace_bytes(3, 2, 200, 128) == 2 * al(3 * 2 * 200 * 128 * 2) + al(3 * 2 * 2 * 8)
+    assert tl.tl_ag_attention_workspace_bytes(2, 2, 128, 64) == 0    # head dim other than 128
+    assert tl.tl_ag_attention_workspace_bytes(9, 2, 128, 128) == 0   # W > 8
 
 
 def test_argument_validation_needs_no_gpu(tl):
