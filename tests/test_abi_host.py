@@ -89,6 +89,7 @@ def test_argument_validation_needs_no_gpu(tl):
     assert L.tl_mlp2(None, 2, ptrs, ptrs, ptrs, ptrs, 16, 1 << 20, 256, 256, 256, None) == tl.TL_ERR_INVALID
     assert L.tl_moe_combine(None, 16, 16, 2, 16, 16, 16, 16, None, None, 16, 1 << 20, 64, 256, 4, 128,
                             None) == tl.TL_ERR_INVALID
+    assert L.tl_ag_attention(None, 2, 0, 16, ptrs, ptrs, 16, 16, 1 << 20, 2, 128, 128, None) == tl.TL_ERR_INVALID
     assert L.tl_ag_gemm_static_scratch(None, 2, 0, ptrs, 16, 16, 128, 256, 256, None) == tl.TL_ERR_INVALID
     assert L.tl_allgather(None, 2, 0, ptrs, 16, 1 << 20, 128, 256, None) == tl.TL_ERR_INVALID
     assert L.tl_ctx_check(None) == tl.TL_ERR_INVALID
