@@ -8,7 +8,7 @@
 // is non-causal flash attention over all W shards on tcgen05, head dim 128:
 //   warp 0    TMA producer: the item's Q, then per 128-key block K (2 boxes) and V (4 boxes)
 //             through 2-stage rings; the first block of a remote shard slice waits on the
-//             slice's 16 block signals (one warp-wide poll).
+//             slice's block signals (one warp-wide poll).
 //   warp 1    TMEM allocation and the MMAs: S_j = Q K_j^T into one of two S buffers, then
 //             O += P_{j-1} V_{j-1} once the softmax warps have published P_{j-1}.
 //   warps 2-5 softmax, one query row per thread: S row from TMEM, running max and sum in
@@ -19,10 +19,13 @@
 //             max, which cancels in O / l.  A move rescales the warp's O rows in TMEM after
 //             the previous P V has completed; writing P waits only for the P V two blocks
 //             back.  Finally O / l as bf16.
-//   warps 6-7 movers: remote K/V blocks (32 KB each) into the shard-major gathered buffers,
-//             one release signal per block, the local shard last.
+//   warps 6-7 movers: remote K/V blocks (up to 32 KB each) into the shard-major gathered
+//             buffers, one release signal per block, the local shard last.
 // The pipeline counters run on across items.  TMEM columns: S0 [0, 128), S1 [128, 256),
 // O [256, 384).  Every wait is bounded.
+// Shard lengths need not be multiples of 128 (the Ragged instantiation): a shard's last key
+// block and the last query tile may be partial.  TMA zero-fills the absent rows, the softmax
+// gives the absent keys no weight, and the absent query rows are not stored.
 #include "tl_host.h"
 
 namespace tl {
