@@ -366,11 +366,13 @@ def tl_ag_gemm_static_scratch(ctx: Context, a_shards, b, c, rank: int = 0, strea
     fixed 16 MiB device array, so problems needing more raise TLError(TL_ERR_WORKSPACE),
     and calls whose GPU work overlaps race on that array."""
     W = len(a_shards)
+    m_per_rank, k = a_shards[0].shape
+    n = b.shape[1]
+    if b.shape[0] != k or tuple(c.shape) != (W * m_per_rank, n) or any(tuple(a.shape) != (m_per_rank, k) for a in a_shards):
+        raise ValueError("inconsistent shapes")
     for i, a in enumerate(a_shards):
         _need(a, "bf16", f"a_shards[{i}]")
     _need(b, "bf16", "b"); _need(c, "bf16", "c")
-    m_per_rank, k = a_shards[0].shape
-    n = b.shape[1]
     rc = lib().tl_ag_gemm_static_scratch(ctx.handle, W, rank, _ptrs(a_shards), _ptr(b), _ptr(c), m_per_rank, n, k,
                                          _stream(stream))
     _check(rc, "tl_ag_gemm_static_scratch")

@@ -490,8 +490,6 @@ __global__ void __launch_bounds__(kMaxMoverWarps * 32) allgather_kernel(const __
 using namespace tl;
 
 // ============================================================================ C ABI
-static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
 static bool ag_shape_ok(int W, int mpr, int n, int k) {
   return W >= 1 && W <= 8 && mpr >= 0 && n >= 0 && k >= 0 && mpr % kBM == 0 && n % 8 == 0 && k % 8 == 0;
 }
@@ -499,32 +497,50 @@ static bool ag_shape_ok(int W, int mpr, int n, int k) {
 // Tile rows used for a row extent: 256 when every block of the extent is a 256 multiple.
 static int pick_bm(int rows) { return rows % 256 == 0 ? 256 : 128; }
 
+namespace tl {
+AgLayout ag_layout(int W, int m_per_rank, int k) {
+  AgLayout L;
+  L.gath_bytes = static_cast<size_t>(W) * m_per_rank * k * 2;
+  L.flags_off = align256(L.gath_bytes);
+  L.flags_bytes = static_cast<size_t>(W) * (m_per_rank / kBM) * 32 * 8;
+  L.total = L.flags_off + align256(L.flags_bytes);
+  return L;
+}
+
+int ag_gemm_check(const tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b, const void* c,
+                  int m_per_rank, int n, int k) {
+  if (!ctx || !ag_shape_ok(W, m_per_rank, n, k) || rank < 0 || rank >= W) return TL_ERR_INVALID;
+  if (m_per_rank == 0 || n == 0 || k == 0) return TL_OK;
+  if (!a_shards || !b || !c) return TL_ERR_INVALID;
+  for (int r = 0; r < W; ++r)
+    if (!a_shards[r] || !aligned16(a_shards[r])) return TL_ERR_INVALID;
+  if (!aligned16(b) || !aligned16(c)) return TL_ERR_INVALID;
+  return TL_OK;
+}
+}  // namespace tl
+
 extern "C" size_t tl_ag_gemm_workspace_bytes(int W, int m_per_rank, int n, int k) {
   if (!ag_shape_ok(W, m_per_rank, n, k)) return 0;
-  const size_t gath = static_cast<size_t>(W) * m_per_rank * k * 2;
-  const size_t flags = static_cast<size_t>(W) * (m_per_rank / kBM) * 32 * 8;
-  return align256(gath) + align256(flags);
+  return ag_layout(W, m_per_rank, k).total;
 }
 
 extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b, void* c,
                           void* workspace, size_t workspace_bytes, int m_per_rank, int n, int k,
                           tl_stream_t stream) {
-  if (!ctx || !ag_shape_ok(W, m_per_rank, n, k) || rank < 0 || rank >= W) return TL_ERR_INVALID;
+  const int chk = ag_gemm_check(ctx, W, rank, a_shards, b, c, m_per_rank, n, k);
+  if (chk != TL_OK) return chk;
   if (m_per_rank == 0 || n == 0 || k == 0) return TL_OK;
-  if (!a_shards || !b || !c || !workspace) return TL_ERR_INVALID;
-  for (int r = 0; r < W; ++r)
-    if (!a_shards[r] || !aligned16(a_shards[r])) return TL_ERR_INVALID;
-  if (!aligned16(b) || !aligned16(c) || !aligned16(workspace)) return TL_ERR_INVALID;
-  if (workspace_bytes < tl_ag_gemm_workspace_bytes(W, m_per_rank, n, k)) return TL_ERR_WORKSPACE;
+  if (!workspace || !aligned16(workspace)) return TL_ERR_INVALID;
+  const AgLayout L = ag_layout(W, m_per_rank, k);
+  if (workspace_bytes < L.total) return TL_ERR_WORKSPACE;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
 
   AgParams p;
   std::memset(&p, 0, sizeof(p));
   const int M = W * m_per_rank;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t gath_bytes = static_cast<size_t>(M) * k * 2;
   p.gath = ws;
-  p.flags = reinterpret_cast<uint64_t*>(ws + align256(gath_bytes));
+  p.flags = reinterpret_cast<uint64_t*>(ws + L.flags_off);
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int bm = pick_bm(m_per_rank);
   const bool pair = bm == 256 && ctx->cfg.pair_ctas == 1;
@@ -720,13 +736,14 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   if (W == 1) return TL_OK;  // nothing to gather
   for (int r = 0; r < W; ++r)
     if (!a_shards[r] || !aligned16(a_shards[r])) return TL_ERR_INVALID;
-  if (workspace_bytes < tl_ag_gemm_workspace_bytes(W, m_per_rank, 8, k)) return TL_ERR_WORKSPACE;
+  const AgLayout L = ag_layout(W, m_per_rank, k);
+  if (workspace_bytes < L.total) return TL_ERR_WORKSPACE;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
   AgParams p;
   std::memset(&p, 0, sizeof(p));
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.gath = ws;
-  p.flags = reinterpret_cast<uint64_t*>(ws + align256(static_cast<size_t>(W) * m_per_rank * k * 2));
+  p.flags = reinterpret_cast<uint64_t*>(ws + L.flags_off);
   p.common = make_common(ctx);
   // The standalone mover kernel has no dynamic shared memory for span counters: no trace.
   p.common.trace_hdr = nullptr;

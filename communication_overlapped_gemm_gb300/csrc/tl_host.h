@@ -53,6 +53,27 @@ inline Common make_common(tl_ctx* ctx) {
 
 int set_smem_attr(const void* kern);
 
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace of the AllGather (alone or fused with the GEMM): the gathered operand T
+// (W x m_per_rank x k bf16, rank order) at offset 0, then the per-chunk signal words
+// (W x m_per_rank/128 slabs x 32 chunks, 8 bytes each), each region 256-byte aligned.
+// tl_ag_gemm_workspace_bytes, tl_ag_gemm, tl_allgather and tl_ag_gemm_static_scratch all
+// take their offsets from here.
+struct AgLayout {
+  size_t gath_bytes;   // the gathered operand
+  size_t flags_off;    // first signal word
+  size_t flags_bytes;  // all signal words
+  size_t total;
+};
+AgLayout ag_layout(int W, int m_per_rank, int k);
+
+// The argument checks of tl_ag_gemm that need no workspace (context, shape, rank, null and
+// misaligned pointers): TL_OK or the code tl_ag_gemm returns for them.  An empty problem
+// (a zero dimension) passes without looking at the pointers.
+int ag_gemm_check(const tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b, const void* c,
+                  int m_per_rank, int n, int k);
+
 
 // Cooperative launch of one persistent CTA per SM (or cfg.grid_ctas), so that every CTA
 // that waits on a signal is co-resident with the CTAs that will set it.  While the context

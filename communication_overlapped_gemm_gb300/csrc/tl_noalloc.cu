@@ -13,7 +13,10 @@
 // The array is kTlStaticScratchBytes (16 MiB) per GPU and stays allocated on every GPU
 // that loads this module until the process exits.  Its device address is looked up once
 // per device (cudaGetSymbolAddress with that device current) by the first call on that
-// device, so that first call should happen before any stream capture begins.  Every call
+// device, so that first call should happen before any stream capture begins.  The address
+// is kept for the life of the process: after cudaDeviceReset (or anything else that
+// destroys the device's primary context) it is stale, and this entry point must not be
+// called on that device again.  Every call
 // reuses the same array: the signal words are cleared at the start of each call and the
 // gathered operand is fully overwritten, so nothing carries over; but two calls whose GPU
 // work overlaps in time (unordered streams, several host threads) race on the array and
@@ -55,23 +58,21 @@ int scratch_address(int device, void** out) {
 }  // namespace tl
 
 // The fused AllGather + GEMM of tl_ag_gemm with the fixed array above as its workspace.
-// Problems whose workspace (tl_ag_gemm_workspace_bytes) exceeds the array are rejected
-// with TL_ERR_WORKSPACE before anything is enqueued.
+// Every argument check of tl_ag_gemm, and the size check against the array, runs before
+// anything is enqueued, so a refused call leaves the array and the stream untouched.
 extern "C" int tl_ag_gemm_static_scratch(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b,
                                          void* c, int m_per_rank, int n, int k, tl_stream_t stream) {
-  if (!ctx) return TL_ERR_INVALID;
-  if (m_per_rank == 0 || n == 0 || k == 0)  // empty problem: validated and finished without scratch
-    return tl_ag_gemm(ctx, W, rank, a_shards, b, c, nullptr, 0, m_per_rank, n, k, stream);
-  const size_t need = tl_ag_gemm_workspace_bytes(W, m_per_rank, n, k);
-  if (need == 0) return TL_ERR_INVALID;  // shape outside what tl_ag_gemm accepts
-  if (need > tl::kTlStaticScratchBytes) return TL_ERR_WORKSPACE;
+  const int chk = tl::ag_gemm_check(ctx, W, rank, a_shards, b, c, m_per_rank, n, k);
+  if (chk != TL_OK) return chk;
+  if (m_per_rank == 0 || n == 0 || k == 0) return TL_OK;  // empty problem: nothing to do, no scratch
+  const tl::AgLayout L = tl::ag_layout(W, m_per_rank, k);
+  if (L.total > tl::kTlStaticScratchBytes) return TL_ERR_WORKSPACE;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
   void* scratch = nullptr;
   const int rc = tl::scratch_address(ctx->device, &scratch);
   if (rc != TL_OK) return rc;
-  // Clear the signal words left by the previous call (they follow the gathered operand).
-  const size_t gath = (static_cast<size_t>(W) * m_per_rank * k * 2 + 255) & ~size_t(255);
-  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + gath, 0, need - gath,
+  // Clear the signal words the previous call left (another context's values included).
+  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + L.flags_off, 0, L.flags_bytes,
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_CUDA;

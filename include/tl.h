@@ -285,9 +285,13 @@ int tl_ag_attention(tl_ctx* ctx, int W, int rank, const void* q, const void* con
  * size is rejected with TL_ERR_WORKSPACE before anything is enqueued.  The entry point
  * allocates nothing (no cudaMalloc, cudaFree or allocating library call).  Its first call on a
  * device looks up the array's device address with that device current; make that first call
- * before any stream capture begins.  All calls share the one array (each call clears the
- * signals and overwrites the gathered operand), so calls whose GPU work overlaps in time race
- * and give undefined results: order them on one stream or with events.
+ * before any stream capture begins.  The address is kept for the life of the process: after
+ * cudaDeviceReset on that device (or anything else that destroys its primary context) the
+ * entry point must not be called on that device again.  Every argument check (those of
+ * tl_ag_gemm, then the size check) runs before anything is enqueued.  All calls share the one
+ * array (each call clears the signals and overwrites the gathered operand), so calls whose GPU
+ * work overlaps in time race and give undefined results: order them on one stream or with
+ * events.
  */
 #define TL_AG_GEMM_STATIC_SCRATCH_BYTES (16u << 20)
 int tl_ag_gemm_static_scratch(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b, void* c,

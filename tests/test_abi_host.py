@@ -150,3 +150,20 @@ def test_tile_order_rejects_bad_shapes(tl):
         tl.tl_ag_tile_order(2, 2, 128, 256, 1)
     with pytest.raises(tl.TLError):
         tl.tl_rs_tile_order(3, 1000, 256, 1)
+
+
+def test_static_scratch_binding_checks_shapes_before_any_call(tl):
+    """A wrong-shaped output or an uneven shard is refused by the binding itself, before the
+    library (or the GPU) sees the call: the kernel's tensor maps would otherwise be built for
+    shapes the buffers do not have."""
+    import torch
+    a = [torch.zeros((128, 256), dtype=torch.bfloat16) for _ in range(2)]
+    b = torch.zeros((256, 256), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="inconsistent shapes"):
+        tl.tl_ag_gemm_static_scratch(None, a, b, torch.zeros((128, 256), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="inconsistent shapes"):
+        tl.tl_ag_gemm_static_scratch(None, [a[0], torch.zeros((256, 256), dtype=torch.bfloat16)], b,
+                                     torch.zeros((256, 256), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="inconsistent shapes"):
+        tl.tl_ag_gemm_static_scratch(None, a, torch.zeros((128, 256), dtype=torch.bfloat16),
+                                     torch.zeros((256, 256), dtype=torch.bfloat16))

@@ -37,6 +37,24 @@ def test_static_scratch_matches_workspace_entry_point_on_two_calls():
             assert_close(got, oracle.ag_gemm(inp["a_shards"], inp["b"]), f"static scratch vs oracle W={W}")
 
 
+def test_static_scratch_after_another_context():
+    """Calls from two contexts share the one array: a call in a second context (its own,
+    unrelated signal values), then a call in the first, both match the oracle.  Each call
+    clears the signal words the other context left."""
+    import torch
+    inp = make_inputs("ag_gemm", 93, W=4, m_per_rank=128, n=256, k=384)
+    ref = oracle.ag_gemm(inp["a_shards"], inp["b"])
+    a = [to_dev_bf16(x) for x in inp["a_shards"]]
+    b = to_dev_bf16(inp["b"])
+    with tl.Context(0) as c1, tl.Context(0) as c2:
+        for ctx, rank in ((c2, 2), (c1, 0), (c2, 3), (c1, 1)):
+            c = torch.full((4 * 128, 256), float("nan"), dtype=torch.bfloat16, device="cuda")
+            tl.tl_ag_gemm_static_scratch(ctx, a, b, c, rank=rank)
+            torch.cuda.synchronize()
+            assert ctx.check() == tl.TL_OK
+            assert_close(bf16_to_f64(c), ref, f"static scratch, rank {rank}")
+
+
 def test_static_scratch_rejects_too_large_problem():
     import torch
     with tl.Context(0) as ctx:
