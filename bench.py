@@ -42,6 +42,7 @@ WORKLOAD = "ag_70b"
 METRIC = "fused AG+GEMM / GEMM+RS TFLOP/s on 1 GB300 (W emulated ranks); % BF16 peak"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+MOE_LAUNCHES = 3  # routing, permutation, the persistent expert-GEMM + combine kernel
 
 # DRAM bytes per launch of the dominant kernel from ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the hash of the kernel's sources (AG_KERNEL_SOURCES) they
@@ -322,6 +323,7 @@ def overlap_ag(tl, ctx, a, b, c, ws, flush, stream, device, fused_times, W, mpr,
         "t_fused_us": round(t_fused * 1e3, 2),
         "efficiency": round((t_copy + t_gemm - t_fused) / min(t_copy, t_gemm), 4),
         "copy_alone_gbs": round(moved / (t_copy * 1e-3) / 1e9, 1),
+        "copy_alone_hbm_frac": round(moved / (t_copy * 1e-3) / 1e9 / pk["hbm"], 4),
         "gemm_alone_tflops": round(ag_flops(W, mpr, n, k) / (t_gemm * 1e-3) / 1e12, 2),
         "gemm_alone_frac": round(ag_flops(W, mpr, n, k) / (t_gemm * 1e-3) / 1e12 / pk["bf16"], 4),
     }
@@ -352,6 +354,24 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
         r["gemm_alone_us"] = round(t * 1e3, 2)
         r["gemm_alone_tflops"] = round(flops / (t * 1e-3) / 1e12, 2)
         r["fused_over_gemm_alone"] = round(r["us"] / (t * 1e3), 4)
+
+    def rs_alone(r, fn, nbytes, extra=None):
+        """t_copy_alone of a fused GEMM+RS: its communication (and, for the MLP chain, its
+        AllGathers) alone; with t_gemm_alone and t_fused gives the overlap efficiency
+        (t_copy + t_gemm - t_fused) / min(t_copy, t_gemm)."""
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        if ctx.check() != tl.TL_OK:
+            raise RuntimeError("communication alone: device status not OK")
+        t = statistics.median(timed_steps(fn, max(5, reps), flush, stream))
+        tg, tf = r["gemm_alone_us"] * 1e-3, r["us"] * 1e-3
+        r["copy_alone_us"] = round(t * 1e3, 2)
+        r["copy_alone_gbs"] = round(nbytes / (t * 1e-3) / 1e9, 1)
+        r["copy_alone_hbm_frac"] = round(nbytes / (t * 1e-3) / 1e9 / pk["hbm"], 4)
+        r["overlap_efficiency"] = round((t + tg - tf) / min(t, tg), 4)
+        if extra:
+            r["copy_alone"] = extra
 
     def rec(name, fn, flops, bytes_alg, bound, launches):
         for _ in range(3):
@@ -398,8 +418,13 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     ws1 = torch.zeros(tl.tl_ag_gemm_workspace_bytes(1, m, n, kr), dtype=torch.uint8, device=device)
     gemm_alone(out["rs_70b"], lambda: [tl.tl_ag_gemm(ctx, [a[p]], b[p], cp, ws1, stream=stream) for p in range(W)],
                2.0 * W * m * n * kr)
+    del cp, ws1
+    # the communication alone: the ReduceScatter of the W ranks' fp32 partials (m x n each)
+    parts = [torch.randn((m, n), dtype=torch.float32, device=device) for _ in range(W)]
+    rs_alone(out["rs_70b"], lambda: tl.tl_reduce_scatter(ctx, parts, o, stream=stream), W * m * n * 4 + m * n * 2)
+    del parts
     oracle_time(out["rs_70b"], "rs_70b", inp, args)
-    del a, b, o, ws, cp, ws1
+    del a, b, o, ws
 
     # MLP chain
     d = WORKLOADS["mlp2_8b"].dims
@@ -424,8 +449,21 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
             tl.tl_ag_gemm(ctx, [xg], w1[r], hbuf, ws1, stream=stream)
             tl.tl_ag_gemm(ctx, [hbuf], w2[r], ybuf, ws1, stream=stream)
     gemm_alone(out["mlp2_8b"], mlp_plain, 2.0 * W * T * hdim * f * 2)
+    del xg, hbuf, ybuf, ws1
+    # the communication alone: every rank's AllGather of X, then the ReduceScatter of the W
+    # ranks' fp32 layer-2 partials (T x hidden each)
+    ws_ag = torch.zeros(tl.tl_ag_gemm_workspace_bytes(W, T // W, 8, hdim), dtype=torch.uint8, device=device)
+    parts = [torch.randn((T, hdim), dtype=torch.float32, device=device) for _ in range(W)]
+
+    def mlp_comm():
+        for r in range(W):
+            tl.tl_allgather(ctx, x, ws_ag, rank=r, stream=stream)
+        tl.tl_reduce_scatter(ctx, parts, o, stream=stream)
+    rs_alone(out["mlp2_8b"], mlp_comm, W * 2 * T * hdim * 2 + W * T * hdim * 4 + T * hdim * 2,
+             f"{W} AllGathers of X (tl_allgather, rank r each) + tl_reduce_scatter of {W} fp32 partials")
+    del ws_ag, parts
     oracle_time(out["mlp2_8b"], "mlp2_8b", inp, args)
-    del x, w1, w2, o, ws, xg, hbuf, ybuf, ws1
+    del x, w1, w2, o, ws
 
     # MoE layer
     d = WORKLOADS["moe_64e"].dims
@@ -441,7 +479,15 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     # layer materialises (the gathered rows Xp, h and y, all bf16) written once and read once
     moe_bytes = 3.0 * E * H * F * 2 + T * H * 2 + T * E * 4 + T * H * 4 + 2.0 * T * kk * (H * 2 + F * 2 + H * 2)
     rec("moe_64e", lambda: tl.tl_moe_combine(ctx, xx, lg, kk, wg, wu, wd, oo, ws, stream=stream), moe_flops,
-        moe_bytes, "hbm", 4)
+        moe_bytes, "hbm", MOE_LAUNCHES)
+    out["moe_64e"]["combine_sms"] = ctx.config.combine_ctas
+    # the workload as stated: the combine partition on 8 reserved SMs
+    with tl.Context(ctx.device, combine_ctas=8) as c8:
+        rec("moe_64e_8sm", lambda: tl.tl_moe_combine(c8, xx, lg, kk, wg, wu, wd, oo, ws, stream=stream), moe_flops,
+            moe_bytes, "hbm", MOE_LAUNCHES)
+        if c8.check() != tl.TL_OK:
+            raise RuntimeError("moe_64e_8sm: device status not OK")
+    out["moe_64e_8sm"]["combine_sms"] = 8
     oracle_time(out["moe_64e"], "moe_64e", inp, args)
     del xx, lg, wg, wu, wd, oo, ws
 

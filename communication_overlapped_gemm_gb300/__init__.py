@@ -22,7 +22,7 @@ from . import _build
 __all__ = [
     "TL_OK", "TL_ERR_INVALID", "TL_ERR_UNSUPPORTED", "TL_ERR_CUDA", "TL_ERR_TIMEOUT", "TL_ERR_WORKSPACE",
     "TLError", "Config", "Context", "lib", "library_path", "build",
-    "tl_ag_gemm", "tl_allgather", "tl_gemm_rs", "tl_mlp2", "tl_moe_combine",
+    "tl_ag_gemm", "tl_allgather", "tl_gemm_rs", "tl_reduce_scatter", "tl_mlp2", "tl_moe_combine",
     "tl_ag_gemm_workspace_bytes", "tl_gemm_rs_workspace_bytes", "tl_mlp2_workspace_bytes",
     "tl_moe_workspace_bytes", "tl_ag_tile_order", "tl_rs_tile_order", "tl_trace_bytes", "tl_ag_attention",
     "tl_ag_attention_workspace_bytes", "EXPORTED_SYMBOLS",
@@ -54,6 +54,7 @@ class Config(ctypes.Structure):
         ("debug_skip_chunk", _i),
         ("timeout_ns", ctypes.c_ulonglong),
         ("pair_ctas", _i),
+        ("moe_renorm", _i),
     ]
 
 
@@ -79,6 +80,7 @@ _SIGS = {
                      _vp, _c_size, _i, _i, _i, _vp]),
     "tl_moe_workspace_bytes": (_c_size, [_i, _i, _i, _i, _i]),
     "tl_moe_combine": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_size, _i, _i, _i, _i, _vp]),
+    "tl_reduce_scatter": (_i, [_vp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i, _i, _vp]),
     "tl_ag_gemm_static_scratch": (_i, [_vp, _i, _i, ctypes.POINTER(_vp), _vp, _vp, _i, _i, _i, _vp]),
     "tl_ag_attention_workspace_bytes": (_c_size, [_i, _i, _i, _i]),
     "tl_ag_attention": (_i, [_vp, _i, _i, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _vp, _c_size, _i, _i,
@@ -289,6 +291,20 @@ def tl_gemm_rs(ctx: Context, a, b, out, workspace, stream=None) -> None:
     rc = lib().tl_gemm_rs(ctx.handle, W, _ptrs(a), _ptrs(b), _ptrs(out), _ptr(workspace), workspace.numel(),
                           m, n, k_r, _stream(stream))
     _check(rc, "tl_gemm_rs")
+
+
+def tl_reduce_scatter(ctx: Context, partials, out, stream=None) -> None:
+    """ReduceScatter alone: out_o = rows_o(P_0 + ... + P_{W-1}) (fp32 partials, summed in order
+    p = 0..W-1, bf16 out)."""
+    W = len(partials)
+    m, n = partials[0].shape
+    if len(out) != W or any(tuple(x.shape) != (m, n) for x in partials) or \
+            any(tuple(x.shape) != (m // W, n) for x in out) or m % W:
+        raise ValueError("inconsistent shapes")
+    for i in range(W):
+        _need(partials[i], "f32", f"partials[{i}]"); _need(out[i], "bf16", f"out[{i}]")
+    rc = lib().tl_reduce_scatter(ctx.handle, W, _ptrs(partials), _ptrs(out), m, n, _stream(stream))
+    _check(rc, "tl_reduce_scatter")
 
 
 def tl_mlp2(ctx: Context, x_shards, w1, w2, out, workspace, stream=None) -> None:

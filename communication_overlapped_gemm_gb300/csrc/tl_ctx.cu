@@ -77,6 +77,7 @@ int tl_config_default(tl_config* cfg) {
   cfg->debug_skip_chunk = -1;
   cfg->timeout_ns = 2000000000ull;
   cfg->pair_ctas = 2;
+  cfg->moe_renorm = 0;
   return TL_OK;
 }
 
@@ -92,7 +93,7 @@ int tl_ctx_create(tl_ctx** out, int device, const tl_config* cfg) {
     tl_config_default(&c);
   if (c.mover_warps < 1 || c.mover_warps > tl::kMaxMoverWarps || !pow2_le32(c.chunks_per_slab) ||
       (c.swizzle != 0 && c.swizzle != 1) || c.grid_ctas < 0 || c.combine_ctas < 1 || c.timeout_ns == 0 ||
-      c.pair_ctas < 0 || c.pair_ctas > 2)
+      c.pair_ctas < 0 || c.pair_ctas > 2 || (c.moe_renorm != 0 && c.moe_renorm != 1))
     return TL_ERR_INVALID;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
@@ -232,7 +233,7 @@ int tl_rs_tile_order(int W, int m, int n, int swizzle, int* producer, int* owner
   if (!producer && !owner && !m_block && !n_block) return total;
   if (!producer || !owner || !m_block || !n_block || cap < total) return TL_ERR_INVALID;
   for (int t = 0; t < total; ++t) {
-    tl::RsTile r = tl::rs_tile(t, W, mbo, nbk, swizzle);
+    tl::RsTile r = tl::rs_tile(t, W, mbo, nbk, bm, swizzle);
     producer[t] = r.p;
     owner[t] = r.o;
     m_block[t] = r.mb * (bm / tl::kBM);

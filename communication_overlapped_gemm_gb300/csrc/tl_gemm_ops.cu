@@ -49,6 +49,10 @@ __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + copysignf(e, x));
 }
 
+#ifndef TL_RS_DISCARD
+#define TL_RS_DISCARD 1
+#endif
+
 // GEMM+RS epilogue on one BM x 256 partial tile of producer `prod` (of W), reduced into
 // the fp32 slot tile at (grow, n0); the last producer writes bf16 rows of `out` at orow.
 // Order of the fp32 sums is fixed: slot = P_0; slot += P_1; ...; out = slot + P_{W-1}.
@@ -97,6 +101,15 @@ __device__ __forceinline__ void rs_epilogue(const CUtensorMap* acc_map, const fl
               v[4 * i + 2] += s.z;
               v[4 * i + 3] += s.w;
             }
+#if TL_RS_DISCARD
+            // This producer is the slot tile's last reader in this call, and the next call's
+            // first producer overwrites it: drop its two 128-byte lines from L2 rather than
+            // write them back (rows start on 128-byte lines when n % 32 == 0).
+            if ((n & 31) == 0) {
+              discard_l2_line(src);
+              discard_l2_line(src + 32);
+            }
+#endif
           } else {
 #pragma unroll
             for (int i = 0; i < 64; ++i)
@@ -121,11 +134,12 @@ struct AgParams {
   uint64_t* flags;  // [W][spr][chunks]
   long long shard_bytes, slab_bytes;
   int W, rank, m_per_rank, mps, spr, n, nbk, kblocks, swizzle, chunks, skip_chunk;
-  int boost;  // chunks [0, boost) are split with the epilogue warps (see ag_mover)
+  int boost;      // chunks [0, boost) are split with the epilogue warps (see ag_mover)
+  int copy_self;  // 1: the self rank's shard is copied too (last); 0: only the W-1 remote shards
 };
 
-// The shard mover: pull every shard (the self rank's last) into the gathered buffer in
-// 128-row slabs of `chunks` chunks, one release signal per chunk.  Chunk g belongs to CTA
+// The shard mover: pull the remote shards (and, with copy_self, the self rank's own, last)
+// into the gathered buffer in 128-row slabs of `chunks` chunks, one release signal per chunk.  Chunk g belongs to CTA
 // g mod grid.  The first `boost` chunks (the shards the first wave of tiles waits for) are
 // shared with the epilogue warps, which are idle until their first tile: in every other
 // round of the head (g / grid odd) the mover warps copy, in the others the epilogue warps
@@ -133,7 +147,7 @@ struct AgParams {
 template <bool Trace>
 __device__ __forceinline__ void ag_copy(const AgParams& p, int tid, int nthreads, int group, int bar) {
   const int per_shard = p.spr * p.chunks;
-  const int total = group == 1 ? p.boost : p.W * per_shard;
+  const int total = group == 1 ? p.boost : (p.W - 1 + p.copy_self) * per_shard;
   const size_t chunk_bytes = static_cast<size_t>(p.slab_bytes / p.chunks);
   for (int g = blockIdx.x; g < total; g += gridDim.x) {
     if (g < p.boost && ((g / static_cast<int>(gridDim.x)) & 1) == (group == 1 ? 1 : 0)) continue;
@@ -256,7 +270,7 @@ struct RsOp : OpBase<RsParams> {
   static constexpr uint32_t kTxBytes = Pair ? Geo2::kStageBytes : Geo<BM>::kStageBytes;
   static __device__ int num_tiles(const Params& p) { return rs_num_tiles(p.W, p.mbo, p.nbk); }
   static __device__ Job job(const Params& p, int t) {
-    const RsTile r = rs_tile(t, p.W, p.mbo, p.nbk, p.swizzle);
+    const RsTile r = rs_tile(t, p.W, p.mbo, p.nbk, BM, p.swizzle);
     Job j;
     j.kind = 0;
     j.a_sel = r.p;
@@ -450,13 +464,14 @@ struct Mlp2Op : OpBase<Mlp2Params> {
     }
   }
   // Every emulated rank r gathers the other ranks' X shards into its own copy of X
-  // (rows r*T ..), in its swizzled order; rank 0's gather first.
+  // (rows r*T ..), in its swizzled order; rank 0's gather first.  A rank's own shard is read
+  // in place by its layer-1 tiles, so its slot of the copy is not written.
   template <bool Trace>
   static __device__ void mover(const Params& p, int mw, int lane) {
     const int nthreads = p.common.mover_warps * 32;
     const int tid = mw * 32 + lane;
     const int per_shard = p.spr * p.chunks;
-    const int per_rank = p.W * per_shard;
+    const int per_rank = (p.W - 1) * per_shard;
     const int total = p.W * per_rank;
     const size_t chunk_bytes = static_cast<size_t>(p.slab_bytes / p.chunks);
     for (int g = blockIdx.x; g < total; g += gridDim.x) {
@@ -481,8 +496,48 @@ struct Mlp2Op : OpBase<Mlp2Params> {
 // distributed ...", §3.2 Algorithm 2, without a consumer): the same mover code, chunk
 // geometry, order and signals as the fused AllGather+GEMM, run by mover_warps warps in
 // each of the persistent CTAs.
-__global__ void __launch_bounds__(kMaxMoverWarps * 32) allgather_kernel(const __grid_constant__ AgParams p) {
+constexpr int kAllgatherWarps = 16;  // copy warps per CTA of the standalone AllGather
+__global__ void __launch_bounds__(kAllgatherWarps * 32) allgather_kernel(const __grid_constant__ AgParams p) {
   ag_mover<false>(p, threadIdx.x >> 5, threadIdx.x & 31);
+}
+
+// ============================================================================ ReduceScatter alone
+// The push-mode ReduceScatter of "Triton-distributed ...", §3.3 Algorithm 3, as its own
+// kernel: each owner o receives rows [o*m/W, (o+1)*m/W) of the W ranks' fp32 partials and
+// sums them, R = T[0] + T[1] + ... + T[W-1], in that order (the order of tl_gemm_rs's
+// chain), rounded to bf16 once.  Every thread takes 4 columns of one row per pass (a 16-byte
+// vector from each partial, W loads in flight, then an 8-byte bf16 store); two 512-thread
+// blocks per SM; the partials are read once, with the streaming (evict-first) hint.
+struct RsAloneParams {
+  const float4* part[8];
+  uint2* out[8];
+  long long units;  // m * n / 4
+  int W, mo, n4;
+};
+
+__global__ void __launch_bounds__(512, 2) reduce_scatter_kernel(const __grid_constant__ RsAloneParams p) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; u < p.units; u += stride) {
+    float4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < p.W) v[q] = __ldcs(p.part[q] + u);
+    float4 acc = v[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) {
+      if (q < p.W) {
+        acc.x += v[q].x;
+        acc.y += v[q].y;
+        acc.z += v[q].z;
+        acc.w += v[q].w;
+      }
+    }
+    const long long row = u / p.n4;
+    const int c4 = static_cast<int>(u - row * p.n4);
+    const int o = static_cast<int>(row / p.mo);
+    const long long orow = row - static_cast<long long>(o) * p.mo;
+    p.out[o][orow * p.n4 + c4] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  }
 }
 
 }  // namespace tl
@@ -565,6 +620,7 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
   p.boost = (W > 1 ? (W - 1 < 2 ? W - 1 : 2) : 0) * p.spr * p.chunks;  // the next two shards
+  p.copy_self = 0;  // the GEMM reads the self shard in place; its slot of T is not written
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int movers = ctx->cfg.mover_warps;
   if (W == 1) {  // nothing to gather: the plain GEMM on shard 0 in place, no mover, no signals
@@ -757,8 +813,38 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   p.swizzle = ctx->cfg.swizzle;
   p.chunks = ctx->cfg.chunks_per_slab;
   p.skip_chunk = -1;
+  p.copy_self = 1;
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
-  allgather_kernel<<<ctx->ctas, ctx->cfg.mover_warps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  // Alone, the copy has the whole GPU: kAllgatherWarps warps in each of the persistent CTAs
+  // run the same chunk loop as the fused kernel's mover warps.
+  p.common.mover_warps = kAllgatherWarps;
+  allgather_kernel<<<ctx->ctas, kAllgatherWarps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? TL_OK : TL_ERR_CUDA;
+}
+
+extern "C" int tl_reduce_scatter(tl_ctx* ctx, int W, const float* const* partials, void* const* out, int m, int n,
+                                 tl_stream_t stream) {
+  if (!ctx || W < 1 || W > 8 || m < 0 || n < 0 || m % W != 0 || n % 4 != 0) return TL_ERR_INVALID;
+  if (m == 0 || n == 0) return TL_OK;
+  if (!partials || !out) return TL_ERR_INVALID;
+  for (int r = 0; r < W; ++r)
+    if (!partials[r] || !out[r] || !aligned16(partials[r]) || !aligned16(out[r])) return TL_ERR_INVALID;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
+  RsAloneParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int r = 0; r < W; ++r) {
+    p.part[r] = reinterpret_cast<const float4*>(partials[r]);
+    p.out[r] = static_cast<uint2*>(out[r]);
+  }
+  p.W = W;
+  p.mo = m / W;
+  p.n4 = n / 4;
+  p.units = static_cast<long long>(m) * (n / 4);
+  // Two 512-thread blocks per SM (the launch bounds), enough 16-byte loads in flight to
+  // keep HBM busy; a grid-stride loop covers the rest.
+  long long blocks = (p.units + 511) / 512;
+  if (blocks > 2LL * ctx->sms) blocks = 2LL * ctx->sms;
+  reduce_scatter_kernel<<<static_cast<unsigned>(blocks), 512, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? TL_OK : TL_ERR_CUDA;
 }

@@ -21,10 +21,10 @@ constexpr int kMaxTopk = 8;
 
 // ---------------------------------------------------------------------------- routing
 // One warp per token: top-k of the fp32 logits (larger first, equal values to the
-// lower expert index), softmax over all E logits in fp32 taken at the chosen experts.
-// Also zeroes the token's fp32 output row (the combine adds into it).
-__global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E, int topk, int* __restrict__ experts,
-                                 float* __restrict__ gates) {
+// lower expert index), softmax over all E logits in fp32 taken at the chosen experts,
+// optionally divided by their sum over the chosen experts (renorm).
+__global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E, int topk, int renorm,
+                                 int* __restrict__ experts, float* __restrict__ gates) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
@@ -49,6 +49,8 @@ __global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E,
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
 
   uint32_t taken = 0;
+  float g[kMaxTopk];
+  float gsum = 0.f;
   for (int j = 0; j < topk; ++j) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
@@ -70,11 +72,12 @@ __global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E,
       }
     }
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == 0) {
-      experts[t * topk + j] = bi;
-      gates[t * topk + j] = expf(bv - mx) / s;
-    }
+    g[j < kMaxTopk ? j : 0] = expf(bv - mx) / s;
+    gsum += g[j < kMaxTopk ? j : 0];
+    if (lane == 0) experts[t * topk + j] = bi;
   }
+  if (lane == 0)
+    for (int j = 0; j < topk; ++j) gates[t * topk + j] = renorm ? g[j] / gsum : g[j];
 }
 
 // ---------------------------------------------------------------------------- permutation
@@ -619,7 +622,7 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
   __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
 
-  moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, experts, gates);
+  moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, ctx->cfg.moe_renorm, experts, gates);
   const int zero_ctas = ctx->sms > E ? ctx->sms - E : 1;
   moe_permute_kernel<<<E + zero_ctas, 1024, 0, st>>>(experts, T * topk, E, topk, gates, perm, row_meta, tile_expert,
                                                      tile_rows, num_mtiles, counts, perm_out, counts_out,

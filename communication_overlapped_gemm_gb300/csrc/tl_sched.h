@@ -8,8 +8,8 @@
 // Distributed AI Systems with the Triton Compiler", §3.7:
 //   AllGather+GEMM: step s computes with the shard of rank (rank + s) mod W, so each
 //     rank starts on its local shard while the next one is being pulled.
-//   GEMM+ReduceScatter: producer p walks owners (p + 1 + s) mod W, its own rows last,
-//     so the chunk that must travel furthest is produced first.
+//   GEMM+ReduceScatter: inside each L2-sized band of the output, producer p starts at the
+//     rows of owner (p + 1) mod W (see rs_tile).
 // The same functions are compiled for the host (tl_*_tile_order, used by the tests)
 // and for the device (the persistent kernels), so both agree by construction.
 #pragma once
@@ -65,32 +65,58 @@ struct RsTile {
   int nb;  // column block
 };
 
-// GEMM + ReduceScatter: producers in order p = 0..W-1 (the fixed fp32 summation order).
-// Producer p walks its W owners in the order (p + 1 + s) mod W, s = 0..W-1, taken in groups
-// of kRsOwnerGroup consecutive owners.  Inside a group the column block is the slowest
-// index and the owner's row block the fastest, so the tiles that run at the same time
-// share a few column slabs of B_p and the group's rows of A_p: B_p is read once per owner
-// group rather than once per wave of tiles.  Owners still come first in the rotated order,
-// the producer's own rows in the last group.
-constexpr int kRsOwnerGroup = 4;
+// GEMM + ReduceScatter, banded.  The m x n output is cut into bands of kRsBandRows rows x
+// kRsBandCols columns (the last band in each direction may be smaller), visited in
+// row-major order.  Inside a band the producers run in the order p = 0..W-1, the fixed fp32
+// summation order, and producer p's tiles of the band run with the column block slowest and
+// the row block fastest.  So the W partial tiles of one output tile are produced one band
+// pass apart, while the band's fp32 slot tiles (2048 x 4096 x 4 B = 32 MiB) stay in L2; a
+// producer's pass reads its A rows of the band once and each B column slab once per band.
+// (A producer-major order, every producer over the whole output in turn, streams the whole
+// m x n fp32 slot through DRAM once per producer.)
+// Rank swizzle ("Triton-distributed ...", §3.7: start from the next rank's chunk, the local
+// chunk last): inside a band, producer p starts at the first row of owner (p + 1) mod W
+// when that owner has rows in the band, and wraps around the band's rows from there.
+#ifndef TL_RS_BAND_ROWS
+#define TL_RS_BAND_ROWS 2048
+#endif
+#ifndef TL_RS_BAND_COLS
+#define TL_RS_BAND_COLS 4096
+#endif
+constexpr int kRsBandRows = TL_RS_BAND_ROWS;
+constexpr int kRsBandCols = TL_RS_BAND_COLS;
 TL_HD int rs_num_tiles(int W, int mbo, int nbk) { return W * W * mbo * nbk; }
+// Owner order of one producer's pass over all owners (the MLP chain's layer 2): (p + 1 + s) mod W.
 TL_HD int rs_owner(int W, int p, int s, int swizzle) { return swizzle ? (p + 1 + s) % W : s; }
-TL_HD RsTile rs_tile(int t, int W, int mbo, int nbk, int swizzle) {
-  const int per_prod = W * mbo * nbk;
+TL_HD int rs_band_mt(int bm) { return kRsBandRows / bm > 0 ? kRsBandRows / bm : 1; }
+TL_HD int rs_band_nt() { return kRsBandCols / kBN > 0 ? kRsBandCols / kBN : 1; }
+// mbo: row tiles per owner (tiles of bm rows); nbk: column tiles of the output.
+TL_HD RsTile rs_tile(int t, int W, int mbo, int nbk, int bm, int swizzle) {
+  const int mt = W * mbo;  // row tiles of the whole output
+  const int bmt = rs_band_mt(bm), bnt = rs_band_nt();
+  const int per_rowband = W * bmt * nbk;  // tiles of a full band row (all producers)
+  const int br = t / per_rowband;
+  int rem = t - br * per_rowband;
+  const int r0 = br * bmt;
+  const int R = mt - r0 < bmt ? mt - r0 : bmt;  // rows of this band
+  const int bc = rem / (W * R * bnt);
+  rem -= bc * W * R * bnt;
+  const int c0 = bc * bnt;
+  const int C = nbk - c0 < bnt ? nbk - c0 : bnt;  // columns of this band
   RsTile r;
-  r.p = t / per_prod;
-  int rem = t - r.p * per_prod;
-  const int full_group = kRsOwnerGroup * mbo * nbk;  // tiles of a group of kRsOwnerGroup owners
-  const int g = rem / full_group;                     // every group but the last is full
-  rem -= g * full_group;
-  const int s0 = g * kRsOwnerGroup;
-  const int gsz = W - s0 < kRsOwnerGroup ? W - s0 : kRsOwnerGroup;  // owners in this group
-  r.nb = rem / (gsz * mbo);
-  rem -= r.nb * gsz * mbo;
-  const int s = s0 + rem / mbo;
-  r.mb = rem - (s - s0) * mbo;
-  r.o = rs_owner(W, r.p, s, swizzle);
+  r.p = rem / (R * C);
+  rem -= r.p * R * C;
+  r.nb = c0 + rem / R;
+  const int i = rem - (rem / R) * R;
+  int start = 0;  // rotation of the band's rows for this producer
+  if (swizzle) {
+    const int os = (r.p + 1) % W;  // the owner this producer serves first
+    const int rs = os * mbo;        // that owner's first row tile
+    if (rs + mbo > r0 && rs < r0 + R) start = rs > r0 ? rs - r0 : 0;
+  }
+  int row = r0 + (i + start) % R;
+  r.o = row / mbo;
+  r.mb = row - r.o * mbo;
   return r;
 }
-
 }  // namespace tl

@@ -85,6 +85,9 @@ typedef struct tl_config {
                                  every op; 2 (default) CTA pairs for tl_gemm_rs and tl_mlp2, whose
                                  heavier epilogues gain from the pair's double-buffered
                                  accumulators, single CTAs for tl_ag_gemm                           */
+  int moe_renorm;             /* MoE gates: 0 (default) the softmax over all E logits taken at the
+                                 chosen experts; 1 those values divided by their sum over the topk
+                                 chosen experts (they then sum to 1 per token)                      */
 } tl_config;
 
 typedef struct tl_ctx tl_ctx;
@@ -154,12 +157,14 @@ int tl_ctx_set_trace(tl_ctx* ctx, void* buf, size_t bytes, int spans_per_warp);
  * a_shards: host array of W device pointers, shard r is bf16 [m_per_rank x k] (rank r's
  *           "local buffer").  b: bf16 [k x n].  c: bf16 [(W*m_per_rank) x n] (output).
  * workspace: device buffer of tl_ag_gemm_workspace_bytes(); its first W*m_per_rank*k*2
- *           bytes receive the gathered A (the symmetric buffer T of Algorithm 2, rank order),
- *           the rest holds the per-chunk ready signals.
+ *           bytes are the gathered A (the symmetric buffer T of Algorithm 2, rank order), the
+ *           rest holds the per-chunk ready signals.
  * The emulated self rank `rank` (0 <= rank < W) reads its own shard in place; the mover pulls
- * shards (rank+1) mod W, (rank+2) mod W, ... into T in that order (its own shard last), and the
- * GEMM visits row blocks of shard rank first, then (rank+1) mod W, ... waiting on each slab's
- * signals before its first load.  The result does not depend on `rank` or the swizzle.
+ * the remote shards (rank+1) mod W, (rank+2) mod W, ... into their slots of T in that order,
+ * and the GEMM visits row blocks of shard rank first, then (rank+1) mod W, ... waiting on each
+ * slab's signals before its first load.  The self rank's slot of T is not written (nothing
+ * reads it; tl_allgather fills all W slots).  The result does not depend on `rank` or the
+ * swizzle.
  * W = 1 has nothing to gather: the call is the plain GEMM on shard 0, read in place, and the
  * gathered region of the workspace is not written.
  * Shapes: 1 <= W <= 8; m_per_rank % 128 == 0; n % 8 == 0; k % 8 == 0 (n, k need not be
@@ -172,11 +177,12 @@ int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const 
 
 /* ---------------------------------------------------------------- AllGather alone
  * [TD] §3.2 Algorithm 2 (pull-mode one-sided AllGather) as its own kernel: the shard mover of
- * tl_ag_gemm (same chunks, order and signals) without the GEMM, run by cfg.mover_warps warps
- * in each persistent CTA.  Fills the gathered buffer at the start of `workspace` (sized by
- * tl_ag_gemm_workspace_bytes(W, m_per_rank, 8, k)) with [A_0; ...; A_{W-1}] and releases every
- * chunk signal.  Shapes and errors as tl_ag_gemm; W = 1 is a no-op.  This is the
- * "communication alone" leg of the overlap measurement.
+ * tl_ag_gemm (same chunks, order and signals) without the GEMM, run by 16 warps in each
+ * persistent CTA (alone, the copy has the whole GPU).  Fills the gathered buffer at the start
+ * of `workspace` (sized by tl_ag_gemm_workspace_bytes(W, m_per_rank, 8, k)) with all of
+ * [A_0; ...; A_{W-1}], the self rank's shard last, and releases every chunk signal.  Shapes
+ * and errors as tl_ag_gemm; W = 1 is a no-op.  This is the "communication alone" leg of the
+ * overlap measurement.
  */
 int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_shards, void* workspace, size_t workspace_bytes,
                  int m_per_rank, int k, tl_stream_t stream);
@@ -204,6 +210,22 @@ size_t tl_gemm_rs_workspace_bytes(int W, int m, int n, int k_r);
 int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* const* b, void* const* out,
                void* workspace, size_t workspace_bytes, int m, int n, int k_r, tl_stream_t stream);
 
+/* ---------------------------------------------------------------- ReduceScatter alone
+ * [TD] §3.3 Algorithm 3 (push-mode ReduceScatter) as its own kernel, without a GEMM: the
+ * communication half of tl_gemm_rs, and its "communication alone" leg in an overlap
+ * measurement.
+ *
+ *   out_o [(m/W) x n] = rows [o*m/W, (o+1)*m/W) of  P_0 + P_1 + ... + P_{W-1}
+ *
+ * partials: host array of W device pointers, P_p fp32 [m x n] row-major (rank p's partial);
+ * out: W device pointers, out_o bf16 [(m/W) x n].  The sum is taken in fp32 in the order
+ * p = 0, 1, ..., W-1 (the order of tl_gemm_rs's chain) and rounded to bf16 once, so the
+ * result is bit-identical run to run.  No workspace.  Partials are read once.
+ * Shapes: 1 <= W <= 8; m % W == 0; n % 4 == 0.  m == 0 or n == 0 is a no-op.
+ */
+int tl_reduce_scatter(tl_ctx* ctx, int W, const float* const* partials, void* const* out, int m, int n,
+                      tl_stream_t stream);
+
 /* ---------------------------------------------------------------- 2-layer MLP chain
  * [TL] §2.1 (AG + GEMM -> activation -> GEMM + RS), [RA] CTA-pipelining (the second GEMM's
  * CTAs start as soon as the first GEMM's CTAs that produce their inputs are done).
@@ -213,8 +235,10 @@ int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* const* b, v
  *
  * x_shards: W pointers, X_r bf16 [(tokens/W) x hidden]; w1: W pointers, bf16 [hidden x f_r];
  * w2: W pointers, bf16 [f_r x hidden]; out: W pointers, bf16 [(tokens/W) x hidden].
- * workspace: tl_mlp2_workspace_bytes(): per-rank gathered X (W x tokens x hidden bf16), the
- * intermediate H (W x tokens x f_r bf16), the fp32 reduction slot (tokens x hidden) and signals.
+ * workspace: tl_mlp2_workspace_bytes(): per-rank gathered X (W x tokens x hidden bf16; rank
+ * r's own shard is read in place, its slot of r's copy is not written) at offset 0, then, each at the next 256-byte boundary, the intermediate H (W x tokens x f_r bf16,
+ * H_r at rows r*tokens.., readable after the call), the fp32 reduction slot (tokens x hidden)
+ * and the signals.
  * One persistent launch runs, per emulated rank r: the mover (gather X into rank r's copy),
  * layer-1 tiles (wait on the slab signals, GELU epilogue, notify per H tile) and layer-2 tiles
  * (wait on the H tiles covering their K range, then the GEMM+RS chain above).
@@ -236,7 +260,8 @@ int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const void* const* 
  * perm_out (optional, may be NULL): int32 [T*topk]: perm_out[pos] = t*topk + j, assignments
  *   ordered by (expert, t, j).  counts_out (optional): int32 [E] assignments per expert.
  * Routing: experts = the topk largest logits (ties to the lower expert index), gates = softmax
- * over all E logits taken at those experts (no renormalisation).
+ * over all E logits taken at those experts; with cfg.moe_renorm = 1 the topk gates of a token
+ * are divided by their sum (the pages define no router: both readings are offered).
  *   y_(t,j) = (SiLU(x_t . Wg_e) * (x_t . Wu_e)) . Wd_e   (h kept in bf16, y in bf16)
  *   out_t   = sum_j gate_(t,j) * y_(t,j)                  (fp32)
  * workspace: tl_moe_workspace_bytes().

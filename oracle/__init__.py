@@ -36,8 +36,8 @@ except Exception:  # pragma: no cover - fallback keeps the oracle usable without
     _erf = np.vectorize(math.erf, otypes=[np.float64])
 
 __all__ = [
-    "widen_bf16", "ag_gather_bits", "ag_gemm", "ag_gemm_entries", "gemm_rs",
-    "gemm_rs_entries", "gelu", "silu", "mlp2", "mlp2_entries", "moe_route", "moe_permute",
+    "widen_bf16", "ag_gather_bits", "ag_gemm", "ag_gemm_entries", "gemm_rs", "reduce_scatter",
+    "gemm_rs_entries", "gemm_rs_rows", "gelu", "silu", "mlp2", "mlp2_entries", "mlp2_rows", "mlp2_h", "moe_route", "moe_permute",
     "moe", "moe_rows", "static_tile_map", "round_bf16", "attn_gather", "ag_attention", "ag_attention_rows",
 ]
 
@@ -116,6 +116,25 @@ def gemm_rs(a_list, b_list) -> list:
     return [S[o * mo:(o + 1) * mo] for o in range(W)]
 
 
+def reduce_scatter(partials) -> list:
+    """out_o = rows [o*M/W, (o+1)*M/W) of P_0 + P_1 + ... + P_{W-1}, float64.
+
+    [TD] §3.3 Alg. 3 (one-sided push-mode ReduceScatter) without a GEMM in
+    front of it: rank p's partial T[p] reaches the owner, which accumulates
+    R = R + T[p] over every rank and keeps its own rows.  The partials are
+    float32 arrays (the GPU path's message precision), widened exactly.
+    """
+    W = len(partials)
+    S = None
+    for p in range(W):
+        P = np.asarray(partials[p], dtype=np.float32).astype(np.float64)
+        S = P if S is None else S + P
+    M = S.shape[0]
+    assert M % W == 0
+    mo = M // W
+    return [S[o * mo:(o + 1) * mo] for o in range(W)]
+
+
 def gemm_rs_entries(a_list, b_list, owner, rows, cols) -> np.ndarray:
     """Selected entries out_owner[rows[i], cols[i]], each summed over producers p = 0..W-1."""
     W = len(a_list)
@@ -128,6 +147,19 @@ def gemm_rs_entries(a_list, b_list, owner, rows, cols) -> np.ndarray:
         for p in range(W):
             acc += float(np.dot(widen_bf16(a_list[p][gr]), widen_bf16(np.ascontiguousarray(b_list[p][:, c]))))
         out[i] = acc
+    return out
+
+
+def gemm_rs_rows(a_list, b_list, owner, rows) -> np.ndarray:
+    """Whole rows out_owner[rows[i], :], each the plain sum over producers p = 0..W-1 of
+    (row of A_p) . B_p (the definition of gemm_rs, one row at a time)."""
+    W = len(a_list)
+    mo = np.asarray(a_list[0]).shape[0] // W
+    gr = [owner * mo + r for r in rows]
+    out = None
+    for p in range(W):
+        part = widen_bf16(np.asarray(a_list[p])[gr]) @ widen_bf16(b_list[p])
+        out = part if out is None else out + part
     return out
 
 
@@ -187,6 +219,26 @@ def mlp2_entries(x_shards, w1, w2, owner, rows, cols) -> np.ndarray:
             acc += float(np.dot(cache[gr][q], widen_bf16(np.ascontiguousarray(w2[q][:, c]))))
         out[i] = acc
     return out
+
+
+def mlp2_rows(x_shards, w1, w2, owner, rows) -> np.ndarray:
+    """Whole rows out_owner[rows[i], :]: for each row the gathered X row, its GELU rows of
+    every H_r, and sum_r H_r row . W2_r (the definition of mlp2, one row at a time)."""
+    W = len(w1)
+    T_per = np.asarray(x_shards[0]).shape[0]
+    X = widen_bf16(np.stack([np.asarray(x_shards[(owner * T_per + r) // T_per])[(owner * T_per + r) % T_per]
+                             for r in rows]))
+    out = None
+    for q in range(W):
+        part = gelu(X @ widen_bf16(w1[q])) @ widen_bf16(w2[q])
+        out = part if out is None else out + part
+    return out
+
+
+def mlp2_h(x_shards, w1, rank) -> np.ndarray:
+    """The intermediate H_rank = GELU(X . W1_rank) of the MLP chain, float64 ([TL] §2.1)."""
+    X = widen_bf16(ag_gather_bits(x_shards))
+    return gelu(X @ widen_bf16(w1[rank]))
 
 
 # ----------------------------------------------------------------------------- MoE

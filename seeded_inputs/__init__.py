@@ -99,6 +99,7 @@ def make_inputs(kind: str, seed: int, **d) -> dict:
       mlp2:    x_shards [W] (tokens/W, hidden); w1 [W] (hidden, f_r); w2 [W] (f_r, hidden)
       moe:     x (T, H); logits (T, E) fp32; w_gate, w_up (E, H, F); w_down (E, F, H)
       ag_attn: q (heads, l_r, d); k_shards, v_shards [W] (heads, l_r, d)
+      reduce_scatter: partials [W] (m, n) fp32, N(0, 1)
     """
     base = seed * 1000
     if kind == "ag_gemm":
@@ -128,6 +129,9 @@ def make_inputs(kind: str, seed: int, **d) -> dict:
             w_up=normal_bf16(base + 3, (E, H, F), 0.02),
             w_down=normal_bf16(base + 4, (E, F, H), 0.02),
         )
+    if kind == "reduce_scatter":
+        W, m, n = d["W"], d["m"], d["n"]
+        return dict(partials=[normal_f32(base + p, (m, n), 1.0) for p in range(W)])
     if kind == "ag_attn":
         W, Hh, L, hd = d["W"], d["heads"], d["l_r"], d["d"]
         return dict(

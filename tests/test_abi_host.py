@@ -52,7 +52,7 @@ def test_config_defaults_and_strerror(tl):
     c = tl.Config()
     assert tl.lib().tl_config_default(ctypes.byref(c)) == tl.TL_OK
     assert (c.mover_warps, c.chunks_per_slab, c.swizzle, c.grid_ctas, c.combine_ctas) == (4, 32, 1, 0, 16)
-    assert c.debug_skip_chunk == -1 and c.timeout_ns == 2_000_000_000 and c.pair_ctas == 2
+    assert c.debug_skip_chunk == -1 and c.timeout_ns == 2_000_000_000 and c.pair_ctas == 2 and c.moe_renorm == 0
     assert tl.lib().tl_config_default(None) == tl.TL_ERR_INVALID
     for code in (tl.TL_OK, tl.TL_ERR_INVALID, tl.TL_ERR_UNSUPPORTED, tl.TL_ERR_CUDA, tl.TL_ERR_TIMEOUT,
                  tl.TL_ERR_WORKSPACE):
@@ -92,6 +92,7 @@ def test_argument_validation_needs_no_gpu(tl):
     assert L.tl_ag_attention(None, 2, 0, 16, ptrs, ptrs, 16, 16, 1 << 20, 2, 128, 128, None) == tl.TL_ERR_INVALID
     assert L.tl_ag_gemm_static_scratch(None, 2, 0, ptrs, 16, 16, 128, 256, 256, None) == tl.TL_ERR_INVALID
     assert L.tl_allgather(None, 2, 0, ptrs, 16, 1 << 20, 128, 256, None) == tl.TL_ERR_INVALID
+    assert L.tl_reduce_scatter(None, 2, ptrs, ptrs, 256, 256, None) == tl.TL_ERR_INVALID
     assert L.tl_ctx_check(None) == tl.TL_ERR_INVALID
 
 
@@ -117,32 +118,45 @@ def test_ag_tile_order_is_rank_swizzled_and_matches_static_map(tl, W, rank, mpr,
     assert s0[:per].tolist() == [0] * per  # identity order starts at rank 0
 
 
-@pytest.mark.parametrize("W,m,n", [(8, 8192, 8192), (4, 1024, 520), (1, 128, 256), (6, 1536, 768), (5, 640, 300)])
-def test_rs_tile_order_producer_major_owner_swizzled(tl, W, m, n):
-    p, o, mb, nb = tl.tl_rs_tile_order(W, m, n, 1)
+def _rs_band_order(W, m, n, swizzle, band_rows=2048, band_cols=4096):
+    """The documented GEMM+RS walk, restated: bands of band_rows x band_cols of the output in
+    row-major order; inside a band producers 0..W-1; a producer's band tiles with the column
+    block slowest and the row block fastest, the rows rotated to start at owner (p+1) mod W."""
     bm = 256 if (m // W) % 256 == 0 else 128
     mbo, nbk = m // W // bm, -(-n // 256)
-    assert len(p) == W * W * mbo * nbk
-    assert len(set(zip(p.tolist(), o.tolist(), mb.tolist(), nb.tolist()))) == len(p)
-    assert np.all(np.diff(p) >= 0)  # producers visited 0..W-1 (fixed fp32 summation order)
-    G = 4  # owners per group
-    for q in range(W):
-        oq, nq, mq = o[p == q], nb[p == q], mb[p == q]
-        rot = [(q + 1 + s) % W for s in range(W)]
-        first = list(dict.fromkeys(oq.tolist()))
-        assert first == rot  # next rank's rows first, own rows last
-        # groups of G owners in rotated order; inside a group the column block is the slowest
-        # index and the row block the fastest
-        pos = 0
-        for g0 in range(0, W, G):
-            grp = rot[g0:g0 + G]
-            size = len(grp) * mbo * nbk
-            exp = [(grp[s], r * (bm // 128), c) for c in range(nbk) for s in range(len(grp)) for r in range(mbo)]
-            got = list(zip(oq[pos:pos + size].tolist(), mq[pos:pos + size].tolist(), nq[pos:pos + size].tolist()))
-            assert got == exp
-            pos += size
-    p0, o0, _, _ = tl.tl_rs_tile_order(W, m, n, 0)
-    assert list(dict.fromkeys(o0[p0 == 0].tolist())) == list(range(W))
+    mt, BR, BC = W * mbo, max(1, band_rows // bm), max(1, band_cols // 256)
+    out = []
+    for r0 in range(0, mt, BR):
+        rows0 = list(range(r0, min(mt, r0 + BR)))
+        for c0 in range(0, nbk, BC):
+            for q in range(W):
+                rows = rows0
+                if swizzle:
+                    first = [r for r in rows0 if r // mbo == (q + 1) % W]
+                    if first:
+                        k = rows0.index(first[0])
+                        rows = rows0[k:] + rows0[:k]
+                for c in range(c0, min(nbk, c0 + BC)):
+                    out += [(q, r // mbo, (r % mbo) * (bm // 128), c) for r in rows]
+    return out
+
+
+@pytest.mark.parametrize("W,m,n", [(8, 8192, 8192), (4, 1024, 520), (1, 128, 256), (6, 1536, 768), (5, 640, 300),
+                                   (8, 1024, 264), (2, 8192, 8200)])
+def test_rs_tile_order_banded_and_owner_swizzled(tl, W, m, n):
+    bm = 256 if (m // W) % 256 == 0 else 128
+    mbo, nbk = m // W // bm, -(-n // 256)
+    for swz in (1, 0):
+        p, o, mb, nb = tl.tl_rs_tile_order(W, m, n, swz)
+        got = list(zip(p.tolist(), o.tolist(), mb.tolist(), nb.tolist()))
+        assert len(got) == W * W * mbo * nbk and len(set(got)) == len(got)
+        assert got == _rs_band_order(W, m, n, swz)
+        # every output tile's W partials come in the producer order 0..W-1 (the fixed fp32
+        # summation order the peer signals chain)
+        seen = {}
+        for q, oo, r, c in got:
+            assert seen.get((oo, r, c), -1) == q - 1
+            seen[(oo, r, c)] = q
 
 
 def test_tile_order_rejects_bad_shapes(tl):

@@ -68,3 +68,35 @@ def test_moe_full_size_routing_exact_and_sampled_rows(ctx):
     toks = sorted(set(rng.integers(0, 4096, 40).tolist()) | {0, 4095})
     rows, _, _ = oracle.moe_rows(inp["x"], inp["logits"], inp["w_gate"], inp["w_up"], inp["w_down"], 2, toks)
     assert_close(out[toks], rows, "moe_64e sampled tokens")
+
+
+@pytest.mark.parametrize("T,H,E,F,k", [(300, 512, 16, 256, 2), (200, 256, 8, 384, 3)])
+def test_moe_renormalised_gates_match_oracle(T, H, E, F, k):
+    """cfg.moe_renorm = 1: the top-k gates of a token divided by their sum (the other reading
+    of the pages' unspecified router), against oracle.moe(..., renorm=True)."""
+    inp = make_inputs("moe", 90 + E, T=T, H=H, E=E, F=F)
+    with tl.Context(0, moe_renorm=1) as c2:
+        out, perm, counts = run_moe(c2, inp, k)
+    ref = oracle.moe(inp["x"], inp["logits"], inp["w_gate"], inp["w_up"], inp["w_down"], k, renorm=True)
+    assert np.array_equal(perm, ref["perm"]) and np.array_equal(counts, ref["counts"])
+    assert_close(out, ref["out"], f"moe renorm T={T} E={E} k={k}")
+    plain = oracle.moe(inp["x"], inp["logits"], inp["w_gate"], inp["w_up"], inp["w_down"], k)["out"]
+    assert np.max(np.abs(out - plain)) > 0.1 * np.max(np.abs(plain))  # the flag reached the kernel
+
+
+def test_moe_full_size_on_eight_combine_sms(ctx):
+    """The MoE workload as stated (combine kernel on 8 reserved SMs): routing bit-exact,
+    sampled tokens against the oracle, and the output bit-identical to the default partition
+    (top-2 into a zeroed fp32 out: the order of the two adds does not matter)."""
+    inp = workload_inputs("moe_64e")
+    with tl.Context(0, combine_ctas=8) as c8:
+        out8, perm, counts = run_moe(c8, inp, 2)
+    ex, _ = oracle.moe_route(inp["logits"], 2)
+    c_ref, _, perm_ref, _ = oracle.moe_permute(ex, 64)
+    assert np.array_equal(perm, perm_ref) and np.array_equal(counts, c_ref)
+    rng = np.random.default_rng(15)
+    toks = sorted(set(rng.integers(0, 4096, 40).tolist()) | {0, 4095})
+    rows, _, _ = oracle.moe_rows(inp["x"], inp["logits"], inp["w_gate"], inp["w_up"], inp["w_down"], 2, toks)
+    assert_close(out8[toks], rows, "moe_64e on 8 combine SMs, sampled tokens")
+    out16, _, _ = run_moe(ctx, inp, 2)
+    assert np.array_equal(out8, out16)

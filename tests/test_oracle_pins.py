@@ -148,6 +148,32 @@ def test_gemm_rs_brute_force_and_closed_form():
     assert np.allclose(np.concatenate(outs, axis=0), Acat @ Bcat, rtol=1e-13, atol=1e-13)
 
 
+def test_reduce_scatter_hand_brute_force_and_gemm_rs():
+    # hand case, W = 2: owner 0 keeps row 0 of the sum, owner 1 row 1 (a swapped owner or a
+    # dropped rank fails)
+    p0 = np.array([[1.0, -2.0], [3.0, 4.0]], dtype=np.float32)
+    p1 = np.array([[10.0, 20.0], [-30.0, 0.5]], dtype=np.float32)
+    out = oracle.reduce_scatter([p0, p1])
+    assert [o.tolist() for o in out] == [[[11.0, 18.0]], [[-27.0, 4.5]]]
+    # brute force, W = 3, every element a sum over ranks in a Python loop
+    rng = np.random.default_rng(3)
+    parts = [rng.standard_normal((6, 5)).astype(np.float32) for _ in range(3)]
+    out = oracle.reduce_scatter(parts)
+    for o in range(3):
+        for i in range(2):
+            for j in range(5):
+                acc = 0.0
+                for p in range(3):
+                    acc += float(parts[p][o * 2 + i][j])
+                assert out[o][i][j] == acc
+    # with the ranks' products as partials it is the GEMM + ReduceScatter (whose own pins are
+    # the brute force and the column-concatenated GEMM above)
+    inp = make_inputs("gemm_rs", 5, W=2, m=4, n=3, k_r=8)
+    prods = [(oracle.widen_bf16(a) @ oracle.widen_bf16(b)).astype(np.float32) for a, b in zip(inp["a"], inp["b"])]
+    for x, y in zip(oracle.reduce_scatter(prods), oracle.gemm_rs(inp["a"], inp["b"])):
+        assert np.allclose(x, y, rtol=1e-6, atol=1e-7)
+
+
 def test_gemm_rs_entries_match_full():
     W, m, kr, n = 4, 64, 32, 48
     a = [normal_bf16(500 + p, (m, kr), 1.0) for p in range(W)]
@@ -158,6 +184,7 @@ def test_gemm_rs_entries_match_full():
     for o in range(W):
         got = oracle.gemm_rs_entries(a, b, o, rows, cols)
         assert np.allclose(got, outs[o][rows, cols], rtol=1e-12, atol=1e-12)
+        assert np.allclose(oracle.gemm_rs_rows(a, b, o, [5, 0, 15]), outs[o][[5, 0, 15]], rtol=1e-12, atol=1e-12)
 
 
 def test_mlp2_brute_force():
@@ -183,6 +210,13 @@ def test_mlp2_brute_force():
     for o in range(W):
         got = oracle.mlp2_entries(x, w1, w2, o, rows, cols)
         assert np.allclose(got, outs[o][rows, cols], rtol=1e-12, atol=1e-14)
+        # whole rows: the row sampler against the brute-force S
+        assert np.allclose(oracle.mlp2_rows(x, w1, w2, o, [1, 0]), np.array(S[o * mo:(o + 1) * mo])[[1, 0]],
+                           rtol=1e-12, atol=1e-14)
+    # H_r against the brute-force GELU(X . W1_r)
+    for r in range(W):
+        Hm = [[0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0))) for v in row] for row in _bf_matmul(X, _py(w1[r]))]
+        assert np.allclose(oracle.mlp2_h(x, w1, r), np.array(Hm), rtol=1e-12, atol=1e-14)
 
 
 def test_moe_route_ties_and_gates():
