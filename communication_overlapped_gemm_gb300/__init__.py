@@ -23,7 +23,8 @@ __all__ = [
     "TL_OK", "TL_ERR_INVALID", "TL_ERR_UNSUPPORTED", "TL_ERR_CUDA", "TL_ERR_TIMEOUT", "TL_ERR_WORKSPACE",
     "TLError", "Config", "Context", "lib", "library_path", "build",
     "tl_ag_gemm", "tl_allgather", "tl_gemm_rs", "tl_reduce_scatter", "tl_mlp2", "tl_moe_combine",
-    "tl_ag_gemm_workspace_bytes", "tl_gemm_rs_workspace_bytes", "tl_mlp2_workspace_bytes",
+    "tl_ag_gemm_workspace_bytes", "tl_gemm_rs_workspace_bytes", "tl_gemm_rs_ring_workspace_bytes",
+    "tl_mlp2_workspace_bytes", "tl_rs_ring_tile_order",
     "tl_moe_workspace_bytes", "tl_ag_tile_order", "tl_rs_tile_order", "tl_trace_bytes", "tl_ag_attention",
     "tl_ag_attention_workspace_bytes", "EXPORTED_SYMBOLS",
 ]
@@ -55,6 +56,7 @@ class Config(ctypes.Structure):
         ("timeout_ns", ctypes.c_ulonglong),
         ("pair_ctas", _i),
         ("moe_renorm", _i),
+        ("rs_ring", _i),
     ]
 
 
@@ -73,6 +75,7 @@ _SIGS = {
     "tl_ag_gemm": (_i, [_vp, _i, _i, ctypes.POINTER(_vp), _vp, _vp, _vp, _c_size, _i, _i, _i, _vp]),
     "tl_allgather": (_i, [_vp, _i, _i, ctypes.POINTER(_vp), _vp, _c_size, _i, _i, _vp]),
     "tl_gemm_rs_workspace_bytes": (_c_size, [_i, _i, _i, _i]),
+    "tl_gemm_rs_ring_workspace_bytes": (_c_size, [_i, _i, _i, _i]),
     "tl_gemm_rs": (_i, [_vp, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _c_size,
                         _i, _i, _i, _vp]),
     "tl_mlp2_workspace_bytes": (_c_size, [_i, _i, _i, _i]),
@@ -87,6 +90,7 @@ _SIGS = {
                              _i, _vp]),
     "tl_ag_tile_order": (_i, [_i, _i, _i, _i, _i, _vp, _vp, _vp, _i]),
     "tl_rs_tile_order": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _i]),
+    "tl_rs_ring_tile_order": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -216,6 +220,10 @@ def tl_ag_gemm_workspace_bytes(W, m_per_rank, n, k) -> int:
 
 def tl_gemm_rs_workspace_bytes(W, m, n, k_r) -> int:
     return lib().tl_gemm_rs_workspace_bytes(W, m, n, k_r)
+
+
+def tl_gemm_rs_ring_workspace_bytes(W, m, n, k_r) -> int:
+    return lib().tl_gemm_rs_ring_workspace_bytes(W, m, n, k_r)
 
 
 def tl_mlp2_workspace_bytes(W, tokens, hidden, f_r) -> int:
@@ -369,6 +377,19 @@ def tl_rs_tile_order(W, m, n, swizzle):
     rc = L.tl_rs_tile_order(W, m, n, swizzle, *[o.ctypes.data for o in out], cnt)
     if rc < 0:
         raise TLError(rc, "tl_rs_tile_order")
+    return tuple(out)
+
+
+def tl_rs_ring_tile_order(W, m, n):
+    import numpy as np
+    L = lib()
+    cnt = L.tl_rs_ring_tile_order(W, m, n, None, None, None, None, None, 0)
+    if cnt < 0:
+        raise TLError(cnt, "tl_rs_ring_tile_order")
+    out = [np.zeros(cnt, dtype=np.int32) for _ in range(5)]
+    rc = L.tl_rs_ring_tile_order(W, m, n, *[o.ctypes.data for o in out], cnt)
+    if rc < 0:
+        raise TLError(rc, "tl_rs_ring_tile_order")
     return tuple(out)
 
 

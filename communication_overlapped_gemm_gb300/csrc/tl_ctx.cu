@@ -78,6 +78,7 @@ int tl_config_default(tl_config* cfg) {
   cfg->timeout_ns = 2000000000ull;
   cfg->pair_ctas = 2;
   cfg->moe_renorm = 0;
+  cfg->rs_ring = 0;
   return TL_OK;
 }
 
@@ -93,7 +94,8 @@ int tl_ctx_create(tl_ctx** out, int device, const tl_config* cfg) {
     tl_config_default(&c);
   if (c.mover_warps < 1 || c.mover_warps > tl::kMaxMoverWarps || !pow2_le32(c.chunks_per_slab) ||
       (c.swizzle != 0 && c.swizzle != 1) || c.grid_ctas < 0 || c.combine_ctas < 1 || c.timeout_ns == 0 ||
-      c.pair_ctas < 0 || c.pair_ctas > 2 || (c.moe_renorm != 0 && c.moe_renorm != 1))
+      c.pair_ctas < 0 || c.pair_ctas > 2 || (c.moe_renorm != 0 && c.moe_renorm != 1) ||
+      (c.rs_ring != 0 && c.rs_ring != 1))
     return TL_ERR_INVALID;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
@@ -238,6 +240,25 @@ int tl_rs_tile_order(int W, int m, int n, int swizzle, int* producer, int* owner
     owner[t] = r.o;
     m_block[t] = r.mb * (bm / tl::kBM);
     n_block[t] = r.nb;
+  }
+  return total;
+}
+
+int tl_rs_ring_tile_order(int W, int m, int n, int* producer, int* owner, int* m_block, int* n_block, int* hop,
+                          int cap) {
+  if (W < 1 || W > 8 || m <= 0 || m % (tl::kBM * W) || n <= 0) return TL_ERR_INVALID;
+  const int bm = (m / W) % 256 == 0 ? 256 : 128;  // the tile rows tl_gemm_rs uses
+  const int mbo = m / W / bm, nbk = tl::ceil_div(n, tl::kBN);
+  const int total = tl::rs_num_tiles(W, mbo, nbk);
+  if (!producer && !owner && !m_block && !n_block && !hop) return total;
+  if (!producer || !owner || !m_block || !n_block || !hop || cap < total) return TL_ERR_INVALID;
+  for (int t = 0; t < total; ++t) {
+    tl::RsTile r = tl::rs_ring_tile(t, W, mbo, nbk, bm);
+    producer[t] = r.p;
+    owner[t] = r.o;
+    m_block[t] = r.mb * (bm / tl::kBM);
+    n_block[t] = r.nb;
+    hop[t] = r.s;
   }
   return total;
 }

@@ -49,30 +49,28 @@ __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + copysignf(e, x));
 }
 
-#ifndef TL_RS_DISCARD
-#define TL_RS_DISCARD 1
-#endif
-
-// GEMM+RS epilogue on one BM x 256 partial tile of producer `prod` (of W), reduced into
-// the fp32 slot tile at (grow, n0); the last producer writes bf16 rows of `out` at orow.
-// Order of the fp32 sums is fixed: slot = P_0; slot += P_1; ...; out = slot + P_{W-1}.
-// Rows 128h..128h+127 of the tile are TMEM columns [256h, 256h+256).
+// One step of a GEMM+RS summation chain, on a BM x 256 partial tile held in TMEM (rows
+// 128h..128h+127 of the tile are TMEM columns [256h, 256h+256)).  The chain of an output tile
+// has W steps, pos = 0..W-1; step pos > 0 first waits for step pos-1's signal on the tile
+// (peer_tile_wait).  Then:
+//   - a non-final step writes its fp32 result to st_map at rows st_row..: a TMA store, or
+//     with `reduce` a TMA bulk reduce-add (the owner-slot chain's middle steps);
+//   - with `prev`, the step first adds the running partial at prev (row-major, stride n,
+//     the tile's first row) in registers (a ring hop, or the slot chain's final step);
+//   - the final step writes bf16 rows of `out_map` at orow.
+// The fp32 order of every output element is therefore fixed by the chain order.
 template <int BM>
-__device__ __forceinline__ void rs_epilogue(const CUtensorMap* acc_map, const float* acc_ptr,
-                                            const CUtensorMap* out_map, const uint64_t* flag, int prod, int W,
-                                            int grow, int orow, int n0, int n, const Common& c, uint32_t taddr,
-                                            int q, int lane, EpiStage& es, int h0, int h1) {
-  const bool first = prod == 0;
-  const bool last = prod == W - 1;
-  if (!first) {
-    // peer_tile_wait: producer prod-1 has finished its contribution to this tile.
-    warp_wait_one(flag, (c.epoch << 4) | static_cast<unsigned long long>(prod), c, lane, kSitePeer,
-                  static_cast<unsigned long long>(grow) << 20 | static_cast<unsigned>(n0));
-  }
+__device__ __forceinline__ void rs_epilogue(const CUtensorMap* st_map, int st_row, bool reduce, const float* prev,
+                                            const CUtensorMap* out_map, int orow, const uint64_t* flag, int pos,
+                                            int W, int n0, int n, const Common& c, uint32_t taddr, int q, int lane,
+                                            EpiStage& es, int h0, int h1, unsigned long long info) {
+  const bool last = pos == W - 1;
+  if (pos > 0) warp_wait_one(flag, (c.epoch << 4) | static_cast<unsigned long long>(pos), c, lane, kSitePeer, info);
 #pragma unroll 1
   for (int h = h0; h < h1; ++h) {
     const uint32_t th = taddr + h * 256;
-    const int gr = grow + h * 128 + q * 32;
+    const int r = h * 128 + q * 32;  // this warp's first row inside the tile
+    const float* src_row = prev ? prev + static_cast<size_t>(r + lane) * n : nullptr;
     if (!last) {
 #pragma unroll 1
       for (int ch = 0; ch < kBN / 32; ++ch) {
@@ -80,43 +78,50 @@ __device__ __forceinline__ void rs_epilogue(const CUtensorMap* acc_map, const fl
         if (x >= n) break;
         float v[32];
         tmem_ld32(th + ch * 32, v);
-        store_f32_chunk(acc_map, es, lane, v, x, gr, !first);
+        if (prev) {
+          const float* src = src_row + x;
+          if (x + 32 <= n) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 s4 = __ldcg(reinterpret_cast<const float4*>(src) + i);
+              v[4 * i] += s4.x;
+              v[4 * i + 1] += s4.y;
+              v[4 * i + 2] += s4.z;
+              v[4 * i + 3] += s4.w;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (x + i < n) v[i] += __ldcg(src + i);
+          }
+        }
+        store_f32_chunk(st_map, es, lane, v, x, st_row + r, reduce);
       }
     } else {
-      const int row = gr + lane;
 #pragma unroll 1
       for (int ch = 0; ch < kBN / 64; ++ch) {
         const int x = n0 + ch * 64;
         if (x >= n) break;
         float v[64];
         tmem_ld64(th, ch * 64, v);
-        if (!first) {
-          const float* src = acc_ptr + static_cast<size_t>(row) * n + x;
+        if (prev) {
+          const float* src = src_row + x;
           if (x + 64 <= n) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float4 s = __ldcg(reinterpret_cast<const float4*>(src) + i);
-              v[4 * i] += s.x;
-              v[4 * i + 1] += s.y;
-              v[4 * i + 2] += s.z;
-              v[4 * i + 3] += s.w;
+              const float4 s4 = __ldcg(reinterpret_cast<const float4*>(src) + i);
+              v[4 * i] += s4.x;
+              v[4 * i + 1] += s4.y;
+              v[4 * i + 2] += s4.z;
+              v[4 * i + 3] += s4.w;
             }
-#if TL_RS_DISCARD
-            // This producer is the slot tile's last reader in this call, and the next call's
-            // first producer overwrites it: drop its two 128-byte lines from L2 rather than
-            // write them back (rows start on 128-byte lines when n % 32 == 0).
-            if ((n & 31) == 0) {
-              discard_l2_line(src);
-              discard_l2_line(src + 32);
-            }
-#endif
           } else {
 #pragma unroll
             for (int i = 0; i < 64; ++i)
               if (x + i < n) v[i] += __ldcg(src + i);
           }
         }
-        store_bf16_chunk(out_map, es, lane, v, x, orow + h * 128 + q * 32);
+        store_bf16_chunk(out_map, es, lane, v, x, orow + r);
       }
     }
   }
@@ -252,11 +257,12 @@ struct RsParams {
   CUtensorMap a[8];    // A_p: {k_r, m}, box {64, BM}
   CUtensorMap b[8];    // B_p: {n, k_r}, box {64, 64}
   CUtensorMap out[8];  // out_o: {n, m/W}, box {64, 32}
-  CUtensorMap acc;     // fp32 slot: {n, m}, box {32, 32}
+  CUtensorMap acc;     // owner-slot chain: the fp32 slot {n, m}; ring: the W receive buffers
+                       // {n, W*m} (rank q's at rows q*m ..); box {32, 32}
   Common common;
   const float* acc_ptr;
   uint64_t* flags;  // [m/128][nbk] (a tile uses the signal of its first 128-row block)
-  int W, m, mo, mbo, n, nbk, kblocks, swizzle;
+  int W, m, mo, mbo, n, nbk, kblocks, swizzle, ring;
 };
 
 template <int BM, bool Pair = false>
@@ -270,9 +276,9 @@ struct RsOp : OpBase<RsParams> {
   static constexpr uint32_t kTxBytes = Pair ? Geo2::kStageBytes : Geo<BM>::kStageBytes;
   static __device__ int num_tiles(const Params& p) { return rs_num_tiles(p.W, p.mbo, p.nbk); }
   static __device__ Job job(const Params& p, int t) {
-    const RsTile r = rs_tile(t, p.W, p.mbo, p.nbk, BM, p.swizzle);
+    const RsTile r = p.ring ? rs_ring_tile(t, p.W, p.mbo, p.nbk, BM) : rs_tile(t, p.W, p.mbo, p.nbk, BM, p.swizzle);
     Job j;
-    j.kind = 0;
+    j.kind = r.s;  // position in the tile's summation chain
     j.a_sel = r.p;
     j.a_row = r.o * p.mo + r.mb * BM;
     j.b_sel = r.p;
@@ -301,15 +307,30 @@ struct RsOp : OpBase<RsParams> {
   static __device__ int tile_id(const Params& p, const Job& j) {
     return (j.a_row / 128 + (Pair ? j.rank : 0)) * p.nbk + j.x3;
   }
+  // Owner-slot chain: step p stores (p = 0) or TMA-adds (0 < p < W-1) its partial into the
+  // owner's slot, the last producer adds the slot in registers and writes bf16.  Ring: hop s
+  // (producer q) adds the running partial in its own receive buffer (s > 0) and stores the sum
+  // into rank q+1's receive buffer, the owner (last hop) writes bf16.
   static __device__ void epilogue(const Params& p, const Job& j, uint32_t taddr, int q, int lane, EpiStage& es,
                                  int h0, int h1) {
-    rs_epilogue<BM>(&p.acc, p.acc_ptr, &p.out[j.x1], p.flags + tile_id(p, j), j.x0, p.W, j.a_row, j.x2 * BM,
-                    j.b_col, p.n, p.common, taddr, q, lane, es, h0, h1);
+    const int pos = j.kind, grow = j.a_row;
+    const unsigned long long info = static_cast<unsigned long long>(grow) << 20 | static_cast<unsigned>(j.b_col);
+    const uint64_t* flag = p.flags + tile_id(p, j);
+    if (p.ring) {
+      const int next = (j.x0 + 1) % p.W;
+      const float* prev = pos > 0 ? p.acc_ptr + (static_cast<size_t>(j.x0) * p.m + grow) * p.n : nullptr;
+      rs_epilogue<BM>(&p.acc, next * p.m + grow, false, prev, &p.out[j.x1], j.x2 * BM, flag, pos, p.W, j.b_col, p.n,
+                      p.common, taddr, q, lane, es, h0, h1, info);
+    } else {
+      const float* prev = (pos > 0 && pos == p.W - 1) ? p.acc_ptr + static_cast<size_t>(grow) * p.n : nullptr;
+      rs_epilogue<BM>(&p.acc, grow, pos > 0, prev, &p.out[j.x1], j.x2 * BM, flag, pos, p.W, j.b_col, p.n, p.common,
+                      taddr, q, lane, es, h0, h1, info);
+    }
   }
-  // peer_tile_notify: producer p's contribution to this slot tile is complete.
-  static __device__ bool publishes(const Params& p, const Job& j) { return j.x0 != p.W - 1; }
+  // peer_tile_notify: step pos of this tile's chain is complete.
+  static __device__ bool publishes(const Params& p, const Job& j) { return j.kind != p.W - 1; }
   static __device__ void publish(const Params& p, const Job& j) {
-    st_release_gpu(p.flags + tile_id(p, j), (p.common.epoch << 4) | static_cast<unsigned long long>(j.x0 + 1));
+    st_release_gpu(p.flags + tile_id(p, j), (p.common.epoch << 4) | static_cast<unsigned long long>(j.kind + 1));
   }
 };
 
@@ -448,8 +469,11 @@ struct Mlp2Op : OpBase<Mlp2Params> {
         }
       }
     } else {
-      rs_epilogue<BM>(&p.acc, p.acc_ptr, &p.out[j.x1], p.rs_flags + rs_tile_id(p, j), j.x0, p.W,
-                      j.x1 * p.Tr + j.x2 * BM, j.x2 * BM, j.b_col, p.h, p.common, taddr, q, lane, es, h0, h1);
+      const int grow = j.x1 * p.Tr + j.x2 * BM, pos = j.x0;
+      const float* prev = (pos > 0 && pos == p.W - 1) ? p.acc_ptr + static_cast<size_t>(grow) * p.h : nullptr;
+      rs_epilogue<BM>(&p.acc, grow, pos > 0, prev, &p.out[j.x1], j.x2 * BM, p.rs_flags + rs_tile_id(p, j), pos, p.W,
+                      j.b_col, p.h, p.common, taddr, q, lane, es, h0, h1,
+                      static_cast<unsigned long long>(grow) << 20 | static_cast<unsigned>(j.b_col));
     }
   }
   static __device__ bool publishes(const Params& p, const Job& j) { return j.kind == 1 || j.x0 != p.W - 1; }
@@ -497,6 +521,9 @@ struct Mlp2Op : OpBase<Mlp2Params> {
 // geometry, order and signals as the fused AllGather+GEMM, run by mover_warps warps in
 // each of the persistent CTAs.
 constexpr int kAllgatherWarps = 16;  // copy warps per CTA of the standalone AllGather
+#ifndef TL_AG_ALONE_CTAS_PER_SM
+#define TL_AG_ALONE_CTAS_PER_SM 4
+#endif
 __global__ void __launch_bounds__(kAllgatherWarps * 32) allgather_kernel(const __grid_constant__ AgParams p) {
   ag_mover<false>(p, threadIdx.x >> 5, threadIdx.x & 31);
 }
@@ -639,11 +666,23 @@ static bool rs_shape_ok(int W, int m, int n, int kr) {
   return W >= 1 && W <= 8 && m >= 0 && n >= 0 && kr >= 0 && m % (kBM * W) == 0 && n % 8 == 0 && kr % 8 == 0;
 }
 
+// GEMM+RS workspace: the fp32 partial buffers (the owner slot, m x n; or, for the ring, W
+// receive buffers of m x n), then one signal per 128-row block and 256-column block.
+static size_t rs_acc_bytes(int W, int m, int n, bool ring) {
+  return align256(static_cast<size_t>(ring ? W : 1) * m * n * 4);
+}
+static size_t rs_ws_bytes(int W, int m, int n, bool ring) {
+  return rs_acc_bytes(W, m, n, ring) + align256(static_cast<size_t>(m / kBM) * ceil_div(n, kBN) * 8);
+}
+
 extern "C" size_t tl_gemm_rs_workspace_bytes(int W, int m, int n, int k_r) {
   if (!rs_shape_ok(W, m, n, k_r)) return 0;
-  const size_t acc = static_cast<size_t>(m) * n * 4;
-  const size_t flags = static_cast<size_t>(m / kBM) * ceil_div(n, kBN) * 8;
-  return align256(acc) + align256(flags);
+  return rs_ws_bytes(W, m, n, false);
+}
+
+extern "C" size_t tl_gemm_rs_ring_workspace_bytes(int W, int m, int n, int k_r) {
+  if (!rs_shape_ok(W, m, n, k_r)) return 0;
+  return rs_ws_bytes(W, m, n, true);
 }
 
 extern "C" int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* const* b, void* const* out,
@@ -654,7 +693,8 @@ extern "C" int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* 
   for (int r = 0; r < W; ++r)
     if (!a[r] || !b[r] || !out[r] || !aligned16(a[r]) || !aligned16(b[r]) || !aligned16(out[r]))
       return TL_ERR_INVALID;
-  if (workspace_bytes < tl_gemm_rs_workspace_bytes(W, m, n, k_r)) return TL_ERR_WORKSPACE;
+  const bool ring = ctx->cfg.rs_ring != 0;
+  if (workspace_bytes < rs_ws_bytes(W, m, n, ring)) return TL_ERR_WORKSPACE;
   if (k_r == 0) return TL_ERR_INVALID;  // an empty reduction has no tiles to chain; reject
   if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
 
@@ -663,7 +703,8 @@ extern "C" int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* acc = reinterpret_cast<float*>(ws);
   p.acc_ptr = acc;
-  p.flags = reinterpret_cast<uint64_t*>(ws + align256(static_cast<size_t>(m) * n * 4));
+  p.flags = reinterpret_cast<uint64_t*>(ws + rs_acc_bytes(W, m, n, ring));
+  p.ring = ring ? 1 : 0;
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int mo = m / W;
   const int bm = pick_bm(mo);
@@ -673,7 +714,8 @@ extern "C" int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* 
         !tmap_2d(&p.out[r], BF, 2, out[r], n, mo, 64, 32))
       return TL_ERR_CUDA;
   }
-  if (!tmap_2d(&p.acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, n, m, 32, 32)) return TL_ERR_CUDA;
+  if (!tmap_2d(&p.acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, n, static_cast<uint64_t>(ring ? W : 1) * m, 32, 32))
+    return TL_ERR_CUDA;
   p.common = make_common(ctx);
   p.W = W;
   p.m = m;
@@ -816,10 +858,12 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   p.copy_self = 1;
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
-  // Alone, the copy has the whole GPU: kAllgatherWarps warps in each of the persistent CTAs
-  // run the same chunk loop as the fused kernel's mover warps.
+  // Alone, the copy has the whole GPU: TL_AG_ALONE_CTAS_PER_SM CTAs of kAllgatherWarps warps
+  // on each SM run the same chunk loop as the fused kernel's mover warps, so one CTA's fence
+  // and barrier after a chunk overlap the other CTAs' loads.
   p.common.mover_warps = kAllgatherWarps;
-  allgather_kernel<<<ctx->ctas, kAllgatherWarps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  allgather_kernel<<<ctx->ctas * TL_AG_ALONE_CTAS_PER_SM, kAllgatherWarps * 32, 0,
+                     reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? TL_OK : TL_ERR_CUDA;
 }
 

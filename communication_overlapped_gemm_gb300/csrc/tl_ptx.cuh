@@ -42,11 +42,6 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu_u32(const uint32_t* p) {
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
-// Drop one 128-byte line (128-byte aligned) from L2 without writing it back: its memory
-// then holds an undefined value.  For scratch lines whose last reader has read them.
-__device__ __forceinline__ void discard_l2_line(const void* p) {
-  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

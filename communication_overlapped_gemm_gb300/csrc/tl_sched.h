@@ -63,6 +63,7 @@ struct RsTile {
   int o;   // owner of the output rows
   int mb;  // row block inside the owner's rows
   int nb;  // column block
+  int s;   // position of this partial in the tile's summation chain (0 .. W-1)
 };
 
 // GEMM + ReduceScatter, banded.  The m x n output is cut into bands of kRsBandRows rows x
@@ -117,6 +118,39 @@ TL_HD RsTile rs_tile(int t, int W, int mbo, int nbk, int bm, int swizzle) {
   int row = r0 + (i + start) % R;
   r.o = row / mbo;
   r.mb = row - r.o * mbo;
+  r.s = r.p;
+  return r;
+}
+
+// GEMM + ReduceScatter as a ring ("TileLink ...", §5, Figure 4 text: each rank reduces the
+// partial it receives with its own and passes the result on, peer_tile_wait /
+// peer_tile_notify between neighbours).  The partial of an output tile of owner o starts at
+// rank o + 1 and travels o+1 -> o+2 -> ... -> o (mod W): hop s is computed by producer
+// (o + 1 + s) mod W, and the owner, the last hop, writes bf16.  Order: owner by owner; each
+// owner's rows in bands of kRsBandRows rows x kRsBandCols columns; inside a band the hops
+// s = 0..W-1 in turn (every tile of a band at one hop shares one producer, so its B column
+// slabs serve all the band's rows), and inside a hop the column block slowest, the row block
+// fastest.  A hop waits only on the same tile's previous hop, earlier in the sequence.
+TL_HD RsTile rs_ring_tile(int t, int W, int mbo, int nbk, int bm) {
+  const int bmt = rs_band_mt(bm), bnt = rs_band_nt();
+  const int per_owner = W * mbo * nbk;
+  RsTile r;
+  r.o = t / per_owner;
+  int rem = t - r.o * per_owner;
+  const int per_rowband = W * bmt * nbk;
+  const int br = rem / per_rowband;
+  rem -= br * per_rowband;
+  const int r0 = br * bmt;
+  const int R = mbo - r0 < bmt ? mbo - r0 : bmt;
+  const int bc = rem / (W * R * bnt);
+  rem -= bc * W * R * bnt;
+  const int c0 = bc * bnt;
+  const int C = nbk - c0 < bnt ? nbk - c0 : bnt;
+  r.s = rem / (R * C);
+  rem -= r.s * R * C;
+  r.nb = c0 + rem / R;
+  r.mb = r0 + rem - (rem / R) * R;
+  r.p = (r.o + 1 + r.s) % W;
   return r;
 }
 }  // namespace tl

@@ -88,6 +88,9 @@ typedef struct tl_config {
   int moe_renorm;             /* MoE gates: 0 (default) the softmax over all E logits taken at the
                                  chosen experts; 1 those values divided by their sum over the topk
                                  chosen experts (they then sum to 1 per token)                      */
+  int rs_ring;                /* tl_gemm_rs reduction: 0 (default) the owner-slot chain; 1 a ring
+                                 ([TL] §5, Figure 4 text), workspace from
+                                 tl_gemm_rs_ring_workspace_bytes                                    */
 } tl_config;
 
 typedef struct tl_ctx tl_ctx;
@@ -177,8 +180,8 @@ int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const 
 
 /* ---------------------------------------------------------------- AllGather alone
  * [TD] §3.2 Algorithm 2 (pull-mode one-sided AllGather) as its own kernel: the shard mover of
- * tl_ag_gemm (same chunks, order and signals) without the GEMM, run by 16 warps in each
- * persistent CTA (alone, the copy has the whole GPU).  Fills the gathered buffer at the start
+ * tl_ag_gemm (same chunks, order and signals) without the GEMM, run by four CTAs of 16 warps
+ * per SM (alone, the copy has the whole GPU).  Fills the gathered buffer at the start
  * of `workspace` (sized by tl_ag_gemm_workspace_bytes(W, m_per_rank, 8, k)) with all of
  * [A_0; ...; A_{W-1}], the self rank's shard last, and releases every chunk signal.  Shapes
  * and errors as tl_ag_gemm; W = 1 is a no-op.  This is the "communication alone" leg of the
@@ -196,17 +199,26 @@ int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_shards, void
  *
  * a: W device pointers, A_p bf16 [m x k_r];  b: W device pointers, B_p bf16 [k_r x n];
  * out: W device pointers, out_o bf16 [(m/W) x n].
- * workspace: tl_gemm_rs_workspace_bytes(): an fp32 [m x n] accumulation slot (owner o owns
- * rows o*m/W..) plus one signal per output tile.  Producers are visited p = 0..W-1; producer
- * p walks owners (p+1) mod W, (p+2) mod W, ..., p (swizzle = 1) or 0..W-1 (swizzle = 0).
- * Producer 0 stores its partial tile into the slot, producer p > 0 waits for producer p-1's
- * signal on that tile (peer_tile_wait) and adds its partial with a TMA bulk reduction, and
- * producer W-1 adds its partial to the slot in registers and writes bf16 out_o.  The fp32
- * summation order is therefore fixed (p = 0, 1, ..., W-1): results are bit-identical across
- * runs, swizzle modes and grid sizes.
+ * Owner-slot chain (cfg.rs_ring = 0, default).  workspace: tl_gemm_rs_workspace_bytes(): an
+ * fp32 [m x n] accumulation slot (owner o owns rows o*m/W..) plus one signal per 128-row block
+ * and 256-column block of the output.  The output is walked in bands of 2048 rows x 4096
+ * columns; inside a band the producers run p = 0..W-1, producer p starting at the rows of
+ * owner (p+1) mod W when the band holds some (swizzle = 1).  Producer 0 stores its partial
+ * tile into the slot, producer p > 0 waits for producer p-1's signal on that tile
+ * (peer_tile_wait) and adds its partial with a TMA bulk reduction, and producer W-1 adds its
+ * partial to the slot in registers and writes bf16 out_o.  The fp32 summation order is fixed
+ * (p = 0, 1, ..., W-1): results are bit-identical across runs, swizzle modes and grid sizes.
+ * Ring (cfg.rs_ring = 1).  workspace: tl_gemm_rs_ring_workspace_bytes(): W fp32 [m x n]
+ * receive buffers (rank q's at q*m*n*4 bytes), then the signals.  The partial of an output
+ * tile of owner o starts at rank o+1 and travels o+1 -> o+2 -> ... -> o (mod W): each rank
+ * waits for its predecessor's signal on the tile (peer_tile_wait), adds the partial in its
+ * receive buffer to its own, stores the sum into the next rank's receive buffer and signals
+ * it (peer_tile_notify); the owner, last, writes bf16 out_o.  The fp32 order of owner o's
+ * rows is P_{o+1} + P_{o+2} + ... + P_o: fixed, so results are bit-identical run to run.
  * Shapes: 1 <= W <= 8; m % (128*W) == 0; n % 8 == 0; k_r % 8 == 0.
  */
 size_t tl_gemm_rs_workspace_bytes(int W, int m, int n, int k_r);
+size_t tl_gemm_rs_ring_workspace_bytes(int W, int m, int n, int k_r);
 int tl_gemm_rs(tl_ctx* ctx, int W, const void* const* a, const void* const* b, void* const* out,
                void* workspace, size_t workspace_bytes, int m, int n, int k_r, tl_stream_t stream);
 
@@ -333,13 +345,17 @@ int tl_ag_gemm_static_scratch(tl_ctx* ctx, int W, int rank, const void* const* a
  *   rank, the row block inside that rank's shard and the column block.  Returns the number of
  *   tiles, or TL_ERR_INVALID.  Arrays may be NULL to query the count; otherwise they must hold
  *   `cap` entries.
- * tl_rs_tile_order: the same for GEMM + ReduceScatter: producer, owner, row block within the
- *   owner's rows, column block.
+ * tl_rs_tile_order: the same for GEMM + ReduceScatter (owner-slot chain): producer, owner, row
+ *   block within the owner's rows, column block.
+ * tl_rs_ring_tile_order: the same for the ring (cfg.rs_ring = 1), plus each tile's hop (its
+ *   position 0..W-1 on the ring of its owner's partial).
  */
 int tl_ag_tile_order(int W, int rank, int m_per_rank, int n, int swizzle, int* src_rank, int* m_block,
                      int* n_block, int cap);
 int tl_rs_tile_order(int W, int m, int n, int swizzle, int* producer, int* owner, int* m_block, int* n_block,
                      int cap);
+int tl_rs_ring_tile_order(int W, int m, int n, int* producer, int* owner, int* m_block, int* n_block, int* hop,
+                          int cap);
 
 #ifdef __cplusplus
 }

@@ -53,6 +53,7 @@ def test_config_defaults_and_strerror(tl):
     assert tl.lib().tl_config_default(ctypes.byref(c)) == tl.TL_OK
     assert (c.mover_warps, c.chunks_per_slab, c.swizzle, c.grid_ctas, c.combine_ctas) == (4, 32, 1, 0, 16)
     assert c.debug_skip_chunk == -1 and c.timeout_ns == 2_000_000_000 and c.pair_ctas == 2 and c.moe_renorm == 0
+    assert c.rs_ring == 0
     assert tl.lib().tl_config_default(None) == tl.TL_ERR_INVALID
     for code in (tl.TL_OK, tl.TL_ERR_INVALID, tl.TL_ERR_UNSUPPORTED, tl.TL_ERR_CUDA, tl.TL_ERR_TIMEOUT,
                  tl.TL_ERR_WORKSPACE):
@@ -157,6 +158,33 @@ def test_rs_tile_order_banded_and_owner_swizzled(tl, W, m, n):
         for q, oo, r, c in got:
             assert seen.get((oo, r, c), -1) == q - 1
             seen[(oo, r, c)] = q
+
+
+@pytest.mark.parametrize("W,m,n", [(8, 8192, 8192), (4, 1024, 520), (1, 128, 256), (3, 768, 520), (5, 640, 296)])
+def test_rs_ring_tile_order(tl, W, m, n):
+    """The ring: owner by owner, bands of 2048 x 4096, hops 0..W-1 inside a band, column block
+    slowest inside a hop; hop s of owner o is computed by producer (o + 1 + s) mod W, the owner
+    last, and each tile's hops come in order."""
+    bm = 256 if (m // W) % 256 == 0 else 128
+    mbo, nbk = m // W // bm, -(-n // 256)
+    p, o, mb, nb, hop = tl.tl_rs_ring_tile_order(W, m, n)
+    got = list(zip(p.tolist(), o.tolist(), mb.tolist(), nb.tolist(), hop.tolist()))
+    BR, BC = max(1, 2048 // bm), 4096 // 256
+    exp = []
+    for oo in range(W):
+        for r0 in range(0, mbo, BR):
+            for c0 in range(0, nbk, BC):
+                for sh in range(W):
+                    for c in range(c0, min(nbk, c0 + BC)):
+                        exp += [((oo + 1 + sh) % W, oo, r * (bm // 128), c, sh) for r in range(r0, min(mbo, r0 + BR))]
+    assert got == exp
+    seen = {}
+    for q, oo, r, c, sh in got:
+        assert seen.get((oo, r, c), -1) == sh - 1
+        seen[(oo, r, c)] = sh
+    assert all(v == W - 1 for v in seen.values()) and len(seen) == W * mbo * nbk
+    al = lambda x: (x + 255) // 256 * 256
+    assert tl.tl_gemm_rs_ring_workspace_bytes(W, m, n, 64) == al(W * m * n * 4) + al((m // 128) * nbk * 8)
 
 
 def test_tile_order_rejects_bad_shapes(tl):

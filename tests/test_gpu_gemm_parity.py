@@ -121,7 +121,8 @@ def run_rs(ctx, inp):
     m, kr = a[0].shape
     n = b[0].shape[1]
     out = [torch.empty((m // W, n), dtype=torch.bfloat16, device="cuda") for _ in range(W)]
-    ws = workspace(tl.tl_gemm_rs_workspace_bytes(W, m, n, kr))
+    size = tl.tl_gemm_rs_ring_workspace_bytes if ctx.config.rs_ring else tl.tl_gemm_rs_workspace_bytes
+    ws = workspace(size(W, m, n, kr))
     tl.tl_gemm_rs(ctx, a, b, out, ws)
     torch.cuda.synchronize()
     assert ctx.check() == tl.TL_OK
@@ -147,6 +148,37 @@ def test_gemm_rs_deterministic_across_orders():
                 outs.append([bf16_bits(o) for o in run_rs(c2, inp)])
     for o in outs[1:]:
         assert all(np.array_equal(x, y) for x, y in zip(o, outs[0]))
+
+
+@pytest.mark.parametrize("W,m,n,kr", [(1, 128, 256, 64), (2, 256, 256, 128), (4, 512, 328, 200),
+                                      (8, 1024, 264, 72), (3, 768, 520, 3584)])
+def test_gemm_rs_ring_matches_oracle(W, m, n, kr):
+    """Ring reduction (cfg.rs_ring = 1): each owner's partial travels o+1 -> ... -> o, every
+    rank adding its own; within tolerance of the oracle and bit-identical run to run and
+    across the CTA-pair / single-CTA engines and grid sizes (the ring order is fixed)."""
+    inp = make_inputs("gemm_rs", 31 + W, W=W, m=m, n=n, k_r=kr)
+    ref = oracle.gemm_rs(inp["a"], inp["b"])
+    outs = []
+    for cfg in [dict(), dict(pair_ctas=0), dict(grid_ctas=23)]:
+        with tl.Context(0, rs_ring=1, **cfg) as c2:
+            for _ in range(2):
+                out = run_rs(c2, inp)
+                outs.append([bf16_bits(o) for o in out])
+                for o in range(W):
+                    assert_close(bf16_to_f64(out[o]), ref[o], f"ring W={W} owner {o} {cfg}")
+    for o in outs[1:]:
+        assert all(np.array_equal(x, y) for x, y in zip(o, outs[0]))
+
+
+def test_gemm_rs_ring_full_size_whole_rows():
+    """Full-size ring GEMM+RS (W=8, 8192x8192, K = 8 x 3584): whole rows of every owner."""
+    inp = workload_inputs("rs_70b")
+    with tl.Context(0, rs_ring=1) as c2:
+        out = run_rs(c2, inp)
+    for o in range(8):
+        rows = [0, 300, 1023]
+        ref = oracle.gemm_rs_rows(inp["a"], inp["b"], o, rows)
+        assert_close(bf16_to_f64(out[o])[rows], ref, f"ring rs_70b owner {o}")
 
 
 def test_gemm_rs_full_size_whole_rows(ctx):

@@ -65,7 +65,7 @@ def test_trace_ag_gemm_tiles_and_chunks():
         once_each(sp, 4, ntiles)          # MMA tile
         once_each(sp, 1, ntiles)          # producer tile
         once_each(sp, 7, ntiles, per=8)   # epilogue tile, 8 epilogue warps (one warpgroup per row half)
-        once_each(sp, 9, 4 * 2 * 32)      # mover chunk: W x 128-row slabs x chunks
+        once_each(sp, 9, 3 * 2 * 32)      # mover chunk: W-1 remote shards x 128-row slabs x chunks
         assert set(sp["warp"][sp["kind"] == 4].tolist()) == {1}
         assert set(sp["warp"][sp["kind"] == 1].tolist()) == {0}
 
