@@ -138,34 +138,78 @@ struct AgParams {
   uint8_t* gath;
   uint64_t* flags;  // [W][spr][chunks]
   long long shard_bytes, slab_bytes;
-  int W, rank, m_per_rank, mps, spr, n, nbk, kblocks, swizzle, chunks, skip_chunk;
+  int W, rank, m_per_rank, mps, spr, n, k, nbk, kblocks, swizzle, chunks, skip_chunk;
   int boost;      // chunks [0, boost) are split with the epilogue warps (see ag_mover)
   int copy_self;  // 1: the self rank's shard is copied too (last); 0: only the W-1 remote shards
+  int quarters;   // K parts of a slab (1..4); a slab's chunks are cpq row pieces of each part
+  int cpq;        // chunks per K part (chunks = quarters * cpq)
+  int qcols;      // columns per K part (a multiple of 64; the last part may be shorter or empty)
+  int kb_q;       // 64-column k-blocks per K part (qcols / 64)
 };
 
+// Copy `rows` rows of `row_bytes` bytes (a multiple of 16) from src to dst, both with a row
+// stride of `stride` bytes, by `nthreads` threads: 16-byte vectors, 8 loads in flight.
+__device__ __forceinline__ void copy_rows(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, size_t stride,
+                                          int rows, int row_bytes, int tid, int nthreads) {
+  const int vr = row_bytes / 16;
+  const int nvec = rows * vr;
+  constexpr int U = 8;
+  int i = tid;
+  for (; i + (U - 1) * nthreads < nvec; i += U * nthreads) {
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = i + u * nthreads;
+      r[u] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(v / vr) * stride) + v % vr);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = i + u * nthreads;
+      reinterpret_cast<uint4*>(dst + static_cast<size_t>(v / vr) * stride)[v % vr] = r[u];
+    }
+  }
+  for (; i < nvec; i += nthreads)
+    reinterpret_cast<uint4*>(dst + static_cast<size_t>(i / vr) * stride)[i % vr] =
+        __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(i / vr) * stride) + i % vr);
+}
+
 // The shard mover: pull the remote shards (and, with copy_self, the self rank's own, last)
-// into the gathered buffer in 128-row slabs of `chunks` chunks, one release signal per chunk.  Chunk g belongs to CTA
-// g mod grid.  The first `boost` chunks (the shards the first wave of tiles waits for) are
-// shared with the epilogue warps, which are idle until their first tile: in every other
-// round of the head (g / grid odd) the mover warps copy, in the others the epilogue warps
-// (group = 1), so the head arrives up to twice as fast.
+// into the gathered buffer, one release signal per chunk.  A 128-row slab is cut along K into
+// `quarters` parts of qcols columns, and each part into cpq pieces of 128/cpq rows: a chunk
+// is one piece of one part.  Chunks go K part first: part 0 of every slab of every shard (in
+// the mover's shard order), then part 1, ..., so a tile can start its first k-blocks as soon
+// as part 0 of its rows has landed, while the later parts are still being copied (each tile
+// waits for part q before its k-block q * kb_q).  Chunk g belongs to CTA g mod grid.  The
+// first `boost` chunks are shared with the epilogue warps, which are idle until their first
+// tile: in every other round of the head (g / grid odd) the mover warps copy, in the others
+// the epilogue warps (group = 1), so the head arrives up to twice as fast.
 template <bool Trace>
 __device__ __forceinline__ void ag_copy(const AgParams& p, int tid, int nthreads, int group, int bar) {
-  const int per_shard = p.spr * p.chunks;
-  const int total = group == 1 ? p.boost : (p.W - 1 + p.copy_self) * per_shard;
-  const size_t chunk_bytes = static_cast<size_t>(p.slab_bytes / p.chunks);
+  const int shards = p.W - 1 + p.copy_self;
+  const int per_part = shards * p.spr * p.cpq;  // chunks of one K part, every shard
+  const int total = group == 1 ? p.boost : p.quarters * per_part;
+  const int piece_rows = kBM / p.cpq;
+  const size_t row_stride = static_cast<size_t>(p.k) * 2;
   for (int g = blockIdx.x; g < total; g += gridDim.x) {
     if (g < p.boost && ((g / static_cast<int>(gridDim.x)) & 1) == (group == 1 ? 1 : 0)) continue;
-    const int i = g / per_shard;
-    const int rem = g - i * per_shard;
-    const int slab = rem / p.chunks;
-    const int ch = rem - slab * p.chunks;
+    const int q = g / per_part;
+    int rem = g - q * per_part;
+    const int i = rem / (p.spr * p.cpq);
+    rem -= i * p.spr * p.cpq;
+    const int slab = rem / p.cpq;
+    const int piece = rem - slab * p.cpq;
     const int r = ag_mover_rank(p.W, p.rank, p.swizzle, i);
-    const size_t off = static_cast<size_t>(slab) * p.slab_bytes + static_cast<size_t>(ch) * chunk_bytes;
+    const int c0 = q * p.qcols;
+    const int cols = c0 >= p.k ? 0 : (p.k - c0 < p.qcols ? p.k - c0 : p.qcols);
+    const size_t off = (static_cast<size_t>(slab) * kBM + static_cast<size_t>(piece) * piece_rows) * row_stride +
+                       static_cast<size_t>(c0) * 2;
     const uint64_t t0 = Trace ? globaltimer() : 0;
-    mover_chunk(p.shard[r] + off, p.gath + static_cast<size_t>(r) * p.shard_bytes + off, chunk_bytes,
-                p.flags + (static_cast<size_t>(r) * p.spr + slab) * p.chunks + ch, g != p.skip_chunk, p.common, tid,
-                nthreads, bar);
+    copy_rows(p.shard[r] + off, p.gath + static_cast<size_t>(r) * p.shard_bytes + off, row_stride, piece_rows,
+              cols * 2, tid, nthreads);
+    __threadfence();
+    named_bar_sync(bar, nthreads);
+    if (tid == 0 && g != p.skip_chunk)
+      st_release_gpu(p.flags + (static_cast<size_t>(r) * p.spr + slab) * p.chunks + q * p.cpq + piece, p.common.epoch);
     if (Trace && tid == 0) trace_span(p.common, kTrMoverChunk, g, t0, globaltimer());
   }
 }
@@ -209,14 +253,18 @@ struct AgOp : OpBase<AgParams> {
     tma_prefetch_map(&p.b);
     tma_prefetch_map(&p.c);
   }
-  // consumer_tile_wait: a remote row block is read only after every chunk of its
-  // BM/128 slabs has been released by the mover.
+  // consumer_tile_wait: the k-blocks of K part q of a remote row block are read only after
+  // the part's chunks of its BM/128 slabs (this CTA's slab, on a pair) have been released.
   static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
-    if (kb != 0 || j.a_sel == 0) return;
+    if (j.a_sel == 0 || kb % p.kb_q != 0) return;
+    const int q = kb / p.kb_q;
     constexpr int kSlabs = Pair ? 1 : BM / 128;  // 128-row slabs this CTA reads
     const int slab0 = j.x1 * (BM / 128) + (Pair ? j.rank : 0);
-    const uint64_t* f = p.flags + (static_cast<size_t>(j.x0) * p.spr + slab0) * p.chunks;
-    wait_slab(f, kSlabs * p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x0) << 32) | j.x1);
+#pragma unroll
+    for (int sl = 0; sl < kSlabs; ++sl) {
+      const uint64_t* f = p.flags + (static_cast<size_t>(j.x0) * p.spr + slab0 + sl) * p.chunks + q * p.cpq;
+      wait_slab(f, p.cpq, p.common, lane, (static_cast<unsigned long long>(j.x0) << 32) | (j.x1 << 4) | q);
+    }
   }
   static __device__ void load(const Params& p, const Job& j, int kb, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
     const int r0 = Pair ? 128 * j.rank : 0;
@@ -579,6 +627,17 @@ static bool ag_shape_ok(int W, int mpr, int n, int k) {
 // Tile rows used for a row extent: 256 when every block of the extent is a 256 multiple.
 static int pick_bm(int rows) { return rows % 256 == 0 ? 256 : 128; }
 
+// The mover's K parts of a slab (see ag_copy): up to four parts of whole 64-column k-blocks,
+// cpq = chunks / parts row pieces each.
+static void ag_parts(AgParams& p, int k) {
+  p.k = k;
+  p.quarters = p.chunks < 4 ? p.chunks : 4;
+  p.cpq = p.chunks / p.quarters;
+  const int kbq = ceil_div(ceil_div(k, kBK), p.quarters);
+  p.kb_q = kbq > 0 ? kbq : 1;
+  p.qcols = p.kb_q * kBK;
+}
+
 namespace tl {
 AgLayout ag_layout(int W, int m_per_rank, int k) {
   AgLayout L;
@@ -646,8 +705,11 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   p.skip_chunk = ctx->cfg.debug_skip_chunk;
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
-  p.boost = (W > 1 ? (W - 1 < 2 ? W - 1 : 2) : 0) * p.spr * p.chunks;  // the next two shards
   p.copy_self = 0;  // the GEMM reads the self shard in place; its slot of T is not written
+  ag_parts(p, k);
+  // The epilogue warps help with K parts 0 and 1 of every remote shard: what the first wave
+  // of tiles reads in its first half.
+  p.boost = (p.quarters < 2 ? p.quarters : 2) * (W - 1) * p.spr * p.cpq;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int movers = ctx->cfg.mover_warps;
   if (W == 1) {  // nothing to gather: the plain GEMM on shard 0 in place, no mover, no signals
@@ -856,6 +918,7 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   p.chunks = ctx->cfg.chunks_per_slab;
   p.skip_chunk = -1;
   p.copy_self = 1;
+  ag_parts(p, k);
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
   // Alone, the copy has the whole GPU: TL_AG_ALONE_CTAS_PER_SM CTAs of kAllgatherWarps warps
