@@ -422,9 +422,21 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     # the communication alone: the ReduceScatter of the W ranks' fp32 partials (m x n each)
     parts = [torch.randn((m, n), dtype=torch.float32, device=device) for _ in range(W)]
     rs_alone(out["rs_70b"], lambda: tl.tl_reduce_scatter(ctx, parts, o, stream=stream), W * m * n * 4 + m * n * 2)
+    del ws
+    # the ring reduction ([TL] §5): the same products, partials passed rank to rank
+    with tl.Context(ctx.device, rs_ring=1) as cr:
+        wsr = torch.zeros(tl.tl_gemm_rs_ring_workspace_bytes(W, m, n, kr), dtype=torch.uint8, device=device)
+        rec("rs_70b_ring", lambda: tl.tl_gemm_rs(cr, a, b, o, wsr, stream=stream), 2.0 * W * m * n * kr, 0, "tensor", 1)
+        if cr.check() != tl.TL_OK:
+            raise RuntimeError("rs_70b_ring: device status not OK")
+        del wsr
+    for key in ("gemm_alone_us", "gemm_alone_tflops"):
+        out["rs_70b_ring"][key] = out["rs_70b"][key]
+    out["rs_70b_ring"]["fused_over_gemm_alone"] = round(out["rs_70b_ring"]["us"] / out["rs_70b"]["gemm_alone_us"], 4)
+    rs_alone(out["rs_70b_ring"], lambda: tl.tl_reduce_scatter(ctx, parts, o, stream=stream), W * m * n * 4 + m * n * 2)
     del parts
     oracle_time(out["rs_70b"], "rs_70b", inp, args)
-    del a, b, o, ws
+    del a, b, o
 
     # MLP chain
     d = WORKLOADS["mlp2_8b"].dims
@@ -461,6 +473,12 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
         tl.tl_reduce_scatter(ctx, parts, o, stream=stream)
     rs_alone(out["mlp2_8b"], mlp_comm, W * 2 * T * hdim * 2 + W * T * hdim * 4 + T * hdim * 2,
              f"{W} AllGathers of X (tl_allgather, rank r each) + tl_reduce_scatter of {W} fp32 partials")
+    # the same chain with the push-mode AllGather ([TD] §3.2 Algorithm 1)
+    with tl.Context(ctx.device, ag_push=1) as cp_:
+        rec("mlp2_8b_push", lambda: tl.tl_mlp2(cp_, x, w1, w2, o, ws, stream=stream), 2.0 * W * T * hdim * f * 2, 0,
+            "tensor", 1)
+        if cp_.check() != tl.TL_OK:
+            raise RuntimeError("mlp2_8b_push: device status not OK")
     del ws_ag, parts
     oracle_time(out["mlp2_8b"], "mlp2_8b", inp, args)
     del x, w1, w2, o, ws

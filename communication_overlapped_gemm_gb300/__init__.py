@@ -57,6 +57,7 @@ class Config(ctypes.Structure):
         ("pair_ctas", _i),
         ("moe_renorm", _i),
         ("rs_ring", _i),
+        ("ag_push", _i),
     ]
 
 

@@ -8,6 +8,12 @@
 
 #include "tl_host.h"
 
+// L2 promotion of every TMA tile access (CUtensorMapL2promotion: 0 none, 1 64 B, 2 128 B,
+// 3 256 B sectors).
+#ifndef TL_L2_PROMOTION
+#define TL_L2_PROMOTION 3
+#endif
+
 namespace tl {
 
 namespace {
@@ -32,7 +38,7 @@ static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
   const uint32_t inner_bytes = box[0] * (dt == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4u : 2u);
   const CUtensorMapSwizzle sw = inner_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult r = g_encode(m, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, static_cast<CUtensorMapL2promotion>(TL_L2_PROMOTION),
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -79,6 +85,7 @@ int tl_config_default(tl_config* cfg) {
   cfg->pair_ctas = 2;
   cfg->moe_renorm = 0;
   cfg->rs_ring = 0;
+  cfg->ag_push = 0;
   return TL_OK;
 }
 
@@ -95,7 +102,7 @@ int tl_ctx_create(tl_ctx** out, int device, const tl_config* cfg) {
   if (c.mover_warps < 1 || c.mover_warps > tl::kMaxMoverWarps || !pow2_le32(c.chunks_per_slab) ||
       (c.swizzle != 0 && c.swizzle != 1) || c.grid_ctas < 0 || c.combine_ctas < 1 || c.timeout_ns == 0 ||
       c.pair_ctas < 0 || c.pair_ctas > 2 || (c.moe_renorm != 0 && c.moe_renorm != 1) ||
-      (c.rs_ring != 0 && c.rs_ring != 1))
+      (c.rs_ring != 0 && c.rs_ring != 1) || (c.ag_push != 0 && c.ag_push != 1))
     return TL_ERR_INVALID;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) {

@@ -145,6 +145,7 @@ struct AgParams {
   int cpq;        // chunks per K part (chunks = quarters * cpq)
   int qcols;      // columns per K part (a multiple of 64; the last part may be shorter or empty)
   int kb_q;       // 64-column k-blocks per K part (qcols / 64)
+  int head;       // shards at the head of the mover order, copied K part first together
 };
 
 // Copy `rows` rows of `row_bytes` bytes (a multiple of 16) from src to dst, both with a row
@@ -173,32 +174,76 @@ __device__ __forceinline__ void copy_rows(const uint8_t* __restrict__ src, uint8
         __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(i / vr) * stride) + i % vr);
 }
 
+// Position of chunk g of one gather (see ag_copy): shard i of the mover's order, K part q,
+// slab, row piece.  The first `head` shards go K part first together, the others one by one,
+// each K part first as well.
+struct ChunkPos {
+  int i, q, slab, piece;
+};
+__device__ __forceinline__ ChunkPos chunk_pos(int g, int head, int spr, int chunks, int cpq) {
+  const int per_shard = spr * chunks;
+  const int head_chunks = head * per_shard;
+  const bool in_head = g < head_chunks;
+  const int grp0 = in_head ? 0 : head + (g - head_chunks) / per_shard;  // first shard of the group
+  const int gsz = in_head ? head : 1;
+  int rem = in_head ? g : (g - head_chunks) % per_shard;
+  ChunkPos c;
+  c.q = rem / (gsz * spr * cpq);
+  rem -= c.q * gsz * spr * cpq;
+  c.i = grp0 + rem / (spr * cpq);
+  rem -= (c.i - grp0) * spr * cpq;
+  c.slab = rem / cpq;
+  c.piece = rem - c.slab * cpq;
+  return c;
+}
+
+// copy_rows to `ndst` destinations at once (the push of one source chunk to every peer):
+// each vector is loaded once and stored ndst times.
+__device__ __forceinline__ void copy_rows_multi(const uint8_t* __restrict__ src, uint8_t* const (&dst)[8], int ndst,
+                                                size_t stride, int rows, int row_bytes, int tid, int nthreads) {
+  const int vr = row_bytes / 16;
+  const int nvec = rows * vr;
+  constexpr int U = 8;
+  for (int i = tid; i < nvec; i += U * nthreads) {
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = i + u * nthreads;
+      if (v < nvec) r[u] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(v / vr) * stride) + v % vr);
+    }
+#pragma unroll 1
+    for (int d = 0; d < ndst; ++d) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = i + u * nthreads;
+        if (v < nvec) reinterpret_cast<uint4*>(dst[d] + static_cast<size_t>(v / vr) * stride)[v % vr] = r[u];
+      }
+    }
+  }
+}
+
 // The shard mover: pull the remote shards (and, with copy_self, the self rank's own, last)
 // into the gathered buffer, one release signal per chunk.  A 128-row slab is cut along K into
 // `quarters` parts of qcols columns, and each part into cpq pieces of 128/cpq rows: a chunk
-// is one piece of one part.  Chunks go K part first: part 0 of every slab of every shard (in
-// the mover's shard order), then part 1, ..., so a tile can start its first k-blocks as soon
-// as part 0 of its rows has landed, while the later parts are still being copied (each tile
-// waits for part q before its k-block q * kb_q).  Chunk g belongs to CTA g mod grid.  The
-// first `boost` chunks are shared with the epilogue warps, which are idle until their first
-// tile: in every other round of the head (g / grid odd) the mover warps copy, in the others
-// the epilogue warps (group = 1), so the head arrives up to twice as fast.
+// is one piece of one part.  Order: the first `head` shards of the mover's order (those the
+// first wave of tiles reads) go K part first, part 0 of all their slabs, then part 1, ..., so
+// those tiles start once part 0 of their rows has landed and later parts arrive ahead of
+// their k-blocks (a tile waits for part q before its k-block q * kb_q); the later shards
+// follow one after another, each K part first as well.  Chunk g belongs to CTA g mod grid.
+// The first `boost` chunks (the head) are shared with the epilogue warps, which are idle
+// until their first tile: in every other round of the head (g / grid odd) the mover warps
+// copy, in the others the epilogue warps (group = 1), so the head arrives up to twice as fast.
 template <bool Trace>
 __device__ __forceinline__ void ag_copy(const AgParams& p, int tid, int nthreads, int group, int bar) {
   const int shards = p.W - 1 + p.copy_self;
-  const int per_part = shards * p.spr * p.cpq;  // chunks of one K part, every shard
-  const int total = group == 1 ? p.boost : p.quarters * per_part;
+  const int total = group == 1 ? p.boost : shards * p.spr * p.chunks;
   const int piece_rows = kBM / p.cpq;
   const size_t row_stride = static_cast<size_t>(p.k) * 2;
   for (int g = blockIdx.x; g < total; g += gridDim.x) {
     if (g < p.boost && ((g / static_cast<int>(gridDim.x)) & 1) == (group == 1 ? 1 : 0)) continue;
-    const int q = g / per_part;
-    int rem = g - q * per_part;
-    const int i = rem / (p.spr * p.cpq);
-    rem -= i * p.spr * p.cpq;
-    const int slab = rem / p.cpq;
-    const int piece = rem - slab * p.cpq;
-    const int r = ag_mover_rank(p.W, p.rank, p.swizzle, i);
+    const ChunkPos cp = chunk_pos(g, p.head, p.spr, p.chunks, p.cpq);
+    const int q = cp.q, slab = cp.slab, piece = cp.piece;
+    const int r = ag_mover_rank(p.W, p.rank, p.swizzle, cp.i);
     const int c0 = q * p.qcols;
     const int cols = c0 >= p.k ? 0 : (p.k - c0 < p.qcols ? p.k - c0 : p.qcols);
     const size_t off = (static_cast<size_t>(slab) * kBM + static_cast<size_t>(piece) * piece_rows) * row_stride +
@@ -401,6 +446,8 @@ struct Mlp2Params {
   uint64_t* rs_flags;  // [T/128][nb2]
   long long shard_bytes, slab_bytes;
   int W, T, Tr, h, f, mps, spr, nb1, kb1, nb2, kb2, swizzle, chunks, skip_chunk;
+  int quarters, cpq, qcols, kb_q, head;  // K parts of the gather's chunks (as AgParams)
+  int push;  // 1: each shard is read once and pushed to the W-1 other ranks' copies; 0: pull
 };
 
 template <int BM, bool Pair = false>
@@ -465,14 +512,17 @@ struct Mlp2Op : OpBase<Mlp2Params> {
     return (j.x1 * p.Tr) / 128 + j.x2 * kSub + (Pair ? j.rank : 0);
   }
   static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
-    if (kb != 0) return;
     if (j.kind == 1) {
-      if (j.a_sel == 0) return;
-      const uint64_t* f = p.ag_flags +
-                          ((static_cast<size_t>(j.x0) * p.W + j.x1) * p.spr + j.x2 * kSub + (Pair ? j.rank : 0)) *
-                              p.chunks;
-      wait_slab(f, kOwn * p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x1) << 32) | j.x2);
+      // K part q of a gathered row block: its chunks in each of the kOwn slabs this CTA reads
+      if (j.a_sel == 0 || kb % p.kb_q != 0) return;
+      const int q = kb / p.kb_q;
+      const size_t slab0 = (static_cast<size_t>(j.x0) * p.W + j.x1) * p.spr + j.x2 * kSub + (Pair ? j.rank : 0);
+#pragma unroll
+      for (int sl = 0; sl < kOwn; ++sl)
+        wait_slab(p.ag_flags + (slab0 + sl) * p.chunks + q * p.cpq, p.cpq, p.common, lane,
+                  (static_cast<unsigned long long>(j.x1) << 32) | (j.x2 << 4) | q);
     } else {
+      if (kb != 0) return;
       // CTA-level chain: the layer-1 tiles that produce this row block of H_r are done.
       const int rb = row_block(p, j);
       const uint64_t* f = p.h_flags + (static_cast<size_t>(j.x0) * (p.T / 128) + rb) * p.nb1;
@@ -535,30 +585,45 @@ struct Mlp2Op : OpBase<Mlp2Params> {
       st_release_gpu(p.rs_flags + rs_tile_id(p, j), (p.common.epoch << 4) | static_cast<unsigned long long>(j.x0 + 1));
     }
   }
-  // Every emulated rank r gathers the other ranks' X shards into its own copy of X
-  // (rows r*T ..), in its swizzled order; rank 0's gather first.  A rank's own shard is read
-  // in place by its layer-1 tiles, so its slot of the copy is not written.
+  // Every emulated rank r needs the other ranks' X shards in its own copy of X (rows r*T ..);
+  // a rank's own shard is read in place by its layer-1 tiles, so its slot of the copy is not
+  // written.  Chunks are K parts x row pieces of 128-row slabs, ordered as in ag_copy.
+  //   pull ("Triton-distributed ...", §3.2 Algorithm 2): rank r, in turn (rank 0's first),
+  //     copies shards (r+1) mod W, (r+2) mod W, ... into its copy;
+  //   push (§3.2 Algorithm 1): each shard, in the order 1, 2, ..., W-1, 0, is read once and
+  //     written into the W-1 other ranks' copies, each with its own release signal.
   template <bool Trace>
   static __device__ void mover(const Params& p, int mw, int lane) {
     const int nthreads = p.common.mover_warps * 32;
     const int tid = mw * 32 + lane;
     const int per_shard = p.spr * p.chunks;
-    const int per_rank = (p.W - 1) * per_shard;
-    const int total = p.W * per_rank;
-    const size_t chunk_bytes = static_cast<size_t>(p.slab_bytes / p.chunks);
+    const int piece_rows = kBM / p.cpq;
+    const size_t row_stride = static_cast<size_t>(p.h) * 2;
+    const int total = p.W < 2 ? 0 : (p.push ? p.W * per_shard : p.W * (p.W - 1) * per_shard);
     for (int g = blockIdx.x; g < total; g += gridDim.x) {
-      const int r = g / per_rank;
-      int rem = g - r * per_rank;
-      const int i = rem / per_shard;
-      rem -= i * per_shard;
-      const int slab = rem / p.chunks;
-      const int ch = rem - slab * p.chunks;
-      const int src = ag_mover_rank(p.W, r, p.swizzle, i);
-      const size_t off = static_cast<size_t>(slab) * p.slab_bytes + static_cast<size_t>(ch) * chunk_bytes;
-      uint8_t* dst = p.xg + (static_cast<size_t>(r) * p.T + static_cast<size_t>(src) * p.Tr) * p.h * 2 + off;
-      mover_chunk(p.x[src] + off, dst, chunk_bytes,
-                  p.ag_flags + ((static_cast<size_t>(r) * p.W + src) * p.spr + slab) * p.chunks + ch,
-                  g != p.skip_chunk, p.common, tid, nthreads);
+      int r = -1, gg = g;  // r: the one gathering rank (pull); all others (push)
+      if (!p.push) {
+        r = g / ((p.W - 1) * per_shard);
+        gg = g - r * (p.W - 1) * per_shard;
+      }
+      const ChunkPos cp = chunk_pos(gg, p.head, p.spr, p.chunks, p.cpq);
+      const int src = ag_mover_rank(p.W, p.push ? 0 : r, p.swizzle, cp.i);
+      const int c0 = cp.q * p.qcols;
+      const int cols = c0 >= p.h ? 0 : (p.h - c0 < p.qcols ? p.h - c0 : p.qcols);
+      const size_t off = (static_cast<size_t>(cp.slab) * kBM + static_cast<size_t>(cp.piece) * piece_rows) *
+                             row_stride + static_cast<size_t>(c0) * 2;
+      uint8_t* dst[8];
+      int nd = 0;
+      for (int d = 0; d < p.W; ++d)
+        if (d != src && (p.push || d == r))
+          dst[nd++] = p.xg + (static_cast<size_t>(d) * p.T + static_cast<size_t>(src) * p.Tr) * p.h * 2 + off;
+      copy_rows_multi(p.x[src] + off, dst, nd, row_stride, piece_rows, cols * 2, tid, nthreads);
+      __threadfence();
+      named_bar_sync(2, nthreads);
+      if (tid < p.W && tid != src && (p.push || tid == r) && g != p.skip_chunk)
+        st_release_gpu(p.ag_flags + ((static_cast<size_t>(tid) * p.W + src) * p.spr + cp.slab) * p.chunks +
+                           cp.q * p.cpq + cp.piece,
+                       p.common.epoch);
     }
   }
 };
@@ -627,15 +692,30 @@ static bool ag_shape_ok(int W, int mpr, int n, int k) {
 // Tile rows used for a row extent: 256 when every block of the extent is a 256 multiple.
 static int pick_bm(int rows) { return rows % 256 == 0 ? 256 : 128; }
 
-// The mover's K parts of a slab (see ag_copy): up to four parts of whole 64-column k-blocks,
+// The mover's K parts of a slab (see ag_copy): 1, 2 or 4 parts of whole 64-column k-blocks,
+// at least 16 k-blocks each (a short K is one part: a wait per part costs a signal round trip),
 // cpq = chunks / parts row pieces each.
+struct KParts {
+  int quarters, cpq, kb_q, qcols;
+};
+static KParts k_parts(int chunks, int k) {
+  KParts r;
+  const int kblocks = ceil_div(k, kBK);
+  r.quarters = 1;
+  while (r.quarters < 4 && r.quarters * 2 <= chunks && kblocks >= 16 * r.quarters * 2) r.quarters *= 2;
+  r.cpq = chunks / r.quarters;
+  const int kbq = ceil_div(kblocks, r.quarters);
+  r.kb_q = kbq > 0 ? kbq : 1;
+  r.qcols = r.kb_q * kBK;
+  return r;
+}
 static void ag_parts(AgParams& p, int k) {
+  const KParts kp = k_parts(p.chunks, k);
   p.k = k;
-  p.quarters = p.chunks < 4 ? p.chunks : 4;
-  p.cpq = p.chunks / p.quarters;
-  const int kbq = ceil_div(ceil_div(k, kBK), p.quarters);
-  p.kb_q = kbq > 0 ? kbq : 1;
-  p.qcols = p.kb_q * kBK;
+  p.quarters = kp.quarters;
+  p.cpq = kp.cpq;
+  p.kb_q = kp.kb_q;
+  p.qcols = kp.qcols;
 }
 
 namespace tl {
@@ -707,9 +787,10 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
   p.copy_self = 0;  // the GEMM reads the self shard in place; its slot of T is not written
   ag_parts(p, k);
-  // The epilogue warps help with K parts 0 and 1 of every remote shard: what the first wave
-  // of tiles reads in its first half.
-  p.boost = (p.quarters < 2 ? p.quarters : 2) * (W - 1) * p.spr * p.cpq;
+  // The head: the next two shards, which the first wave of tiles reads; the epilogue warps
+  // help copy it.
+  p.head = W - 1 < 2 ? W - 1 : 2;
+  p.boost = p.head * p.spr * p.chunks;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int movers = ctx->cfg.mover_warps;
   if (W == 1) {  // nothing to gather: the plain GEMM on shard 0 in place, no mover, no signals
@@ -882,6 +963,13 @@ extern "C" int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const vo
   p.skip_chunk = ctx->cfg.debug_skip_chunk;
   p.shard_bytes = static_cast<long long>(Tr) * hidden * 2;
   p.slab_bytes = static_cast<long long>(kBM) * hidden * 2;
+  p.push = ctx->cfg.ag_push;
+  const KParts kp = k_parts(p.chunks, hidden);
+  p.quarters = kp.quarters;
+  p.cpq = kp.cpq;
+  p.kb_q = kp.kb_q;
+  p.qcols = kp.qcols;
+  p.head = p.push ? (W < 2 ? W : 2) : (W - 1 < 2 ? W - 1 : 2);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (pair) return launch_persistent_pair<Mlp2Op<256, true>>(ctx, p, st, ctx->cfg.mover_warps);
   return bm == 256 ? launch_persistent<Mlp2Op<256>>(ctx, p, st, ctx->cfg.mover_warps)
@@ -919,6 +1007,7 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   p.skip_chunk = -1;
   p.copy_self = 1;
   ag_parts(p, k);
+  p.head = W < 2 ? W : 2;
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
   // Alone, the copy has the whole GPU: TL_AG_ALONE_CTAS_PER_SM CTAs of kAllgatherWarps warps

@@ -91,6 +91,11 @@ typedef struct tl_config {
   int rs_ring;                /* tl_gemm_rs reduction: 0 (default) the owner-slot chain; 1 a ring
                                  ([TL] §5, Figure 4 text), workspace from
                                  tl_gemm_rs_ring_workspace_bytes                                    */
+  int ag_push;                /* tl_mlp2's AllGather, where every rank gathers: 0 (default) pull
+                                 ([TD] §3.2 Algorithm 2, each rank reads every other shard); 1 push
+                                 (Algorithm 1, each shard read once and written to the other ranks'
+                                 copies).  tl_ag_gemm and tl_allgather gather into one rank, where
+                                 both modes move the same bytes: they always pull              */
 } tl_config;
 
 typedef struct tl_ctx tl_ctx;
@@ -251,9 +256,10 @@ int tl_reduce_scatter(tl_ctx* ctx, int W, const float* const* partials, void* co
  * r's own shard is read in place, its slot of r's copy is not written) at offset 0, then, each at the next 256-byte boundary, the intermediate H (W x tokens x f_r bf16,
  * H_r at rows r*tokens.., readable after the call), the fp32 reduction slot (tokens x hidden)
  * and the signals.
- * One persistent launch runs, per emulated rank r: the mover (gather X into rank r's copy),
- * layer-1 tiles (wait on the slab signals, GELU epilogue, notify per H tile) and layer-2 tiles
- * (wait on the H tiles covering their K range, then the GEMM+RS chain above).
+ * One persistent launch runs, per emulated rank r: the mover (gather X into rank r's copy, by
+ * pull or, with cfg.ag_push, push), layer-1 tiles (wait for each K quarter of their gathered
+ * rows, GELU epilogue, notify per H tile) and layer-2 tiles (wait on the H tiles covering their
+ * K range, then the owner-slot GEMM+RS chain; cfg.rs_ring does not apply here).
  * Shapes: 1 <= W <= 8; tokens % (128*W) == 0; hidden % 8 == 0; f_r % 8 == 0.
  */
 size_t tl_mlp2_workspace_bytes(int W, int tokens, int hidden, int f_r);

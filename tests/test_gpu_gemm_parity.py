@@ -242,6 +242,42 @@ def test_mlp2_matches_oracle(ctx, W, T, h, f):
         assert_close(bf16_to_f64(out[o]), ref[o], f"mlp2 W={W} owner {o}")
 
 
+@pytest.mark.parametrize("W,T,h,f", [(2, 512, 264, 328), (4, 1024, 512, 384), (8, 1024, 136, 256)])
+def test_mlp2_push_gather_matches_oracle_and_pull(W, T, h, f):
+    """Push-mode AllGather inside the MLP chain (cfg.ag_push = 1: every shard read once and
+    written into the other ranks' copies): the gathered copies equal pull's bit for bit (every
+    rank's copy holds the other ranks' shards, its own slot untouched), and the output is
+    bit-identical to pull's and within tolerance of the oracle."""
+    import torch
+    inp = make_inputs("mlp2", 61 + W, W=W, tokens=T, hidden=h, f_r=f)
+    res = {}
+    for push in (0, 1):
+        with tl.Context(0, ag_push=push) as c2:
+            x = [to_dev_bf16(v) for v in inp["x_shards"]]
+            w1 = [to_dev_bf16(v) for v in inp["w1"]]
+            w2 = [to_dev_bf16(v) for v in inp["w2"]]
+            out = [torch.empty((T // W, h), dtype=torch.bfloat16, device="cuda") for _ in range(W)]
+            ws = workspace(tl.tl_mlp2_workspace_bytes(W, T, h, f))
+            tl.tl_mlp2(c2, x, w1, w2, out, ws)
+            torch.cuda.synchronize()
+            assert c2.check() == tl.TL_OK
+            xg = bf16_bits(ws[: W * T * h * 2].view(torch.bfloat16).view(W, T, h))
+            res[push] = (xg, [bf16_bits(o) for o in out])
+    gath = oracle.ag_gather_bits(inp["x_shards"])
+    tr = T // W
+    for r in range(W):
+        for src in range(W):
+            rows = slice(src * tr, (src + 1) * tr)
+            for push in (0, 1):
+                got = res[push][0][r][rows]
+                assert (not got.any()) if src == r else np.array_equal(got, gath[rows])
+    assert all(np.array_equal(a, b) for a, b in zip(res[0][1], res[1][1]))
+    ref = oracle.mlp2(inp["x_shards"], inp["w1"], inp["w2"])
+    for o in range(W):
+        assert_close((res[1][1][o].astype(np.uint32) << 16).view(np.float32).astype(np.float64), ref[o],
+                     f"mlp2 push W={W} owner {o}")
+
+
 def test_mlp2_full_size_whole_rows(ctx):
     """Full-size MLP chain (W=4, 4096 tokens, hidden 4096, ffn 4 x 3584): whole rows of every
     owner, each through all four ranks' layer-1 tiles, GELU and layer-2 chains."""
@@ -272,7 +308,8 @@ def test_mlp2_layer1_h_bit_identical_across_orders_engines_and_grids():
     inp = make_inputs("mlp2", 74, W=W, tokens=T, hidden=h, f_r=f)
     hs, outs = [], []
     for cfg in [dict(), dict(swizzle=0), dict(pair_ctas=0), dict(pair_ctas=0, grid_ctas=37),
-                dict(grid_ctas=38), dict(chunks_per_slab=4, mover_warps=1)]:
+                dict(grid_ctas=38), dict(chunks_per_slab=4, mover_warps=1), dict(ag_push=1),
+                dict(ag_push=1, chunks_per_slab=2, pair_ctas=0)]:
         with tl.Context(0, **cfg) as c2:
             x = [to_dev_bf16(v) for v in inp["x_shards"]]
             w1 = [to_dev_bf16(v) for v in inp["w1"]]
