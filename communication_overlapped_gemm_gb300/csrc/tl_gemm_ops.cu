@@ -174,6 +174,10 @@ __device__ __forceinline__ void copy_rows(const uint8_t* __restrict__ src, uint8
         __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(i / vr) * stride) + i % vr);
 }
 
+#ifndef TL_MLP2_COPY_EACH
+#define TL_MLP2_COPY_EACH 0
+#endif
+
 // Position of chunk g of one gather (see ag_copy): shard i of the mover's order, K part q,
 // slab, row piece.  The first `head` shards go K part first together, the others one by one,
 // each K part first as well.
@@ -230,38 +234,47 @@ __device__ __forceinline__ void copy_rows_multi(const uint8_t* __restrict__ src,
 // those tiles start once part 0 of their rows has landed and later parts arrive ahead of
 // their k-blocks (a tile waits for part q before its k-block q * kb_q); the later shards
 // follow one after another, each K part first as well.  Chunk g belongs to CTA g mod grid.
-// The first `boost` chunks (the head) are shared with the epilogue warps, which are idle
-// until their first tile: in every other round of the head (g / grid odd) the mover warps
-// copy, in the others the epilogue warps (group = 1), so the head arrives up to twice as fast.
+// With `boost`, the epilogue warps, idle until their first tile, join the mover warps on the
+// head: the two groups copy each head chunk together (named barrier 4 over both), so part 0
+// lands first and in the least time; the mover warps then copy the rest alone.
 template <bool Trace>
-__device__ __forceinline__ void ag_copy(const AgParams& p, int tid, int nthreads, int group, int bar) {
-  const int shards = p.W - 1 + p.copy_self;
-  const int total = group == 1 ? p.boost : shards * p.spr * p.chunks;
+__device__ __forceinline__ void ag_chunk(const AgParams& p, int g, int tid, int nthreads, int bar) {
+  const ChunkPos cp = chunk_pos(g, p.head, p.spr, p.chunks, p.cpq);
+  const int r = ag_mover_rank(p.W, p.rank, p.swizzle, cp.i);
+  const int c0 = cp.q * p.qcols;
+  const int cols = c0 >= p.k ? 0 : (p.k - c0 < p.qcols ? p.k - c0 : p.qcols);
   const int piece_rows = kBM / p.cpq;
   const size_t row_stride = static_cast<size_t>(p.k) * 2;
-  for (int g = blockIdx.x; g < total; g += gridDim.x) {
-    if (g < p.boost && ((g / static_cast<int>(gridDim.x)) & 1) == (group == 1 ? 1 : 0)) continue;
-    const ChunkPos cp = chunk_pos(g, p.head, p.spr, p.chunks, p.cpq);
-    const int q = cp.q, slab = cp.slab, piece = cp.piece;
-    const int r = ag_mover_rank(p.W, p.rank, p.swizzle, cp.i);
-    const int c0 = q * p.qcols;
-    const int cols = c0 >= p.k ? 0 : (p.k - c0 < p.qcols ? p.k - c0 : p.qcols);
-    const size_t off = (static_cast<size_t>(slab) * kBM + static_cast<size_t>(piece) * piece_rows) * row_stride +
-                       static_cast<size_t>(c0) * 2;
-    const uint64_t t0 = Trace ? globaltimer() : 0;
-    copy_rows(p.shard[r] + off, p.gath + static_cast<size_t>(r) * p.shard_bytes + off, row_stride, piece_rows,
-              cols * 2, tid, nthreads);
-    __threadfence();
-    named_bar_sync(bar, nthreads);
-    if (tid == 0 && g != p.skip_chunk)
-      st_release_gpu(p.flags + (static_cast<size_t>(r) * p.spr + slab) * p.chunks + q * p.cpq + piece, p.common.epoch);
-    if (Trace && tid == 0) trace_span(p.common, kTrMoverChunk, g, t0, globaltimer());
+  const size_t off = (static_cast<size_t>(cp.slab) * kBM + static_cast<size_t>(cp.piece) * piece_rows) * row_stride +
+                     static_cast<size_t>(c0) * 2;
+  const uint64_t t0 = Trace ? globaltimer() : 0;
+  copy_rows(p.shard[r] + off, p.gath + static_cast<size_t>(r) * p.shard_bytes + off, row_stride, piece_rows, cols * 2,
+            tid, nthreads);
+  __threadfence();
+  named_bar_sync(bar, nthreads);
+  if (tid == 0 && g != p.skip_chunk)
+    st_release_gpu(p.flags + (static_cast<size_t>(r) * p.spr + cp.slab) * p.chunks + cp.q * p.cpq + cp.piece,
+                   p.common.epoch);
+  if (Trace && tid == 0) trace_span(p.common, kTrMoverChunk, g, t0, globaltimer());
+}
+
+// group 0: the mover warps (tid < movers * 32); group 1: the epilogue warps (boost only).
+template <bool Trace>
+__device__ __forceinline__ void ag_copy(const AgParams& p, int tid, int nthreads, int group, int epi_threads) {
+  const int total = (p.W - 1 + p.copy_self) * p.spr * p.chunks;
+  int g = blockIdx.x;
+  if (p.boost > 0) {
+    const int both = nthreads + epi_threads;  // mover + epilogue threads of this CTA
+    const int t = group == 0 ? tid : nthreads + tid;
+    for (; g < p.boost; g += gridDim.x) ag_chunk<Trace>(p, g, t, both, 4);
+    if (group == 1) return;
   }
+  for (; g < total; g += gridDim.x) ag_chunk<Trace>(p, g, tid, nthreads, 2);
 }
 
 template <bool Trace>
-__device__ __forceinline__ void ag_mover(const AgParams& p, int mw, int lane) {
-  ag_copy<Trace>(p, mw * 32 + lane, p.common.mover_warps * 32, 0, 2);
+__device__ __forceinline__ void ag_mover(const AgParams& p, int mw, int lane, int epi_threads) {
+  ag_copy<Trace>(p, mw * 32 + lane, p.common.mover_warps * 32, 0, epi_threads);
 }
 
 // Pair = true: 256-row tiles on a CTA pair (tl_engine2.cuh); this CTA owns rows and B
@@ -337,11 +350,11 @@ struct AgOp : OpBase<AgParams> {
   }
   template <bool Trace>
   static __device__ void mover(const Params& p, int mw, int lane) {
-    ag_mover<Trace>(p, mw, lane);
+    ag_mover<Trace>(p, mw, lane, kEpiWarps * 32);
   }
   template <bool Trace>
   static __device__ void epilogue_prologue(const Params& p, int ew, int lane) {
-    if (p.boost > 0) ag_copy<Trace>(p, ew * 32 + lane, kEpiWarps * 32, 1, 3);
+    if (p.boost > 0) ag_copy<Trace>(p, ew * 32 + lane, p.common.mover_warps * 32, 1, kEpiWarps * 32);
   }
 };
 
@@ -617,7 +630,11 @@ struct Mlp2Op : OpBase<Mlp2Params> {
       for (int d = 0; d < p.W; ++d)
         if (d != src && (p.push || d == r))
           dst[nd++] = p.xg + (static_cast<size_t>(d) * p.T + static_cast<size_t>(src) * p.Tr) * p.h * 2 + off;
+#if TL_MLP2_COPY_EACH
+      for (int d = 0; d < nd; ++d) copy_rows(p.x[src] + off, dst[d], row_stride, piece_rows, cols * 2, tid, nthreads);
+#else
       copy_rows_multi(p.x[src] + off, dst, nd, row_stride, piece_rows, cols * 2, tid, nthreads);
+#endif
       __threadfence();
       named_bar_sync(2, nthreads);
       if (tid < p.W && tid != src && (p.push || tid == r) && g != p.skip_chunk)
@@ -638,7 +655,7 @@ constexpr int kAllgatherWarps = 16;  // copy warps per CTA of the standalone All
 #define TL_AG_ALONE_CTAS_PER_SM 4
 #endif
 __global__ void __launch_bounds__(kAllgatherWarps * 32) allgather_kernel(const __grid_constant__ AgParams p) {
-  ag_mover<false>(p, threadIdx.x >> 5, threadIdx.x & 31);
+  ag_mover<false>(p, threadIdx.x >> 5, threadIdx.x & 31, 0);  // boost is 0 here
 }
 
 // ============================================================================ ReduceScatter alone
