@@ -174,10 +174,6 @@ __device__ __forceinline__ void copy_rows(const uint8_t* __restrict__ src, uint8
         __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(i / vr) * stride) + i % vr);
 }
 
-#ifndef TL_MLP2_COPY_EACH
-#define TL_MLP2_COPY_EACH 0
-#endif
-
 // Position of chunk g of one gather (see ag_copy): shard i of the mover's order, K part q,
 // slab, row piece.  The first `head` shards go K part first together, the others one by one,
 // each K part first as well.
@@ -243,9 +239,9 @@ __device__ __forceinline__ void ag_chunk(const AgParams& p, int g, int tid, int 
   const int r = ag_mover_rank(p.W, p.rank, p.swizzle, cp.i);
   const int c0 = cp.q * p.qcols;
   const int cols = c0 >= p.k ? 0 : (p.k - c0 < p.qcols ? p.k - c0 : p.qcols);
-  const int piece_rows = kBM / p.cpq;
+  const int piece_rows = tl::kBM / p.cpq;
   const size_t row_stride = static_cast<size_t>(p.k) * 2;
-  const size_t off = (static_cast<size_t>(cp.slab) * kBM + static_cast<size_t>(cp.piece) * piece_rows) * row_stride +
+  const size_t off = (static_cast<size_t>(cp.slab) * tl::kBM + static_cast<size_t>(cp.piece) * piece_rows) * row_stride +
                      static_cast<size_t>(c0) * 2;
   const uint64_t t0 = Trace ? globaltimer() : 0;
   copy_rows(p.shard[r] + off, p.gath + static_cast<size_t>(r) * p.shard_bytes + off, row_stride, piece_rows, cols * 2,
@@ -610,7 +606,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
     const int nthreads = p.common.mover_warps * 32;
     const int tid = mw * 32 + lane;
     const int per_shard = p.spr * p.chunks;
-    const int piece_rows = kBM / p.cpq;
+    const int piece_rows = tl::kBM / p.cpq;  // slabs are 128 rows (not this op's tile rows)
     const size_t row_stride = static_cast<size_t>(p.h) * 2;
     const int total = p.W < 2 ? 0 : (p.push ? p.W * per_shard : p.W * (p.W - 1) * per_shard);
     for (int g = blockIdx.x; g < total; g += gridDim.x) {
@@ -623,18 +619,14 @@ struct Mlp2Op : OpBase<Mlp2Params> {
       const int src = ag_mover_rank(p.W, p.push ? 0 : r, p.swizzle, cp.i);
       const int c0 = cp.q * p.qcols;
       const int cols = c0 >= p.h ? 0 : (p.h - c0 < p.qcols ? p.h - c0 : p.qcols);
-      const size_t off = (static_cast<size_t>(cp.slab) * kBM + static_cast<size_t>(cp.piece) * piece_rows) *
+      const size_t off = (static_cast<size_t>(cp.slab) * tl::kBM + static_cast<size_t>(cp.piece) * piece_rows) *
                              row_stride + static_cast<size_t>(c0) * 2;
       uint8_t* dst[8];
       int nd = 0;
       for (int d = 0; d < p.W; ++d)
         if (d != src && (p.push || d == r))
           dst[nd++] = p.xg + (static_cast<size_t>(d) * p.T + static_cast<size_t>(src) * p.Tr) * p.h * 2 + off;
-#if TL_MLP2_COPY_EACH
-      for (int d = 0; d < nd; ++d) copy_rows(p.x[src] + off, dst[d], row_stride, piece_rows, cols * 2, tid, nthreads);
-#else
       copy_rows_multi(p.x[src] + off, dst, nd, row_stride, piece_rows, cols * 2, tid, nthreads);
-#endif
       __threadfence();
       named_bar_sync(2, nthreads);
       if (tid < p.W && tid != src && (p.push || tid == r) && g != p.skip_chunk)
