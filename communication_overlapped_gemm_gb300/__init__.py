@@ -58,6 +58,7 @@ class Config(ctypes.Structure):
         ("moe_renorm", _i),
         ("rs_ring", _i),
         ("ag_push", _i),
+        ("mover_kparts", _i),
     ]
 
 

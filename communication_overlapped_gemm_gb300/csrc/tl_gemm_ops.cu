@@ -701,25 +701,25 @@ static bool ag_shape_ok(int W, int mpr, int n, int k) {
 // Tile rows used for a row extent: 256 when every block of the extent is a 256 multiple.
 static int pick_bm(int rows) { return rows % 256 == 0 ? 256 : 128; }
 
-// The mover's K parts of a slab (see ag_copy): 1, 2 or 4 parts of whole 64-column k-blocks,
-// at least 16 k-blocks each (a short K is one part: a wait per part costs a signal round trip),
-// cpq = chunks / parts row pieces each.
+// The mover's K parts of a slab (see ag_copy): up to `want` (cfg.mover_kparts: 1, 2 or 4)
+// parts of whole 64-column k-blocks, at least 16 k-blocks each (a wait per part costs a
+// signal round trip), cpq = chunks / parts row pieces each.
 struct KParts {
   int quarters, cpq, kb_q, qcols;
 };
-static KParts k_parts(int chunks, int k) {
+static KParts k_parts(int chunks, int k, int want) {
   KParts r;
   const int kblocks = ceil_div(k, kBK);
   r.quarters = 1;
-  while (r.quarters < 4 && r.quarters * 2 <= chunks && kblocks >= 16 * r.quarters * 2) r.quarters *= 2;
+  while (r.quarters < want && r.quarters * 2 <= chunks && kblocks >= 16 * r.quarters * 2) r.quarters *= 2;
   r.cpq = chunks / r.quarters;
   const int kbq = ceil_div(kblocks, r.quarters);
   r.kb_q = kbq > 0 ? kbq : 1;
   r.qcols = r.kb_q * kBK;
   return r;
 }
-static void ag_parts(AgParams& p, int k) {
-  const KParts kp = k_parts(p.chunks, k);
+static void ag_parts(AgParams& p, int k, int want) {
+  const KParts kp = k_parts(p.chunks, k, want);
   p.k = k;
   p.quarters = kp.quarters;
   p.cpq = kp.cpq;
@@ -795,7 +795,7 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
   p.copy_self = 0;  // the GEMM reads the self shard in place; its slot of T is not written
-  ag_parts(p, k);
+  ag_parts(p, k, ctx->cfg.mover_kparts);
   // The head: the next two shards, which the first wave of tiles reads; the epilogue warps
   // help copy it.
   p.head = W - 1 < 2 ? W - 1 : 2;
@@ -973,7 +973,7 @@ extern "C" int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const vo
   p.shard_bytes = static_cast<long long>(Tr) * hidden * 2;
   p.slab_bytes = static_cast<long long>(kBM) * hidden * 2;
   p.push = ctx->cfg.ag_push;
-  const KParts kp = k_parts(p.chunks, hidden);
+  const KParts kp = k_parts(p.chunks, hidden, ctx->cfg.mover_kparts);
   p.quarters = kp.quarters;
   p.cpq = kp.cpq;
   p.kb_q = kp.kb_q;
@@ -1015,7 +1015,7 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   p.chunks = ctx->cfg.chunks_per_slab;
   p.skip_chunk = -1;
   p.copy_self = 1;
-  ag_parts(p, k);
+  ag_parts(p, k, ctx->cfg.mover_kparts);
   p.head = W < 2 ? W : 2;
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;

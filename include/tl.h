@@ -96,6 +96,11 @@ typedef struct tl_config {
                                  (Algorithm 1, each shard read once and written to the other ranks'
                                  copies).  tl_ag_gemm and tl_allgather gather into one rank, where
                                  both modes move the same bytes: they always pull              */
+  int mover_kparts;           /* the mover's chunks along K ([TL] §3.1, the communication tile): 1
+                                 (default) each chunk is whole rows of a 128-row slab; 2 or 4 each
+                                 slab is also cut into that many K parts (of at least 16 64-column
+                                 k-blocks), copied part by part, and a tile waits for each part
+                                 before its first k-block in it                                 */
 } tl_config;
 
 typedef struct tl_ctx tl_ctx;
@@ -283,6 +288,10 @@ int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const void* const* 
  *   y_(t,j) = (SiLU(x_t . Wg_e) * (x_t . Wu_e)) . Wd_e   (h kept in bf16, y in bf16)
  *   out_t   = sum_j gate_(t,j) * y_(t,j)                  (fp32)
  * workspace: tl_moe_workspace_bytes().
+ * One persistent cooperative launch: every CTA first routes its share of the tokens, then
+ * (after a grid-wide barrier) one CTA per expert builds the permutation and tile tables while
+ * the others zero `out`, and after a second barrier the GEMM partition runs the gather and the
+ * grouped GEMMs while the combine partition adds finished y tiles into `out`.
  * Shapes: T >= 1; 1 <= topk <= 8; topk <= E <= 256; H % 256 == 0; F % 128 == 0.
  */
 size_t tl_moe_workspace_bytes(int T, int H, int E, int F, int topk);

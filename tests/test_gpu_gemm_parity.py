@@ -94,6 +94,34 @@ def test_ag_gemm_invariant_to_order_and_geometry():
                  oracle.ag_gemm(inp["a_shards"], inp["b"]), "ag invariance")
 
 
+def test_mover_k_parts_are_bit_identical():
+    """cfg.mover_kparts: the mover cuts each slab into 2 or 4 K parts and a tile waits for each
+    part before its k-blocks in it.  With K long enough for every split (4096: 64 k-blocks),
+    the AllGather+GEMM and the MLP chain give the same bits with 1, 2 and 4 parts, and the
+    gathered operand is exact."""
+    import torch
+    inp = make_inputs("ag_gemm", 23, W=3, m_per_rank=256, n=264, k=4096)
+    outs = []
+    for kp, extra in [(1, {}), (2, {}), (4, {}), (4, dict(chunks_per_slab=4)), (4, dict(pair_ctas=1))]:
+        with tl.Context(0, mover_kparts=kp, **extra) as c2:
+            c, ws = run_ag(c2, inp, rank=1)
+            outs.append(bf16_bits(c))
+            check_gathered(ws, inp, 1)
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    assert_close(bf16_to_f64(torch.from_numpy(outs[0].view(np.int16)).view(torch.bfloat16)),
+                 oracle.ag_gemm(inp["a_shards"], inp["b"]), "ag with K parts")
+    mi = make_inputs("mlp2", 24, W=2, tokens=512, hidden=4096, f_r=264)
+    mouts = []
+    for kp, extra in [(1, {}), (4, {}), (2, dict(ag_push=1)), (4, dict(pair_ctas=0))]:
+        with tl.Context(0, mover_kparts=kp, **extra) as c2:
+            mouts.append(np.concatenate([bf16_bits(o) for o in run_mlp2(c2, mi)]))
+    for o in mouts[1:]:
+        assert np.array_equal(o, mouts[0])
+    ref = np.concatenate(oracle.mlp2(mi["x_shards"], mi["w1"], mi["w2"]))
+    assert_close((mouts[0].astype(np.uint32) << 16).view(np.float32).astype(np.float64), ref, "mlp2 with K parts")
+
+
 def test_ag_gemm_llama70b_sampled(ctx):
     """Full-size AllGather+GEMM (W=8, 8192x3584x8192) checked on sampled entries."""
     inp = workload_inputs("ag_70b")
