@@ -148,30 +148,68 @@ struct AgParams {
   int head;       // shards at the head of the mover order, copied K part first together
 };
 
-// Copy `rows` rows of `row_bytes` bytes (a multiple of 16) from src to dst, both with a row
-// stride of `stride` bytes, by `nthreads` threads: 16-byte vectors, 8 loads in flight.
-__device__ __forceinline__ void copy_rows(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, size_t stride,
-                                          int rows, int row_bytes, int tid, int nthreads) {
-  const int vr = row_bytes / 16;
-  const int nvec = rows * vr;
-  constexpr int U = 8;
-  int i = tid;
-  for (; i + (U - 1) * nthreads < nvec; i += U * nthreads) {
-    uint4 r[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int v = i + u * nthreads;
-      r[u] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(v / vr) * stride) + v % vr);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int v = i + u * nthreads;
-      reinterpret_cast<uint4*>(dst + static_cast<size_t>(v / vr) * stride)[v % vr] = r[u];
+// Offsets (bytes) of the 16-byte vectors v = tid + u * nthreads, u = 0..7, of a block of rows
+// with `vr` vectors per row and a row stride of `stride` bytes, stepped from (row, col)
+// without a division per vector (the movers share the SM's issue slots with the GEMM roles).
+struct RowWalk {
+  int row, col, drow, dcol, vr;
+  size_t stride;
+  __device__ __forceinline__ RowWalk(int v0, int nthreads, int vr_, size_t stride_) : vr(vr_), stride(stride_) {
+    row = v0 / vr;
+    col = v0 - row * vr;
+    drow = nthreads / vr;
+    dcol = nthreads - drow * vr;
+  }
+  __device__ __forceinline__ size_t offset() const { return static_cast<size_t>(row) * stride + col * 16; }
+  __device__ __forceinline__ void step() {
+    row += drow;
+    col += dcol;
+    if (col >= vr) {
+      col -= vr;
+      ++row;
     }
   }
-  for (; i < nvec; i += nthreads)
-    reinterpret_cast<uint4*>(dst + static_cast<size_t>(i / vr) * stride)[i % vr] =
-        __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(i / vr) * stride) + i % vr);
+};
+
+// Copy `rows` rows of `row_bytes` bytes (a multiple of 16) from src to each of the `ndst`
+// destinations, all with a row stride of `stride` bytes, by `nthreads` threads: 16-byte
+// vectors, 8 loads in flight, each vector loaded once and stored ndst times (the push of one
+// source chunk to every peer).  Whole rows (row_bytes == stride) are one contiguous block.
+__device__ __forceinline__ void copy_rows_multi(const uint8_t* __restrict__ src, uint8_t* const (&dst)[8], int ndst,
+                                                size_t stride, int rows, int row_bytes, int tid, int nthreads) {
+  int vr = row_bytes / 16;
+  int nr = rows;
+  if (static_cast<size_t>(row_bytes) == stride) {  // contiguous: one row of rows * vr vectors
+    vr *= rows;
+    nr = 1;
+  }
+  const int nvec = nr * vr;
+  if (nvec == 0) return;
+  constexpr int U = 8;
+  RowWalk w(tid, nthreads, vr, stride);
+  for (int i = tid; i < nvec; i += U * nthreads) {
+    uint4 r[U];
+    size_t off[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      off[u] = w.offset();
+      w.step();
+      if (i + u * nthreads < nvec) r[u] = __ldg(reinterpret_cast<const uint4*>(src + off[u]));
+    }
+#pragma unroll 1
+    for (int d = 0; d < ndst; ++d) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (i + u * nthreads < nvec) *reinterpret_cast<uint4*>(dst[d] + off[u]) = r[u];
+    }
+  }
+}
+
+// One destination.
+__device__ __forceinline__ void copy_rows(const uint8_t* __restrict__ src, uint8_t* dst, size_t stride, int rows,
+                                          int row_bytes, int tid, int nthreads) {
+  uint8_t* const d[8] = {dst, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  copy_rows_multi(src, d, 1, stride, rows, row_bytes, tid, nthreads);
 }
 
 // Position of chunk g of one gather (see ag_copy): shard i of the mover's order, K part q,
@@ -195,31 +233,6 @@ __device__ __forceinline__ ChunkPos chunk_pos(int g, int head, int spr, int chun
   c.slab = rem / cpq;
   c.piece = rem - c.slab * cpq;
   return c;
-}
-
-// copy_rows to `ndst` destinations at once (the push of one source chunk to every peer):
-// each vector is loaded once and stored ndst times.
-__device__ __forceinline__ void copy_rows_multi(const uint8_t* __restrict__ src, uint8_t* const (&dst)[8], int ndst,
-                                                size_t stride, int rows, int row_bytes, int tid, int nthreads) {
-  const int vr = row_bytes / 16;
-  const int nvec = rows * vr;
-  constexpr int U = 8;
-  for (int i = tid; i < nvec; i += U * nthreads) {
-    uint4 r[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int v = i + u * nthreads;
-      if (v < nvec) r[u] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(v / vr) * stride) + v % vr);
-    }
-#pragma unroll 1
-    for (int d = 0; d < ndst; ++d) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = i + u * nthreads;
-        if (v < nvec) reinterpret_cast<uint4*>(dst[d] + static_cast<size_t>(v / vr) * stride)[v % vr] = r[u];
-      }
-    }
-  }
 }
 
 // The shard mover: pull the remote shards (and, with copy_self, the self rank's own, last)
@@ -709,6 +722,7 @@ struct KParts {
 };
 static KParts k_parts(int chunks, int k, int want) {
   KParts r;
+  if (want <= 0) want = 1;
   const int kblocks = ceil_div(k, kBK);
   r.quarters = 1;
   while (r.quarters < want && r.quarters * 2 <= chunks && kblocks >= 16 * r.quarters * 2) r.quarters *= 2;
@@ -795,7 +809,7 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
   p.copy_self = 0;  // the GEMM reads the self shard in place; its slot of T is not written
-  ag_parts(p, k, ctx->cfg.mover_kparts);
+  ag_parts(p, k, ctx->cfg.mover_kparts > 0 ? ctx->cfg.mover_kparts : 4);
   // The head: the next two shards, which the first wave of tiles reads; the epilogue warps
   // help copy it.
   p.head = W - 1 < 2 ? W - 1 : 2;
@@ -973,7 +987,7 @@ extern "C" int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const vo
   p.shard_bytes = static_cast<long long>(Tr) * hidden * 2;
   p.slab_bytes = static_cast<long long>(kBM) * hidden * 2;
   p.push = ctx->cfg.ag_push;
-  const KParts kp = k_parts(p.chunks, hidden, ctx->cfg.mover_kparts);
+  const KParts kp = k_parts(p.chunks, hidden, ctx->cfg.mover_kparts > 0 ? ctx->cfg.mover_kparts : 1);
   p.quarters = kp.quarters;
   p.cpq = kp.cpq;
   p.kb_q = kp.kb_q;
@@ -1015,7 +1029,7 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   p.chunks = ctx->cfg.chunks_per_slab;
   p.skip_chunk = -1;
   p.copy_self = 1;
-  ag_parts(p, k, ctx->cfg.mover_kparts);
+  ag_parts(p, k, ctx->cfg.mover_kparts > 0 ? ctx->cfg.mover_kparts : 4);
   p.head = W < 2 ? W : 2;
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;

@@ -272,29 +272,23 @@ struct MoeOp : OpBase<MoeParams> {
   // The tile count and the tile tables are written by the prologue's permutation in other
   // CTAs before a grid barrier: read through L2.
   static __device__ int mtiles(const Params& p) { return __ldcg(p.num_mtiles); }
-  // Prologue of every CTA (cooperative launch): route the tokens (a warp per token), a grid
-  // barrier, then the permutation (a CTA per expert) while the other CTAs zero `out` (the
-  // combine adds into it), and a second grid barrier before the GEMM and combine roles start.
+  // Prologue of every CTA (cooperative launch): zero `out` (the combine adds into it) and
+  // route the tokens (a warp per token), a grid barrier, the permutation (a CTA per expert),
+  // and a second grid barrier before the GEMM and combine roles start.
   template <bool Trace>
   static __device__ void grid_prologue(const Params& p, uint8_t* scratch) {
     const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float4* o = reinterpret_cast<float4*>(p.out);
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.out_vec;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+      o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int t = blockIdx.x * warps + warp; t < p.T; t += gridDim.x * warps)
       route_token(p.logits, t, p.E, p.topk, p.renorm, p.experts, p.gates, lane);
     grid_barrier(p.gbar, 1u, p.common);
     const int n = p.T * p.topk;
-    const int G = gridDim.x;
-    for (int e = blockIdx.x; e < p.E; e += G)
+    for (int e = blockIdx.x; e < p.E; e += gridDim.x)
       permute_expert(e, p.experts, n, p.E, p.topk, p.gates, p.perm, p.row_meta, p.tile_expert, p.tile_rows,
                      p.num_mtiles, p.counts, p.perm_out, p.counts_out, reinterpret_cast<int*>(scratch));
-    // zero-fill: by the CTAs without an expert, or by all when the experts cover the grid
-    const int zc = G > p.E ? G - p.E : G;
-    const int zi = G > p.E ? static_cast<int>(blockIdx.x) - p.E : static_cast<int>(blockIdx.x);
-    if (zi >= 0) {
-      float4* o = reinterpret_cast<float4*>(p.out);
-      for (size_t i = static_cast<size_t>(zi) * blockDim.x + threadIdx.x; i < p.out_vec;
-           i += static_cast<size_t>(zc) * blockDim.x)
-        o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
     grid_barrier(p.gbar + 2, 2u, p.common);
   }
   static __device__ int num_tiles(const Params& p) { return mtiles(p) * (p.n_up + p.n_down); }
