@@ -64,7 +64,7 @@ constexpr unsigned kStatusTimeout = 4;
 // Places a wait can run out (recorded in DevStatus::where).
 enum WaitSite : unsigned {
   kSiteSignal = 1, kSiteEmpty = 2, kSiteFull = 3, kSiteTmemEmpty = 4, kSiteTmemFull = 5,
-  kSitePeer = 6, kSiteDrain = 7, kSiteCombine = 8, kSiteGrid = 9
+  kSitePeer = 6, kSiteDrain = 7, kSiteCombine = 8
 };
 
 struct DevStatus {
@@ -234,39 +234,6 @@ __device__ __forceinline__ bool warp_wait_signals(const uint64_t* flags, int cou
   return ok;
 }
 
-// Grid-wide barrier of a cooperative launch, over two 64-bit words of the workspace:
-// w[0] counts arrivals (the last arriver resets it to 0) and w[1] receives the release value
-// (epoch << 2 | phase), which is unique to this call and barrier.  All threads of the CTA
-// call it; the wait is bounded like every other (on timeout the error is recorded and the
-// CTA goes on: the call's results are then undefined, as for any timeout).
-__device__ __forceinline__ void grid_barrier(uint64_t* w, unsigned phase, const Common& c) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned long long want = (c.epoch << 2) | phase;
-    __threadfence();
-    unsigned long long* cnt = reinterpret_cast<unsigned long long*>(w);
-    if (atomicAdd(cnt, 1ull) == gridDim.x - 1ull) {
-      atomicExch(cnt, 0ull);
-      __threadfence();
-      st_release_gpu(w + 1, want);
-    } else {
-      uint64_t t0 = 0;
-      uint32_t n = 0;
-      while (ld_acquire_gpu(w + 1) != want) {
-        if ((++n & 63u) == 0u) {
-          const uint64_t now = globaltimer();
-          if (t0 == 0) t0 = now;
-          if (now - t0 > c.timeout_ns || aborted(c.status)) {
-            report_timeout(c.status, kSiteGrid, phase);
-            break;
-          }
-        }
-      }
-    }
-  }
-  __syncthreads();
-}
-
 // Single-signal wait by every lane of a warp (used by epilogue warps for peer signals).
 __device__ __forceinline__ bool warp_wait_one(const uint64_t* flag, uint64_t want, const Common& c, int lane,
                                               unsigned site, unsigned long long info) {
@@ -296,10 +263,6 @@ struct OpBase {
   template <bool Trace>
   static __device__ void side_role(const P&, int, int, uint8_t*) {}
   static __device__ void producer_init(const P&) {}
-  // Work of all threads of every CTA at kernel start, before the partition split and the
-  // barrier setup; `scratch` is the 1024-aligned start of dynamic shared memory (free then).
-  template <bool Trace>
-  static __device__ void grid_prologue(const P&, uint8_t*) {}
   static __device__ void prefetch(const P&) {}
   static __device__ bool publishes(const P&, const Job&) { return false; }
   static __device__ void publish(const P&, const Job&) {}
@@ -563,9 +526,6 @@ __global__ void __launch_bounds__(op_max_threads<Op>(), 1)
     trace_begin();
     __syncthreads();
   }
-  // Work of every CTA before the roles start (e.g. the MoE routing, with grid-wide barriers:
-  // the launch is cooperative, so all CTAs are resident).
-  Op::template grid_prologue<Trace>(p, base);
   // CTAs outside the GEMM partition (e.g. a combine partition) run the op's side role.
   int gi = blockIdx.x, gn = gridDim.x;
   if (!Op::gemm_partition(p, gi, gn)) {

@@ -20,11 +20,15 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxTopk = 8;
 
 // ---------------------------------------------------------------------------- routing
-// Routing of token t by one warp: top-k of the fp32 logits (larger first, equal values to
-// the lower expert index), softmax over all E logits in fp32 taken at the chosen experts,
+// One warp per token: top-k of the fp32 logits (larger first, equal values to the
+// lower expert index), softmax over all E logits in fp32 taken at the chosen experts,
 // optionally divided by their sum over the chosen experts (renorm).
-__device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int topk, int renorm,
-                                            int* __restrict__ experts, float* __restrict__ gates, int lane) {
+__global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E, int topk, int renorm,
+                                 int* __restrict__ experts, float* __restrict__ gates) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+
   constexpr int kPer = kMaxExperts / 32;
   float v[kPer];
   const float* row = logits + static_cast<size_t>(t) * E;
@@ -77,30 +81,39 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
 }
 
 // ---------------------------------------------------------------------------- permutation
-// The permutation of expert e's assignments, by all threads of one CTA.  Every CTA doing
-// one histograms all assignments (so each knows all offsets without another grid-wide
-// step), then ranks the assignments of its own expert in (t, j) order with a block-wide
-// ballot scan.  Outputs:
+// One block per expert e.  Every block histograms all assignments (so each knows all
+// offsets without a grid-wide step), then ranks the assignments of its own expert in
+// (t, j) order with a block-wide ballot scan.  Outputs:
 //   perm[off_e + pos] = a                      (unpadded order: expert, t, j)
 //   row_meta[row] = {token, gate bits} of the row's assignment ({-1, 0} on padding rows), so
 //     the combine reads one 8-byte record per row instead of two dependent loads
 //   tile_expert / tile_rows for each 128-row tile of the padded layout (the f_R / f_S tables)
-// experts and gates were written by other CTAs before a grid barrier: read through L2.
-// sh: shared scratch of 2 * kMaxExperts + 66 ints.
-__device__ void permute_expert(int e, const int* experts, int n, int E, int topk, const float* gates,
-                               int* __restrict__ perm, int2* __restrict__ row_meta, int* __restrict__ tile_expert,
-                               int* __restrict__ tile_rows, int* __restrict__ num_mtiles, int* __restrict__ counts,
-                               int* __restrict__ perm_out, int* __restrict__ counts_out, int* sh) {
-  int* hist = sh;
-  int* off = hist + kMaxExperts;
-  int* poff = off + kMaxExperts + 1;
-  int* warp_tot = poff + kMaxExperts + 1;
-  int* warp_pre = warp_tot + 32;
+__global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict__ experts, int n, int E, int topk,
+                                                           const float* __restrict__ gates,
+                                                           int* __restrict__ perm, int2* __restrict__ row_meta,
+                                                           int* __restrict__ tile_expert, int* __restrict__ tile_rows,
+                                                           int* __restrict__ num_mtiles, int* __restrict__ counts,
+                                                           int* __restrict__ perm_out, int* __restrict__ counts_out,
+                                                           float4* __restrict__ out, size_t out_vec) {
+  __shared__ int hist[kMaxExperts];
+  __shared__ int off[kMaxExperts + 1];
+  __shared__ int poff[kMaxExperts + 1];
+  __shared__ int warp_tot[32];
+  __shared__ int warp_pre[32];
+  const int e = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (e >= E) {
+    // CTAs past the experts zero the fp32 output the combine partition adds into, on the
+    // SMs the per-expert CTAs leave idle.
+    const size_t nz = gridDim.x - E;
+    for (size_t i = (e - E) * static_cast<size_t>(blockDim.x) + tid; i < out_vec; i += nz * blockDim.x)
+      out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
   for (int i = tid; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   for (int a = tid; a < n; a += blockDim.x) {
-    const unsigned ex = static_cast<unsigned>(__ldcg(experts + a));
+    const unsigned ex = static_cast<unsigned>(experts[a]);
     if (ex < static_cast<unsigned>(E)) atomicAdd(&hist[ex], 1);  // never index outside the table
   }
   __syncthreads();
@@ -154,7 +167,7 @@ __device__ void permute_expert(int e, const int* experts, int n, int E, int topk
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int a = a0 + 32 * u + lane;
-      ex[u] = a < s1 ? __ldcg(experts + a) : -1;
+      ex[u] = a < s1 ? experts[a] : -1;
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) mine_cnt += __popc(__ballot_sync(0xffffffffu, ex[u] == e));
@@ -178,7 +191,7 @@ __device__ void permute_expert(int e, const int* experts, int n, int E, int topk
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int a = a0 + 32 * u + lane;
-      ex[u] = a < s1 ? __ldcg(experts + a) : -1;
+      ex[u] = a < s1 ? experts[a] : -1;
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -189,7 +202,7 @@ __device__ void permute_expert(int e, const int* experts, int n, int E, int topk
         const int pos = running + __popc(ball & ((1u << lane) - 1u));
         perm[off[e] + pos] = a;
         if (perm_out) perm_out[off[e] + pos] = a;
-        row_meta[poff[e] + pos] = make_int2(a / topk, __float_as_int(__ldcg(gates + a)));
+        row_meta[poff[e] + pos] = make_int2(a / topk, __float_as_int(gates[a]));
       }
       running += __popc(ball);
     }
@@ -209,7 +222,6 @@ __device__ void permute_expert(int e, const int* experts, int n, int E, int topk
     if (counts_out) counts_out[e] = cnt;
     if (e == 0) *num_mtiles = poff[E] / kBM;
   }
-  __syncthreads();  // the scratch is reused by the CTA's next expert
 }
 
 // ---------------------------------------------------------------------------- grouped GEMMs + combine
@@ -223,21 +235,10 @@ struct MoeParams {
   CUtensorMap y_st;  // y {H, R}, box {64, 32}
   CUtensorMap y_ld;  // y {H, R}, box {64, 128} (combine partition loads)
   Common common;
-  int* num_mtiles;
-  int* tile_expert;
-  int* tile_rows;
-  int2* row_meta;
-  // routing and permutation, in the kernel's prologue
-  const float* logits;
-  int* experts;  // [T * topk]
-  float* gates;  // [T * topk]
-  int* perm;
-  int* perm_out;
-  int* counts;
-  int* counts_out;
-  uint64_t* gbar;  // [4]: two grid barriers (arrival count, release word)
-  size_t out_vec;            // float4 vectors of out
-  int renorm;
+  const int* num_mtiles;
+  const int* tile_expert;
+  const int* tile_rows;
+  const int2* row_meta;
   const __nv_bfloat16* x;  // tokens, gathered into xp by the mover warps
   __nv_bfloat16* xp_rows;  // the gathered rows (xp's memory)
   uint64_t* x_flags;       // [R/128][kGatherPieces]: piece of a row tile gathered
@@ -269,28 +270,10 @@ struct MoeOp : OpBase<MoeParams> {
   // combine partition's CTAs.
   static constexpr int kMaxMovers = 2;
   static constexpr uint32_t kTxBytes = Geo<128>::kStageBytes;
-  // The tile count and the tile tables are written by the prologue's permutation in other
-  // CTAs before a grid barrier: read through L2.
-  static __device__ int mtiles(const Params& p) { return __ldcg(p.num_mtiles); }
-  // Prologue of every CTA (cooperative launch): zero `out` (the combine adds into it) and
-  // route the tokens (a warp per token), a grid barrier, the permutation (a CTA per expert),
-  // and a second grid barrier before the GEMM and combine roles start.
-  template <bool Trace>
-  static __device__ void grid_prologue(const Params& p, uint8_t* scratch) {
-    const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float4* o = reinterpret_cast<float4*>(p.out);
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.out_vec;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x)
-      o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int t = blockIdx.x * warps + warp; t < p.T; t += gridDim.x * warps)
-      route_token(p.logits, t, p.E, p.topk, p.renorm, p.experts, p.gates, lane);
-    grid_barrier(p.gbar, 1u, p.common);
-    const int n = p.T * p.topk;
-    for (int e = blockIdx.x; e < p.E; e += gridDim.x)
-      permute_expert(e, p.experts, n, p.E, p.topk, p.gates, p.perm, p.row_meta, p.tile_expert, p.tile_rows,
-                     p.num_mtiles, p.counts, p.perm_out, p.counts_out, reinterpret_cast<int*>(scratch));
-    grid_barrier(p.gbar + 2, 2u, p.common);
-  }
+  // The tile count and tile table come from the permutation kernel, which completed
+  // before this kernel started: read-only for this kernel, so they go through the
+  // non-coherent cache (one L2 trip per SM, then L1 hits).
+  static __device__ int mtiles(const Params& p) { return __ldg(p.num_mtiles); }
   static __device__ int num_tiles(const Params& p) { return mtiles(p) * (p.n_up + p.n_down); }
   static __device__ bool gemm_partition(const Params& p, int& gi, int& gn) {
     gn = gridDim.x - p.combine_ctas;
@@ -361,7 +344,7 @@ struct MoeOp : OpBase<MoeParams> {
     j.a_sel = 0;
     j.b_sel = 0;
     j.a_row = j.x0 * kBM;
-    j.b_z = __ldcg(p.tile_expert + j.x0);
+    j.b_z = __ldg(p.tile_expert + j.x0);
     j.x2 = 0;
     j.x3 = 0;
     return j;
@@ -398,7 +381,7 @@ struct MoeOp : OpBase<MoeParams> {
       const uint64_t t0 = Trace ? globaltimer() : 0;
 #pragma unroll 1
       for (int r = q * kGatherRows; r < (q + 1) * kGatherRows; ++r) {
-        const int tok = __ldcg(&p.row_meta[r].x);
+        const int tok = __ldg(&p.row_meta[r].x);
         uint4* dst = reinterpret_cast<uint4*>(p.xp_rows + static_cast<size_t>(r) * p.H);
         if (tok >= 0) {
           const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(tok) * p.H);
@@ -572,7 +555,7 @@ static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct MoeLayout {
   size_t experts, gates, perm, row_meta, tile_expert, tile_rows, num_mtiles, counts, xp, h, y, up_flags, y_flags,
-      x_flags, gbar, total;
+      x_flags, total;
   int rmax;
 };
 
@@ -597,7 +580,6 @@ static MoeLayout moe_layout(int T, int H, int E, int F, int topk) {
   L.up_flags = o; o += al256(tiles * (F / 128) * 8);
   L.y_flags = o; o += al256(tiles * (H / kBN) * 8);
   L.x_flags = o; o += al256(tiles * kGatherPieces * 8);
-  L.gbar = o; o += 256;
   L.total = o;
   return L;
 }
@@ -640,6 +622,14 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
   __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
 
+  moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, ctx->cfg.moe_renorm, experts, gates);
+  const int zero_ctas = ctx->sms > E ? ctx->sms - E : 1;
+  moe_permute_kernel<<<E + zero_ctas, 1024, 0, st>>>(experts, T * topk, E, topk, gates, perm, row_meta, tile_expert,
+                                                     tile_rows, num_mtiles, counts, perm_out, counts_out,
+                                                     reinterpret_cast<float4*>(out),
+                                                     static_cast<size_t>(T) * H / 4);
+  if (cudaGetLastError() != cudaSuccess) return TL_ERR_CUDA;
+
   MoeParams p;
   std::memset(&p, 0, sizeof(p));
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -649,16 +639,6 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
       !tmap_2d(&p.y_st, BF, 2, yb, H, L.rmax, 64, 32) || !tmap_2d(&p.y_ld, BF, 2, yb, H, L.rmax, 64, 128))
     return TL_ERR_CUDA;
   p.common = make_common(ctx);
-  p.logits = logits;
-  p.experts = experts;
-  p.gates = gates;
-  p.perm = perm;
-  p.perm_out = perm_out;
-  p.counts = counts;
-  p.counts_out = counts_out;
-  p.gbar = reinterpret_cast<uint64_t*>(ws + L.gbar);
-  p.out_vec = static_cast<size_t>(T) * H / 4;
-  p.renorm = ctx->cfg.moe_renorm;
   p.num_mtiles = num_mtiles;
   p.tile_expert = tile_expert;
   p.tile_rows = tile_rows;

@@ -289,10 +289,10 @@ int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const void* const* 
  *   y_(t,j) = (SiLU(x_t . Wg_e) * (x_t . Wu_e)) . Wd_e   (h kept in bf16, y in bf16)
  *   out_t   = sum_j gate_(t,j) * y_(t,j)                  (fp32)
  * workspace: tl_moe_workspace_bytes().
- * One persistent cooperative launch: every CTA first routes its share of the tokens, then
- * (after a grid-wide barrier) one CTA per expert builds the permutation and tile tables while
- * the others zero `out`, and after a second barrier the GEMM partition runs the gather and the
- * grouped GEMMs while the combine partition adds finished y tiles into `out`.
+ * Three launches: the routing (a warp per token), the permutation and tile tables (a CTA per
+ * expert, while the remaining CTAs zero `out`), then one persistent cooperative launch whose
+ * GEMM partition runs the gather and the grouped GEMMs while the combine partition adds
+ * finished y tiles into `out`.
  * Shapes: T >= 1; 1 <= topk <= 8; topk <= E <= 256; H % 256 == 0; F % 128 == 0.
  */
 size_t tl_moe_workspace_bytes(int T, int H, int E, int F, int topk);
