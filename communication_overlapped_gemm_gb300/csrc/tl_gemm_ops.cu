@@ -205,11 +205,48 @@ __device__ __forceinline__ void copy_rows_multi(const uint8_t* __restrict__ src,
   }
 }
 
-// One destination.
-__device__ __forceinline__ void copy_rows(const uint8_t* __restrict__ src, uint8_t* dst, size_t stride, int rows,
-                                          int row_bytes, int tid, int nthreads) {
-  uint8_t* const d[8] = {dst, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
-  copy_rows_multi(src, d, 1, stride, rows, row_bytes, tid, nthreads);
+// A contiguous block of nvec 16-byte vectors, 8 loads in flight per thread.
+__device__ __forceinline__ void copy_contig(const uint4* __restrict__ s4, uint4* __restrict__ d4, int nvec, int tid,
+                                            int nthreads) {
+  constexpr int U = 8;
+  for (int i = tid; i < nvec; i += U * nthreads) {
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i + u * nthreads < nvec) r[u] = __ldg(s4 + i + u * nthreads);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i + u * nthreads < nvec) d4[i + u * nthreads] = r[u];
+  }
+}
+
+// One destination: the same vectors, with the store offsets walked again rather than kept
+// in registers.
+__device__ __forceinline__ void copy_rows(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, size_t stride,
+                                          int rows, int row_bytes, int tid, int nthreads) {
+  constexpr int U = 8;
+  if (static_cast<size_t>(row_bytes) == stride) {
+    copy_contig(reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), rows * (row_bytes / 16), tid,
+                nthreads);
+    return;
+  }
+  const int vr = row_bytes / 16;
+  const int nvec = rows * vr;
+  RowWalk wl(tid, nthreads, vr, stride);
+  RowWalk wst = wl;
+  for (int i = tid; i < nvec; i += U * nthreads) {
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (i + u * nthreads < nvec) r[u] = __ldg(reinterpret_cast<const uint4*>(src + wl.offset()));
+      wl.step();
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (i + u * nthreads < nvec) *reinterpret_cast<uint4*>(dst + wst.offset()) = r[u];
+      wst.step();
+    }
+  }
 }
 
 // Position of chunk g of one gather (see ag_copy): shard i of the mover's order, K part q,
@@ -468,7 +505,6 @@ struct Mlp2Params {
   uint64_t* rs_flags;  // [T/128][nb2]
   long long shard_bytes, slab_bytes;
   int W, T, Tr, h, f, mps, spr, nb1, kb1, nb2, kb2, swizzle, chunks, skip_chunk;
-  int quarters, cpq, qcols, kb_q, head;  // K parts of the gather's chunks (as AgParams)
   int push;  // 1: each shard is read once and pushed to the W-1 other ranks' copies; 0: pull
 };
 
@@ -533,18 +569,18 @@ struct Mlp2Op : OpBase<Mlp2Params> {
   static __device__ int row_block(const Params& p, const Job& j) {
     return (j.x1 * p.Tr) / 128 + j.x2 * kSub + (Pair ? j.rank : 0);
   }
+  // Once per tile, before its first k-block: the gathered slabs a layer-1 tile reads, or the
+  // layer-1 tiles of the row block a layer-2 tile reads.  (The chain's gather is not cut
+  // along K: per-part waits measured slower here, as most layer-1 tiles read remote rows.)
   static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
+    if (kb != 0) return;
     if (j.kind == 1) {
-      // K part q of a gathered row block: its chunks in each of the kOwn slabs this CTA reads
-      if (j.a_sel == 0 || kb % p.kb_q != 0) return;
-      const int q = kb / p.kb_q;
-      const size_t slab0 = (static_cast<size_t>(j.x0) * p.W + j.x1) * p.spr + j.x2 * kSub + (Pair ? j.rank : 0);
-#pragma unroll
-      for (int sl = 0; sl < kOwn; ++sl)
-        wait_slab(p.ag_flags + (slab0 + sl) * p.chunks + q * p.cpq, p.cpq, p.common, lane,
-                  (static_cast<unsigned long long>(j.x1) << 32) | (j.x2 << 4) | q);
+      if (j.a_sel == 0) return;
+      const uint64_t* f = p.ag_flags +
+                          ((static_cast<size_t>(j.x0) * p.W + j.x1) * p.spr + j.x2 * kSub + (Pair ? j.rank : 0)) *
+                              p.chunks;
+      wait_slab(f, kOwn * p.chunks, p.common, lane, (static_cast<unsigned long long>(j.x1) << 32) | j.x2);
     } else {
-      if (kb != 0) return;
       // CTA-level chain: the layer-1 tiles that produce this row block of H_r are done.
       const int rb = row_block(p, j);
       const uint64_t* f = p.h_flags + (static_cast<size_t>(j.x0) * (p.T / 128) + rb) * p.nb1;
@@ -609,7 +645,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
   }
   // Every emulated rank r needs the other ranks' X shards in its own copy of X (rows r*T ..);
   // a rank's own shard is read in place by its layer-1 tiles, so its slot of the copy is not
-  // written.  Chunks are K parts x row pieces of 128-row slabs, ordered as in ag_copy.
+  // written.  Chunks are row pieces of 128-row slabs, a shard's slabs in order.
   //   pull ("Triton-distributed ...", §3.2 Algorithm 2): rank r, in turn (rank 0's first),
   //     copies shards (r+1) mod W, (r+2) mod W, ... into its copy;
   //   push (§3.2 Algorithm 1): each shard, in the order 1, 2, ..., W-1, 0, is read once and
@@ -619,7 +655,7 @@ struct Mlp2Op : OpBase<Mlp2Params> {
     const int nthreads = p.common.mover_warps * 32;
     const int tid = mw * 32 + lane;
     const int per_shard = p.spr * p.chunks;
-    const int piece_rows = tl::kBM / p.cpq;  // slabs are 128 rows (not this op's tile rows)
+    const int piece_rows = tl::kBM / p.chunks;  // slabs are 128 rows (not this op's tile rows)
     const size_t row_stride = static_cast<size_t>(p.h) * 2;
     const int total = p.W < 2 ? 0 : (p.push ? p.W * per_shard : p.W * (p.W - 1) * per_shard);
     for (int g = blockIdx.x; g < total; g += gridDim.x) {
@@ -628,23 +664,20 @@ struct Mlp2Op : OpBase<Mlp2Params> {
         r = g / ((p.W - 1) * per_shard);
         gg = g - r * (p.W - 1) * per_shard;
       }
-      const ChunkPos cp = chunk_pos(gg, p.head, p.spr, p.chunks, p.cpq);
+      const ChunkPos cp = chunk_pos(gg, 0, p.spr, p.chunks, p.chunks);
       const int src = ag_mover_rank(p.W, p.push ? 0 : r, p.swizzle, cp.i);
-      const int c0 = cp.q * p.qcols;
-      const int cols = c0 >= p.h ? 0 : (p.h - c0 < p.qcols ? p.h - c0 : p.qcols);
       const size_t off = (static_cast<size_t>(cp.slab) * tl::kBM + static_cast<size_t>(cp.piece) * piece_rows) *
-                             row_stride + static_cast<size_t>(c0) * 2;
+                         row_stride;
       uint8_t* dst[8];
       int nd = 0;
       for (int d = 0; d < p.W; ++d)
         if (d != src && (p.push || d == r))
           dst[nd++] = p.xg + (static_cast<size_t>(d) * p.T + static_cast<size_t>(src) * p.Tr) * p.h * 2 + off;
-      copy_rows_multi(p.x[src] + off, dst, nd, row_stride, piece_rows, cols * 2, tid, nthreads);
+      copy_rows_multi(p.x[src] + off, dst, nd, row_stride, piece_rows, p.h * 2, tid, nthreads);
       __threadfence();
       named_bar_sync(2, nthreads);
       if (tid < p.W && tid != src && (p.push || tid == r) && g != p.skip_chunk)
-        st_release_gpu(p.ag_flags + ((static_cast<size_t>(tid) * p.W + src) * p.spr + cp.slab) * p.chunks +
-                           cp.q * p.cpq + cp.piece,
+        st_release_gpu(p.ag_flags + ((static_cast<size_t>(tid) * p.W + src) * p.spr + cp.slab) * p.chunks + cp.piece,
                        p.common.epoch);
     }
   }
@@ -652,15 +685,31 @@ struct Mlp2Op : OpBase<Mlp2Params> {
 
 // ============================================================================ AllGather alone
 // The pull-mode AllGather as its own kernel (the communication task of "Triton-
-// distributed ...", §3.2 Algorithm 2, without a consumer): the same mover code, chunk
-// geometry, order and signals as the fused AllGather+GEMM, run by mover_warps warps in
-// each of the persistent CTAs.
+// distributed ...", §3.2 Algorithm 2, without a consumer): the fused AllGather+GEMM's chunk
+// order and signals with whole-row chunks (no K parts: nothing waits on them here), every
+// shard including the self rank's (last), on several CTAs of copy warps per SM.  With whole
+// rows a chunk is one contiguous block: chunk g of the gather is block g mod (spr * chunks)
+// of shard i = g / (spr * chunks) in the mover's order.
 constexpr int kAllgatherWarps = 16;  // copy warps per CTA of the standalone AllGather
 #ifndef TL_AG_ALONE_CTAS_PER_SM
 #define TL_AG_ALONE_CTAS_PER_SM 4
 #endif
-__global__ void __launch_bounds__(kAllgatherWarps * 32) allgather_kernel(const __grid_constant__ AgParams p) {
-  ag_mover<false>(p, threadIdx.x >> 5, threadIdx.x & 31, 0);  // boost is 0 here
+__global__ void __launch_bounds__(kAllgatherWarps * 32, 2) allgather_kernel(const __grid_constant__ AgParams p) {
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int per_shard = p.spr * p.chunks;
+  const int total = p.W * per_shard;
+  const size_t piece_bytes = static_cast<size_t>(tl::kBM / p.chunks) * p.k * 2;
+  for (int g = blockIdx.x; g < total; g += gridDim.x) {
+    const int i = g / per_shard, rem = g - i * per_shard;
+    const int r = ag_mover_rank(p.W, p.rank, p.swizzle, i);
+    const size_t off = static_cast<size_t>(rem) * piece_bytes;
+    copy_contig(reinterpret_cast<const uint4*>(p.shard[r] + off),
+                reinterpret_cast<uint4*>(p.gath + static_cast<size_t>(r) * p.shard_bytes + off),
+                static_cast<int>(piece_bytes / 16), tid, nthreads);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0 && g != p.skip_chunk) st_release_gpu(p.flags + static_cast<size_t>(r) * per_shard + rem, p.common.epoch);
+  }
 }
 
 // ============================================================================ ReduceScatter alone
@@ -987,12 +1036,6 @@ extern "C" int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const vo
   p.shard_bytes = static_cast<long long>(Tr) * hidden * 2;
   p.slab_bytes = static_cast<long long>(kBM) * hidden * 2;
   p.push = ctx->cfg.ag_push;
-  const KParts kp = k_parts(p.chunks, hidden, ctx->cfg.mover_kparts > 0 ? ctx->cfg.mover_kparts : 1);
-  p.quarters = kp.quarters;
-  p.cpq = kp.cpq;
-  p.kb_q = kp.kb_q;
-  p.qcols = kp.qcols;
-  p.head = p.push ? (W < 2 ? W : 2) : (W - 1 < 2 ? W - 1 : 2);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (pair) return launch_persistent_pair<Mlp2Op<256, true>>(ctx, p, st, ctx->cfg.mover_warps);
   return bm == 256 ? launch_persistent<Mlp2Op<256>>(ctx, p, st, ctx->cfg.mover_warps)
@@ -1029,13 +1072,13 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   p.chunks = ctx->cfg.chunks_per_slab;
   p.skip_chunk = -1;
   p.copy_self = 1;
-  ag_parts(p, k, ctx->cfg.mover_kparts > 0 ? ctx->cfg.mover_kparts : 4);
+  ag_parts(p, k, 1);  // no consumer waits on K parts here: whole-row chunks copy fastest
   p.head = W < 2 ? W : 2;
   p.shard_bytes = static_cast<long long>(m_per_rank) * k * 2;
   p.slab_bytes = static_cast<long long>(kBM) * k * 2;
   // Alone, the copy has the whole GPU: TL_AG_ALONE_CTAS_PER_SM CTAs of kAllgatherWarps warps
-  // on each SM run the same chunk loop as the fused kernel's mover warps, so one CTA's fence
-  // and barrier after a chunk overlap the other CTAs' loads.
+  // per SM (two resident at a time), so one CTA's fence and barrier after a chunk overlap the
+  // other CTA's loads.
   p.common.mover_warps = kAllgatherWarps;
   allgather_kernel<<<ctx->ctas * TL_AG_ALONE_CTAS_PER_SM, kAllgatherWarps * 32, 0,
                      reinterpret_cast<cudaStream_t>(stream)>>>(p);

@@ -96,12 +96,13 @@ typedef struct tl_config {
                                  (Algorithm 1, each shard read once and written to the other ranks'
                                  copies).  tl_ag_gemm and tl_allgather gather into one rank, where
                                  both modes move the same bytes: they always pull              */
-  int mover_kparts;           /* the mover's chunks along K ([TL] §3.1, the communication tile): 1
-                                 each chunk is whole rows of a 128-row slab; 2 or 4 each slab is
-                                 also cut into that many K parts (of at least 16 64-column
-                                 k-blocks), copied part by part, and a tile waits for each part
-                                 before its first k-block in it; 0 (default) 4 for tl_ag_gemm and
-                                 tl_allgather, 1 for tl_mlp2 (as measured on GB300)            */
+  int mover_kparts;           /* tl_ag_gemm's mover chunks along K ([TL] §3.1, the communication
+                                 tile): 1 each chunk is whole rows of a 128-row slab; 2 or 4 each
+                                 slab of the first two shards gathered is also cut into that many
+                                 K parts (of at least 16 64-column k-blocks), copied part by
+                                 part, and a tile waits for each part before its first k-block in
+                                 it; 0 (default) 4.  tl_allgather and tl_mlp2 always copy whole
+                                 rows (as measured on GB300, K parts only slow them)          */
 } tl_config;
 
 typedef struct tl_ctx tl_ctx;
