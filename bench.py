@@ -402,6 +402,14 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
                      device=device)
     rec("ag_tiny", lambda: tl.tl_ag_gemm(ctx, a, b, c, ws, stream=stream),
         ag_flops(d["W"], d["m_per_rank"], d["n"], d["k"]), 0, "latency", 1)
+    out["ag_tiny"]["gather"] = "pull: mover chunks, one release signal each"
+    # the same call with the low-latency push gather (LL words carry the call's signal)
+    with tl.Context(ctx.device, ag_ll=1) as cl:
+        rec("ag_tiny_ll", lambda: tl.tl_ag_gemm(cl, a, b, c, ws, stream=stream),
+            ag_flops(d["W"], d["m_per_rank"], d["n"], d["k"]), 0, "latency", 1)
+        if cl.check() != tl.TL_OK:
+            raise RuntimeError("ag_tiny_ll: device status not OK")
+        out["ag_tiny_ll"]["gather"] = "low-latency push: flag-in-payload LL words, no separate signal"
     del a, b, c, ws
 
     # GEMM + ReduceScatter

@@ -22,7 +22,8 @@ from . import _build
 __all__ = [
     "TL_OK", "TL_ERR_INVALID", "TL_ERR_UNSUPPORTED", "TL_ERR_CUDA", "TL_ERR_TIMEOUT", "TL_ERR_WORKSPACE",
     "TLError", "Config", "Context", "lib", "library_path", "build",
-    "tl_ag_gemm", "tl_allgather", "tl_gemm_rs", "tl_reduce_scatter", "tl_mlp2", "tl_moe_combine",
+    "tl_ag_gemm", "tl_ag_gemm_ll_capable", "tl_allgather", "tl_gemm_rs", "tl_reduce_scatter", "tl_mlp2",
+    "tl_moe_combine",
     "tl_ag_gemm_workspace_bytes", "tl_gemm_rs_workspace_bytes", "tl_gemm_rs_ring_workspace_bytes",
     "tl_mlp2_workspace_bytes", "tl_rs_ring_tile_order",
     "tl_moe_workspace_bytes", "tl_ag_tile_order", "tl_rs_tile_order", "tl_trace_bytes", "tl_ag_attention",
@@ -59,6 +60,7 @@ class Config(ctypes.Structure):
         ("rs_ring", _i),
         ("ag_push", _i),
         ("mover_kparts", _i),
+        ("ag_ll", _i),
     ]
 
 
@@ -75,6 +77,7 @@ _SIGS = {
     "tl_strerror": (ctypes.c_char_p, [_i]),
     "tl_ag_gemm_workspace_bytes": (_c_size, [_i, _i, _i, _i]),
     "tl_ag_gemm": (_i, [_vp, _i, _i, ctypes.POINTER(_vp), _vp, _vp, _vp, _c_size, _i, _i, _i, _vp]),
+    "tl_ag_gemm_ll_capable": (_i, [_vp, _i, _i, _i, _i]),
     "tl_allgather": (_i, [_vp, _i, _i, ctypes.POINTER(_vp), _vp, _c_size, _i, _i, _vp]),
     "tl_gemm_rs_workspace_bytes": (_c_size, [_i, _i, _i, _i]),
     "tl_gemm_rs_ring_workspace_bytes": (_c_size, [_i, _i, _i, _i]),
@@ -218,6 +221,11 @@ class Context:
 # ---------------------------------------------------------------- workspace sizes
 def tl_ag_gemm_workspace_bytes(W, m_per_rank, n, k) -> int:
     return lib().tl_ag_gemm_workspace_bytes(W, m_per_rank, n, k)
+
+
+def tl_ag_gemm_ll_capable(ctx: Context, W, m_per_rank, n, k) -> bool:
+    """Whether tl_ag_gemm on ctx with ag_ll=1 takes the low-latency gather for this shape."""
+    return lib().tl_ag_gemm_ll_capable(ctx.handle, W, m_per_rank, n, k) == 1
 
 
 def tl_gemm_rs_workspace_bytes(W, m, n, k_r) -> int:

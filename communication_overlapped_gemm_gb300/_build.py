@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 BUILDDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(LIBDIR, "libtlgb300.so")
-SOURCES = ["tl_ctx.cu", "tl_gemm_ops.cu", "tl_moe.cu", "tl_noalloc.cu", "tl_attn.cu"]
+SOURCES = ["tl_ctx.cu", "tl_gemm_ops.cu", "tl_moe.cu", "tl_noalloc.cu", "tl_attn.cu", "tl_ag_ll.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

@@ -796,7 +796,10 @@ AgLayout ag_layout(int W, int m_per_rank, int k) {
   L.gath_bytes = static_cast<size_t>(W) * m_per_rank * k * 2;
   L.flags_off = align256(L.gath_bytes);
   L.flags_bytes = static_cast<size_t>(W) * (m_per_rank / kBM) * 32 * 8;
-  L.total = L.flags_off + align256(L.flags_bytes);
+  L.ll_off = L.flags_off + align256(L.flags_bytes);
+  const long long elems = static_cast<long long>(W) * m_per_rank * k;
+  L.ll_bytes = elems <= kLLMaxElems ? static_cast<size_t>(elems) * 4 : 0;
+  L.total = L.ll_off + align256(L.ll_bytes);
   return L;
 }
 
@@ -827,6 +830,9 @@ extern "C" int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_sha
   const AgLayout L = ag_layout(W, m_per_rank, k);
   if (workspace_bytes < L.total) return TL_ERR_WORKSPACE;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
+  if (ctx->cfg.ag_ll && W > 1)
+    return ag_ll_launch(ctx, W, rank, a_shards, b, c, static_cast<uint8_t*>(workspace), m_per_rank, n, k,
+                        reinterpret_cast<cudaStream_t>(stream));
 
   AgParams p;
   std::memset(&p, 0, sizeof(p));

@@ -34,7 +34,12 @@ bool tmap_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Next signal value of this context (never 0; < 2^59 so that (epoch << 4) | 15 fits in 64 bits).
-inline unsigned long long next_epoch(tl_ctx* ctx) { return ++ctx->epoch; }
+// Values whose low 32 bits are 0 are skipped: the low-latency gather carries those 32 bits in
+// every word, and a zero-filled workspace must never look written.
+inline unsigned long long next_epoch(tl_ctx* ctx) {
+  if ((++ctx->epoch & 0xffffffffull) == 0) ++ctx->epoch;
+  return ctx->epoch;
+}
 
 inline Common make_common(tl_ctx* ctx) {
   Common c;
@@ -57,13 +62,18 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace of the AllGather (alone or fused with the GEMM): the gathered operand T
 // (W x m_per_rank x k bf16, rank order) at offset 0, then the per-chunk signal words
-// (W x m_per_rank/128 slabs x 32 chunks, 8 bytes each), each region 256-byte aligned.
-// tl_ag_gemm_workspace_bytes, tl_ag_gemm, tl_allgather and tl_ag_gemm_static_scratch all
-// take their offsets from here.
+// (W x m_per_rank/128 slabs x 32 chunks, 8 bytes each), then, for problems small enough for
+// the low-latency gather (W * m_per_rank * k <= kLLMaxElems), the LL slabs: one 8-byte word
+// {two bf16, call signal} per pair of elements of every shard (W x m_per_rank x k/2 words).
+// Each region is 256-byte aligned.  tl_ag_gemm_workspace_bytes, tl_ag_gemm, tl_allgather and
+// tl_ag_gemm_static_scratch all take their offsets from here.
+constexpr long long kLLMaxElems = 1LL << 20;
 struct AgLayout {
   size_t gath_bytes;   // the gathered operand
   size_t flags_off;    // first signal word
   size_t flags_bytes;  // all signal words
+  size_t ll_off;       // first LL word
+  size_t ll_bytes;     // all LL words (0: the problem is too large for the LL gather)
   size_t total;
 };
 AgLayout ag_layout(int W, int m_per_rank, int k);
@@ -73,6 +83,13 @@ AgLayout ag_layout(int W, int m_per_rank, int k);
 // (a zero dimension) passes without looking at the pointers.
 int ag_gemm_check(const tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b, const void* c,
                   int m_per_rank, int n, int k);
+
+// The low-latency push gather + GEMM (tl_ag_ll.cu): whether a problem can take it on this
+// context (its workspace has LL slabs and its 128 x 256 tiles leave at least one CTA to push),
+// and the launch (TL_ERR_UNSUPPORTED when it cannot).
+int ag_ll_capable(const tl_ctx* ctx, int W, int m_per_rank, int n, int k);
+int ag_ll_launch(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b, void* c, uint8_t* ws,
+                 int m_per_rank, int n, int k, cudaStream_t stream);
 
 
 // Cooperative launch of one persistent CTA per SM (or cfg.grid_ctas), so that every CTA

@@ -71,8 +71,8 @@ extern "C" int tl_ag_gemm_static_scratch(tl_ctx* ctx, int W, int rank, const voi
   void* scratch = nullptr;
   const int rc = tl::scratch_address(ctx->device, &scratch);
   if (rc != TL_OK) return rc;
-  // Clear the signal words the previous call left (another context's values included).
-  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + L.flags_off, 0, L.flags_bytes,
+  // Clear the signal words (and LL words) the previous call left, another context's included.
+  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + L.flags_off, 0, L.total - L.flags_off,
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_CUDA;

@@ -103,6 +103,13 @@ typedef struct tl_config {
                                  part, and a tile waits for each part before its first k-block in
                                  it; 0 (default) 4.  tl_allgather and tl_mlp2 always copy whole
                                  rows (as measured on GB300, K parts only slow them)          */
+  int ag_ll;                  /* tl_ag_gemm's gather protocol: 0 (default) pull with one signal
+                                 per chunk; 1 low-latency push ([TD] §3.2 Algorithm 1 with the
+                                 flag carried in every word): the remote shards' owners write
+                                 8-byte words {bf16 x 2, call signal} into the workspace's LL
+                                 slabs and each tile reads them straight into its operand
+                                 buffer, with no separate signal or fence.  For small problems
+                                 only (tl_ag_gemm_ll_capable); otherwise TL_ERR_UNSUPPORTED  */
 } tl_config;
 
 typedef struct tl_ctx tl_ctx;
@@ -185,10 +192,23 @@ int tl_ctx_set_trace(tl_ctx* ctx, void* buf, size_t bytes, int spans_per_warp);
  * Shapes: 1 <= W <= 8; m_per_rank % 128 == 0; n % 8 == 0; k % 8 == 0 (n, k need not be
  * tile multiples: ragged edges are zero-filled by TMA on load and clipped on store).
  * Any zero dimension is a no-op returning TL_OK.
+ * Low-latency gather (cfg.ag_ll = 1, W > 1): instead of the mover and its chunk signals, the
+ * owners of the remote shards push them as LL words {bf16 x 2, low 32 bits of the call's
+ * signal} into the workspace's LL slabs, after the signal words, and every 128 x 256 output
+ * tile reads the words of its rows straight into its operand buffer, polling only those that
+ * do not carry this call's signal yet.  The gathered region is not written.  The result is
+ * the same operation; for m_per_rank % 256 != 0 it is bit-identical to the pull path (the
+ * same 128-row MMAs in the same k order).  Only problems with W * m_per_rank * k <= 2^20
+ * (their workspace has the LL slabs) and at most (the context's CTAs - 1) output tiles can
+ * take it (tl_ag_gemm_ll_capable); others return TL_ERR_UNSUPPORTED with nothing enqueued.
+ * The LL slabs need no zeroing between calls on one context.
  */
 size_t tl_ag_gemm_workspace_bytes(int W, int m_per_rank, int n, int k);
 int tl_ag_gemm(tl_ctx* ctx, int W, int rank, const void* const* a_shards, const void* b, void* c,
                void* workspace, size_t workspace_bytes, int m_per_rank, int n, int k, tl_stream_t stream);
+/* 1 if tl_ag_gemm on ctx with cfg.ag_ll = 1 runs the low-latency gather for this shape, else 0
+ * (also 0 for a NULL ctx or a negative size; W = 1 has nothing to gather: 0). */
+int tl_ag_gemm_ll_capable(const tl_ctx* ctx, int W, int m_per_rank, int n, int k);
 
 /* ---------------------------------------------------------------- AllGather alone
  * [TD] §3.2 Algorithm 2 (pull-mode one-sided AllGather) as its own kernel: the shard mover of

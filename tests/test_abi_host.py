@@ -53,7 +53,7 @@ def test_config_defaults_and_strerror(tl):
     assert tl.lib().tl_config_default(ctypes.byref(c)) == tl.TL_OK
     assert (c.mover_warps, c.chunks_per_slab, c.swizzle, c.grid_ctas, c.combine_ctas) == (4, 32, 1, 0, 16)
     assert c.debug_skip_chunk == -1 and c.timeout_ns == 2_000_000_000 and c.pair_ctas == 2 and c.moe_renorm == 0
-    assert c.rs_ring == 0 and c.ag_push == 0 and c.mover_kparts == 0
+    assert c.rs_ring == 0 and c.ag_push == 0 and c.mover_kparts == 0 and c.ag_ll == 0
     assert tl.lib().tl_config_default(None) == tl.TL_ERR_INVALID
     for code in (tl.TL_OK, tl.TL_ERR_INVALID, tl.TL_ERR_UNSUPPORTED, tl.TL_ERR_CUDA, tl.TL_ERR_TIMEOUT,
                  tl.TL_ERR_WORKSPACE):
@@ -65,6 +65,10 @@ def test_workspace_sizes(tl):
     # gathered A (W*m*k*2) + 32 signals of 8 bytes per 128-row slab, each 256-aligned
     assert tl.tl_ag_gemm_workspace_bytes(8, 1024, 3584, 8192) == 8 * 1024 * 8192 * 2 + 8 * 8 * 32 * 8
     assert tl.tl_ag_gemm_workspace_bytes(2, 100, 256, 256) == 0       # m_per_rank not a 128 multiple
+    # small problems (W * m_per_rank * k <= 2^20) add the LL slabs: 4 bytes per element
+    assert tl.tl_ag_gemm_workspace_bytes(2, 128, 256, 256) == 2 * 128 * 256 * 2 + 2 * 1 * 32 * 8 + 2 * 128 * 256 * 4
+    assert tl.tl_ag_gemm_workspace_bytes(8, 128, 256, 1024) == 8 * 128 * 1024 * 2 + 8 * 32 * 8 + 8 * 128 * 1024 * 4
+    assert tl.tl_ag_gemm_workspace_bytes(8, 128, 256, 1032) == 8 * 128 * 1032 * 2 + 8 * 32 * 8   # over 2^20
     assert tl.tl_ag_gemm_workspace_bytes(9, 128, 256, 256) == 0       # W > 8
     assert tl.tl_gemm_rs_workspace_bytes(8, 8192, 8192, 3584) == 8192 * 8192 * 4 + 64 * 32 * 8
     assert tl.tl_gemm_rs_workspace_bytes(8, 1000, 256, 64) == 0
