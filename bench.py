@@ -30,6 +30,7 @@ import glob
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -48,7 +49,7 @@ MOE_LAUNCHES = 3  # routing, permutation, the persistent expert-GEMM + combine k
 # dram__bytes_write.sum), keyed by the hash of the kernel's sources (AG_KERNEL_SOURCES) they
 # were taken on.
 # A kernel changed since the capture reports traffic null.
-NCU_TRAFFIC = {"ag_70b": {"769ac3237f10e3e9": 618025472}}  # profiles/ag_70b_persistent_kernel_ncu.md
+NCU_TRAFFIC = {"ag_70b": {"6a3c490d15b78876": 588217600}}  # profiles/ag_70b_persistent_kernel_ncu.md
 
 
 # The sources the AllGather+GEMM kernel is compiled from: its translation unit and every
@@ -62,18 +63,27 @@ AG_KERNEL_SOURCES = ["communication_overlapped_gemm_gb300/csrc/tl_gemm_ops.cu",
                      "include/tl.h"]
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments and with whitespace runs collapsed: a change of
+    documentation does not change the code a profile was taken of.  (String literals in these
+    sources hold no comment markers.)"""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def src_hash(files=None) -> str:
-    """Hash of the given source files (paths from the repository root), by default of every
-    file of the CUDA sources."""
+    """Hash of the code (comments stripped) of the given source files (paths from the
+    repository root), by default of every file of the CUDA sources."""
     if files is None:
         paths = sorted(glob.glob(os.path.join(ROOT, "communication_overlapped_gemm_gb300", "csrc", "*")))
     else:
         paths = [os.path.join(ROOT, f) for f in sorted(files)]
     h = hashlib.sha256()
     for f in paths:
-        with open(f, "rb") as fh:
+        with open(f, encoding="utf-8") as fh:
             h.update(os.path.basename(f).encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -777,25 +787,38 @@ def run_profile(args):
     from seeded_inputs import WORKLOADS, workload_inputs
     torch.cuda.set_device(0)
     device = torch.device("cuda", 0)
-    ctx = tl.Context(0)
     name = args.profile
-    d = WORKLOADS[name].dims
-    inp = workload_inputs(name)
-    if WORKLOADS[name].kind == "ag_gemm":
+    # the communication-alone legs and the low-latency gather run on their workloads' inputs
+    base = {"allgather_70b": "ag_70b", "reduce_scatter_70b": "rs_70b", "ag_tiny_ll": "ag_tiny"}.get(name, name)
+    ctx = tl.Context(0, ag_ll=1) if name == "ag_tiny_ll" else tl.Context(0)
+    d = WORKLOADS[base].dims
+    inp = workload_inputs(base) if name != "reduce_scatter_70b" else None
+    if name == "allgather_70b":
+        a = [dev_bf16(x, device) for x in inp["a_shards"]]
+        ws = torch.zeros(tl.tl_ag_gemm_workspace_bytes(d["W"], d["m_per_rank"], d["n"], d["k"]), dtype=torch.uint8,
+                         device=device)
+        call = lambda: tl.tl_allgather(ctx, a, ws)
+    elif name == "reduce_scatter_70b":
+        # the W fp32 partials of the GEMM+RS workload (values do not matter for the copy's profile)
+        g = torch.Generator(device=device).manual_seed(5)
+        parts = [torch.randn((d["m"], d["n"]), dtype=torch.float32, device=device, generator=g) for _ in range(d["W"])]
+        o = [torch.empty((d["m"] // d["W"], d["n"]), dtype=torch.bfloat16, device=device) for _ in range(d["W"])]
+        call = lambda: tl.tl_reduce_scatter(ctx, parts, o)
+    elif WORKLOADS[base].kind == "ag_gemm":
         a = [dev_bf16(x, device) for x in inp["a_shards"]]
         b = dev_bf16(inp["b"], device)
         c = torch.empty((d["W"] * d["m_per_rank"], d["n"]), dtype=torch.bfloat16, device=device)
         ws = torch.zeros(tl.tl_ag_gemm_workspace_bytes(d["W"], d["m_per_rank"], d["n"], d["k"]), dtype=torch.uint8,
                          device=device)
         call = lambda: tl.tl_ag_gemm(ctx, a, b, c, ws)
-    elif WORKLOADS[name].kind == "gemm_rs":
+    elif WORKLOADS[base].kind == "gemm_rs":
         a = [dev_bf16(x, device) for x in inp["a"]]
         b = [dev_bf16(x, device) for x in inp["b"]]
         o = [torch.empty((d["m"] // d["W"], d["n"]), dtype=torch.bfloat16, device=device) for _ in range(d["W"])]
         ws = torch.zeros(tl.tl_gemm_rs_workspace_bytes(d["W"], d["m"], d["n"], d["k_r"]), dtype=torch.uint8,
                          device=device)
         call = lambda: tl.tl_gemm_rs(ctx, a, b, o, ws)
-    elif WORKLOADS[name].kind == "mlp2":
+    elif WORKLOADS[base].kind == "mlp2":
         x = [dev_bf16(v, device) for v in inp["x_shards"]]
         w1 = [dev_bf16(v, device) for v in inp["w1"]]
         w2 = [dev_bf16(v, device) for v in inp["w2"]]
@@ -803,7 +826,7 @@ def run_profile(args):
         o = [torch.empty((T // W, d["hidden"]), dtype=torch.bfloat16, device=device) for _ in range(W)]
         ws = torch.zeros(tl.tl_mlp2_workspace_bytes(W, T, d["hidden"], d["f_r"]), dtype=torch.uint8, device=device)
         call = lambda: tl.tl_mlp2(ctx, x, w1, w2, o, ws)
-    elif WORKLOADS[name].kind == "ag_attn":
+    elif WORKLOADS[base].kind == "ag_attn":
         q = dev_bf16(inp["q"], device)
         ks = [dev_bf16(x, device) for x in inp["k_shards"]]
         vs = [dev_bf16(x, device) for x in inp["v_shards"]]
@@ -868,7 +891,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work in --impl reference")
     ap.add_argument("--quick", action="store_true", help="headline only (no extra workloads / e2e / overlap)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--profile", choices=["ag_tiny", "ag_70b", "rs_70b", "mlp2_8b", "moe_64e", "attn_16k"],
+    ap.add_argument("--profile", choices=["ag_tiny", "ag_tiny_ll", "ag_70b", "allgather_70b", "rs_70b",
+                                          "reduce_scatter_70b", "mlp2_8b", "moe_64e", "attn_16k"],
                     help="only run this workload's call 4 times (target of an ncu capture), no timing")
     ap.add_argument("--trace", metavar="PATH", help="with --profile: trace one call (after 3 warm-up calls and an "
                     "L2 flush) and write its per-CTA timeline to PATH: Chrome trace JSON, or the decoded spans "

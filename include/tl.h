@@ -212,9 +212,10 @@ int tl_ag_gemm_ll_capable(const tl_ctx* ctx, int W, int m_per_rank, int n, int k
 
 /* ---------------------------------------------------------------- AllGather alone
  * [TD] §3.2 Algorithm 2 (pull-mode one-sided AllGather) as its own kernel: the shard mover of
- * tl_ag_gemm (same chunks, order and signals) without the GEMM, run by four CTAs of 16 warps
- * per SM (alone, the copy has the whole GPU).  Fills the gathered buffer at the start
- * of `workspace` (sized by tl_ag_gemm_workspace_bytes(W, m_per_rank, 8, k)) with all of
+ * tl_ag_gemm (same chunk order and signals, whole-row chunks) without the GEMM, run by four
+ * CTAs of 16 warps per SM, two resident at a time (alone, the copy has the whole GPU).  Fills
+ * the gathered buffer at the start of `workspace` (sized by tl_ag_gemm_workspace_bytes(W,
+ * m_per_rank, 8, k)) with all of
  * [A_0; ...; A_{W-1}], the self rank's shard last, and releases every chunk signal.  Shapes
  * and errors as tl_ag_gemm; W = 1 is a no-op.  This is the "communication alone" leg of the
  * overlap measurement.
