@@ -4,26 +4,43 @@
 // one per rank, gathered while the attention of the rank's queries runs over the shards as
 // they arrive; "Triton-distributed ...", §3.7 swizzle: the local shard first).
 //
-// One persistent cooperative CTA per SM walks (head, 128-query tile) work items; each item
-// is non-causal flash attention over all W shards on tcgen05, head dim 128:
-//   warp 0    TMA producer: the item's Q, then per 128-key block K (2 boxes) and V (4 boxes)
-//             through 2-stage rings; the first block of a remote shard slice waits on the
-//             slice's block signals (one warp-wide poll).
-//   warp 1    TMEM allocation and the MMAs: S_j = Q K_j^T into one of two S buffers, then
-//             O += P_{j-1} V_{j-1} once the softmax warps have published P_{j-1}.
-//   warps 2-5 softmax, one query row per thread: S row from TMEM, running max and sum in
-//             base 2 (the 1/sqrt(d) scale folded into one multiply-add per score), P (bf16)
-//             into one of two shared-memory buffers in the MMA's K-major 128-byte-swizzled
-//             layout.  The running max of a row moves only when the block's max exceeds it
-//             by more than 2^8 (kRescaleLog2): until then P <= 256 and O, l keep the stale
-//             max, which cancels in O / l.  A move rescales the warp's O rows in TMEM after
-//             the previous P V has completed; writing P waits only for the P V two blocks
-//             back.  Finally O / l as bf16.
-//   warps 6-7 movers: remote K/V blocks (up to 32 KB each) into the shard-major gathered
-//             buffers, one release signal per block, the local shard last.
-// The pipeline counters run on across items.  TMEM columns: S0 [0, 128), S1 [128, 256),
-// O [256, 384).  Every wait is bounded.
-// Shard lengths need not be multiples of 128 (the Ragged instantiation): a shard's last key
+// Persistent clusters of two CTAs (one per SM) walk (head, 256-query tile) work items; CTA r
+// of a pair owns queries [128 r, 128 r + 128) of the tile.  Each item is non-causal flash
+// attention over all W shards in blocks of 256 keys, on tcgen05 pair MMAs (cta_group::2):
+//   S_J = Q K_J^T      M = 256 queries, N = 256 keys, K = 128 head dims: CTA r's A is its
+//                      128 query rows, its B half the keys [128 r, 128 r + 128) of the block
+//                      (K-major), and its TMEM gets its rows' 256 scores;
+//   O_g += P_g V_g     for each half g of the block's keys: M = 256 queries, N = 128 head
+//                      dims, K = 128 keys: CTA r's A is its rows of P_g, its B half the head
+//                      dims [64 r, 64 r + 64) of V (MN-major).  The two halves keep separate
+//                      accumulators O_0, O_1 (and separate running max and sum), combined
+//                      once per item: a flash-decoding style split of the keys inside the block.
+// Warps of each CTA:
+//   warp 0     TMA producer: its Q rows, then per key block its K half (2 boxes) and V half
+//              (4 boxes) through 2-stage rings; every load completes on the pair leader's
+//              barrier; the first block of a remote shard slice waits on the slice's block
+//              signals (one warp-wide poll).
+//   warp 1     TMEM allocation (both CTAs); in the leader the pair MMAs (one thread), in the
+//              peer the relay of its softmax warps' arrivals to the leader's barriers.
+//   warps 2-9  softmax, two warpgroups: warpgroup g takes keys [128 g, 128 g + 128) of every
+//              block for all 128 rows (one row per thread), with its own running max m_g and
+//              sum l_g in base 2 (the 1/sqrt(d) scale folded into one multiply-add per score);
+//              P_g (bf16) goes into its half of the shared-memory P buffer in the MMA's
+//              K-major 128-byte-swizzled layout.  The running max of a row moves only when
+//              the block's max exceeds it by more than 2^8 (kRescaleLog2): until then P <= 256
+//              and O_g, l_g keep the stale max, which cancels in the final division; a move
+//              rescales O_g in TMEM after the previous P_g V_g has completed.  At the end of
+//              an item the groups exchange m_g, l_g and each writes 64 head dims of
+//              (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)) as bf16.
+//   warps 10-11 movers: remote K/V blocks (up to 32 KB each) into the shard-major gathered
+//              buffers, one release signal per 128-key block, in the order the items need
+//              them (groups of heads one wave covers, shard by shard, the local shard last).
+// The peer's softmax warps arrive on its own barriers for "S read" and "P_g written" and one
+// relay thread of the peer forwards each phase to the leader's (one cluster-scope arrival
+// instead of eight); the leader's MMA commits arrive on both CTAs' barriers.  TMEM columns (each CTA, its 128 rows): S [0, 256),
+// O_0 [256, 384), O_1 [384, 512).  The pipeline counters run on across items.  Every wait
+// is bounded.
+// Shard lengths need not be multiples of 256 (the Ragged instantiation): a shard's last key
 // block and the last query tile may be partial.  TMA zero-fills the absent rows, the softmax
 // gives the absent keys no weight, and the absent query rows are not stored.
 #include "tl_host.h"
@@ -31,20 +48,25 @@
 namespace tl {
 
 namespace attn {
-constexpr int kD = 128;        // head dim
-constexpr int kBQ = 128;       // queries per work item
-constexpr int kBKV = 128;      // keys per block
-constexpr int kBlk = 16384;    // one 64-column SW128 box of 128 rows
-constexpr int kQBytes = 2 * kBlk;
-constexpr int kKBytes = 2 * kBlk;   // K block: 2 boxes of 64 head-dim columns
-constexpr int kVBytes = 2 * kBlk;   // V block: 4 boxes of 64 keys x 64 head-dim columns
-constexpr int kPBytes = 2 * kBlk;
+constexpr int kD = 128;          // head dim
+constexpr int kBQ = 128;         // queries per CTA (a pair's tile is 256)
+constexpr int kBKV = 256;        // keys per block
+constexpr int kSigBlk = 128;     // keys per mover block (one signal each)
+constexpr int kBox = 16384;      // one 64-column SW128 box of 128 rows
+constexpr int kQBytes = 2 * kBox;   // this CTA's 128 queries x 128 dims
+constexpr int kKBytes = 2 * kBox;   // this CTA's 128 keys of a block x 128 dims
+constexpr int kVBytes = 4 * 8192;   // 256 keys x this CTA's 64 dims: 4 boxes of 64 keys
+constexpr int kPBytes = 4 * kBox;   // 128 rows x 256 keys: 4 boxes of 64 keys
 constexpr int kStages = 2;
-constexpr int kSmem = 1024 + kQBytes + kStages * (kKBytes + kVBytes) + 2 * kPBytes + 256;
+constexpr int kRedBytes = 2 * kBQ * 4;  // one float per row and softmax warpgroup
+constexpr int kBarBytes = 192;
+constexpr int kSmem = 1024 + kQBytes + kStages * (kKBytes + kVBytes) + kPBytes + kRedBytes + kBarBytes;
 constexpr float kRescaleLog2 = 8.0f;  // move the running max once it grows by more than this
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kSoftWarps = 8;
 constexpr int kMovers = 2;
-constexpr int kThreads = (6 + kMovers) * 32;
+constexpr int kThreads = (2 + kSoftWarps + kMovers) * 32;
+static_assert(kSmem <= 232448, "shared memory");
 }  // namespace attn
 
 struct AttnParams {
@@ -59,36 +81,63 @@ struct AttnParams {
   uint8_t* kg;
   uint8_t* vg;
   __nv_bfloat16* out;  // [H, Lq, d]
-  uint64_t* flags;     // [W][H][Lr / 128]: K and V block gathered
+  uint64_t* flags;     // [W][H][ceil(Lr / 128)]: K and V block gathered
   int W, rank, Lq, Lr, heads;
   float scale;  // 1 / sqrt(d)
 };
 
-// S_j = Q K_j^T: M = 128 queries, N = 128 keys, K = 128 head dims (K is a K-major B operand).
+// A 3-D TMA box into this CTA's shared memory, completing on the pair leader's mbarrier
+// (given by its shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x, int y,
+                                                 int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// S_J = Q K_J^T on the pair: M = 256, N = 256, K = 128 (8 steps of 16 head dims).
 __device__ __forceinline__ void attn_mma_s(uint32_t d, uint32_t q0, uint32_t k0) {
-  constexpr uint32_t idesc = umma_idesc_bf16(128, 128, false);
+  constexpr uint32_t idesc = umma_idesc_bf16(256, 256, false);
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      umma_bf16(d, umma_desc_sw128(q0 + kb * attn::kBlk + k * 32, 16, 1024),
-                umma_desc_sw128(k0 + kb * attn::kBlk + k * 32, 16, 1024), idesc, (kb | k) ? 1u : 0u);
+      umma_bf16_pair(d, umma_desc_sw128(q0 + kb * attn::kBox + k * 32, 16, 1024),
+                     umma_desc_sw128(k0 + kb * attn::kBox + k * 32, 16, 1024), idesc, (kb | k) ? 1u : 0u);
 }
 
-// O (+)= P_j V_j: M = 128 queries, N = 128 head dims, K = 128 keys (V is an MN-major B operand,
-// its two 64-column groups 8 KB apart inside a 64-key box pair).
+// O_g (+)= P_g V_g on the pair: M = 256, N = 128, K = 128 keys (8 steps); each CTA's V half
+// is 64 head dims wide (one 64-column group), its 64-key boxes 8 KB apart.
 __device__ __forceinline__ void attn_mma_pv(uint32_t d, uint32_t p0, uint32_t v0, bool acc) {
-  constexpr uint32_t idesc = umma_idesc_bf16(128, 128, true);
+  constexpr uint32_t idesc = umma_idesc_bf16(256, 128, true);
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      umma_bf16(d, umma_desc_sw128(p0 + kb * attn::kBlk + k * 32, 16, 1024),
-                umma_desc_sw128(v0 + kb * attn::kBlk + k * 2048, 8192, 1024), idesc,
-                (acc || kb || k) ? 1u : 0u);
+      umma_bf16_pair(d, umma_desc_sw128(p0 + kb * attn::kBox + k * 32, 16, 1024),
+                     umma_desc_sw128(v0 + kb * 8192 + k * 2048, 8192, 1024), idesc, (acc || kb || k) ? 1u : 0u);
 }
 
-// Ragged: some shard length l_r is not a multiple of 128 (a partial last key block of every
+// Relaxed arrival on an mbarrier given by its shared::cluster address: no memory ordering is
+// implied (a release at cluster scope costs a full memory barrier on every call).  Used where
+// what the arrival announces is already ordered: TMEM reads finished (tcgen05.wait::ld) and,
+// for P, shared-memory writes made visible to the tensor core by fence.proxy.async before the
+// local barrier this thread acquired.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Arrive once on the mbarrier at `bar`'s offset in both CTAs of the pair when every pair MMA
+// issued so far has completed (one multicast commit).
+__device__ __forceinline__ void commit_both(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               ::"r"(smem_u32(bar)), "h"(static_cast<uint16_t>(3))
+               : "memory");
+}
+
+// Ragged: some shard length l_r is not a multiple of 256 (a partial last key block of every
 // shard and a partial last query tile); the common case is compiled without those checks.
 template <bool Ragged>
 __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
@@ -99,25 +148,36 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
   uint8_t* sk = sq + kQBytes;
   uint8_t* sv = sk + kStages * kKBytes;
   uint8_t* sp = sv + kStages * kVBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sp + 2 * kPBytes);
+  float* red = reinterpret_cast<float*>(sp + kPBytes);  // [group][row]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sp + kPBytes + kRedBytes);
+  // counted on the leader (the peer's copies are unused): loads of both CTAs, arrivals of
+  // both CTAs' softmax warps
   uint64_t* qfull = bars;
-  uint64_t* kfull = bars + 1;   // [2]
-  uint64_t* kempty = bars + 3;  // [2]
-  uint64_t* vfull = bars + 5;   // [2]
-  uint64_t* vempty = bars + 7;  // [2]
-  uint64_t* sfull = bars + 9;   // [2] S of block J in TMEM buffer J % 2
-  uint64_t* sfree = bars + 11;  // [2] softmax has read the S buffer
-  uint64_t* pready = bars + 13; // [2] P of block J in buffer J % 2 written, O rescaled
-  uint64_t* pfree = bars + 15;  // [2] P V of block J (P buffer J % 2) complete
-  uint64_t* drain = bars + 17;
-  uint64_t* qempty = bars + 18; // the item's last S MMA has read Q
+  uint64_t* kfull = bars + 1;    // [2]
+  uint64_t* vfull = bars + 3;    // [2]
+  uint64_t* sfree = bars + 5;    // every softmax warp of the pair has read its S half
+  uint64_t* pready = bars + 6;   // [2] group g: its 8 warps of the pair wrote P_g, O_g rescaled
+  // in both CTAs, arrived on by the leader's MMA commits
+  uint64_t* qempty = bars + 8;   // the item's last S MMA has read Q
+  uint64_t* kempty = bars + 9;   // [2]
+  uint64_t* vempty = bars + 11;  // [2]
+  uint64_t* sfull = bars + 13;   // S_J is in TMEM
+  uint64_t* pfree = bars + 14;   // [2] group g: P_g V_g of the block complete (P_g free, O_g stable)
+  uint64_t* drain = bars + 16;
+  // this CTA's softmax warps, once per item
+  uint64_t* xw = bars + 17;      // all 8 wrote their m_g, l_g to red
+  uint64_t* xr = bars + 18;      // all 8 read the other group's
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 19);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const bool leader = crank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const Common& c = p.common;
-  const int bps = (p.Lr + kBKV - 1) / kBKV;  // key blocks per shard (the last may be partial)
-  const int nblk = p.W * bps;                 // key blocks per item
-  const int nqt = (p.Lq + kBQ - 1) / kBQ;     // query tiles (the last may be partial)
+  const int bps = (p.Lr + kBKV - 1) / kBKV;       // 256-key blocks per shard (the last may be partial)
+  const int sbs = (p.Lr + kSigBlk - 1) / kSigBlk;  // 128-key signal blocks per shard
+  const int nblk = p.W * bps;                      // key blocks per item
+  const int nqt = (p.Lq + 2 * kBQ - 1) / (2 * kBQ);  // 256-query tiles (the last may be partial)
   const int nwork = p.heads * nqt;
   if (threadIdx.x == 0) {
     mbar_init(qfull, 1);
@@ -128,13 +188,17 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sfull[s], 1);
-      mbar_init(&sfree[s], 4);
-      mbar_init(&pready[s], 4);
-      mbar_init(&pfree[s], 1);
+    mbar_init(sfull, 1);
+    // The leader's sfree / pready count its own softmax warps plus one relayed arrival from
+    // the peer; the peer's copies count the peer's softmax warps, watched by its relay thread.
+    mbar_init(sfree, kSoftWarps + (leader ? 1 : 0));
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&pready[g], kSoftWarps / 2 + (leader ? 1 : 0));
+      mbar_init(&pfree[g], 1);
     }
     mbar_init(drain, 1);
+    mbar_init(xw, kSoftWarps);
+    mbar_init(xr, kSoftWarps);
     fence_mbar_init();
     tma_prefetch_map(&p.q);
     tma_prefetch_map(&p.k_loc);
@@ -143,27 +207,30 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
     tma_prefetch_map(&p.v_gat);
   }
   if (warp == 1) {
-    tmem_alloc(tslot, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(tslot, 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers and TMEM are ready before any remote arrival or MMA
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  auto lead = [](uint64_t* bar) { return mapa_shared(smem_u32(bar), 0); };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer (both CTAs)
     bool ok = true;
-    uint32_t filled = 0, par = 0;  // K stages (bits 0-1) and V stages (bits 2-3) in flight
+    uint32_t filled = 0, par = 0;  // leader's drain: K stages (bits 0-1), V stages (bits 2-3)
     int J = 0, kq = 0;
-    for (int it = blockIdx.x; it < nwork && ok; it += gridDim.x, ++kq) {
+    for (int it = pair; it < nwork && ok; it += npairs, ++kq) {
       const int h = it / nqt, qt = it - h * nqt;
       if (lane == 0) {
         ok = mbar_wait(qempty, (kq & 1) ^ 1u, c, kSiteEmpty);
         if (ok) {
-          mbar_arrive_expect_tx(qfull, kQBytes);
-          tma_load_3d(sq, &p.q, qfull, 0, qt * kBQ, h);
-          tma_load_3d(sq + kBlk, &p.q, qfull, 64, qt * kBQ, h);
+          if (leader) mbar_arrive_expect_tx(qfull, 2 * kQBytes);
+          const int y = qt * 2 * kBQ + static_cast<int>(crank) * kBQ;
+          tma_load_3d_pair(sq, &p.q, lead(qfull), 0, y, h);
+          tma_load_3d_pair(sq + kBox, &p.q, lead(qfull), 64, y, h);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -173,7 +240,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         const bool local = step == 0;
         if (!local && blk == 0) {
           // consumer_tile_wait on the shard's slice of this head: all its blocks gathered
-          ok = warp_wait_signals(p.flags + (static_cast<size_t>(r) * p.heads + h) * bps, bps, c.epoch, c, lane,
+          ok = warp_wait_signals(p.flags + (static_cast<size_t>(r) * p.heads + h) * sbs, sbs, c.epoch, c, lane,
                                  kSiteSignal, (7ull << 60) | (static_cast<unsigned long long>(r) << 32) | h);
           if (!ok) break;
         }
@@ -186,20 +253,20 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         if (lane == 0) {
           ok = mbar_wait(&kempty[s], ph ^ 1u, c, kSiteEmpty);
           if (ok) {
-            mbar_arrive_expect_tx(&kfull[s], kKBytes);
-            tma_load_3d(sk + s * kKBytes, km, &kfull[s], 0, y, z);
-            tma_load_3d(sk + s * kKBytes + kBlk, km, &kfull[s], 64, y, z);
+            if (leader) mbar_arrive_expect_tx(&kfull[s], 2 * kKBytes);
+            const int yk = y + static_cast<int>(crank) * kBQ;  // this CTA's 128 keys of the block
+            tma_load_3d_pair(sk + s * kKBytes, km, lead(&kfull[s]), 0, yk, z);
+            tma_load_3d_pair(sk + s * kKBytes + kBox, km, lead(&kfull[s]), 64, yk, z);
             filled |= 1u << s;
             par = (par & ~(1u << s)) | (ph << s);
           }
           if (ok) ok = mbar_wait(&vempty[s], ph ^ 1u, c, kSiteEmpty);
           if (ok) {
-            mbar_arrive_expect_tx(&vfull[s], kVBytes);
+            if (leader) mbar_arrive_expect_tx(&vfull[s], 2 * kVBytes);
+            const int xv = static_cast<int>(crank) * 64;  // this CTA's 64 head dims
 #pragma unroll
-            for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-              for (int g = 0; g < 2; ++g)
-                tma_load_3d(sv + s * kVBytes + kb * kBlk + g * 8192, vm, &vfull[s], g * 64, y + kb * 64, z);
+            for (int kb = 0; kb < 4; ++kb)
+              tma_load_3d_pair(sv + s * kVBytes + kb * 8192, vm, lead(&vfull[s]), xv, y + kb * 64, z);
             filled |= 4u << s;
             par = (par & ~(4u << s)) | (ph << (s + 2));
           }
@@ -207,7 +274,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       }
     }
-    if (lane == 0) {  // drain: every fill issued has landed before the CTA exits
+    if (lane == 0 && leader) {  // drain: every fill of both CTAs has landed before the pair exits
       if (kq > 0) mbar_wait(qfull, (kq - 1) & 1, c, kSiteDrain);
       for (int s = 0; s < kStages; ++s) {
         if (filled & (1u << s)) mbar_wait(&kfull[s], (par >> s) & 1u, c, kSiteDrain);
@@ -216,84 +283,121 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (leader && lane == 0) {
       bool ok = true;
       const uint32_t q0 = smem_u32(sq), p0 = smem_u32(sp);
-      const uint32_t to = tmem + 256;
+      const uint32_t ts = tmem, to = tmem + 256;  // S; O_0 (O_1 at + 128)
       int J0 = 0, kq = 0;
-      for (int it = blockIdx.x; it < nwork && ok; it += gridDim.x, ++kq, J0 += nblk) {
+      for (int it = pair; it < nwork && ok; it += npairs, ++kq, J0 += nblk) {
         ok = mbar_wait(qfull, kq & 1, c, kSiteFull);
         tc_fence_after();
         for (int j = 0; j <= nblk && ok; ++j) {
-          if (j < nblk) {  // S of block J0 + j
+          if (j < nblk) {  // S of block J0 + j (S has one TMEM buffer: its last reader is done)
             const int J = J0 + j, s = J & 1;
             const uint32_t ph = (J >> 1) & 1;
-            ok = mbar_wait(&sfree[s], ph ^ 1u, c, kSiteTmemEmpty) && mbar_wait(&kfull[s], ph, c, kSiteFull);
+            ok = (J == 0 || mbar_wait(sfree, (J - 1) & 1, c, kSiteTmemEmpty)) && mbar_wait(&kfull[s], ph, c, kSiteFull);
             if (!ok) break;
             tc_fence_after();
-            attn_mma_s(tmem + s * 128, q0, smem_u32(sk + s * kKBytes));
-            umma_commit(&kempty[s]);
-            umma_commit(&sfull[s]);
-            if (j == nblk - 1) umma_commit(qempty);
+            attn_mma_s(ts, q0, smem_u32(sk + s * kKBytes));
+            commit_both(&kempty[s]);
+            commit_both(sfull);
+            if (j == nblk - 1) commit_both(qempty);
           }
-          if (j >= 1) {  // O += P V of block J0 + j - 1
+          if (j >= 1) {  // O_g += P_g V_g of block J0 + j - 1, g = 0, 1
             const int I = J0 + j - 1, s = I & 1;
             const uint32_t ph = (I >> 1) & 1;
-            ok = mbar_wait(&pready[s], ph, c, kSiteFull) && mbar_wait(&vfull[s], ph, c, kSiteFull);
+            ok = mbar_wait(&vfull[s], ph, c, kSiteFull);
             if (!ok) break;
-            tc_fence_after();
-            attn_mma_pv(to, p0 + s * kPBytes, smem_u32(sv + s * kVBytes), j > 1);
-            umma_commit(&vempty[s]);
-            umma_commit(&pfree[s]);
+#pragma unroll 1
+            for (int g = 0; g < 2 && ok; ++g) {
+              ok = mbar_wait(&pready[g], I & 1, c, kSiteFull);
+              if (!ok) break;
+              tc_fence_after();
+              attn_mma_pv(to + g * 128, p0 + g * 2 * kBox, smem_u32(sv + s * kVBytes) + g * 2 * 8192, j > 1);
+              commit_both(&pfree[g]);
+            }
+            if (!ok) break;
+            commit_both(&vempty[s]);
           }
         }
       }
-      umma_commit(drain);
+      umma_commit_pair(drain);
       mbar_wait(drain, 0, c, kSiteDrain);
+    } else if (!leader && lane == 0) {
+      // Relay: the peer's softmax warps arrive on its own barriers (CTA scope); this thread
+      // forwards each completed phase to the leader's barrier with one cluster-scope arrival,
+      // in the order the phases complete: S read, P_0 written, P_1 written, next block.
+      bool ok = true;
+      int J = 0;
+      for (int it = pair; it < nwork && ok; it += npairs)
+        for (int j = 0; j < nblk && ok; ++j, ++J) {
+          ok = mbar_wait(sfree, J & 1, c, kSitePeer);
+          if (ok) mbar_arrive_cluster_relaxed(lead(sfree));
+          for (int g = 0; g < 2 && ok; ++g) {
+            ok = mbar_wait(&pready[g], J & 1, c, kSitePeer);
+            if (ok) mbar_arrive_cluster_relaxed(lead(&pready[g]));
+          }
+        }
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 2 + kSoftWarps) {
     // ------------------------------------------------------------ softmax (one row per thread)
-    const int qd = warp & 3;               // TMEM lane quadrant of this warp
-    const int row = qd * 32 + lane;        // query row inside the tile
+    const int g = (warp - 2) >> 2;          // warpgroup: keys [128 g, 128 g + 128) of a block
+    const int qd = warp & 3;                // TMEM lane quadrant of this warp
+    const int row = qd * 32 + lane;         // query row inside the CTA's 128
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
-    const float sl2 = p.scale * kLog2e;  // raw score -> base-2 exponent
+    const uint32_t tog = tmem + 256 + g * 128;  // O_g
+    const float sl2 = p.scale * kLog2e;     // raw score -> base-2 exponent
     bool ok = true;
     int J0 = 0;
-    for (int it = blockIdx.x; it < nwork && ok; it += gridDim.x, J0 += nblk) {
+    uint32_t nx = 0;  // exchanges so far
+    // Exchange one float per row with the other warpgroup through red (bounded waits: a
+    // timeout elsewhere never leaves a warp blocked here).
+    auto exchange = [&](float mine, float& other) -> bool {
+      if (nx > 0 && !mbar_wait(xr, (nx - 1) & 1, c, kSiteTmemFull)) return false;  // red is free again
+      red[g * kBQ + row] = mine;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xw);
+      if (!mbar_wait(xw, nx & 1, c, kSiteTmemFull)) return false;
+      other = red[(1 - g) * kBQ + row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xr);
+      ++nx;
+      return true;
+    };
+    for (int it = pair; it < nwork && ok; it += npairs, J0 += nblk) {
       const int h = it / nqt, qt = it - h * nqt;
-      float m2 = -INFINITY, l = 0.f;  // running max (base-2 units) and sum of the row
+      float m2 = -INFINITY, l = 0.f;  // this group's running max (base-2 units) and sum
       int blk = -1;                   // block index inside the current shard
       for (int j = 0; j < nblk && ok; ++j) {
-        const int J = J0 + j, s = J & 1;
+        const int J = J0 + j;
         if (++blk == bps) blk = 0;
-        const uint32_t ph = (J >> 1) & 1;
         // The wait results are warp-uniform, as the warp-collective TMEM accesses below need:
         // the converged warp runs each try_wait and timer read as one instruction.
-        ok = mbar_wait(&sfull[s], ph, c, kSiteTmemFull);
+        ok = mbar_wait(sfull, J & 1, c, kSiteTmemFull);
         if (!ok) break;
         tc_fence_after();
         float x[128];
         {
-          uint32_t r[4][32];
+          uint32_t rr[4][32];
 #pragma unroll
-          for (int cb = 0; cb < 4; ++cb) tmem_ld32_issue(tmem + s * 128 + cb * 32 + lane_off, r[cb]);
-          tmem_ld_wait(r[0]);
-          tmem_ld_after(r[1]);
-          tmem_ld_after(r[2]);
-          tmem_ld_after(r[3]);
+          for (int cb = 0; cb < 4; ++cb) tmem_ld32_issue(tmem + g * 128 + cb * 32 + lane_off, rr[cb]);
+          tmem_ld_wait(rr[0]);
+          tmem_ld_after(rr[1]);
+          tmem_ld_after(rr[2]);
+          tmem_ld_after(rr[3]);
 #pragma unroll
-          for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(r[i >> 5][i & 31]);
+          for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(rr[i >> 5][i & 31]);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sfree[s]);
+        if (lane == 0) mbar_arrive(sfree);
         if constexpr (Ragged) {
           // keys past the end of a shard (its partial last block, zero-filled by TMA) get no
           // weight: their scores become -inf before the maximum
-          const int valid = p.Lr - blk * kBKV;
-          if (valid < kBKV) {
+          const int valid = p.Lr - blk * kBKV - g * 128;
+          if (valid < 128) {
 #pragma unroll
             for (int i = 0; i < 128; ++i) x[i] = i < valid ? x[i] : -INFINITY;
           }
@@ -309,26 +413,27 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           for (int i = 0; i < w; ++i) mx[i] = fmaxf(mx[i], mx[i + w]);
         const float bm2 = mx[0] * sl2;  // the scale is positive: max commutes with it
         if (j == 0) {
-          m2 = bm2;  // the item's first P V overwrites O
+          m2 = bm2;  // the item's first P_g V_g overwrites O_g
         } else if (__any_sync(0xffffffffu, bm2 > m2 + kRescaleLog2)) {
           const float mn = fmaxf(m2, bm2);
-          const float corr = ex2_approx(m2 - mn);
-          // O is stable once the P V of the previous block has completed
-          ok = mbar_wait(&pfree[(J - 1) & 1], ((J - 1) >> 1) & 1, c, kSiteTmemFull);
+          const float corr = ex2_approx(m2 - mn);  // 0 while the group has seen only absent keys
+          // O_g is stable once P_g V_g of the previous block has completed
+          ok = mbar_wait(&pfree[g], (J - 1) & 1, c, kSiteTmemFull);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
           for (int cb = 0; cb < 4; ++cb) {
             float o[32];
-            tmem_ld32(tmem + 256 + cb * 32 + lane_off, o);
+            tmem_ld32(tog + cb * 32 + lane_off, o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= corr;
-            tmem_st32(tmem + 256 + cb * 32 + lane_off, o);
+            tmem_st32(tog + cb * 32 + lane_off, o);
           }
           l *= corr;
           m2 = mn;
         }
-        const float nm = -m2;
+        // (Ragged: a group whose keys so far are all absent has m2 = -inf; its P is 0.)
+        const float nm = (Ragged && m2 == -INFINITY) ? 0.f : -m2;
         float sum[8];
         uint32_t pk[64];
 #pragma unroll
@@ -346,44 +451,55 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
 #pragma unroll
           for (int i = 0; i < w; ++i) sum[i] += sum[i + w];
         l += sum[0];
-        // P buffer s was last read by the P V of block J - 2
-        ok = mbar_wait(&pfree[s], ph ^ 1u, c, kSiteTmemEmpty);
+        // P_g's half of the buffer was last read by P_g V_g of block J - 1
+        if (J > 0) ok = mbar_wait(&pfree[g], (J - 1) & 1, c, kSiteTmemEmpty);
         if (!ok) break;
-        // P (bf16) as the K-major, 128-byte-swizzled A operand: keys [64 kb, 64 kb + 64) of
-        // this row are 128 bytes of box kb; 16-byte piece u sits at piece u ^ (row & 7).
-        const uint32_t prow = smem_u32(sp) + s * kPBytes + row * 128;
+        // P_g (bf16) as the K-major, 128-byte-swizzled A operand: keys [64 b, 64 b + 64) of
+        // this row are 128 bytes of box b; 16-byte piece u sits at piece u ^ (row & 7).
+        const uint32_t prow = smem_u32(sp) + row * 128;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const uint32_t* v = pk + kb * 32 + u * 4;
-            st_shared_v4(prow + kb * kBlk + ((u ^ (row & 7)) << 4), v[0], v[1], v[2], v[3]);
+            st_shared_v4(prow + (2 * g + kb) * kBox + ((u ^ (row & 7)) << 4), v[0], v[1], v[2], v[3]);
           }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pready[s]);
+        if (lane == 0) mbar_arrive(&pready[g]);
       }
-      const int Jl = J0 + nblk - 1;  // the item's last P V
-      if (ok) ok = mbar_wait(&pfree[Jl & 1], (Jl >> 1) & 1, c, kSiteTmemFull);
+      // Both halves' last P V of the item have completed: combine
+      //   O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)),
+      // m = max(m_0, m_1); this group writes head dims [64 g, 64 g + 64).
+      const int Jl = J0 + nblk - 1;
+      if (ok) ok = mbar_wait(&pfree[0], Jl & 1, c, kSiteTmemFull) && mbar_wait(&pfree[1], Jl & 1, c, kSiteTmemFull);
       tc_fence_after();
+      float om = 0.f, ol = 0.f;
+      if (ok) ok = exchange(m2, om) && exchange(l, ol);
       if (ok) {
+        const float m = fmaxf(m2, om);
+        const float a_mine = ex2_approx(m2 - m), a_other = ex2_approx(om - m);
+        const float inv = 1.0f / (l * a_mine + ol * a_other);
+        const float c0 = (g == 0 ? a_mine : a_other) * inv, c1 = (g == 0 ? a_other : a_mine) * inv;
         // Every lane takes part in the (warp-collective) TMEM loads; rows past the end of
         // the queries (a partial last tile) are only not stored.
-        const bool live = !Ragged || qt * kBQ + row < p.Lq;
-        const float inv = 1.0f / l;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(h) * p.Lq + qt * kBQ + row) * kD);
+        const int qrow = qt * 2 * kBQ + static_cast<int>(crank) * kBQ + row;
+        const bool live = !Ragged || qrow < p.Lq;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(h) * p.Lq + qrow) * kD + g * 64);
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
-          float o[32];
-          tmem_ld32(tmem + 256 + cb * 32 + lane_off, o);
+        for (int cb = 0; cb < 2; ++cb) {
+          float o0[32], o1[32];
+          tmem_ld32(tmem + 256 + g * 64 + cb * 32 + lane_off, o0);
+          tmem_ld32(tmem + 384 + g * 64 + cb * 32 + lane_off, o1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o0[i] = o0[i] * c0 + o1[i] * c1;
           if (live) {
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              dst[cb * 4 + u] = make_uint4(pack_bf16x2(o[8 * u] * inv, o[8 * u + 1] * inv),
-                                           pack_bf16x2(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
-                                           pack_bf16x2(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
-                                           pack_bf16x2(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
+              dst[cb * 4 + u] = make_uint4(pack_bf16x2(o0[8 * u], o0[8 * u + 1]), pack_bf16x2(o0[8 * u + 2], o0[8 * u + 3]),
+                                           pack_bf16x2(o0[8 * u + 4], o0[8 * u + 5]),
+                                           pack_bf16x2(o0[8 * u + 6], o0[8 * u + 7]));
           }
         }
       }
@@ -392,41 +508,54 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
     }
   } else {
     // ------------------------------------------------------------ movers
-    // Block g of the gather: shard step i = g / (H bps) taken from rank + 1 on (the local
-    // shard last), head and key block inside it; K and V of the block, then its signal.
+    // The gather in the order the work items need it: heads in groups of hg, the heads that
+    // one wave of items (npairs consecutive items) covers; for each group the shard steps
+    // rank + 1, rank + 2, ... (the local shard last), each over the group's heads and their
+    // 128-key blocks.  K and V of a block, then its signal.  Each lane keeps 16 vectors of
+    // 16 bytes in flight.
+    const int mw = warp - 2 - kSoftWarps;
     const int nw = static_cast<int>(gridDim.x) * kMovers;
-    const int per_step = p.heads * bps;
-    const int total = p.W * per_step;
-    for (int g = blockIdx.x * kMovers + (warp - 6); g < total; g += nw) {
-      const int i = g / per_step, rem = g - i * per_step;
-      const int hh = rem / bps, b = rem - hh * bps;
+    const int hg = (npairs + nqt - 1) / nqt < p.heads ? (npairs + nqt - 1) / nqt : p.heads;
+    const int per_grp = p.W * hg * sbs;
+    const int total = p.W * p.heads * sbs;
+    for (int gb = blockIdx.x * kMovers + mw; gb < total; gb += nw) {
+      const int grp = gb / per_grp;
+      int rem = gb - grp * per_grp;
+      const int gs = p.heads - grp * hg < hg ? p.heads - grp * hg : hg;  // heads in this group
+      const int i = rem / (gs * sbs);
+      rem -= i * gs * sbs;
+      const int hh = grp * hg + rem / sbs, b = rem % sbs;
       const int r = (p.rank + 1 + i) % p.W;
-      const size_t rows = static_cast<size_t>(min(kBKV, p.Lr - b * kBKV));  // the last block may be partial
+      const int rows = min(kSigBlk, p.Lr - b * kSigBlk);  // the last block may be partial
       const size_t row_bytes = static_cast<size_t>(kD) * 2;
-      const size_t src = (static_cast<size_t>(hh) * p.Lr + static_cast<size_t>(b) * kBKV) * row_bytes;
-      const size_t dst = ((static_cast<size_t>(r) * p.heads + hh) * p.Lr + static_cast<size_t>(b) * kBKV) * row_bytes;
-      constexpr size_t kFullVec = static_cast<size_t>(kBKV) * kD * 2 / 16;  // a full block in 16-byte vectors
-      if (!Ragged || rows == static_cast<size_t>(kBKV)) {  // full blocks: a compile-time trip count
-        copy_chunk(reinterpret_cast<const uint4*>(p.kshard[r] + src), reinterpret_cast<uint4*>(p.kg + dst), kFullVec,
-                   lane, 32);
-        copy_chunk(reinterpret_cast<const uint4*>(p.vshard[r] + src), reinterpret_cast<uint4*>(p.vg + dst), kFullVec,
-                   lane, 32);
-      } else {
-        copy_chunk(reinterpret_cast<const uint4*>(p.kshard[r] + src), reinterpret_cast<uint4*>(p.kg + dst),
-                   rows * row_bytes / 16, lane, 32);
-        copy_chunk(reinterpret_cast<const uint4*>(p.vshard[r] + src), reinterpret_cast<uint4*>(p.vg + dst),
-                   rows * row_bytes / 16, lane, 32);
+      const size_t src = (static_cast<size_t>(hh) * p.Lr + static_cast<size_t>(b) * kSigBlk) * row_bytes;
+      const size_t dst = ((static_cast<size_t>(r) * p.heads + hh) * p.Lr + static_cast<size_t>(b) * kSigBlk) * row_bytes;
+      const int nvec = (Ragged ? rows : kSigBlk) * static_cast<int>(row_bytes / 16);
+#pragma unroll 1
+      for (int t = 0; t < 2; ++t) {  // K, then V
+        const uint4* s4 = reinterpret_cast<const uint4*>((t ? p.vshard[r] : p.kshard[r]) + src);
+        uint4* d4 = reinterpret_cast<uint4*>((t ? p.vg : p.kg) + dst);
+        for (int v0 = lane; v0 < nvec; v0 += 16 * 32) {
+          uint4 buf[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            if (v0 + u * 32 < nvec) buf[u] = __ldg(s4 + v0 + u * 32);
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            if (v0 + u * 32 < nvec) d4[v0 + u * 32] = buf[u];
+        }
       }
       __threadfence();
       __syncwarp();
-      if (lane == 0) st_release_gpu(p.flags + (static_cast<size_t>(r) * p.heads + hh) * bps + b, c.epoch);
+      if (lane == 0) st_release_gpu(p.flags + (static_cast<size_t>(r) * p.heads + hh) * sbs + b, c.epoch);
     }
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the leader's MMAs are drained and both CTAs are done with TMEM and remote barriers
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -445,7 +574,7 @@ static bool attn_shape_ok(int W, int heads, int l_r, int d) {
 extern "C" size_t tl_ag_attention_workspace_bytes(int W, int heads, int l_r, int d) {
   if (!attn_shape_ok(W, heads, l_r, d)) return 0;
   const size_t kv = static_cast<size_t>(heads) * W * l_r * d * 2;
-  const size_t flags = static_cast<size_t>(W) * heads * ((l_r + attn::kBKV - 1) / attn::kBKV) * 8;
+  const size_t flags = static_cast<size_t>(W) * heads * ((l_r + attn::kSigBlk - 1) / attn::kSigBlk) * 8;
   return 2 * attn_al256(kv) + attn_al256(flags);
 }
 
@@ -491,29 +620,40 @@ extern "C" int tl_ag_attention(tl_ctx* ctx, int W, int rank, const void* q, cons
   p.heads = heads;
   p.scale = 1.0f / sqrtf(static_cast<float>(d));
 
-  // One cooperative CTA per SM: a CTA waiting on a block's signal is co-resident with the
-  // mover warps that will set it.
+  // Clusters of two CTAs, one CTA per SM, no more clusters than can be resident at once: a
+  // CTA waiting on a block's signal is co-resident with the mover warps that will set it.
   auto kern = l_r % attn::kBKV == 0 ? attn_kernel<false> : attn_kernel<true>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmem) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ctx->ctas, 1, 1);
   cfg.blockDim = dim3(attn::kThreads, 1, 1);
   cfg.dynamicSmemBytes = attn::kSmem;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
-  if (e == cudaErrorCooperativeLaunchTooLarge) {
-    (void)cudaGetLastError();
-    return TL_ERR_UNSUPPORTED;
+  static int max_clusters[2] = {-1, -1};  // per instantiation
+  const int ki = l_r % attn::kBKV == 0 ? 0 : 1;
+  if (max_clusters[ki] < 0) {
+    cfg.gridDim = dim3(ctx->sms & ~1, 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      return TL_ERR_UNSUPPORTED;
+    }
+    max_clusters[ki] = n;
   }
-  if (e != cudaSuccess) {
+  int nclusters = ctx->ctas / 2;
+  if (nclusters > max_clusters[ki]) nclusters = max_clusters[ki];
+  if (nclusters < 1) return TL_ERR_UNSUPPORTED;
+  cfg.gridDim = dim3(2 * nclusters, 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_CUDA;
   }
