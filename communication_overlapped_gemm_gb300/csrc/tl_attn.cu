@@ -120,6 +120,32 @@ __device__ __forceinline__ void attn_mma_pv(uint32_t d, uint32_t p0, uint32_t v0
                      umma_desc_sw128(v0 + kb * 8192 + k * 2048, 8192, 1024), idesc, (acc || kb || k) ? 1u : 0u);
 }
 
+// Paired fp32 arithmetic (two lanes of one 64-bit register pair per instruction) and the
+// three-input maximum: the softmax issues about a third fewer instructions per score.
+__device__ __forceinline__ unsigned long long f2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Relaxed arrival on an mbarrier given by its shared::cluster address: no memory ordering is
 // implied (a release at cluster scope costs a full memory barrier on every call).  Used where
 // what the arrival announces is already ordered: TMEM reads finished (tcgen05.wait::ld) and,
@@ -406,12 +432,11 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = x[i];
 #pragma unroll
-        for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+        for (int i = 8; i < 128; i += 16)
 #pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) mx[i] = fmaxf(mx[i], mx[i + w]);
-        const float bm2 = mx[0] * sl2;  // the scale is positive: max commutes with it
+          for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], x[i + k], x[i + 8 + k]);
+        const float bm2 = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+                          sl2;  // the scale is positive: max commutes with it
         if (j == 0) {
           m2 = bm2;  // the item's first P_g V_g overwrites O_g
         } else if (__any_sync(0xffffffffu, bm2 > m2 + kRescaleLog2)) {
@@ -434,23 +459,25 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         }
         // (Ragged: a group whose keys so far are all absent has m2 = -inf; its P is 0.)
         const float nm = (Ragged && m2 == -INFINITY) ? 0.f : -m2;
-        float sum[8];
+        unsigned long long sum2[4];  // 8 partial sums, two per register pair
         uint32_t pk[64];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sum[i] = 0.f;
+        for (int i = 0; i < 4; ++i) sum2[i] = 0ull;
+        const unsigned long long sl2x2 = f2(sl2, sl2), nm2 = f2(nm, nm);
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          const float e0 = ex2_approx(fmaf(x[2 * i], sl2, nm));
-          const float e1 = ex2_approx(fmaf(x[2 * i + 1], sl2, nm));
-          sum[(2 * i) & 7] += e0;
-          sum[(2 * i + 1) & 7] += e1;
+          float y0, y1;
+          f2_split(ffma2(f2(x[2 * i], x[2 * i + 1]), sl2x2, nm2), y0, y1);
+          const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
+          sum2[i & 3] = fadd2(sum2[i & 3], f2(e0, e1));
           pk[i] = pack_bf16x2(e0, e1);
         }
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) sum[i] += sum[i + w];
-        l += sum[0];
+        {
+          const unsigned long long s2 = fadd2(fadd2(sum2[0], sum2[1]), fadd2(sum2[2], sum2[3]));
+          float a, b;
+          f2_split(s2, a, b);
+          l += a + b;
+        }
         // P_g's half of the buffer was last read by P_g V_g of block J - 1
         if (J > 0) ok = mbar_wait(&pfree[g], (J - 1) & 1, c, kSiteTmemEmpty);
         if (!ok) break;
