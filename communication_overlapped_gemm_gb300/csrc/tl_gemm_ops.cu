@@ -360,8 +360,10 @@ struct AgOp : OpBase<AgParams> {
   // consumer_tile_wait: the k-blocks of K part q of a remote row block are read only after
   // the part's chunks of its BM/128 slabs (this CTA's slab, on a pair) have been released.
   static __device__ void wait_deps(const Params& p, const Job& j, int kb, int lane) {
-    if (j.a_sel == 0 || kb % p.kb_q != 0) return;
-    const int q = kb / p.kb_q;
+    // K part q of a gathered row block before its first k-block (at most 4 parts; no division
+    // here: the producer warp's per-k-block work is on the pipeline's critical path)
+    if (j.a_sel == 0 || (kb != 0 && kb != p.kb_q && kb != 2 * p.kb_q && kb != 3 * p.kb_q)) return;
+    const int q = kb == 0 ? 0 : kb == p.kb_q ? 1 : kb == 2 * p.kb_q ? 2 : 3;
     constexpr int kSlabs = Pair ? 1 : BM / 128;  // 128-row slabs this CTA reads
     const int slab0 = j.x1 * (BM / 128) + (Pair ? j.rank : 0);
 #pragma unroll
