@@ -622,14 +622,8 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
   __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
 
-  moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, ctx->cfg.moe_renorm, experts, gates);
-  const int zero_ctas = ctx->sms > E ? ctx->sms - E : 1;
-  moe_permute_kernel<<<E + zero_ctas, 1024, 0, st>>>(experts, T * topk, E, topk, gates, perm, row_meta, tile_expert,
-                                                     tile_rows, num_mtiles, counts, perm_out, counts_out,
-                                                     reinterpret_cast<float4*>(out),
-                                                     static_cast<size_t>(T) * H / 4);
-  if (cudaGetLastError() != cudaSuccess) return TL_ERR_CUDA;
-
+  // The persistent kernel's parameters and tensor maps first, so that its launch follows the
+  // routing and permutation launches without host work in between.
   MoeParams p;
   std::memset(&p, 0, sizeof(p));
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -662,6 +656,14 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   p.combine_ctas = ctx->cfg.combine_ctas;
   p.chunk = 2;  // row tiles per chunk
   p.lag = 6;    // chunks of up work ahead of the down chunk that reads them
+  moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, ctx->cfg.moe_renorm, experts, gates);
+  const int zero_ctas = ctx->sms > E ? ctx->sms - E : 1;
+  moe_permute_kernel<<<E + zero_ctas, 1024, 0, st>>>(experts, T * topk, E, topk, gates, perm, row_meta, tile_expert,
+                                                     tile_rows, num_mtiles, counts, perm_out, counts_out,
+                                                     reinterpret_cast<float4*>(out),
+                                                     static_cast<size_t>(T) * H / 4);
+  if (cudaGetLastError() != cudaSuccess) return TL_ERR_CUDA;
+
   // Two extra warps per CTA: the token gather in the GEMM partition, combine workers in the
   // combine CTAs.
   return launch_persistent<MoeOp>(ctx, p, st, 2);
