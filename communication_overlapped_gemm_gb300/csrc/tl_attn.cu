@@ -20,8 +20,7 @@
 //              (4 boxes) through 2-stage rings; every load completes on the pair leader's
 //              barrier; the first block of a remote shard slice waits on the slice's block
 //              signals (one warp-wide poll).
-//   warp 1     TMEM allocation (both CTAs); in the leader the pair MMAs (one thread), in the
-//              peer the relay of its softmax warps' arrivals to the leader's barriers.
+//   warp 1     TMEM allocation (both CTAs) and, in the leader, the pair MMAs (one thread).
 //   warps 2-9  softmax, two warpgroups: warpgroup g takes keys [128 g, 128 g + 128) of every
 //              block for all 128 rows (one row per thread), with its own running max m_g and
 //              sum l_g in base 2 (the 1/sqrt(d) scale folded into one multiply-add per score);
@@ -35,9 +34,10 @@
 //   warps 10-11 movers: remote K/V blocks (up to 32 KB each) into the shard-major gathered
 //              buffers, one release signal per 128-key block, in the order the items need
 //              them (groups of heads one wave covers, shard by shard, the local shard last).
-// The peer's softmax warps arrive on its own barriers for "S read" and "P_g written" and one
-// relay thread of the peer forwards each phase to the leader's (one cluster-scope arrival
-// instead of eight); the leader's MMA commits arrive on both CTAs' barriers.  TMEM columns (each CTA, its 128 rows): S [0, 256),
+// The softmax warps of both CTAs arrive on the leader's barriers for "S read" and "P_g
+// written" (relaxed cluster-scope arrivals: a release at cluster scope costs a full memory
+// barrier per arrival); the leader's MMA commits arrive on both CTAs' barriers (one
+// multicast commit).  TMEM columns (each CTA, its 128 rows): S [0, 256),
 // O_0 [256, 384), O_1 [384, 512).  The pipeline counters run on across items.  Every wait
 // is bounded.
 // Shard lengths need not be multiples of 256 (the Ragged instantiation): a shard's last key
@@ -148,9 +148,9 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 // Relaxed arrival on an mbarrier given by its shared::cluster address: no memory ordering is
 // implied (a release at cluster scope costs a full memory barrier on every call).  Used where
-// what the arrival announces is already ordered: TMEM reads finished (tcgen05.wait::ld) and,
-// for P, shared-memory writes made visible to the tensor core by fence.proxy.async before the
-// local barrier this thread acquired.
+// what the arrival announces is already complete in this thread: its TMEM reads
+// (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync) or its P stores, made visible to
+// the tensor core by fence.proxy.async before the arrival.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
@@ -215,11 +215,9 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
       mbar_init(&vempty[s], 1);
     }
     mbar_init(sfull, 1);
-    // The leader's sfree / pready count its own softmax warps plus one relayed arrival from
-    // the peer; the peer's copies count the peer's softmax warps, watched by its relay thread.
-    mbar_init(sfree, kSoftWarps + (leader ? 1 : 0));
+    mbar_init(sfree, 2 * kSoftWarps);  // counted on the leader: the softmax warps of both CTAs
     for (int g = 0; g < 2; ++g) {
-      mbar_init(&pready[g], kSoftWarps / 2 + (leader ? 1 : 0));
+      mbar_init(&pready[g], kSoftWarps);  // the 4 warps of group g in each CTA
       mbar_init(&pfree[g], 1);
     }
     mbar_init(drain, 1);
@@ -350,21 +348,6 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
       }
       umma_commit_pair(drain);
       mbar_wait(drain, 0, c, kSiteDrain);
-    } else if (!leader && lane == 0) {
-      // Relay: the peer's softmax warps arrive on its own barriers (CTA scope); this thread
-      // forwards each completed phase to the leader's barrier with one cluster-scope arrival,
-      // in the order the phases complete: S read, P_0 written, P_1 written, next block.
-      bool ok = true;
-      int J = 0;
-      for (int it = pair; it < nwork && ok; it += npairs)
-        for (int j = 0; j < nblk && ok; ++j, ++J) {
-          ok = mbar_wait(sfree, J & 1, c, kSitePeer);
-          if (ok) mbar_arrive_cluster_relaxed(lead(sfree));
-          for (int g = 0; g < 2 && ok; ++g) {
-            ok = mbar_wait(&pready[g], J & 1, c, kSitePeer);
-            if (ok) mbar_arrive_cluster_relaxed(lead(&pready[g]));
-          }
-        }
     }
     __syncwarp();
   } else if (warp < 2 + kSoftWarps) {
@@ -418,7 +401,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sfree);
+        if (lane == 0) mbar_arrive_cluster_relaxed(lead(sfree));
         if constexpr (Ragged) {
           // keys past the end of a shard (its partial last block, zero-filled by TMA) get no
           // weight: their scores become -inf before the maximum
@@ -494,7 +477,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pready[g]);
+        if (lane == 0) mbar_arrive_cluster_relaxed(lead(&pready[g]));
       }
       // Both halves' last P V of the item have completed: combine
       //   O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)),
