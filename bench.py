@@ -319,6 +319,14 @@ def overlap_ag(tl, ctx, a, b, c, ws, flush, stream, device, fused_times, W, mpr,
         tl.tl_allgather(ctx, a, ws, rank=0, stream=stream)
     t_copy = statistics.median(timed_steps(lambda: tl.tl_allgather(ctx, a, ws, rank=0, stream=stream), reps,
                                            flush, stream))
+    # the same AllGather on the TMA units (bulk copies, one thread per SM): the copy-engine mover
+    with tl.Context(ctx.device, mover_tma=1) as ct:
+        for _ in range(3):
+            tl.tl_allgather(ct, a, ws, rank=0, stream=stream)
+        t_copy_tma = statistics.median(timed_steps(lambda: tl.tl_allgather(ct, a, ws, rank=0, stream=stream), reps,
+                                                   flush, stream))
+        if ct.check() != tl.TL_OK:
+            raise RuntimeError("tl_allgather (mover_tma): device status not OK")
     # GEMM alone: the same engine on the already-gathered operand (W = 1, no signals)
     gath = ws[: W * mpr * k * 2].view(torch.bfloat16).view(W * mpr, k)
     ws1 = torch.zeros(tl.tl_ag_gemm_workspace_bytes(1, W * mpr, n, k), dtype=torch.uint8, device=device)
@@ -334,6 +342,8 @@ def overlap_ag(tl, ctx, a, b, c, ws, flush, stream, device, fused_times, W, mpr,
         "efficiency": round((t_copy + t_gemm - t_fused) / min(t_copy, t_gemm), 4),
         "copy_alone_gbs": round(moved / (t_copy * 1e-3) / 1e9, 1),
         "copy_alone_hbm_frac": round(moved / (t_copy * 1e-3) / 1e9 / pk["hbm"], 4),
+        "copy_alone_tma_us": round(t_copy_tma * 1e3, 2),
+        "copy_alone_tma_hbm_frac": round(moved / (t_copy_tma * 1e-3) / 1e9 / pk["hbm"], 4),
         "gemm_alone_tflops": round(ag_flops(W, mpr, n, k) / (t_gemm * 1e-3) / 1e12, 2),
         "gemm_alone_frac": round(ag_flops(W, mpr, n, k) / (t_gemm * 1e-3) / 1e12 / pk["bf16"], 4),
     }

@@ -61,6 +61,7 @@ class Config(ctypes.Structure):
         ("ag_push", _i),
         ("mover_kparts", _i),
         ("ag_ll", _i),
+        ("mover_tma", _i),
     ]
 
 

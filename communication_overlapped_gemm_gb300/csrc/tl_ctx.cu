@@ -88,6 +88,7 @@ int tl_config_default(tl_config* cfg) {
   cfg->ag_push = 0;
   cfg->mover_kparts = 0;
   cfg->ag_ll = 0;
+  cfg->mover_tma = 0;
   return TL_OK;
 }
 
@@ -106,7 +107,7 @@ int tl_ctx_create(tl_ctx** out, int device, const tl_config* cfg) {
       c.pair_ctas < 0 || c.pair_ctas > 2 || (c.moe_renorm != 0 && c.moe_renorm != 1) ||
       (c.rs_ring != 0 && c.rs_ring != 1) || (c.ag_push != 0 && c.ag_push != 1) ||
       (c.mover_kparts != 0 && c.mover_kparts != 1 && c.mover_kparts != 2 && c.mover_kparts != 4) ||
-      (c.ag_ll != 0 && c.ag_ll != 1))
+      (c.ag_ll != 0 && c.ag_ll != 1) || (c.mover_tma != 0 && c.mover_tma != 1))
     return TL_ERR_INVALID;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) {

@@ -714,6 +714,118 @@ __global__ void __launch_bounds__(kAllgatherWarps * 32, 2) allgather_kernel(cons
   }
 }
 
+// The same AllGather moved by the TMA unit instead of the SMs' load/store path (the
+// copy-engine mover of the pages' AG, "TileLink ...", §7.2, in its GB300 form: each SM's own
+// bulk-copy engine): one thread per CTA streams its chunks through kTmaStages shared-memory
+// stages of kTmaStage bytes, a bulk load (completing on the stage's mbarrier) then a bulk
+// store, and releases a chunk's signal once every store of it has completed.  Same chunk
+// order and signals as allgather_kernel.
+constexpr int kTmaStages = 6;
+constexpr int kTmaStage = 32768;
+constexpr int kTmaSmem = kTmaStages * kTmaStage + kTmaStages * 8 + 128;
+
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store_1d(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+               "r"(bytes)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(32, 1) allgather_tma_kernel(const __grid_constant__ AgParams p) {
+  extern __shared__ __align__(128) uint8_t tsm[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tsm + kTmaStages * kTmaStage);
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < kTmaStages; ++s) mbar_init(&bars[s], 1);
+  fence_mbar_init();
+  const Common& c = p.common;
+  const int per_shard = p.spr * p.chunks;
+  const int total = p.W * per_shard;
+  const size_t piece_bytes = static_cast<size_t>(tl::kBM / p.chunks) * p.k * 2;
+  const int subs = static_cast<int>((piece_bytes + kTmaStage - 1) / kTmaStage);  // stage-sized parts per chunk
+  const int mine = total > static_cast<int>(blockIdx.x) ? (total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int njobs = mine * subs;  // this CTA's bulk copies: chunk blockIdx.x + t * grid, part sp
+  // job j -> its chunk's shard slot offset, the part's offset and size
+  auto where = [&](int j, const uint8_t*& src, uint8_t*& dst, uint32_t& bytes, uint64_t*& flag) {
+    const int t = j / subs, sp = j - t * subs;
+    const int g = blockIdx.x + t * gridDim.x;
+    const int i = g / per_shard, rem = g - i * per_shard;
+    const int r = ag_mover_rank(p.W, p.rank, p.swizzle, i);
+    const size_t o = static_cast<size_t>(rem) * piece_bytes + static_cast<size_t>(sp) * kTmaStage;
+    const size_t left = piece_bytes - static_cast<size_t>(sp) * kTmaStage;
+    src = p.shard[r] + o;
+    dst = p.gath + static_cast<size_t>(r) * p.shard_bytes + o;
+    bytes = static_cast<uint32_t>(left < kTmaStage ? left : kTmaStage);
+    flag = (sp == subs - 1 && g != p.skip_chunk) ? p.flags + static_cast<size_t>(r) * per_shard + rem : nullptr;
+  };
+  auto load = [&](int j) {
+    const uint8_t* src;
+    uint8_t* dst;
+    uint32_t bytes;
+    uint64_t* flag;
+    where(j, src, dst, bytes, flag);
+    const int s = j % kTmaStages;
+    mbar_arrive_expect_tx(&bars[s], bytes);
+    bulk_load_1d(tsm + s * kTmaStage, src, bytes, &bars[s]);
+  };
+  // signals of chunks whose last store is issued but not yet known complete, oldest first
+  constexpr int kPend = kTmaStages + 1;
+  uint64_t* pend_flag[kPend];
+  int pend_last[kPend];
+  int npend = 0;
+  auto retire = [&](int upto) {  // release the chunks whose last store is job <= upto
+    int k = 0;
+    while (k < npend && pend_last[k] <= upto) ++k;
+    if (k == 0) return;
+    fence_proxy_async_global();
+    for (int i = 0; i < k; ++i) st_release_gpu(pend_flag[i], c.epoch);
+    for (int i = k; i < npend; ++i) {
+      pend_flag[i - k] = pend_flag[i];
+      pend_last[i - k] = pend_last[i];
+    }
+    npend -= k;
+  };
+  // loads run kTmaStages - 1 jobs ahead of the stores
+  for (int j = 0; j < njobs && j < kTmaStages - 1; ++j) load(j);
+  bool ok = true;
+  for (int j = 0; j < njobs && ok; ++j) {
+    const int s = j % kTmaStages;
+    ok = mbar_wait(&bars[s], (j / kTmaStages) & 1, c, kSiteFull);
+    if (!ok) break;
+    const uint8_t* src;
+    uint8_t* dst;
+    uint32_t bytes;
+    uint64_t* flag;
+    where(j, src, dst, bytes, flag);
+    bulk_store_1d(dst, tsm + s * kTmaStage, bytes);
+    bulk_commit();
+    if (flag) {
+      if (npend == kPend) {  // more chunks in flight than slots: drain the oldest first
+        bulk_wait<0>();
+        retire(j);
+      }
+      pend_flag[npend] = flag;
+      pend_last[npend] = j;
+      ++npend;
+    }
+    const int jn = j + kTmaStages - 1;  // the next load goes into the stage store j - 1 read
+    if (jn < njobs) {
+      bulk_wait_read<1>();
+      load(jn);
+    }
+    if ((j % kTmaStages) == kTmaStages - 1) {  // every kTmaStages jobs: release what has landed
+      bulk_wait<kTmaStages - 1>();
+      retire(j - (kTmaStages - 1));
+    }
+  }
+  bulk_wait<0>();  // every store has completed (and nothing reads shared memory any more)
+  retire(njobs);
+}
+
 // ============================================================================ ReduceScatter alone
 // The push-mode ReduceScatter of "Triton-distributed ...", §3.3 Algorithm 3, as its own
 // kernel: each owner o receives rows [o*m/W, (o+1)*m/W) of the W ranks' fp32 partials and
@@ -1087,6 +1199,15 @@ extern "C" int tl_allgather(tl_ctx* ctx, int W, int rank, const void* const* a_s
   // Alone, the copy has the whole GPU: TL_AG_ALONE_CTAS_PER_SM CTAs of kAllgatherWarps warps
   // per SM (two resident at a time), so one CTA's fence and barrier after a chunk overlap the
   // other CTA's loads.
+  if (ctx->cfg.mover_tma) {
+    if (cudaFuncSetAttribute(allgather_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmem) !=
+        cudaSuccess) {
+      (void)cudaGetLastError();
+      return TL_ERR_CUDA;
+    }
+    allgather_tma_kernel<<<ctx->sms, 32, kTmaSmem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    return cudaGetLastError() == cudaSuccess ? TL_OK : TL_ERR_CUDA;
+  }
   p.common.mover_warps = kAllgatherWarps;
   allgather_kernel<<<ctx->ctas * TL_AG_ALONE_CTAS_PER_SM, kAllgatherWarps * 32, 0,
                      reinterpret_cast<cudaStream_t>(stream)>>>(p);

@@ -110,6 +110,11 @@ typedef struct tl_config {
                                  slabs and each tile reads them straight into its operand
                                  buffer, with no separate signal or fence.  For small problems
                                  only (tl_ag_gemm_ll_capable); otherwise TL_ERR_UNSUPPORTED  */
+  int mover_tma;              /* tl_allgather's copy engine: 0 (default) the SMs' load/store path
+                                 (16-byte vectors, several CTAs of copy warps per SM); 1 the TMA
+                                 unit of each SM (bulk copies through shared-memory stages, one
+                                 issuing thread per SM): the pages' copy-engine mover ([TL]
+                                 §7.2) in its GB300 form.  Same result and signals.          */
 } tl_config;
 
 typedef struct tl_ctx tl_ctx;

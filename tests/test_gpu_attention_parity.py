@@ -45,10 +45,14 @@ def test_ag_attention_matches_oracle(W, H, L, rank):
     assert np.array_equal(np.concatenate(list(kg), axis=1), oracle.attn_gather(inp["k_shards"]))
 
 
-@pytest.mark.parametrize("W,H,L,rank", [(3, 2, 200, 1), (2, 1, 100, 0), (1, 1, 72, 0), (4, 2, 130, 3)])
+@pytest.mark.parametrize("W,H,L,rank", [(3, 2, 200, 1), (2, 1, 100, 0), (1, 1, 72, 0), (4, 2, 130, 3),
+                                        (2, 1, 300, 1), (3, 2, 520, 2), (2, 3, 384, 0)])
 def test_ag_attention_ragged_lengths(W, H, L, rank):
-    """Shard lengths that are not a multiple of 128: each shard's last key block and the last
-    query tile are partial (the absent keys get no weight, the absent rows are not stored)."""
+    """Shard lengths that are not a multiple of the 256-key block: each shard's last key block
+    and the last 256-query tile are partial (the absent keys get no weight, the absent rows are
+    not stored).  Below 128 the second key half of every block is absent for all rows (its
+    group keeps a running max of -inf); 300 and 520 have full blocks before the partial one;
+    384 ends half-way through a block and a query tile."""
     inp = make_inputs("ag_attn", 97 + L, W=W, heads=H, l_r=L, d=128)
     out, kg = run_attn(inp, rank=rank)
     ref = oracle.ag_attention(inp["q"], inp["k_shards"], inp["v_shards"])

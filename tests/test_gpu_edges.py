@@ -21,21 +21,34 @@ def ctx():
     c.close()
 
 
-@pytest.mark.parametrize("W,mpr,k,rank", [(3, 256, 328, 2), (8, 128, 64, 5), (1, 384, 136, 0)])
-def test_standalone_allgather_is_bit_exact(ctx, W, mpr, k, rank):
+@pytest.mark.parametrize("W,mpr,k,rank", [(3, 256, 328, 2), (8, 128, 64, 5), (1, 384, 136, 0), (4, 256, 8192, 1),
+                                        (2, 128, 2056, 0)])
+@pytest.mark.parametrize("tma", [0, 1])
+def test_standalone_allgather_is_bit_exact(W, mpr, k, rank, tma):
+    """Both copy engines (the SMs' load/store path and the TMA unit's bulk copies): the gathered
+    buffer is the rank-order concatenation bit for bit, and every chunk signal carries the
+    call's value.  k = 8192 makes a chunk (4 rows) two 32 KB bulk copies; k = 2056 a chunk
+    that is not a whole number of 32 KB stages."""
     import torch
     inp = make_inputs("ag_gemm", 200 + W, W=W, m_per_rank=mpr, n=64, k=k)
     a = [to_dev_bf16(x) for x in inp["a_shards"]]
     ws = workspace(tl.tl_ag_gemm_workspace_bytes(W, mpr, 8, k))
-    tl.tl_allgather(ctx, a, ws, rank=rank)
-    torch.cuda.synchronize()
-    assert ctx.check() == tl.TL_OK
+    with tl.Context(0, mover_tma=tma) as c2:
+        for _ in range(2):  # a second call on the same workspace: the signals move to the new value
+            tl.tl_allgather(c2, a, ws, rank=rank)
+        torch.cuda.synchronize()
+        assert c2.check() == tl.TL_OK
     gath = oracle.ag_gather_bits(inp["a_shards"])
     got = bf16_bits(ws[: gath.size * 2].view(torch.bfloat16).view(gath.shape))
     if W == 1:  # nothing to gather: a no-op, the zero-filled region stays zero
         assert not got.any()
-    else:
-        assert np.array_equal(got, gath)
+        return
+    assert np.array_equal(got, gath)
+    # every chunk signal (W shards x m_per_rank/128 slabs x 32 chunks) holds one and the same
+    # nonzero value, the second call's
+    off = (gath.size * 2 + 255) // 256 * 256
+    sig = ws[off: off + W * (mpr // 128) * 32 * 8].view(torch.int64).cpu().numpy()
+    assert sig.min() == sig.max() and sig[0] != 0
 
 
 def test_empty_problems_are_noops(ctx):
