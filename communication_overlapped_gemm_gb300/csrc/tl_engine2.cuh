@@ -7,13 +7,13 @@
 // Each SM thus streams half of B per MMA (the pair shares the B slice) and keeps two
 // 256-column accumulators, so one tile's epilogue overlaps the next tile's MMAs.
 //
-// Pair signalling, no multicast of any kind:
+// Pair signalling (no data multicast; each CTA loads its own operands):
 //   full[s]    leader only: its producer's arrive.expect_tx of both halves' bytes; both
 //              CTAs' TMA loads of stage s complete_tx on it (cp.async.bulk.tensor with
 //              .cta_group::2 and the leader's barrier address from mapa).
-//   empty[s]   both: the leader's MMA warp commits twice per stage, once to its own
-//              barrier and once to the peer's (tcgen05.commit to a shared::cluster address).
-//   tfull[a]   both: likewise, two commits per tile.
+//   empty[s]   both: the leader's MMA warp commits once per stage with the multicast form
+//              of tcgen05.commit, arriving on the barrier at the same offset in both CTAs.
+//   tfull[a]   both: likewise, one commit per tile.
 //   tempty[a]  leader only: 4 local + 4 peer epilogue warps arrive (peer remotely).
 // Every wait is bounded as in the single-CTA engine.
 #pragma once
@@ -111,8 +111,6 @@ __device__ __forceinline__ void pair_mma(const typename Op::Params& p, const Sme
   if (rank != 0) return;
   const Common& c = p.common;
   const int ntiles = Op::num_tiles(p);
-  const uint32_t peer_empty0 = mapa_shared(smem_u32(&sm.empty[0]), 1);
-  const uint32_t peer_tfull0 = mapa_shared(smem_u32(&sm.tfull[0]), 1);
   uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
   bool ok = true;
   constexpr bool tr = Trace;
@@ -133,16 +131,14 @@ __device__ __forceinline__ void pair_mma(const typename Op::Params& p, const Sme
         if (!ok) break;
         tc_fence_after();
         mma_stage_pair(d, smem_u32(sm.a(stage)), smem_u32(sm.b(stage)), kb);
-        umma_commit_pair(&sm.empty[stage]);
-        umma_commit_pair_at(peer_empty0 + stage * 8u);
+        umma_commit_pair_both(&sm.empty[stage]);
         if (++stage == Geo2::kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (ok) {
-        umma_commit_pair(&sm.tfull[acc]);
-        umma_commit_pair_at(peer_tfull0 + acc * 8u);
+        umma_commit_pair_both(&sm.tfull[acc]);
       }
       if (tr) {
         trace_span(c, kTrMmaTile, t, tt0, globaltimer());
