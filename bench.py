@@ -49,7 +49,7 @@ MOE_LAUNCHES = 3  # routing, permutation, the persistent expert-GEMM + combine k
 # dram__bytes_write.sum), keyed by the hash of the kernel's sources (AG_KERNEL_SOURCES) they
 # were taken on.
 # A kernel changed since the capture reports traffic null.
-NCU_TRAFFIC = {"ag_70b": {"6a3c490d15b78876": 588217600}}  # profiles/ag_70b_persistent_kernel_ncu.md
+NCU_TRAFFIC = {"ag_70b": {"fe1bb8d7778bd175": 587978240}}  # profiles/ag_70b_persistent_kernel_ncu.md
 
 
 # The sources the AllGather+GEMM kernel is compiled from: its translation unit and every
@@ -799,11 +799,13 @@ def run_profile(args):
     device = torch.device("cuda", 0)
     name = args.profile
     # the communication-alone legs and the low-latency gather run on their workloads' inputs
-    base = {"allgather_70b": "ag_70b", "reduce_scatter_70b": "rs_70b", "ag_tiny_ll": "ag_tiny"}.get(name, name)
-    ctx = tl.Context(0, ag_ll=1) if name == "ag_tiny_ll" else tl.Context(0)
+    base = {"allgather_70b": "ag_70b", "allgather_70b_tma": "ag_70b", "reduce_scatter_70b": "rs_70b",
+            "ag_tiny_ll": "ag_tiny"}.get(name, name)
+    cfg = {"ag_tiny_ll": dict(ag_ll=1), "allgather_70b_tma": dict(mover_tma=1)}.get(name, {})
+    ctx = tl.Context(0, **cfg)
     d = WORKLOADS[base].dims
     inp = workload_inputs(base) if name != "reduce_scatter_70b" else None
-    if name == "allgather_70b":
+    if name in ("allgather_70b", "allgather_70b_tma"):
         a = [dev_bf16(x, device) for x in inp["a_shards"]]
         ws = torch.zeros(tl.tl_ag_gemm_workspace_bytes(d["W"], d["m_per_rank"], d["n"], d["k"]), dtype=torch.uint8,
                          device=device)
@@ -901,7 +903,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work in --impl reference")
     ap.add_argument("--quick", action="store_true", help="headline only (no extra workloads / e2e / overlap)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--profile", choices=["ag_tiny", "ag_tiny_ll", "ag_70b", "allgather_70b", "rs_70b",
+    ap.add_argument("--profile", choices=["ag_tiny", "ag_tiny_ll", "ag_70b", "allgather_70b", "allgather_70b_tma", "rs_70b",
                                           "reduce_scatter_70b", "mlp2_8b", "moe_64e", "attn_16k"],
                     help="only run this workload's call 4 times (target of an ncu capture), no timing")
     ap.add_argument("--trace", metavar="PATH", help="with --profile: trace one call (after 3 warm-up calls and an "
