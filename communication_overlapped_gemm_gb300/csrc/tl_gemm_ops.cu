@@ -774,8 +774,8 @@ __global__ void __launch_bounds__(32, 1) allgather_tma_kernel(const __grid_const
   };
   // signals of chunks whose last store is issued but not yet known complete, oldest first
   constexpr int kPend = kTmaStages + 1;
-  uint64_t* pend_flag[kPend];
-  int pend_last[kPend];
+  uint64_t* pend_flag[kPend] = {};
+  int pend_last[kPend] = {};
   int npend = 0;
   auto retire = [&](int upto) {  // release the chunks whose last store is job <= upto
     int k = 0;
@@ -790,12 +790,14 @@ __global__ void __launch_bounds__(32, 1) allgather_tma_kernel(const __grid_const
     npend -= k;
   };
   // loads run kTmaStages - 1 jobs ahead of the stores
-  for (int j = 0; j < njobs && j < kTmaStages - 1; ++j) load(j);
+  int issued = 0, landed = 0;  // loads issued; loads waited for
+  for (int j = 0; j < njobs && j < kTmaStages - 1; ++j, ++issued) load(j);
   bool ok = true;
   for (int j = 0; j < njobs && ok; ++j) {
     const int s = j % kTmaStages;
     ok = mbar_wait(&bars[s], (j / kTmaStages) & 1, c, kSiteFull);
     if (!ok) break;
+    ++landed;
     const uint8_t* src;
     uint8_t* dst;
     uint32_t bytes;
@@ -816,14 +818,17 @@ __global__ void __launch_bounds__(32, 1) allgather_tma_kernel(const __grid_const
     if (jn < njobs) {
       bulk_wait_read<1>();
       load(jn);
+      ++issued;
     }
     if ((j % kTmaStages) == kTmaStages - 1) {  // every kTmaStages jobs: release what has landed
       bulk_wait<kTmaStages - 1>();
       retire(j - (kTmaStages - 1));
     }
   }
+  // a wait that ran out leaves loads in flight: let them land (bounded) before the CTA exits
+  for (int j = landed; j < issued; ++j) mbar_wait(&bars[j % kTmaStages], (j / kTmaStages) & 1, c, kSiteDrain);
   bulk_wait<0>();  // every store has completed (and nothing reads shared memory any more)
-  retire(njobs);
+  if (ok) retire(njobs);
 }
 
 // ============================================================================ ReduceScatter alone
