@@ -7,38 +7,41 @@
 // Persistent clusters of two CTAs (one per SM) walk (head, 256-query tile) work items; CTA r
 // of a pair owns queries [128 r, 128 r + 128) of the tile.  Each item is non-causal flash
 // attention over all W shards in blocks of 256 keys, on tcgen05 pair MMAs (cta_group::2):
-//   S_J = Q K_J^T      M = 256 queries, N = 256 keys, K = 128 head dims: CTA r's A is its
+//   S(J) = Q K_J^T     M = 256 queries, N = 256 keys, K = 128 head dims: CTA r's A is its
 //                      128 query rows, its B half the keys [128 r, 128 r + 128) of the block
-//                      (K-major), and its TMEM gets its rows' 256 scores;
-//   O_g += P_g V_g     for each half g of the block's keys: M = 256 queries, N = 128 head
-//                      dims, K = 128 keys: CTA r's A is its rows of P_g, its B half the head
-//                      dims [64 r, 64 r + 64) of V (MN-major).  The two halves keep separate
-//                      accumulators O_0, O_1 (and separate running max and sum), combined
-//                      once per item: a flash-decoding style split of the keys inside the block.
+//                      (K-major); TMEM columns [0, 256) of each CTA receive its rows' scores;
+//   O += P(J) V_J      M = 256, N = 128 head dims, K = 256 keys, A from TMEM: the softmax
+//                      writes P (bf16, two per 32-bit column) to columns [256, 384); CTA r's
+//                      B half is head dims [64 r, 64 r + 64) of V (MN-major); O is columns
+//                      [384, 512).
+// S and P have separate columns, so S(J + 1) is computed while the softmax of block J runs,
+// and P(J) V_J while the softmax of block J + 1 runs: the MMA thread issues S(J + 1) as soon
+// as every softmax warp has read S(J), then P(J) V_J once P(J) is written.
 // Warps of each CTA:
-//   warp 0     TMA producer: its Q rows, then per key block its K half (2 boxes) and V half
-//              (4 boxes) through 2-stage rings; every load completes on the pair leader's
+//   warp 0     TMA producer: its Q rows (two buffers, so the next item's Q is loaded early),
+//              per key block its K half (2 boxes) and V half (4 boxes of 64 keys x its 64
+//              head dims) through 2-stage rings; every load completes on the pair leader's
 //              barrier; the first block of a remote shard slice waits on the slice's block
 //              signals (one warp-wide poll).
 //   warp 1     TMEM allocation (both CTAs) and, in the leader, the pair MMAs (one thread).
 //   warps 2-9  softmax, two warpgroups: warpgroup g takes keys [128 g, 128 g + 128) of every
-//              block for all 128 rows (one row per thread), with its own running max m_g and
-//              sum l_g in base 2 (the 1/sqrt(d) scale folded into one multiply-add per score);
-//              P_g (bf16) goes into its half of the shared-memory P buffer in the MMA's
-//              K-major 128-byte-swizzled layout.  The running max of a row moves only when
-//              the block's max exceeds it by more than 2^8 (kRescaleLog2): until then P <= 256
-//              and O_g, l_g keep the stale max, which cancels in the final division; a move
-//              rescales O_g in TMEM after the previous P_g V_g has completed.  At the end of
-//              an item the groups exchange m_g, l_g and each writes 64 head dims of
-//              (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)) as bf16.
+//              block, one row per thread, in base 2 (the 1/sqrt(d) scale folded into one
+//              multiply-add per score).  The two warps of a TMEM lane quadrant (one per group,
+//              the same 32 rows) exchange their block maxima through shared memory, so both
+//              use one running max m per row and one O; each keeps the sum l_g of its own
+//              keys.  m moves only when the block's max exceeds it by more than 2^8
+//              (kRescaleLog2): until then P <= 256 and O, l_g keep the stale max, which cancels
+//              in the final division; a move rescales O in TMEM (group g its head dims
+//              [64 g, 64 g + 64)) once P(J - 1) V_{J-1} has completed.  At the end of an
+//              item the partners exchange l_g and group g writes head dims [64 g, 64 g + 64)
+//              of O / (l_0 + l_1) as bf16.
 //   warps 10-11 movers: remote K/V blocks (up to 32 KB each) into the shard-major gathered
 //              buffers, one release signal per 128-key block, in the order the items need
 //              them (groups of heads one wave covers, shard by shard, the local shard last).
-// The softmax warps of both CTAs arrive on the leader's barriers for "S read" and "P_g
-// written" (relaxed cluster-scope arrivals: a release at cluster scope costs a full memory
-// barrier per arrival); the leader's MMA commits arrive on both CTAs' barriers (one
-// multicast commit).  TMEM columns (each CTA, its 128 rows): S [0, 256),
-// O_0 [256, 384), O_1 [384, 512).  The pipeline counters run on across items.  Every wait
+// The softmax warps of both CTAs arrive on the leader's barriers for "S read", "P written"
+// and "O read by the epilogue" (relaxed cluster-scope arrivals: a release at cluster scope
+// costs a full memory barrier per arrival); the leader's MMA commits arrive on both CTAs'
+// barriers (one multicast commit).  The pipeline counters run on across items.  Every wait
 // is bounded.
 // Shard lengths need not be multiples of 256 (the Ragged instantiation): a shard's last key
 // block and the last query tile may be partial.  TMA zero-fills the absent rows, the softmax
@@ -53,14 +56,17 @@ constexpr int kBQ = 128;         // queries per CTA (a pair's tile is 256)
 constexpr int kBKV = 256;        // keys per block
 constexpr int kSigBlk = 128;     // keys per mover block (one signal each)
 constexpr int kBox = 16384;      // one 64-column SW128 box of 128 rows
-constexpr int kQBytes = 2 * kBox;   // this CTA's 128 queries x 128 dims
-constexpr int kKBytes = 2 * kBox;   // this CTA's 128 keys of a block x 128 dims
-constexpr int kVBytes = 4 * 8192;   // 256 keys x this CTA's 64 dims: 4 boxes of 64 keys
-constexpr int kPBytes = 4 * kBox;   // 128 rows x 256 keys: 4 boxes of 64 keys
+constexpr int kBox64 = 8192;     // one 64-column SW128 box of 64 rows
+constexpr int kQBytes = 2 * kBox;      // this CTA's 128 queries x 128 dims
+constexpr int kKBytes = 2 * kBox;      // this CTA's 128 keys of a block x 128 dims
+constexpr int kVBytes = 4 * kBox64;    // 256 keys x this CTA's 64 dims: 4 boxes of 64 keys
+constexpr int kQStages = 2;
 constexpr int kStages = 2;
-constexpr int kRedBytes = 2 * kBQ * 4;  // one float per row and softmax warpgroup
-constexpr int kBarBytes = 192;
-constexpr int kSmem = 1024 + kQBytes + kStages * (kKBytes + kVBytes) + kPBytes + kRedBytes + kBarBytes;
+constexpr int kRedBytes = 2 * 2 * kBQ * 4;  // [exchange parity][group][row] floats
+constexpr int kBarBytes = 256;
+constexpr int kSmem = 1024 + kQStages * kQBytes + kStages * (kKBytes + kVBytes) + kRedBytes + kBarBytes;
+constexpr uint32_t kColP = 256;  // TMEM columns of P (bf16 pairs; group g at + 64 g)
+constexpr uint32_t kColO = 384;  // TMEM columns of O
 constexpr float kRescaleLog2 = 8.0f;  // move the running max once it grows by more than this
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSoftWarps = 8;
@@ -97,27 +103,56 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// S_J = Q K_J^T on the pair: M = 256, N = 256, K = 128 (8 steps of 16 head dims).
-__device__ __forceinline__ void attn_mma_s(uint32_t d, uint32_t q0, uint32_t k0) {
-  constexpr uint32_t idesc = umma_idesc_bf16(256, 256, false);
-#pragma unroll
-  for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      umma_bf16_pair(d, umma_desc_sw128(q0 + kb * attn::kBox + k * 32, 16, 1024),
-                     umma_desc_sw128(k0 + kb * attn::kBox + k * 32, 16, 1024), idesc, (kb | k) ? 1u : 0u);
+// D[tmem of both CTAs] (+)= A[tmem of both CTAs, M split] * B[smem of both CTAs, N split].
+__device__ __forceinline__ void umma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
-// O_g (+)= P_g V_g on the pair: M = 256, N = 128, K = 128 keys (8 steps); each CTA's V half
-// is 64 head dims wide (one 64-column group), its 64-key boxes 8 KB apart.
-__device__ __forceinline__ void attn_mma_pv(uint32_t d, uint32_t p0, uint32_t v0, bool acc) {
-  constexpr uint32_t idesc = umma_idesc_bf16(256, 128, true);
+// S = Q K^T on the pair: M = 256, N = 256, K = 128 (8 steps of 16 head dims).  Each step's
+// descriptors are the first step's plus a constant: the start-address field (address >> 4,
+// bits 0-13) cannot carry out, shared-memory addresses being below 2^18 bytes.
+__device__ __forceinline__ void attn_mma_s(uint32_t d, uint32_t q0, uint32_t k0) {
+  constexpr uint32_t idesc = umma_idesc_bf16(256, 256, false);
+  const uint64_t a0 = umma_desc_sw128(q0, 16, 1024), b0 = umma_desc_sw128(k0, 16, 1024);
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      umma_bf16_pair(d, umma_desc_sw128(p0 + kb * attn::kBox + k * 32, 16, 1024),
-                     umma_desc_sw128(v0 + kb * 8192 + k * 2048, 8192, 1024), idesc, (acc || kb || k) ? 1u : 0u);
+      umma_bf16_pair(d, a0 + ((kb * attn::kBox + k * 32) >> 4), b0 + ((kb * attn::kBox + k * 32) >> 4), idesc,
+                     (kb | k) ? 1u : 0u);
+}
+
+// O (+)= P V on the pair: M = 256, N = 128, K = 256 keys (16 steps).  P is in TMEM at columns
+// [p, p + 128) (16 keys per 8 columns); this CTA's V half is 64 head dims wide, its 64-key
+// boxes 8 KB apart.
+__device__ __forceinline__ void attn_mma_pv(uint32_t d, uint32_t p, uint32_t v0, bool acc) {
+  constexpr uint32_t idesc = umma_idesc_bf16(256, 128, true);
+  const uint64_t b0 = umma_desc_sw128(v0, 8192, 1024);
+#pragma unroll
+  for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      umma_ts_pair(d, p + (kb * 4 + k) * 8, b0 + ((kb * attn::kBox64 + k * 2048) >> 4), idesc,
+                   (acc || kb || k) ? 1u : 0u);
+}
+
+// Store 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (no wait).
+__device__ __forceinline__ void tmem_st32_raw(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
 }
 
 // Paired fp32 arithmetic (two lanes of one 64-bit register pair per instruction) and the
@@ -149,8 +184,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // Relaxed arrival on an mbarrier given by its shared::cluster address: no memory ordering is
 // implied (a release at cluster scope costs a full memory barrier on every call).  Used where
 // what the arrival announces is already complete in this thread: its TMEM reads
-// (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync) or its P stores, made visible to
-// the tensor core by fence.proxy.async before the arrival.
+// (tcgen05.wait::ld) or writes (tcgen05.wait::st), then tcgen05.fence::before_thread_sync.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
@@ -170,30 +204,29 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
   using namespace attn;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sq = base;
-  uint8_t* sk = sq + kQBytes;
-  uint8_t* sv = sk + kStages * kKBytes;
-  uint8_t* sp = sv + kStages * kVBytes;
-  float* red = reinterpret_cast<float*>(sp + kPBytes);  // [group][row]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sp + kPBytes + kRedBytes);
+  uint8_t* sq = base;                        // [kQStages]
+  uint8_t* sk = sq + kQStages * kQBytes;     // [kStages]
+  uint8_t* sv = sk + kStages * kKBytes;      // [kStages]
+  float* red = reinterpret_cast<float*>(sv + kStages * kVBytes);  // [parity][group][row]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sv + kStages * kVBytes + kRedBytes);
   // counted on the leader (the peer's copies are unused): loads of both CTAs, arrivals of
   // both CTAs' softmax warps
-  uint64_t* qfull = bars;
-  uint64_t* kfull = bars + 1;    // [2]
-  uint64_t* vfull = bars + 3;    // [2]
-  uint64_t* sfree = bars + 5;    // every softmax warp of the pair has read its S half
-  uint64_t* pready = bars + 6;   // [2] group g: its 8 warps of the pair wrote P_g, O_g rescaled
+  uint64_t* qfull = bars;        // [2]
+  uint64_t* kfull = bars + 2;    // [2]
+  uint64_t* vfull = bars + 4;    // [2]
+  uint64_t* sfree = bars + 6;    // all 16 softmax warps of the pair have read S(J)
+  uint64_t* pready = bars + 7;   // all 16 wrote P(J) (and rescaled O)
+  uint64_t* ofree = bars + 8;    // all 16 have read O at the end of an item
   // in both CTAs, arrived on by the leader's MMA commits
-  uint64_t* qempty = bars + 8;   // the item's last S MMA has read Q
-  uint64_t* kempty = bars + 9;   // [2]
-  uint64_t* vempty = bars + 11;  // [2]
-  uint64_t* sfull = bars + 13;   // S_J is in TMEM
-  uint64_t* pfree = bars + 14;   // [2] group g: P_g V_g of the block complete (P_g free, O_g stable)
-  uint64_t* drain = bars + 16;
-  // this CTA's softmax warps, once per item
-  uint64_t* xw = bars + 17;      // all 8 wrote their m_g, l_g to red
-  uint64_t* xr = bars + 18;      // all 8 read the other group's
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 19);
+  uint64_t* qempty = bars + 9;   // [2] the item's last S MMA has read Q
+  uint64_t* kempty = bars + 11;  // [2]
+  uint64_t* vempty = bars + 13;  // [2]
+  uint64_t* sfull = bars + 15;   // S(J) is in TMEM
+  uint64_t* pfree = bars + 16;   // P(J) V_J complete (P free, O stable)
+  uint64_t* drain = bars + 17;
+  // this CTA's partner warps (the two softmax warps of one TMEM lane quadrant), per exchange
+  uint64_t* xq = bars + 18;      // [4]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 22);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();
@@ -206,23 +239,21 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
   const int nqt = (p.Lq + 2 * kBQ - 1) / (2 * kBQ);  // 256-query tiles (the last may be partial)
   const int nwork = p.heads * nqt;
   if (threadIdx.x == 0) {
-    mbar_init(qfull, 1);
-    mbar_init(qempty, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&qfull[s], 1);
+      mbar_init(&qempty[s], 1);
       mbar_init(&kfull[s], 1);
       mbar_init(&kempty[s], 1);
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 1);
     }
+    mbar_init(sfree, 2 * kSoftWarps);
+    mbar_init(pready, 2 * kSoftWarps);
+    mbar_init(ofree, 2 * kSoftWarps);
     mbar_init(sfull, 1);
-    mbar_init(sfree, 2 * kSoftWarps);  // counted on the leader: the softmax warps of both CTAs
-    for (int g = 0; g < 2; ++g) {
-      mbar_init(&pready[g], kSoftWarps);  // the 4 warps of group g in each CTA
-      mbar_init(&pfree[g], 1);
-    }
+    mbar_init(pfree, 1);
     mbar_init(drain, 1);
-    mbar_init(xw, kSoftWarps);
-    mbar_init(xr, kSoftWarps);
+    for (int q = 0; q < 4; ++q) mbar_init(&xq[q], 2);
     fence_mbar_init();
     tma_prefetch_map(&p.q);
     tma_prefetch_map(&p.k_loc);
@@ -244,17 +275,21 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
     bool ok = true;
-    uint32_t filled = 0, par = 0;  // leader's drain: K stages (bits 0-1), V stages (bits 2-3)
+    uint32_t filled = 0, par = 0;  // leader's drain: K stages bits 0-1, V 2-3, Q 4-5
     int J = 0, kq = 0;
     for (int it = pair; it < nwork && ok; it += npairs, ++kq) {
       const int h = it / nqt, qt = it - h * nqt;
+      const int qs = kq & 1;
+      const uint32_t qph = (kq >> 1) & 1;
       if (lane == 0) {
-        ok = mbar_wait(qempty, (kq & 1) ^ 1u, c, kSiteEmpty);
+        ok = mbar_wait(&qempty[qs], qph ^ 1u, c, kSiteEmpty);
         if (ok) {
-          if (leader) mbar_arrive_expect_tx(qfull, 2 * kQBytes);
+          if (leader) mbar_arrive_expect_tx(&qfull[qs], 2 * kQBytes);
           const int y = qt * 2 * kBQ + static_cast<int>(crank) * kBQ;
-          tma_load_3d_pair(sq, &p.q, lead(qfull), 0, y, h);
-          tma_load_3d_pair(sq + kBox, &p.q, lead(qfull), 64, y, h);
+          tma_load_3d_pair(sq + qs * kQBytes, &p.q, lead(&qfull[qs]), 0, y, h);
+          tma_load_3d_pair(sq + qs * kQBytes + kBox, &p.q, lead(&qfull[qs]), 64, y, h);
+          filled |= 16u << qs;
+          par = (par & ~(16u << qs)) | (qph << (qs + 4));
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -290,7 +325,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
             const int xv = static_cast<int>(crank) * 64;  // this CTA's 64 head dims
 #pragma unroll
             for (int kb = 0; kb < 4; ++kb)
-              tma_load_3d_pair(sv + s * kVBytes + kb * 8192, vm, lead(&vfull[s]), xv, y + kb * 64, z);
+              tma_load_3d_pair(sv + s * kVBytes + kb * kBox64, vm, lead(&vfull[s]), xv, y + kb * 64, z);
             filled |= 4u << s;
             par = (par & ~(4u << s)) | (ph << (s + 2));
           }
@@ -299,8 +334,8 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
       }
     }
     if (lane == 0 && leader) {  // drain: every fill of both CTAs has landed before the pair exits
-      if (kq > 0) mbar_wait(qfull, (kq - 1) & 1, c, kSiteDrain);
-      for (int s = 0; s < kStages; ++s) {
+      for (int s = 0; s < 2; ++s) {
+        if (filled & (16u << s)) mbar_wait(&qfull[s], (par >> (s + 4)) & 1u, c, kSiteDrain);
         if (filled & (1u << s)) mbar_wait(&kfull[s], (par >> s) & 1u, c, kSiteDrain);
         if (filled & (4u << s)) mbar_wait(&vfull[s], (par >> (s + 2)) & 1u, c, kSiteDrain);
       }
@@ -308,43 +343,45 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader)
+    // Per block J: S(J + 1) (the next item's first block when J ends an item) once the
+    // softmax has read S(J), then P(J) V_J once P(J) is written.
     if (leader && lane == 0) {
-      bool ok = true;
-      const uint32_t q0 = smem_u32(sq), p0 = smem_u32(sp);
-      const uint32_t ts = tmem, to = tmem + 256;  // S; O_0 (O_1 at + 128)
-      int J0 = 0, kq = 0;
-      for (int it = pair; it < nwork && ok; it += npairs, ++kq, J0 += nblk) {
-        ok = mbar_wait(qfull, kq & 1, c, kSiteFull);
+      const int nitems = pair < nwork ? (nwork - pair + npairs - 1) / npairs : 0;
+      const int total = nitems * nblk;
+      const uint32_t sk0 = smem_u32(sk), sv0 = smem_u32(sv), sq0 = smem_u32(sq);
+      // S of block Jn (position jn in item kqn), and its commits
+      auto issue_s = [&](int Jn, int jn, int kqn) -> bool {
+        const int s = Jn & 1;
+        if (jn == 0 && !mbar_wait(&qfull[kqn & 1], (kqn >> 1) & 1, c, kSiteFull)) return false;
+        if (!mbar_wait(&kfull[s], (Jn >> 1) & 1, c, kSiteFull)) return false;
         tc_fence_after();
-        for (int j = 0; j <= nblk && ok; ++j) {
-          if (j < nblk) {  // S of block J0 + j (S has one TMEM buffer: its last reader is done)
-            const int J = J0 + j, s = J & 1;
-            const uint32_t ph = (J >> 1) & 1;
-            ok = (J == 0 || mbar_wait(sfree, (J - 1) & 1, c, kSiteTmemEmpty)) && mbar_wait(&kfull[s], ph, c, kSiteFull);
-            if (!ok) break;
-            tc_fence_after();
-            attn_mma_s(ts, q0, smem_u32(sk + s * kKBytes));
-            commit_both(&kempty[s]);
-            commit_both(sfull);
-            if (j == nblk - 1) commit_both(qempty);
-          }
-          if (j >= 1) {  // O_g += P_g V_g of block J0 + j - 1, g = 0, 1
-            const int I = J0 + j - 1, s = I & 1;
-            const uint32_t ph = (I >> 1) & 1;
-            ok = mbar_wait(&vfull[s], ph, c, kSiteFull);
-            if (!ok) break;
-#pragma unroll 1
-            for (int g = 0; g < 2 && ok; ++g) {
-              ok = mbar_wait(&pready[g], I & 1, c, kSiteFull);
-              if (!ok) break;
-              tc_fence_after();
-              attn_mma_pv(to + g * 128, p0 + g * 2 * kBox, smem_u32(sv + s * kVBytes) + g * 2 * 8192, j > 1);
-              commit_both(&pfree[g]);
-            }
-            if (!ok) break;
-            commit_both(&vempty[s]);
-          }
+        attn_mma_s(tmem, sq0 + (kqn & 1) * kQBytes, sk0 + s * kKBytes);
+        commit_both(sfull);
+        commit_both(&kempty[s]);
+        if (jn == nblk - 1) commit_both(&qempty[kqn & 1]);
+        return true;
+      };
+      bool ok = true;
+      if (total > 0) ok = issue_s(0, 0, 0);
+      int j = 0, kq = 0;
+      for (int J = 0; J < total && ok; ++J) {
+        const int s = J & 1;
+        const int jn = j + 1 == nblk ? 0 : j + 1, kqn = jn == 0 ? kq + 1 : kq;
+        if (J + 1 < total) {  // S(J + 1) overwrites S(J): every softmax warp has read it
+          ok = mbar_wait(sfree, J & 1, c, kSiteTmemEmpty) && issue_s(J + 1, jn, kqn);
+          if (!ok) break;
         }
+        ok = mbar_wait(&vfull[s], (J >> 1) & 1, c, kSiteFull);
+        // the previous item's epilogue has read O before this item's first P V overwrites it
+        if (ok && j == 0 && kq > 0) ok = mbar_wait(ofree, (kq - 1) & 1, c, kSiteTmemEmpty);
+        if (ok) ok = mbar_wait(pready, J & 1, c, kSiteFull);
+        if (!ok) break;
+        tc_fence_after();
+        attn_mma_pv(tmem + kColO, tmem + kColP, sv0 + s * kVBytes, j > 0);
+        commit_both(pfree);
+        commit_both(&vempty[s]);
+        j = jn;
+        kq = kqn;
       }
       umma_commit_pair(drain);
       mbar_wait(drain, 0, c, kSiteDrain);
@@ -353,31 +390,31 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
   } else if (warp < 2 + kSoftWarps) {
     // ------------------------------------------------------------ softmax (one row per thread)
     const int g = (warp - 2) >> 2;          // warpgroup: keys [128 g, 128 g + 128) of a block
-    const int qd = warp & 3;                // TMEM lane quadrant of this warp
+    const int qd = warp & 3;                // TMEM lane quadrant of this warp (and its partner's)
     const int row = qd * 32 + lane;         // query row inside the CTA's 128
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
-    const uint32_t tog = tmem + 256 + g * 128;  // O_g
+    const uint32_t tog = tmem + kColO + g * 64;  // this group's half of O (head dims [64 g, 64 g + 64))
     const float sl2 = p.scale * kLog2e;     // raw score -> base-2 exponent
     bool ok = true;
     int J0 = 0;
-    uint32_t nx = 0;  // exchanges so far
-    // Exchange one float per row with the other warpgroup through red (bounded waits: a
-    // timeout elsewhere never leaves a warp blocked here).
+    uint32_t nx = 0;  // exchanges with the partner warp so far
+    // Exchange one float per row with the partner warp (same rows, other key group) through
+    // red, double-buffered by exchange parity: exchange n + 2 rewrites a buffer only after the
+    // partner has arrived for exchange n + 1, i.e. after it read exchange n.  Bounded waits.
     auto exchange = [&](float mine, float& other) -> bool {
-      if (nx > 0 && !mbar_wait(xr, (nx - 1) & 1, c, kSiteTmemFull)) return false;  // red is free again
-      red[g * kBQ + row] = mine;
+      float* buf = red + (nx & 1) * 2 * kBQ;
+      buf[g * kBQ + row] = mine;
       __syncwarp();
-      if (lane == 0) mbar_arrive(xw);
-      if (!mbar_wait(xw, nx & 1, c, kSiteTmemFull)) return false;
-      other = red[(1 - g) * kBQ + row];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(xr);
+      if (lane == 0) mbar_arrive(&xq[qd]);
+      if (!mbar_wait(&xq[qd], nx & 1, c, kSiteTmemFull)) return false;
+      other = buf[(1 - g) * kBQ + row];
       ++nx;
       return true;
     };
+    bool pfree_seen = true;  // P(J - 1) V_{J-1} known complete
     for (int it = pair; it < nwork && ok; it += npairs, J0 += nblk) {
       const int h = it / nqt, qt = it - h * nqt;
-      float m2 = -INFINITY, l = 0.f;  // this group's running max (base-2 units) and sum
+      float m2 = -INFINITY, l = 0.f;  // running max (base-2 units, common to both groups), this group's sum
       int blk = -1;                   // block index inside the current shard
       for (int j = 0; j < nblk && ok; ++j) {
         const int J = J0 + j;
@@ -402,6 +439,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_relaxed(lead(sfree));
+        pfree_seen = J == 0;
         if constexpr (Ragged) {
           // keys past the end of a shard (its partial last block, zero-filled by TMA) get no
           // weight: their scores become -inf before the maximum
@@ -418,19 +456,27 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         for (int i = 8; i < 128; i += 16)
 #pragma unroll
           for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], x[i + k], x[i + 8 + k]);
-        const float bm2 = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
-                          sl2;  // the scale is positive: max commutes with it
-        if (j == 0) {
-          m2 = bm2;  // the item's first P_g V_g overwrites O_g
-        } else if (__any_sync(0xffffffffu, bm2 > m2 + kRescaleLog2)) {
-          const float mn = fmaxf(m2, bm2);
-          const float corr = ex2_approx(m2 - mn);  // 0 while the group has seen only absent keys
-          // O_g is stable once P_g V_g of the previous block has completed
-          ok = mbar_wait(&pfree[g], (J - 1) & 1, c, kSiteTmemFull);
+        float bm2 = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+                    sl2;  // the scale is positive: max commutes with it
+        {
+          float other;
+          ok = exchange(bm2, other);
           if (!ok) break;
+          bm2 = fmaxf(bm2, other);  // the block's max over all 256 keys: the same in both partners
+        }
+        if (j == 0) {
+          m2 = bm2;  // the item's first P V overwrites O
+        } else if (__any_sync(0xffffffffu, bm2 > m2 + kRescaleLog2)) {
+          // both partners take this branch (same rows, same values); O is stable once
+          // P(J - 1) V_{J-1} has completed, and P(J) V_J waits for this thread's P
+          const float mn = fmaxf(m2, bm2);
+          const float corr = ex2_approx(m2 - mn);  // 0 while the row has seen only absent keys
+          ok = mbar_wait(pfree, (J - 1) & 1, c, kSiteTmemFull);
+          if (!ok) break;
+          pfree_seen = true;
           tc_fence_after();
 #pragma unroll 1
-          for (int cb = 0; cb < 4; ++cb) {
+          for (int cb = 0; cb < 2; ++cb) {
             float o[32];
             tmem_ld32(tog + cb * 32 + lane_off, o);
 #pragma unroll
@@ -440,7 +486,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           l *= corr;
           m2 = mn;
         }
-        // (Ragged: a group whose keys so far are all absent has m2 = -inf; its P is 0.)
+        // (Ragged: a row whose keys so far are all absent has m2 = -inf; its P is 0.)
         const float nm = (Ragged && m2 == -INFINITY) ? 0.f : -m2;
         unsigned long long sum2[4];  // 8 partial sums, two per register pair
         uint32_t pk[64];
@@ -461,37 +507,29 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           f2_split(s2, a, b);
           l += a + b;
         }
-        // P_g's half of the buffer was last read by P_g V_g of block J - 1
-        if (J > 0) ok = mbar_wait(&pfree[g], (J - 1) & 1, c, kSiteTmemEmpty);
-        if (!ok) break;
-        // P_g (bf16) as the K-major, 128-byte-swizzled A operand: keys [64 b, 64 b + 64) of
-        // this row are 128 bytes of box b; 16-byte piece u sits at piece u ^ (row & 7).
-        const uint32_t prow = smem_u32(sp) + row * 128;
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint32_t* v = pk + kb * 32 + u * 4;
-            st_shared_v4(prow + (2 * g + kb) * kBox + ((u ^ (row & 7)) << 4), v[0], v[1], v[2], v[3]);
-          }
-        fence_proxy_async_smem();
+        // P(J - 1) has been read by P(J - 1) V_{J-1} before P(J) replaces it
+        if (!pfree_seen) {
+          ok = mbar_wait(pfree, (J - 1) & 1, c, kSiteTmemEmpty);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // P (bf16, keys 2i and 2i + 1 of this group in column i)
+        tmem_st32_raw(tmem + kColP + g * 64 + lane_off, pk);
+        tmem_st32_raw(tmem + kColP + g * 64 + 32 + lane_off, pk + 32);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster_relaxed(lead(&pready[g]));
+        if (lane == 0) mbar_arrive_cluster_relaxed(lead(pready));
       }
-      // Both halves' last P V of the item have completed: combine
-      //   O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)),
-      // m = max(m_0, m_1); this group writes head dims [64 g, 64 g + 64).
+      // The item's last P V has completed: O / (l_0 + l_1); this group writes head dims
+      // [64 g, 64 g + 64).
       const int Jl = J0 + nblk - 1;
-      if (ok) ok = mbar_wait(&pfree[0], Jl & 1, c, kSiteTmemFull) && mbar_wait(&pfree[1], Jl & 1, c, kSiteTmemFull);
+      if (ok) ok = mbar_wait(pfree, Jl & 1, c, kSiteTmemFull);
       tc_fence_after();
-      float om = 0.f, ol = 0.f;
-      if (ok) ok = exchange(m2, om) && exchange(l, ol);
+      float ol = 0.f;
+      if (ok) ok = exchange(l, ol);
       if (ok) {
-        const float m = fmaxf(m2, om);
-        const float a_mine = ex2_approx(m2 - m), a_other = ex2_approx(om - m);
-        const float inv = 1.0f / (l * a_mine + ol * a_other);
-        const float c0 = (g == 0 ? a_mine : a_other) * inv, c1 = (g == 0 ? a_other : a_mine) * inv;
+        const float inv = 1.0f / (l + ol);
         // Every lane takes part in the (warp-collective) TMEM loads; rows past the end of
         // the queries (a partial last tile) are only not stored.
         const int qrow = qt * 2 * kBQ + static_cast<int>(crank) * kBQ + row;
@@ -499,19 +537,21 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(h) * p.Lq + qrow) * kD + g * 64);
 #pragma unroll 1
         for (int cb = 0; cb < 2; ++cb) {
-          float o0[32], o1[32];
-          tmem_ld32(tmem + 256 + g * 64 + cb * 32 + lane_off, o0);
-          tmem_ld32(tmem + 384 + g * 64 + cb * 32 + lane_off, o1);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o0[i] = o0[i] * c0 + o1[i] * c1;
+          float o[32];
+          tmem_ld32(tog + cb * 32 + lane_off, o);
           if (live) {
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              dst[cb * 4 + u] = make_uint4(pack_bf16x2(o0[8 * u], o0[8 * u + 1]), pack_bf16x2(o0[8 * u + 2], o0[8 * u + 3]),
-                                           pack_bf16x2(o0[8 * u + 4], o0[8 * u + 5]),
-                                           pack_bf16x2(o0[8 * u + 6], o0[8 * u + 7]));
+              dst[cb * 4 + u] = make_uint4(pack_bf16x2(o[8 * u] * inv, o[8 * u + 1] * inv),
+                                           pack_bf16x2(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
+                                           pack_bf16x2(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
+                                           pack_bf16x2(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
           }
         }
+        // O read: the next item's first P V may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(lead(ofree));
       }
       tc_fence_before();
       __syncwarp();
