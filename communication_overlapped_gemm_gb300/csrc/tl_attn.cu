@@ -5,8 +5,15 @@
 // they arrive; "Triton-distributed ...", §3.7 swizzle: the local shard first).
 //
 // Persistent clusters of two CTAs (one per SM) walk (head, 256-query tile) work items; CTA r
-// of a pair owns queries [128 r, 128 r + 128) of the tile.  Each item is non-causal flash
-// attention over all W shards in blocks of 256 keys, on tcgen05 pair MMAs (cta_group::2):
+// of a pair owns queries [128 r, 128 r + 128) of the tile.  When the items do not fill the
+// last wave evenly (nwork mod pairs = rem, 0 < 2 rem <= pairs) the last rem items are split
+// into two halves of their key blocks, one per pair: a wave of halves replaces a partial wave
+// of whole items.  A half writes its unnormalised O, running max and sum to the workspace;
+// whichever half of an item finishes second (an epoch-tagged exchange on a counter) combines
+// both in a fixed order, (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)),
+// so the result does not depend on which finished first (the flash-decoding split of the keys).
+// Each item is non-causal flash attention over all W shards in blocks of 256 keys, on tcgen05
+// pair MMAs (cta_group::2):
 //   S(J) = Q K_J^T     M = 256 queries, N = 256 keys, K = 128 head dims: CTA r's A is its
 //                      128 query rows, its B half the keys [128 r, 128 r + 128) of the block
 //                      (K-major); TMEM columns [0, 256) of each CTA receive its rows' scores;
@@ -66,6 +73,9 @@ constexpr int kRedBytes = 2 * 2 * kBQ * 4;  // [exchange parity][group][row] flo
 constexpr int kBarBytes = 256;
 constexpr int kSmem = 1024 + kQStages * kQBytes + kStages * (kKBytes + kVBytes) + kRedBytes + kBarBytes;
 constexpr uint32_t kColP = 256;  // TMEM columns of P (bf16 pairs; group g at + 64 g)
+constexpr int kMaxTail = 40;     // split items the workspace holds partial results for
+constexpr size_t kPartO = static_cast<size_t>(kBQ) * kD * 4;  // one CTA's fp32 O of a half
+constexpr size_t kPartML = static_cast<size_t>(kBQ) * 2 * 4;  // one CTA's (m, l) of a half
 constexpr uint32_t kColO = 384;  // TMEM columns of O
 constexpr float kRescaleLog2 = 8.0f;  // move the running max once it grows by more than this
 constexpr float kLog2e = 1.4426950408889634f;
@@ -88,7 +98,11 @@ struct AttnParams {
   uint8_t* vg;
   __nv_bfloat16* out;  // [H, Lq, d]
   uint64_t* flags;     // [W][H][ceil(Lr / 128)]: K and V block gathered
+  float* part_o;       // [tail item][half][CTA of the pair][128 rows][128 dims] fp32
+  float* part_ml;      // [tail item][half][CTA of the pair][128 rows][m, l] fp32
+  unsigned long long* tail_ctr;  // [tail item][CTA of the pair]: epoch of the first half done
   int W, rank, Lq, Lr, heads;
+  int nfull, ntail;    // whole items [0, nfull); items [nfull, nfull + ntail) split in halves
   float scale;  // 1 / sqrt(d)
 };
 
@@ -197,6 +211,31 @@ __device__ __forceinline__ void commit_both(uint64_t* bar) {
                : "memory");
 }
 
+// A pair's work units, in order: the whole items pair, pair + P, ... below nfull, then (for
+// pair < 2 ntail) half pair mod 2 of the split item nfull + pair / 2.  half = -1 for a whole
+// item; key blocks [jb, je) of the item's block order.
+struct AttnUnit {
+  int it, jb, je, half;
+};
+__device__ __forceinline__ int attn_whole_units(int pair, int npairs, int nfull) {
+  return pair < nfull ? (nfull - pair + npairs - 1) / npairs : 0;
+}
+__device__ __forceinline__ AttnUnit attn_unit(int k, int pair, int npairs, int nfull, int nblk) {
+  AttnUnit u;
+  if (k < attn_whole_units(pair, npairs, nfull)) {
+    u.it = pair + k * npairs;
+    u.jb = 0;
+    u.je = nblk;
+    u.half = -1;
+  } else {
+    u.it = nfull + pair / 2;
+    u.half = pair & 1;
+    u.jb = u.half ? nblk / 2 : 0;
+    u.je = u.half ? nblk : nblk / 2;
+  }
+  return u;
+}
+
 // Ragged: some shard length l_r is not a multiple of 256 (a partial last key block of every
 // shard and a partial last query tile); the common case is compiled without those checks.
 template <bool Ragged>
@@ -226,7 +265,12 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
   uint64_t* drain = bars + 17;
   // this CTA's partner warps (the two softmax warps of one TMEM lane quadrant), per exchange
   uint64_t* xq = bars + 18;      // [4]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 22);
+  // this CTA's softmax warps, once per split item: all 8 wrote their partial results; the
+  // counter exchange is done and its outcome is in tail_second
+  uint64_t* tail_w = bars + 22;
+  uint64_t* tail_r = bars + 23;
+  volatile uint32_t* tail_second = reinterpret_cast<volatile uint32_t*>(bars + 24);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 25);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();
@@ -237,7 +281,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
   const int sbs = (p.Lr + kSigBlk - 1) / kSigBlk;  // 128-key signal blocks per shard
   const int nblk = p.W * bps;                      // key blocks per item
   const int nqt = (p.Lq + 2 * kBQ - 1) / (2 * kBQ);  // 256-query tiles (the last may be partial)
-  const int nwork = p.heads * nqt;
+  const int nunits = attn_whole_units(pair, npairs, p.nfull) + (pair < 2 * p.ntail ? 1 : 0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(&qfull[s], 1);
@@ -254,6 +298,8 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
     mbar_init(pfree, 1);
     mbar_init(drain, 1);
     for (int q = 0; q < 4; ++q) mbar_init(&xq[q], 2);
+    mbar_init(tail_w, kSoftWarps);
+    mbar_init(tail_r, 1);
     fence_mbar_init();
     tma_prefetch_map(&p.q);
     tma_prefetch_map(&p.k_loc);
@@ -276,9 +322,10 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
     // ------------------------------------------------------------ producer (both CTAs)
     bool ok = true;
     uint32_t filled = 0, par = 0;  // leader's drain: K stages bits 0-1, V 2-3, Q 4-5
-    int J = 0, kq = 0;
-    for (int it = pair; it < nwork && ok; it += npairs, ++kq) {
-      const int h = it / nqt, qt = it - h * nqt;
+    int J = 0;
+    for (int kq = 0; kq < nunits && ok; ++kq) {
+      const AttnUnit u = attn_unit(kq, pair, npairs, p.nfull, nblk);
+      const int h = u.it / nqt, qt = u.it - h * nqt;
       const int qs = kq & 1;
       const uint32_t qph = (kq >> 1) & 1;
       if (lane == 0) {
@@ -293,11 +340,11 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      for (int j = 0; j < nblk && ok; ++j, ++J) {
+      for (int j = u.jb; j < u.je && ok; ++j, ++J) {
         const int step = j / bps, blk = j - step * bps;
         const int r = (p.rank + step) % p.W;
         const bool local = step == 0;
-        if (!local && blk == 0) {
+        if (!local && (blk == 0 || j == u.jb)) {
           // consumer_tile_wait on the shard's slice of this head: all its blocks gathered
           ok = warp_wait_signals(p.flags + (static_cast<size_t>(r) * p.heads + h) * sbs, sbs, c.epoch, c, lane,
                                  kSiteSignal, (7ull << 60) | (static_cast<unsigned long long>(r) << 32) | h);
@@ -346,8 +393,10 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
     // Per block J: S(J + 1) (the next item's first block when J ends an item) once the
     // softmax has read S(J), then P(J) V_J once P(J) is written.
     if (leader && lane == 0) {
-      const int nitems = pair < nwork ? (nwork - pair + npairs - 1) / npairs : 0;
-      const int total = nitems * nblk;
+      const int nwhole = attn_whole_units(pair, npairs, p.nfull);
+      // key blocks of unit k
+      auto nb_of = [&](int k) { return k < nwhole ? nblk : ((pair & 1) ? nblk - nblk / 2 : nblk / 2); };
+      int total = nwhole * nblk + (nunits > nwhole ? nb_of(nwhole) : 0);
       const uint32_t sk0 = smem_u32(sk), sv0 = smem_u32(sv), sq0 = smem_u32(sq);
       // S of block Jn (position jn in item kqn), and its commits
       auto issue_s = [&](int Jn, int jn, int kqn) -> bool {
@@ -358,7 +407,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         attn_mma_s(tmem, sq0 + (kqn & 1) * kQBytes, sk0 + s * kKBytes);
         commit_both(sfull);
         commit_both(&kempty[s]);
-        if (jn == nblk - 1) commit_both(&qempty[kqn & 1]);
+        if (jn == nb_of(kqn) - 1) commit_both(&qempty[kqn & 1]);
         return true;
       };
       bool ok = true;
@@ -366,7 +415,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
       int j = 0, kq = 0;
       for (int J = 0; J < total && ok; ++J) {
         const int s = J & 1;
-        const int jn = j + 1 == nblk ? 0 : j + 1, kqn = jn == 0 ? kq + 1 : kq;
+        const int jn = j + 1 == nb_of(kq) ? 0 : j + 1, kqn = jn == 0 ? kq + 1 : kq;
         if (J + 1 < total) {  // S(J + 1) overwrites S(J): every softmax warp has read it
           ok = mbar_wait(sfree, J & 1, c, kSiteTmemEmpty) && issue_s(J + 1, jn, kqn);
           if (!ok) break;
@@ -412,11 +461,16 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
       return true;
     };
     bool pfree_seen = true;  // P(J - 1) V_{J-1} known complete
-    for (int it = pair; it < nwork && ok; it += npairs, J0 += nblk) {
-      const int h = it / nqt, qt = it - h * nqt;
+    int ntail_done = 0;  // split items this CTA took part in
+    for (int kq = 0; kq < nunits && ok; ++kq) {
+      int nb, blk;  // the unit's key blocks; the block index inside the current shard
+      {
+        const AttnUnit u = attn_unit(kq, pair, npairs, p.nfull, nblk);
+        nb = u.je - u.jb;
+        blk = u.jb % bps - 1;
+      }
       float m2 = -INFINITY, l = 0.f;  // running max (base-2 units, common to both groups), this group's sum
-      int blk = -1;                   // block index inside the current shard
-      for (int j = 0; j < nblk && ok; ++j) {
+      for (int j = 0; j < nb && ok; ++j) {
         const int J = J0 + j;
         if (++blk == bps) blk = 0;
         // The wait results are warp-uniform, as the warp-collective TMEM accesses below need:
@@ -521,34 +575,107 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_relaxed(lead(pready));
       }
-      // The item's last P V has completed: O / (l_0 + l_1); this group writes head dims
-      // [64 g, 64 g + 64).
-      const int Jl = J0 + nblk - 1;
+      // The unit's last P V has completed.  A whole item writes O / (l_0 + l_1); this group
+      // writes head dims [64 g, 64 g + 64).
+      const int Jl = J0 + nb - 1;
+      J0 += nb;
       if (ok) ok = mbar_wait(pfree, Jl & 1, c, kSiteTmemFull);
       tc_fence_after();
       float ol = 0.f;
       if (ok) ok = exchange(l, ol);
-      if (ok) {
+      const AttnUnit u = attn_unit(kq, pair, npairs, p.nfull, nblk);
+      const int h = u.it / nqt, qt = u.it - h * nqt;
+      // Every lane takes part in the (warp-collective) TMEM loads; rows past the end of the
+      // queries (a partial last tile) are only not stored.
+      const int qrow = qt * 2 * kBQ + static_cast<int>(crank) * kBQ + row;
+      const bool live = !Ragged || qrow < p.Lq;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(h) * p.Lq + qrow) * kD + g * 64);
+      if (ok && u.half < 0) {
         const float inv = 1.0f / (l + ol);
-        // Every lane takes part in the (warp-collective) TMEM loads; rows past the end of
-        // the queries (a partial last tile) are only not stored.
-        const int qrow = qt * 2 * kBQ + static_cast<int>(crank) * kBQ + row;
-        const bool live = !Ragged || qrow < p.Lq;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(h) * p.Lq + qrow) * kD + g * 64);
 #pragma unroll 1
         for (int cb = 0; cb < 2; ++cb) {
           float o[32];
           tmem_ld32(tog + cb * 32 + lane_off, o);
           if (live) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              dst[cb * 4 + u] = make_uint4(pack_bf16x2(o[8 * u] * inv, o[8 * u + 1] * inv),
-                                           pack_bf16x2(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
-                                           pack_bf16x2(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
-                                           pack_bf16x2(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
+            for (int v = 0; v < 4; ++v)
+              dst[cb * 4 + v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
+                                           pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
+                                           pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
+                                           pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
           }
         }
-        // O read: the next item's first P V may overwrite it
+      } else if (ok) {
+        // A half: write this CTA's partial results, then exchange the epoch into the item's
+        // counter; the half that finds this call's epoch there already combines.
+        const int t = u.it - p.nfull;
+        const size_t slot = (static_cast<size_t>(t) * 2 + u.half) * 2 + crank;
+        const size_t other = (static_cast<size_t>(t) * 2 + (1 - u.half)) * 2 + crank;
+        float* po = p.part_o + slot * (kPartO / 4) + static_cast<size_t>(row) * kD + g * 64;
+        float o[2][32];
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {
+          tmem_ld32(tog + cb * 32 + lane_off, o[cb]);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            reinterpret_cast<float4*>(po + cb * 32)[v] =
+                make_float4(o[cb][4 * v], o[cb][4 * v + 1], o[cb][4 * v + 2], o[cb][4 * v + 3]);
+        }
+        const float lt = l + ol;
+        if (g == 0) reinterpret_cast<float2*>(p.part_ml + slot * (kPartML / 4))[row] = make_float2(m2, lt);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tail_w);
+        if (warp == 2 && lane == 0) {
+          ok = mbar_wait(tail_w, ntail_done & 1, c, kSiteTmemFull);
+          if (ok) {
+            __threadfence();
+            const unsigned long long prev = atomicExch(p.tail_ctr + static_cast<size_t>(t) * 2 + crank, c.epoch);
+            *tail_second = prev == c.epoch ? 1u : 0u;
+          }
+          mbar_arrive(tail_r);
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (ok) ok = mbar_wait(tail_r, ntail_done & 1, c, kSiteTmemFull);
+        ++ntail_done;
+        if (ok && *tail_second) {
+          __threadfence();
+          const float* qo = p.part_o + other * (kPartO / 4) + static_cast<size_t>(row) * kD + g * 64;
+          const float2 mlo = __ldcg(reinterpret_cast<const float2*>(p.part_ml + other * (kPartML / 4)) + row);
+          // half 0's values first, whichever half this is
+          const float ma = u.half == 0 ? m2 : mlo.x, la = u.half == 0 ? lt : mlo.y;
+          const float mb = u.half == 0 ? mlo.x : m2, lb = u.half == 0 ? mlo.y : lt;
+          const float m = fmaxf(ma, mb);
+          const float ca = ex2_approx(ma - m), cbb = ex2_approx(mb - m);
+          const float inv = 1.0f / (la * ca + lb * cbb);
+          const float wa = ca * inv, wb = cbb * inv;
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb) {
+            float q[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const float4 t4 = __ldcg(reinterpret_cast<const float4*>(qo + cb * 32) + v);
+              q[4 * v] = t4.x;
+              q[4 * v + 1] = t4.y;
+              q[4 * v + 2] = t4.z;
+              q[4 * v + 3] = t4.w;
+            }
+            float r[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              r[i] = u.half == 0 ? o[cb][i] * wa + q[i] * wb : q[i] * wa + o[cb][i] * wb;
+            if (live) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                dst[cb * 4 + v] = make_uint4(pack_bf16x2(r[8 * v], r[8 * v + 1]), pack_bf16x2(r[8 * v + 2], r[8 * v + 3]),
+                                             pack_bf16x2(r[8 * v + 4], r[8 * v + 5]),
+                                             pack_bf16x2(r[8 * v + 6], r[8 * v + 7]));
+            }
+          }
+        }
+      }
+      if (ok) {
+        // O read: the next unit's first P V may overwrite it
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_relaxed(lead(ofree));
@@ -621,11 +748,35 @@ static bool attn_shape_ok(int W, int heads, int l_r, int d) {
          static_cast<long long>(W) * l_r < (1LL << 30);
 }
 
+// Split items the workspace holds partial results for: at most one per two pairs of any grid
+// up to 2 kMaxTail pairs, and no more than there are items.
+static size_t attn_max_tail(int heads, int l_r) {
+  const size_t nwork = static_cast<size_t>(heads) * ((l_r + 2 * attn::kBQ - 1) / (2 * attn::kBQ));
+  return nwork < static_cast<size_t>(attn::kMaxTail) ? nwork : static_cast<size_t>(attn::kMaxTail);
+}
+
+// Workspace: gathered K, gathered V, block signals, split-item partials (O, then m and l),
+// split-item counters; each region 256-byte aligned.
+struct AttnLayout {
+  size_t kv, v_off, flags_off, part_o_off, part_ml_off, ctr_off, total;
+};
+static AttnLayout attn_layout(int W, int heads, int l_r, int d) {
+  AttnLayout L;
+  L.kv = static_cast<size_t>(heads) * W * l_r * d * 2;
+  const size_t flags = static_cast<size_t>(W) * heads * ((l_r + attn::kSigBlk - 1) / attn::kSigBlk) * 8;
+  const size_t tail = attn_max_tail(heads, l_r);
+  L.v_off = attn_al256(L.kv);
+  L.flags_off = L.v_off + attn_al256(L.kv);
+  L.part_o_off = L.flags_off + attn_al256(flags);
+  L.part_ml_off = L.part_o_off + attn_al256(tail * 4 * attn::kPartO);
+  L.ctr_off = L.part_ml_off + attn_al256(tail * 4 * attn::kPartML);
+  L.total = L.ctr_off + attn_al256(tail * 2 * 8);
+  return L;
+}
+
 extern "C" size_t tl_ag_attention_workspace_bytes(int W, int heads, int l_r, int d) {
   if (!attn_shape_ok(W, heads, l_r, d)) return 0;
-  const size_t kv = static_cast<size_t>(heads) * W * l_r * d * 2;
-  const size_t flags = static_cast<size_t>(W) * heads * ((l_r + attn::kSigBlk - 1) / attn::kSigBlk) * 8;
-  return 2 * attn_al256(kv) + attn_al256(flags);
+  return attn_layout(W, heads, l_r, d).total;
 }
 
 extern "C" int tl_ag_attention(tl_ctx* ctx, int W, int rank, const void* q, const void* const* k_shards,
@@ -640,13 +791,16 @@ extern "C" int tl_ag_attention(tl_ctx* ctx, int W, int rank, const void* q, cons
   if (workspace_bytes < tl_ag_attention_workspace_bytes(W, heads, l_r, d)) return TL_ERR_WORKSPACE;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return TL_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t kv = static_cast<size_t>(heads) * W * l_r * d * 2;
+  const AttnLayout lay = attn_layout(W, heads, l_r, d);
 
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
   p.kg = ws;
-  p.vg = ws + attn_al256(kv);
-  p.flags = reinterpret_cast<uint64_t*>(ws + 2 * attn_al256(kv));
+  p.vg = ws + lay.v_off;
+  p.flags = reinterpret_cast<uint64_t*>(ws + lay.flags_off);
+  p.part_o = reinterpret_cast<float*>(ws + lay.part_o_off);
+  p.part_ml = reinterpret_cast<float*>(ws + lay.part_ml_off);
+  p.tail_ctr = reinterpret_cast<unsigned long long*>(ws + lay.ctr_off);
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint64_t WH = static_cast<uint64_t>(W) * heads;
   if (!tmap_3d(&p.q, BF, 2, q, d, l_r, heads, 64, 128, 1) ||
@@ -703,6 +857,17 @@ extern "C" int tl_ag_attention(tl_ctx* ctx, int W, int rank, const void* q, cons
   if (nclusters > max_clusters[ki]) nclusters = max_clusters[ki];
   if (nclusters < 1) return TL_ERR_UNSUPPORTED;
   cfg.gridDim = dim3(2 * nclusters, 1, 1);
+  // Split the last items into halves when they would fill less than half of the last wave
+  // (and the workspace holds their partials); a half needs at least one key block.
+  {
+    const int nqt = (l_r + 2 * attn::kBQ - 1) / (2 * attn::kBQ);
+    const int nwork = heads * nqt, nblk = W * ((l_r + attn::kBKV - 1) / attn::kBKV);
+    const int rem = nwork % nclusters;
+    const bool split = rem > 0 && 2 * rem <= nclusters && nblk >= 2 &&
+                       static_cast<size_t>(rem) <= attn_max_tail(heads, l_r);
+    p.ntail = split ? rem : 0;
+    p.nfull = nwork - p.ntail;
+  }
   if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_CUDA;

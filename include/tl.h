@@ -336,15 +336,19 @@ int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, int topk, co
  * q: bf16 [heads x l_r x d] (this rank's queries).  k_shards, v_shards: host arrays of W device
  * pointers, shard r bf16 [heads x l_r x d].  out: bf16 [heads x l_r x d].
  * workspace: tl_ag_attention_workspace_bytes(): the gathered K and V, shard-major
- * [W x heads x l_r x d] (shard r at r, filled completely, the local shard last), and one
- * signal per (shard, head, 128-key block).
- * One persistent cooperative launch: mover warps pull the remote shards' K/V blocks into the
- * gathered buffers and release each block's signal; the attention of each (head, 128-query
- * tile) reads its own shard in place first and a remote shard's blocks once all of them are
- * signalled.  The pages run this gather on the copy engine from a second stream; that makes
- * the kernel wait on work outside its own launch, which nothing guarantees to run alongside
- * it, so the gather runs inside the kernel, as for tl_ag_gemm.
- * Shapes: 1 <= W <= 8; d == 128; any l_r (a shard's last 128-key block and the last 128-query
+ * [W x heads x l_r x d] (shard r at r, filled completely, the local shard last), one signal
+ * per (shard, head, 128-key block), and room for the partial results of split items (below).
+ * One persistent launch of CTA pairs (clusters of 2, one CTA per SM): mover warps pull the
+ * remote shards' K/V blocks into the gathered buffers and release each block's signal; the
+ * attention of each (head, 256-query tile) reads its own shard in place first and a remote
+ * shard's blocks once all of them are signalled.  The pages run this gather on the copy
+ * engine from a second stream; that makes the kernel wait on work outside its own launch,
+ * which nothing guarantees to run alongside it, so the gather runs inside the kernel, as for
+ * tl_ag_gemm.  When the (head, tile) items leave the last wave of pairs less than half full,
+ * those last items are each split into two halves of their keys that run on two pairs; the
+ * half that finishes second combines both (in a fixed order: the result does not depend on
+ * which finished first).
+ * Shapes: 1 <= W <= 8; d == 128; any l_r (a shard's last 256-key block and the last 256-query
  * tile may be partial).  heads == 0 or l_r == 0 is a no-op.
  */
 size_t tl_ag_attention_workspace_bytes(int W, int heads, int l_r, int d);

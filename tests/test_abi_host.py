@@ -78,10 +78,17 @@ def test_workspace_sizes(tl):
     assert tl.tl_moe_workspace_bytes(4096, 2000, 64, 1408, 2) == 0    # H not a 256 multiple
     assert tl.tl_moe_workspace_bytes(4096, 2048, 300, 1408, 2) == 0   # E > 256
     al = lambda x: (x + 255) // 256 * 256
-    # attention: gathered K and V, then one signal per (shard, head, 128-key block), the last
-    # block of a shard partial when l_r is not a multiple of 128
-    assert tl.tl_ag_attention_workspace_bytes(8, 32, 2048, 128) == 2 * al(8 * 32 * 2048 * 128 * 2) + al(8 * 32 * 16 * 8)
-    assert tl.tl_ag_attention_workspace_bytes(3, 2, 200, 128) == 2 * al(3 * 2 * 200 * 128 * 2) + al(3 * 2 * 2 * 8)
+    # attention: gathered K and V, one signal per (shard, head, 128-key block) (the last block
+    # of a shard partial when l_r is not a multiple of 128), then the split items' partials:
+    # min(items, 40) items x 2 halves x 2 CTAs of fp32 O (128 x 128) and (m, l) per row, and
+    # one counter per item and CTA
+    def tail(items):
+        t = min(items, 40)
+        return al(t * 4 * 128 * 128 * 4) + al(t * 4 * 128 * 2 * 4) + al(t * 2 * 8)
+    assert tl.tl_ag_attention_workspace_bytes(8, 32, 2048, 128) == \
+        2 * al(8 * 32 * 2048 * 128 * 2) + al(8 * 32 * 16 * 8) + tail(32 * 8)
+    assert tl.tl_ag_attention_workspace_bytes(3, 2, 200, 128) == \
+        2 * al(3 * 2 * 200 * 128 * 2) + al(3 * 2 * 2 * 8) + tail(2 * 1)
     assert tl.tl_ag_attention_workspace_bytes(2, 2, 128, 64) == 0    # head dim other than 128
     assert tl.tl_ag_attention_workspace_bytes(9, 2, 128, 128) == 0   # W > 8
 

@@ -60,6 +60,37 @@ def test_ag_attention_ragged_lengths(W, H, L, rank):
     assert np.array_equal(np.concatenate(list(kg), axis=1), oracle.attn_gather(inp["k_shards"]))
 
 
+@pytest.mark.parametrize("W,H,L,ctas,rank", [
+    (3, 3, 256, 4, 1),   # 3 items on 2 pairs: items 0 and 1 whole, item 2 in halves of 1 and 2 blocks
+    (2, 2, 300, 6, 0),   # ragged: 4 items (2 heads x 2 query tiles) on 3 pairs, the last one split
+    (4, 5, 256, 8, 3),   # 5 items on 4 pairs, halves of 2 blocks each
+    (1, 2, 512, 6, 0),   # one rank: 4 items on 3 pairs, halves of one block
+    (3, 3, 512, 8, 2),   # 6 items on 4 pairs, two split; the second half starts inside a remote shard
+])
+def test_ag_attention_split_tail(W, H, L, ctas, rank):
+    """Grids whose last wave the items would fill less than half: the last items run as two
+    halves of their keys on two pairs and the half that finishes second combines both.
+    Against the oracle, and bit for bit across repeated calls on one workspace (either half
+    may finish second; the combine takes half 0 first either way)."""
+    import torch
+    inp = make_inputs("ag_attn", 120 + W * 10 + H, W=W, heads=H, l_r=L, d=128)
+    q = to_dev_bf16(inp["q"])
+    ks = [to_dev_bf16(x) for x in inp["k_shards"]]
+    vs = [to_dev_bf16(x) for x in inp["v_shards"]]
+    ws = workspace(tl.tl_ag_attention_workspace_bytes(W, H, L, 128))
+    ref = oracle.ag_attention(inp["q"], inp["k_shards"], inp["v_shards"])
+    outs = []
+    with tl.Context(0, timeout_ns=500_000_000, grid_ctas=ctas) as ctx:
+        for _ in range(3):
+            out = torch.full((H, L, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+            tl.tl_ag_attention(ctx, q, ks, vs, out, ws, rank=rank)
+            torch.cuda.synchronize()
+            assert ctx.check() == tl.TL_OK
+            outs.append(bf16_bits(out))
+    assert_close(bf16_to_f64(out), ref, f"attention split tail W={W} H={H} L={L} ctas={ctas}")
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+
+
 def test_ag_attention_peaked_scores():
     """Large-magnitude queries make the softmax peaked and its running maximum move a lot
     from block to block (the rescale of O in TMEM)."""
