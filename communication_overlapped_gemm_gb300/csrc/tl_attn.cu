@@ -478,46 +478,56 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         ok = mbar_wait(sfull, J & 1, c, kSiteTmemFull);
         if (!ok) break;
         tc_fence_after();
-        float x[128];
-        {
-          uint32_t rr[4][32];
-#pragma unroll
-          for (int cb = 0; cb < 4; ++cb) tmem_ld32_issue(tmem + g * 128 + cb * 32 + lane_off, rr[cb]);
+        // Keys past the end of a shard (its partial last block, zero-filled by TMA) get no
+        // weight: their scores become -inf.
+        const int valid = Ragged ? p.Lr - blk * kBKV - g * 128 : 128;
+        // 64 of this group's scores (columns [64 hf, 64 hf + 64)) into x
+        auto load64 = [&](int hf, float (&x)[64]) {
+          uint32_t rr[2][32];
+          tmem_ld32_issue(tmem + g * 128 + hf * 64 + lane_off, rr[0]);
+          tmem_ld32_issue(tmem + g * 128 + hf * 64 + 32 + lane_off, rr[1]);
           tmem_ld_wait(rr[0]);
           tmem_ld_after(rr[1]);
-          tmem_ld_after(rr[2]);
-          tmem_ld_after(rr[3]);
 #pragma unroll
-          for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(rr[i >> 5][i & 31]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster_relaxed(lead(sfree));
-        pfree_seen = J == 0;
-        if constexpr (Ragged) {
-          // keys past the end of a shard (its partial last block, zero-filled by TMA) get no
-          // weight: their scores become -inf before the maximum
-          const int valid = p.Lr - blk * kBKV - g * 128;
-          if (valid < 128) {
+          for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(rr[i >> 5][i & 31]);
+          if constexpr (Ragged) {
+            if (valid < 64 * hf + 64) {
 #pragma unroll
-            for (int i = 0; i < 128; ++i) x[i] = i < valid ? x[i] : -INFINITY;
+              for (int i = 0; i < 64; ++i) x[i] = i + 64 * hf < valid ? x[i] : -INFINITY;
+            }
           }
+        };
+        // First pass over S: the block max of this group's 128 scores, 64 at a time.
+        float bm2;
+        {
+          float mx[8];
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            float x[64];
+            load64(hf, x);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = hf == 0 ? fmax3(x[k], x[8 + k], x[16 + k]) : fmax3(mx[k], x[k], x[8 + k]);
+            // the first 64: x[0, 24), x[24, 56) sixteen at a time, x[56, 64); the second 64:
+            // x[0, 16) onto the first's maxima, then x[16, 64) sixteen at a time
+#pragma unroll
+            for (int i = (hf == 0 ? 24 : 16); i + 16 <= (hf == 0 ? 56 : 64); i += 16)
+#pragma unroll
+              for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], x[i + k], x[i + 8 + k]);
+            if (hf == 0) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], x[56 + k]);
+            }
+          }
+          bm2 = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+                sl2;  // the scale is positive: max commutes with it
         }
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = x[i];
-#pragma unroll
-        for (int i = 8; i < 128; i += 16)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], x[i + k], x[i + 8 + k]);
-        float bm2 = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
-                    sl2;  // the scale is positive: max commutes with it
         {
           float other;
           ok = exchange(bm2, other);
           if (!ok) break;
           bm2 = fmaxf(bm2, other);  // the block's max over all 256 keys: the same in both partners
         }
+        pfree_seen = J == 0;
         if (j == 0) {
           m2 = bm2;  // the item's first P V overwrites O
         } else if (__any_sync(0xffffffffu, bm2 > m2 + kRescaleLog2)) {
@@ -540,6 +550,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           l *= corr;
           m2 = mn;
         }
+        // Second pass over S: P and its sum, 64 scores at a time; then S(J) has been read.
         // (Ragged: a row whose keys so far are all absent has m2 = -inf; its P is 0.)
         const float nm = (Ragged && m2 == -INFINITY) ? 0.f : -m2;
         unsigned long long sum2[4];  // 8 partial sums, two per register pair
@@ -548,12 +559,22 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         for (int i = 0; i < 4; ++i) sum2[i] = 0ull;
         const unsigned long long sl2x2 = f2(sl2, sl2), nm2 = f2(nm, nm);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          float y0, y1;
-          f2_split(ffma2(f2(x[2 * i], x[2 * i + 1]), sl2x2, nm2), y0, y1);
-          const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
-          sum2[i & 3] = fadd2(sum2[i & 3], f2(e0, e1));
-          pk[i] = pack_bf16x2(e0, e1);
+        for (int hf = 0; hf < 2; ++hf) {
+          float x[64];
+          load64(hf, x);
+          if (hf == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(lead(sfree));
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float y0, y1;
+            f2_split(ffma2(f2(x[2 * i], x[2 * i + 1]), sl2x2, nm2), y0, y1);
+            const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
+            sum2[i & 3] = fadd2(sum2[i & 3], f2(e0, e1));
+            pk[32 * hf + i] = pack_bf16x2(e0, e1);
+          }
         }
         {
           const unsigned long long s2 = fadd2(fadd2(sum2[0], sum2[1]), fadd2(sum2[2], sum2[3]));
@@ -612,14 +633,13 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         const size_t slot = (static_cast<size_t>(t) * 2 + u.half) * 2 + crank;
         const size_t other = (static_cast<size_t>(t) * 2 + (1 - u.half)) * 2 + crank;
         float* po = p.part_o + slot * (kPartO / 4) + static_cast<size_t>(row) * kD + g * 64;
-        float o[2][32];
-#pragma unroll
+#pragma unroll 1
         for (int cb = 0; cb < 2; ++cb) {
-          tmem_ld32(tog + cb * 32 + lane_off, o[cb]);
+          float o[32];
+          tmem_ld32(tog + cb * 32 + lane_off, o);
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            reinterpret_cast<float4*>(po + cb * 32)[v] =
-                make_float4(o[cb][4 * v], o[cb][4 * v + 1], o[cb][4 * v + 2], o[cb][4 * v + 3]);
+            reinterpret_cast<float4*>(po + cb * 32)[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
         }
         const float lt = l + ol;
         if (g == 0) reinterpret_cast<float2*>(p.part_ml + slot * (kPartML / 4))[row] = make_float2(m2, lt);
@@ -649,9 +669,11 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           const float ca = ex2_approx(ma - m), cbb = ex2_approx(mb - m);
           const float inv = 1.0f / (la * ca + lb * cbb);
           const float wa = ca * inv, wb = cbb * inv;
-#pragma unroll
+#pragma unroll 1
           for (int cb = 0; cb < 2; ++cb) {
-            float q[32];
+            // this half's O is still in TMEM (the next unit's first P V waits for ofree)
+            float o[32], q[32];
+            tmem_ld32(tog + cb * 32 + lane_off, o);
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
               const float4 t4 = __ldcg(reinterpret_cast<const float4*>(qo + cb * 32) + v);
@@ -660,16 +682,14 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
               q[4 * v + 2] = t4.z;
               q[4 * v + 3] = t4.w;
             }
-            float r[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              r[i] = u.half == 0 ? o[cb][i] * wa + q[i] * wb : q[i] * wa + o[cb][i] * wb;
+            for (int i = 0; i < 32; ++i) o[i] = u.half == 0 ? o[i] * wa + q[i] * wb : q[i] * wa + o[i] * wb;
             if (live) {
 #pragma unroll
               for (int v = 0; v < 4; ++v)
-                dst[cb * 4 + v] = make_uint4(pack_bf16x2(r[8 * v], r[8 * v + 1]), pack_bf16x2(r[8 * v + 2], r[8 * v + 3]),
-                                             pack_bf16x2(r[8 * v + 4], r[8 * v + 5]),
-                                             pack_bf16x2(r[8 * v + 6], r[8 * v + 7]));
+                dst[cb * 4 + v] = make_uint4(pack_bf16x2(o[8 * v], o[8 * v + 1]), pack_bf16x2(o[8 * v + 2], o[8 * v + 3]),
+                                             pack_bf16x2(o[8 * v + 4], o[8 * v + 5]),
+                                             pack_bf16x2(o[8 * v + 6], o[8 * v + 7]));
             }
           }
         }
