@@ -49,7 +49,8 @@ MOE_LAUNCHES = 3  # routing, permutation, the persistent expert-GEMM + combine k
 # dram__bytes_write.sum), keyed by the hash of the kernel's sources (AG_KERNEL_SOURCES) they
 # were taken on.
 # A kernel changed since the capture reports traffic null.
-NCU_TRAFFIC = {"ag_70b": {"fe1bb8d7778bd175": 587978240}}  # profiles/ag_70b_persistent_kernel_ncu.md
+NCU_TRAFFIC = {"ag_70b": {"fe1bb8d7778bd175": 587978240,   # profiles/ag_70b_persistent_kernel_ncu.md
+                           "33004dd266fe890c": 587501056}}  # its traffic re-capture
 
 
 # The sources the AllGather+GEMM kernel is compiled from: its translation unit and every
