@@ -394,6 +394,17 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
         if extra:
             r["copy_alone"] = extra
 
+    def cublas_leg(r, fn, flops):
+        """Context: the same products through cuBLAS (torch.matmul into preallocated bf16
+        outputs), timed like the fused call: the library GEMM under the same tensor load."""
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        t = statistics.median(timed_steps(fn, max(3, reps // 2), flush, stream))
+        r["cublas_gemms_us"] = round(t * 1e3, 2)
+        r["cublas_gemms_tflops"] = round(flops / (t * 1e-3) / 1e12, 2)
+        r["fused_over_cublas_gemms"] = round(r["us"] / (t * 1e3), 4)
+
     def rec(name, fn, flops, bytes_alg, bound, launches):
         for _ in range(3):
             fn()
@@ -447,7 +458,9 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     ws1 = torch.zeros(tl.tl_ag_gemm_workspace_bytes(1, m, n, kr), dtype=torch.uint8, device=device)
     gemm_alone(out["rs_70b"], lambda: [tl.tl_ag_gemm(ctx, [a[p]], b[p], cp, ws1, stream=stream) for p in range(W)],
                2.0 * W * m * n * kr)
-    del cp, ws1
+    del ws1
+    cublas_leg(out["rs_70b"], lambda: [torch.matmul(a[p], b[p], out=cp) for p in range(W)], 2.0 * W * m * n * kr)
+    del cp
     # the communication alone: the ReduceScatter of the W ranks' fp32 partials (m x n each)
     parts = [torch.randn((m, n), dtype=torch.float32, device=device) for _ in range(W)]
     rs_alone(out["rs_70b"], lambda: tl.tl_reduce_scatter(ctx, parts, o, stream=stream), W * m * n * 4 + m * n * 2)
@@ -490,6 +503,12 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
             tl.tl_ag_gemm(ctx, [xg], w1[r], hbuf, ws1, stream=stream)
             tl.tl_ag_gemm(ctx, [hbuf], w2[r], ybuf, ws1, stream=stream)
     gemm_alone(out["mlp2_8b"], mlp_plain, 2.0 * W * T * hdim * f * 2)
+
+    def mlp_cublas():
+        for r in range(W):
+            torch.matmul(xg, w1[r], out=hbuf)
+            torch.matmul(hbuf, w2[r], out=ybuf)
+    cublas_leg(out["mlp2_8b"], mlp_cublas, 2.0 * W * T * hdim * f * 2)
     del xg, hbuf, ybuf, ws1
     # the communication alone: every rank's AllGather of X, then the ReduceScatter of the W
     # ranks' fp32 layer-2 partials (T x hidden each)
