@@ -450,15 +450,20 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
     // Exchange one float per row with the partner warp (same rows, other key group) through
     // red, double-buffered by exchange parity: exchange n + 2 rewrites a buffer only after the
     // partner has arrived for exchange n + 1, i.e. after it read exchange n.  Bounded waits.
-    auto exchange = [&](float mine, float& other) -> bool {
-      float* buf = red + (nx & 1) * 2 * kBQ;
-      buf[g * kBQ + row] = mine;
+    auto post = [&](float mine) {
+      red[(nx & 1) * 2 * kBQ + g * kBQ + row] = mine;
       __syncwarp();
       if (lane == 0) mbar_arrive(&xq[qd]);
+    };
+    auto collect = [&](float& other) -> bool {
       if (!mbar_wait(&xq[qd], nx & 1, c, kSiteTmemFull)) return false;
-      other = buf[(1 - g) * kBQ + row];
+      other = red[(nx & 1) * 2 * kBQ + (1 - g) * kBQ + row];
       ++nx;
       return true;
+    };
+    auto exchange = [&](float mine, float& other) -> bool {
+      post(mine);
+      return collect(other);
     };
     bool pfree_seen = true;  // P(J - 1) V_{J-1} known complete
     int ntail_done = 0;  // split items this CTA took part in
@@ -521,11 +526,27 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           bm2 = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
                 sl2;  // the scale is positive: max commutes with it
         }
+        // The partner's block max arrives while the first 64 scores are reloaded.
+        post(bm2);
+        float x0[64];
         {
+          uint32_t rr[2][32];
+          tmem_ld32_issue(tmem + g * 128 + lane_off, rr[0]);
+          tmem_ld32_issue(tmem + g * 128 + 32 + lane_off, rr[1]);
           float other;
-          ok = exchange(bm2, other);
+          ok = collect(other);
+          tmem_ld_wait(rr[0]);
+          tmem_ld_after(rr[1]);
           if (!ok) break;
           bm2 = fmaxf(bm2, other);  // the block's max over all 256 keys: the same in both partners
+#pragma unroll
+          for (int i = 0; i < 64; ++i) x0[i] = __uint_as_float(rr[i >> 5][i & 31]);
+          if constexpr (Ragged) {
+            if (valid < 64) {
+#pragma unroll
+              for (int i = 0; i < 64; ++i) x0[i] = i < valid ? x0[i] : -INFINITY;
+            }
+          }
         }
         pfree_seen = J == 0;
         if (j == 0) {
@@ -561,8 +582,11 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float x[64];
-          load64(hf, x);
-          if (hf == 1) {
+          if (hf == 0) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) x[i] = x0[i];
+          } else {
+            load64(hf, x);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster_relaxed(lead(sfree));
