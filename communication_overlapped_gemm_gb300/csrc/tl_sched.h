@@ -7,7 +7,8 @@
 // rank swizzle of "Triton-distributed: Programming Overlapping Kernels on
 // Distributed AI Systems with the Triton Compiler", §3.7:
 //   AllGather+GEMM: step s computes with the shard of rank (rank + s) mod W, so each
-//     rank starts on its local shard while the next one is being pulled.
+//     rank starts on its local shard while the next one is being pulled (inside a step,
+//     groups of row blocks: see ag_tile).
 //   GEMM+ReduceScatter: inside each L2-sized band of the output, producer p starts at the
 //     rows of owner (p + 1) mod W (see rs_tile).
 // The same functions are compiled for the host (tl_*_tile_order, used by the tests)
@@ -37,14 +38,30 @@ struct AgTile {
 // AllGather + GEMM: W steps of (mps row blocks x nbk column blocks).
 TL_HD int ag_num_tiles(int W, int mps, int nbk) { return W * mps * nbk; }
 TL_HD int ag_step_rank(int W, int rank, int swizzle, int s) { return swizzle ? (rank + s) % W : s; }
+// Inside a step the tiles run in groups of TL_AG_GROUP row blocks, the row block fastest
+// inside a group: a wave of CTAs then covers a block about 8 row blocks tall instead of a
+// few full rows of tiles, so it needs fewer distinct A and B panels at once (measured: the
+// 8192 x 8192 x 3584 plain GEMM 263-264 us against 268-270 us row-major).  0 = row-major.
+#ifndef TL_AG_GROUP
+#define TL_AG_GROUP 8
+#endif
 TL_HD AgTile ag_tile(int t, int W, int rank, int mps, int nbk, int swizzle) {
   const int per_step = mps * nbk;
   const int s = t / per_step;
   const int rem = t - s * per_step;
   AgTile r;
   r.src = ag_step_rank(W, rank, swizzle, s);
-  r.mb = rem / nbk;
-  r.nb = rem - r.mb * nbk;
+  if (TL_AG_GROUP > 0) {
+    // groups of TL_AG_GROUP row blocks, the row block fastest inside a group
+    const int gsz = TL_AG_GROUP * nbk;
+    const int g = rem / gsz, r2 = rem - g * gsz;
+    const int rows = mps - g * TL_AG_GROUP < TL_AG_GROUP ? mps - g * TL_AG_GROUP : TL_AG_GROUP;
+    r.nb = r2 / rows;
+    r.mb = g * TL_AG_GROUP + (r2 - r.nb * rows);
+  } else {
+    r.mb = rem / nbk;
+    r.nb = rem - r.mb * nbk;
+  }
   return r;
 }
 
