@@ -50,7 +50,8 @@ MOE_LAUNCHES = 3  # routing, permutation, the persistent expert-GEMM + combine k
 # were taken on.
 # A kernel changed since the capture reports traffic null.
 NCU_TRAFFIC = {"ag_70b": {"fe1bb8d7778bd175": 587978240,   # profiles/ag_70b_persistent_kernel_ncu.md
-                           "33004dd266fe890c": 587501056}}  # its traffic re-capture
+                           "33004dd266fe890c": 587501056,   # its traffic re-captures
+                           "c63981ffce7b1bcf": 612093952}}
 
 
 # The sources the AllGather+GEMM kernel is compiled from: its translation unit and every
