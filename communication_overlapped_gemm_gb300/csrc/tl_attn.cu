@@ -195,6 +195,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// Two fp32 values as an f16x2 pair (round to nearest; lo in the low half) and back.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ void unpack_f16x2(uint32_t v, float& lo, float& hi) {
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(v));
+}
+
 // Relaxed arrival on an mbarrier given by its shared::cluster address: no memory ordering is
 // implied (a release at cluster scope costs a full memory barrier on every call).  Used where
 // what the arrival announces is already complete in this thread: its TMEM reads
@@ -486,67 +497,61 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         // Keys past the end of a shard (its partial last block, zero-filled by TMA) get no
         // weight: their scores become -inf.
         const int valid = Ragged ? p.Lr - blk * kBKV - g * 128 : 128;
-        // 64 of this group's scores (columns [64 hf, 64 hf + 64)) into x
-        auto load64 = [&](int hf, float (&x)[64]) {
-          uint32_t rr[2][32];
-          tmem_ld32_issue(tmem + g * 128 + hf * 64 + lane_off, rr[0]);
-          tmem_ld32_issue(tmem + g * 128 + hf * 64 + 32 + lane_off, rr[1]);
+        // One read of this group's 128 scores.  The block max needs them all; then the first
+        // 64 stay in fp32 and the second 64 are kept as f16 pairs of y' = s sl2 - lm (lm this
+        // group's block max, base 2): y' <= 0, and for the weights that matter (y' within
+        // about 2^4 of 0) f16's 11-bit significand is finer than P's bf16 rounding.  S(J) is
+        // then read, and S(J + 1) can be computed while the exponentials run.
+        float x0[64];
+        uint32_t h1[32];
+        float lm;  // this group's block max (base 2)
+        {
+          uint32_t rr[4][32];
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb) tmem_ld32_issue(tmem + g * 128 + cb * 32 + lane_off, rr[cb]);
           tmem_ld_wait(rr[0]);
           tmem_ld_after(rr[1]);
+          tmem_ld_after(rr[2]);
+          tmem_ld_after(rr[3]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_relaxed(lead(sfree));
+          float x[128];
 #pragma unroll
-          for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(rr[i >> 5][i & 31]);
+          for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(rr[i >> 5][i & 31]);
           if constexpr (Ragged) {
-            if (valid < 64 * hf + 64) {
+            if (valid < 128) {
 #pragma unroll
-              for (int i = 0; i < 64; ++i) x[i] = i + 64 * hf < valid ? x[i] : -INFINITY;
+              for (int i = 0; i < 128; ++i) x[i] = i < valid ? x[i] : -INFINITY;
             }
           }
-        };
-        // First pass over S: the block max of this group's 128 scores, 64 at a time.
-        float bm2;
-        {
+          // x[8, 120) sixteen at a time onto x[0, 8), then x[120, 128)
           float mx[8];
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            float x[64];
-            load64(hf, x);
+          for (int k = 0; k < 8; ++k) mx[k] = x[k];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) mx[k] = hf == 0 ? fmax3(x[k], x[8 + k], x[16 + k]) : fmax3(mx[k], x[k], x[8 + k]);
-            // the first 64: x[0, 24), x[24, 56) sixteen at a time, x[56, 64); the second 64:
-            // x[0, 16) onto the first's maxima, then x[16, 64) sixteen at a time
+          for (int i = 8; i < 120; i += 16)
 #pragma unroll
-            for (int i = (hf == 0 ? 24 : 16); i + 16 <= (hf == 0 ? 56 : 64); i += 16)
+            for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], x[i + k], x[i + 8 + k]);
 #pragma unroll
-              for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], x[i + k], x[i + 8 + k]);
-            if (hf == 0) {
+          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], x[120 + k]);
+          lm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+               sl2;  // the scale is positive: max commutes with it
+          // (Ragged: a group with no valid key in this block has lm = -inf; its y' are -inf.)
+          const float nlm = (Ragged && lm == -INFINITY) ? 0.f : -lm;
 #pragma unroll
-              for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], x[56 + k]);
-            }
-          }
-          bm2 = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
-                sl2;  // the scale is positive: max commutes with it
+          for (int i = 0; i < 64; ++i) x0[i] = x[i];
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            h1[i] = pack_f16x2(fmaf(x[64 + 2 * i], sl2, nlm), fmaf(x[65 + 2 * i], sl2, nlm));
         }
-        // The partner's block max arrives while the first 64 scores are reloaded.
-        post(bm2);
-        float x0[64];
+        post(lm);
+        float bm2;
         {
-          uint32_t rr[2][32];
-          tmem_ld32_issue(tmem + g * 128 + lane_off, rr[0]);
-          tmem_ld32_issue(tmem + g * 128 + 32 + lane_off, rr[1]);
           float other;
           ok = collect(other);
-          tmem_ld_wait(rr[0]);
-          tmem_ld_after(rr[1]);
           if (!ok) break;
-          bm2 = fmaxf(bm2, other);  // the block's max over all 256 keys: the same in both partners
-#pragma unroll
-          for (int i = 0; i < 64; ++i) x0[i] = __uint_as_float(rr[i >> 5][i & 31]);
-          if constexpr (Ragged) {
-            if (valid < 64) {
-#pragma unroll
-              for (int i = 0; i < 64; ++i) x0[i] = i < valid ? x0[i] : -INFINITY;
-            }
-          }
+          bm2 = fmaxf(lm, other);  // the block's max over all 256 keys: the same in both partners
         }
         pfree_seen = J == 0;
         if (j == 0) {
@@ -571,33 +576,36 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           l *= corr;
           m2 = mn;
         }
-        // Second pass over S: P and its sum, 64 scores at a time; then S(J) has been read.
+        // P and its sum: the first 64 from the scores, the second 64 from y' + (lm - m2) (<= 2^8:
+        // lm <= the block max <= m2 + 2^8).
         // (Ragged: a row whose keys so far are all absent has m2 = -inf; its P is 0.)
         const float nm = (Ragged && m2 == -INFINITY) ? 0.f : -m2;
+        const float d1 = (Ragged && (lm == -INFINITY || m2 == -INFINITY)) ? 0.f : lm - m2;
         unsigned long long sum2[4];  // 8 partial sums, two per register pair
         uint32_t pk[64];
 #pragma unroll
         for (int i = 0; i < 4; ++i) sum2[i] = 0ull;
-        const unsigned long long sl2x2 = f2(sl2, sl2), nm2 = f2(nm, nm);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float x[64];
-          if (hf == 0) {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) x[i] = x0[i];
-          } else {
-            load64(hf, x);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster_relaxed(lead(sfree));
-          }
+        {
+          const unsigned long long sl2x2 = f2(sl2, sl2), nm2 = f2(nm, nm);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             float y0, y1;
-            f2_split(ffma2(f2(x[2 * i], x[2 * i + 1]), sl2x2, nm2), y0, y1);
+            f2_split(ffma2(f2(x0[2 * i], x0[2 * i + 1]), sl2x2, nm2), y0, y1);
             const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
             sum2[i & 3] = fadd2(sum2[i & 3], f2(e0, e1));
-            pk[32 * hf + i] = pack_bf16x2(e0, e1);
+            pk[i] = pack_bf16x2(e0, e1);
+          }
+        }
+        {
+          const unsigned long long d2 = f2(d1, d1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float y0, y1;
+            unpack_f16x2(h1[i], y0, y1);
+            f2_split(fadd2(f2(y0, y1), d2), y0, y1);
+            const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
+            sum2[i & 3] = fadd2(sum2[i & 3], f2(e0, e1));
+            pk[32 + i] = pack_bf16x2(e0, e1);
           }
         }
         {
