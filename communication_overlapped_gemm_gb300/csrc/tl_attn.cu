@@ -33,7 +33,9 @@
 //   warp 1     TMEM allocation (both CTAs) and, in the leader, the pair MMAs (one thread).
 //   warps 2-9  softmax, two warpgroups: warpgroup g takes keys [128 g, 128 g + 128) of every
 //              block, one row per thread, in base 2 (the 1/sqrt(d) scale folded into one
-//              multiply-add per score).  The two warps of a TMEM lane quadrant (one per group,
+//              multiply-add per score).  A thread reads its 128 scores from TMEM once and
+//              announces "S read" at once; it keeps 64 of them in fp32 and 64 as f16 offsets
+//              from its block max (the register budget).  The two warps of a TMEM lane quadrant (one per group,
 //              the same 32 rows) exchange their block maxima through shared memory, so both
 //              use one running max m per row and one O; each keeps the sum l_g of its own
 //              keys.  m moves only when the block's max exceeds it by more than 2^8
