@@ -543,9 +543,13 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           const float nlm = (Ragged && lm == -INFINITY) ? 0.f : -lm;
 #pragma unroll
           for (int i = 0; i < 64; ++i) x0[i] = x[i];
+          const unsigned long long sl2x2 = f2(sl2, sl2), nlm2 = f2(nlm, nlm);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            h1[i] = pack_f16x2(fmaf(x[64 + 2 * i], sl2, nlm), fmaf(x[65 + 2 * i], sl2, nlm));
+          for (int i = 0; i < 32; ++i) {
+            float y0, y1;
+            f2_split(ffma2(f2(x[64 + 2 * i], x[65 + 2 * i]), sl2x2, nlm2), y0, y1);
+            h1[i] = pack_f16x2(y0, y1);
+          }
         }
         post(lm);
         float bm2;
