@@ -507,6 +507,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         float x0[64];
         uint32_t h1[32];
         float lm;  // this group's block max (base 2)
+        float r1;  // the reference the f16 offsets are taken from
         {
           uint32_t rr[4][32];
 #pragma unroll
@@ -539,8 +540,13 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], x[120 + k]);
           lm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
                sl2;  // the scale is positive: max commutes with it
-          // (Ragged: a group with no valid key in this block has lm = -inf; its y' are -inf.)
-          const float nlm = (Ragged && lm == -INFINITY) ? 0.f : -lm;
+          // The offsets are taken from the running max before this block, unless this group's
+          // block max exceeds it by more than 2^8 (an item's first block included), then from
+          // the block max: y' <= 2^8 either way, and unless the max moves they are the
+          // exponents themselves.  (Ragged: an item's first block with no valid key in this
+          // group has r1 = -inf and y' = -inf.)
+          r1 = lm > m2 + kRescaleLog2 ? lm : m2;
+          const float nlm = (Ragged && r1 == -INFINITY) ? 0.f : -r1;
 #pragma unroll
           for (int i = 0; i < 64; ++i) x0[i] = x[i];
           const unsigned long long sl2x2 = f2(sl2, sl2), nlm2 = f2(nlm, nlm);
@@ -586,7 +592,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         // lm <= the block max <= m2 + 2^8).
         // (Ragged: a row whose keys so far are all absent has m2 = -inf; its P is 0.)
         const float nm = (Ragged && m2 == -INFINITY) ? 0.f : -m2;
-        const float d1 = (Ragged && (lm == -INFINITY || m2 == -INFINITY)) ? 0.f : lm - m2;
+        const float d1 = (Ragged && (r1 == -INFINITY || m2 == -INFINITY)) ? 0.f : r1 - m2;
         unsigned long long sum2[4];  // 8 partial sums, two per register pair
         uint32_t pk[64];
 #pragma unroll
@@ -603,15 +609,26 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           }
         }
         {
-          const unsigned long long d2 = f2(d1, d1);
+          if (__any_sync(0xffffffffu, d1 != 0.f)) {  // the max moved (or an item's first block)
+            const unsigned long long d2 = f2(d1, d1);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float y0, y1;
-            unpack_f16x2(h1[i], y0, y1);
-            f2_split(fadd2(f2(y0, y1), d2), y0, y1);
-            const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
-            sum2[i & 3] = fadd2(sum2[i & 3], f2(e0, e1));
-            pk[32 + i] = pack_bf16x2(e0, e1);
+            for (int i = 0; i < 32; ++i) {
+              float y0, y1;
+              unpack_f16x2(h1[i], y0, y1);
+              f2_split(fadd2(f2(y0, y1), d2), y0, y1);
+              const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
+              sum2[i & 3] = fadd2(sum2[i & 3], f2(e0, e1));
+              pk[32 + i] = pack_bf16x2(e0, e1);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float y0, y1;
+              unpack_f16x2(h1[i], y0, y1);
+              const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
+              sum2[i & 3] = fadd2(sum2[i & 3], f2(e0, e1));
+              pk[32 + i] = pack_bf16x2(e0, e1);
+            }
           }
         }
         {
