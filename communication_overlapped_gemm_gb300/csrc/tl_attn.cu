@@ -79,6 +79,11 @@ constexpr int kMaxTail = 40;     // split items the workspace holds partial resu
 constexpr size_t kPartO = static_cast<size_t>(kBQ) * kD * 4;  // one CTA's fp32 O of a half
 constexpr size_t kPartML = static_cast<size_t>(kBQ) * 2 * 4;  // one CTA's (m, l) of a half
 constexpr uint32_t kColO = 384;  // TMEM columns of O
+// Of a thread's 128 scores, those kept in fp32 (the rest as f16 offsets).  64 measured best
+// (attn_16k 389 us); keeping more in fp32 raises register pressure past the 168-register cap:
+// 96 gave 397 us, 80 gave 442 us and 112 gave 841 us.
+constexpr int kKeepF32 = 64;
+static_assert(kKeepF32 % 2 == 0 && kKeepF32 <= 128, "fp32 / f16 split");
 constexpr float kRescaleLog2 = 8.0f;  // move the running max once it grows by more than this
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSoftWarps = 8;
@@ -504,8 +509,8 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         // group's block max, base 2): y' <= 0, and for the weights that matter (y' within
         // about 2^4 of 0) f16's 11-bit significand is finer than P's bf16 rounding.  S(J) is
         // then read, and S(J + 1) can be computed while the exponentials run.
-        float x0[64];
-        uint32_t h1[32];
+        float x0[kKeepF32];
+        uint32_t h1[(128 - kKeepF32) / 2];
         float lm;  // this group's block max (base 2)
         float r1;  // the reference the f16 offsets are taken from
         {
@@ -548,12 +553,12 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           r1 = lm > m2 + kRescaleLog2 ? lm : m2;
           const float nlm = (Ragged && r1 == -INFINITY) ? 0.f : -r1;
 #pragma unroll
-          for (int i = 0; i < 64; ++i) x0[i] = x[i];
+          for (int i = 0; i < kKeepF32; ++i) x0[i] = x[i];
           const unsigned long long sl2x2 = f2(sl2, sl2), nlm2 = f2(nlm, nlm);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < (128 - kKeepF32) / 2; ++i) {
             float y0, y1;
-            f2_split(ffma2(f2(x[64 + 2 * i], x[65 + 2 * i]), sl2x2, nlm2), y0, y1);
+            f2_split(ffma2(f2(x[kKeepF32 + 2 * i], x[kKeepF32 + 1 + 2 * i]), sl2x2, nlm2), y0, y1);
             h1[i] = pack_f16x2(y0, y1);
           }
         }
@@ -600,7 +605,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
         {
           const unsigned long long sl2x2 = f2(sl2, sl2), nm2 = f2(nm, nm);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < kKeepF32 / 2; ++i) {
             float y0, y1;
             f2_split(ffma2(f2(x0[2 * i], x0[2 * i + 1]), sl2x2, nm2), y0, y1);
             const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
@@ -612,22 +617,22 @@ __global__ void __launch_bounds__(attn::kThreads, 1) attn_kernel(const __grid_co
           if (__any_sync(0xffffffffu, d1 != 0.f)) {  // the max moved (or an item's first block)
             const unsigned long long d2 = f2(d1, d1);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < (128 - kKeepF32) / 2; ++i) {
               float y0, y1;
               unpack_f16x2(h1[i], y0, y1);
               f2_split(fadd2(f2(y0, y1), d2), y0, y1);
               const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
               sum2[i & 3] = fadd2(sum2[i & 3], f2(e0, e1));
-              pk[32 + i] = pack_bf16x2(e0, e1);
+              pk[kKeepF32 / 2 + i] = pack_bf16x2(e0, e1);
             }
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < (128 - kKeepF32) / 2; ++i) {
               float y0, y1;
               unpack_f16x2(h1[i], y0, y1);
               const float e0 = ex2_approx(y0), e1 = ex2_approx(y1);
               sum2[i & 3] = fadd2(sum2[i & 3], f2(e0, e1));
-              pk[32 + i] = pack_bf16x2(e0, e1);
+              pk[kKeepF32 / 2 + i] = pack_bf16x2(e0, e1);
             }
           }
         }
