@@ -51,7 +51,11 @@ MOE_LAUNCHES = 3  # routing, permutation, the persistent expert-GEMM + combine k
 # A kernel changed since the capture reports traffic null.
 NCU_TRAFFIC = {"ag_70b": {"fe1bb8d7778bd175": 587978240,   # profiles/ag_70b_persistent_kernel_ncu.md
                            "33004dd266fe890c": 587501056,   # its traffic re-captures
-                           "c63981ffce7b1bcf": 612093952}}
+                           "c63981ffce7b1bcf": 612093952},
+               # GEMM+RS, owner-slot chain and ring order, captured back to back on one box
+               # (profiles/rs_70b_ring_persistent_kernel_pair_ncu.md)
+               "rs_70b": {"c63981ffce7b1bcf": 5608278016},
+               "rs_70b_ring": {"c63981ffce7b1bcf": 8656728064}}
 
 
 # The sources the AllGather+GEMM kernel is compiled from: its translation unit and every
@@ -475,6 +479,9 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
         del wsr
     for key in ("gemm_alone_us", "gemm_alone_tflops"):
         out["rs_70b_ring"][key] = out["rs_70b"][key]
+    h = src_hash(AG_KERNEL_SOURCES)
+    for key in ("rs_70b", "rs_70b_ring"):
+        out[key]["ncu_dram_bytes"] = NCU_TRAFFIC[key].get(h)  # null once the kernel changed
     out["rs_70b_ring"]["fused_over_gemm_alone"] = round(out["rs_70b_ring"]["us"] / out["rs_70b"]["gemm_alone_us"], 4)
     rs_alone(out["rs_70b_ring"], lambda: tl.tl_reduce_scatter(ctx, parts, o, stream=stream), W * m * n * 4 + m * n * 2)
     del parts
@@ -821,8 +828,8 @@ def run_profile(args):
     name = args.profile
     # the communication-alone legs and the low-latency gather run on their workloads' inputs
     base = {"allgather_70b": "ag_70b", "allgather_70b_tma": "ag_70b", "reduce_scatter_70b": "rs_70b",
-            "ag_tiny_ll": "ag_tiny"}.get(name, name)
-    cfg = {"ag_tiny_ll": dict(ag_ll=1), "allgather_70b_tma": dict(mover_tma=1)}.get(name, {})
+            "ag_tiny_ll": "ag_tiny", "rs_70b_ring": "rs_70b"}.get(name, name)
+    cfg = {"ag_tiny_ll": dict(ag_ll=1), "allgather_70b_tma": dict(mover_tma=1), "rs_70b_ring": dict(rs_ring=1)}.get(name, {})
     ctx = tl.Context(0, **cfg)
     d = WORKLOADS[base].dims
     inp = workload_inputs(base) if name != "reduce_scatter_70b" else None
@@ -848,8 +855,8 @@ def run_profile(args):
         a = [dev_bf16(x, device) for x in inp["a"]]
         b = [dev_bf16(x, device) for x in inp["b"]]
         o = [torch.empty((d["m"] // d["W"], d["n"]), dtype=torch.bfloat16, device=device) for _ in range(d["W"])]
-        ws = torch.zeros(tl.tl_gemm_rs_workspace_bytes(d["W"], d["m"], d["n"], d["k_r"]), dtype=torch.uint8,
-                         device=device)
+        wsb = tl.tl_gemm_rs_ring_workspace_bytes if name == "rs_70b_ring" else tl.tl_gemm_rs_workspace_bytes
+        ws = torch.zeros(wsb(d["W"], d["m"], d["n"], d["k_r"]), dtype=torch.uint8, device=device)
         call = lambda: tl.tl_gemm_rs(ctx, a, b, o, ws)
     elif WORKLOADS[base].kind == "mlp2":
         x = [dev_bf16(v, device) for v in inp["x_shards"]]
@@ -925,7 +932,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only (no extra workloads / e2e / overlap)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile", choices=["ag_tiny", "ag_tiny_ll", "ag_70b", "allgather_70b", "allgather_70b_tma", "rs_70b",
-                                          "reduce_scatter_70b", "mlp2_8b", "moe_64e", "attn_16k"],
+                                          "rs_70b_ring", "reduce_scatter_70b", "mlp2_8b", "moe_64e", "attn_16k"],
                     help="only run this workload's call 4 times (target of an ncu capture), no timing")
     ap.add_argument("--trace", metavar="PATH", help="with --profile: trace one call (after 3 warm-up calls and an "
                     "L2 flush) and write its per-CTA timeline to PATH: Chrome trace JSON, or the decoded spans "
