@@ -273,6 +273,10 @@ struct OpBase {
   static __device__ void epilogue_prologue(const P&, int, int) {}
   static constexpr int kEpiWarps = 4;   // epilogue warps (4, or 8 = one warpgroup per 128-row half)
   static constexpr int kMaxMovers = 4;  // mover warps the launch bounds allow
+  // Dependent launch: the kernel is launched with programmatic stream serialization, so its
+  // CTAs may start (barrier set-up, TMEM allocation) while the kernel that writes its tables
+  // still runs; every role waits for that kernel (grid_dep_wait) before its first read.
+  static constexpr bool kDependentLaunch = false;
 };
 
 // Threads per CTA the launch bounds of an op's kernel allow.
@@ -529,6 +533,7 @@ __global__ void __launch_bounds__(op_max_threads<Op>(), 1)
   // CTAs outside the GEMM partition (e.g. a combine partition) run the op's side role.
   int gi = blockIdx.x, gn = gridDim.x;
   if (!Op::gemm_partition(p, gi, gn)) {
+    if constexpr (Op::kDependentLaunch) grid_dep_wait();
     Op::template side_role<Trace>(p, warp, lane, smem_raw);
     if constexpr (Trace) {
       __syncthreads();
@@ -559,6 +564,7 @@ __global__ void __launch_bounds__(op_max_threads<Op>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_slot;
+  if constexpr (Op::kDependentLaunch) grid_dep_wait();
 
   if (warp == 0) {
     role_producer<Op, Trace>(p, sm, lane, gi, gn);

@@ -92,9 +92,12 @@ int ag_ll_launch(tl_ctx* ctx, int W, int rank, const void* const* a_shards, cons
                  int m_per_rank, int n, int k, cudaStream_t stream);
 
 
-// Cooperative launch of one persistent CTA per SM (or cfg.grid_ctas), so that every CTA
-// that waits on a signal is co-resident with the CTAs that will set it.  While the context
-// has a trace buffer the span-recording instantiation runs.
+// Launch of one persistent CTA per SM (or cfg.grid_ctas), so that every CTA that waits on a
+// signal is co-resident with the CTAs that will set it: a cooperative launch, or for an op
+// with kDependentLaunch a launch with programmatic stream serialization after a check that
+// the device holds the whole grid at once (the two attributes are not combined; the kernel
+// before it never waits on this one, so its CTAs only delay this grid's start).  While the
+// context has a trace buffer the span-recording instantiation runs.
 template <class Op>
 int launch_persistent(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t stream, int mover_warps) {
   auto kern = ctx->trace_buf ? persistent_kernel<Op, true> : persistent_kernel<Op, false>;
@@ -109,8 +112,19 @@ int launch_persistent(tl_ctx* ctx, const typename Op::Params& p, cudaStream_t st
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if constexpr (Op::kDependentLaunch) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, cfg.blockDim.x, kSmemBytes) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return TL_ERR_CUDA;
+    }
+    if (per_sm * ctx->sms < ctx->ctas) return TL_ERR_UNSUPPORTED;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, q);

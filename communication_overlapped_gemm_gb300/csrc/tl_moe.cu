@@ -22,11 +22,13 @@ constexpr int kMaxTopk = 8;
 // ---------------------------------------------------------------------------- routing
 // One warp per token: top-k of the fp32 logits (larger first, equal values to the
 // lower expert index), softmax over all E logits in fp32 taken at the chosen experts,
-// optionally divided by their sum over the chosen experts (renorm).
+// optionally divided by their sum over the chosen experts (renorm).  It lets the
+// permutation kernel start at once (that kernel waits for this one before its first read).
 __global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E, int topk, int renorm,
                                  int* __restrict__ experts, float* __restrict__ gates) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  grid_dep_launch();
   if (t >= T) return;
 
   constexpr int kPer = kMaxExperts / 32;
@@ -88,6 +90,9 @@ __global__ void moe_route_kernel(const float* __restrict__ logits, int T, int E,
 //   row_meta[row] = {token, gate bits} of the row's assignment ({-1, 0} on padding rows), so
 //     the combine reads one 8-byte record per row instead of two dependent loads
 //   tile_expert / tile_rows for each 128-row tile of the padded layout (the f_R / f_S tables)
+// Launched as a dependent of the routing kernel: the zeroing CTAs run alongside it, the
+// expert CTAs wait for it (grid_dep_wait) before they read the routing; the persistent
+// kernel after it may start as soon as every CTA of this one is running.
 __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict__ experts, int n, int E, int topk,
                                                            const float* __restrict__ gates,
                                                            int* __restrict__ perm, int2* __restrict__ row_meta,
@@ -102,6 +107,7 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
   __shared__ int warp_pre[32];
   const int e = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  grid_dep_launch();
   if (e >= E) {
     // CTAs past the experts zero the fp32 output the combine partition adds into, on the
     // SMs the per-expert CTAs leave idle.
@@ -111,6 +117,7 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
     return;
   }
   for (int i = tid; i < E; i += blockDim.x) hist[i] = 0;
+  grid_dep_wait();
   __syncthreads();
   for (int a = tid; a < n; a += blockDim.x) {
     const unsigned ex = static_cast<unsigned>(experts[a]);
@@ -270,9 +277,10 @@ struct MoeOp : OpBase<MoeParams> {
   // combine partition's CTAs.
   static constexpr int kMaxMovers = 2;
   static constexpr uint32_t kTxBytes = Geo<128>::kStageBytes;
-  // The tile count and tile table come from the permutation kernel, which completed
-  // before this kernel started: read-only for this kernel, so they go through the
-  // non-coherent cache (one L2 trip per SM, then L1 hits).
+  static constexpr bool kDependentLaunch = true;
+  // The tile count and tile table come from the permutation kernel, which has completed
+  // before any role of this kernel reads them (grid_dep_wait): read-only from then on, so
+  // they go through the non-coherent cache (one L2 trip per SM, then L1 hits).
   static __device__ int mtiles(const Params& p) { return __ldg(p.num_mtiles); }
   static __device__ int num_tiles(const Params& p) { return mtiles(p) * (p.n_up + p.n_down); }
   static __device__ bool gemm_partition(const Params& p, int& gi, int& gn) {
@@ -657,12 +665,24 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   p.chunk = 2;  // row tiles per chunk
   p.lag = 6;    // chunks of up work ahead of the down chunk that reads them
   moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, ctx->cfg.moe_renorm, experts, gates);
-  const int zero_ctas = ctx->sms > E ? ctx->sms - E : 1;
-  moe_permute_kernel<<<E + zero_ctas, 1024, 0, st>>>(experts, T * topk, E, topk, gates, perm, row_meta, tile_expert,
-                                                     tile_rows, num_mtiles, counts, perm_out, counts_out,
-                                                     reinterpret_cast<float4*>(out),
-                                                     static_cast<size_t>(T) * H / 4);
   if (cudaGetLastError() != cudaSuccess) return TL_ERR_CUDA;
+  const int zero_ctas = ctx->sms > E ? ctx->sms - E : 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(E + zero_ctas, 1, 1);
+  lc.blockDim = dim3(1024, 1, 1);
+  lc.stream = st;
+  cudaLaunchAttribute la[1];
+  la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  la[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = la;
+  lc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&lc, moe_permute_kernel, static_cast<const int*>(experts), T * topk, E, topk,
+                         static_cast<const float*>(gates), perm, row_meta, tile_expert, tile_rows, num_mtiles, counts,
+                         perm_out, counts_out, reinterpret_cast<float4*>(out),
+                         static_cast<size_t>(T) * H / 4) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TL_ERR_CUDA;
+  }
 
   // Two extra warps per CTA: the token gather in the GEMM partition, combine workers in the
   // combine CTAs.

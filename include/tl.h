@@ -317,9 +317,12 @@ int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const void* const* 
  *   out_t   = sum_j gate_(t,j) * y_(t,j)                  (fp32)
  * workspace: tl_moe_workspace_bytes().
  * Three launches: the routing (a warp per token), the permutation and tile tables (a CTA per
- * expert, while the remaining CTAs zero `out`), then one persistent cooperative launch whose
- * GEMM partition runs the gather and the grouped GEMMs while the combine partition adds
- * finished y tiles into `out`.
+ * expert, while the remaining CTAs zero `out`), then one persistent launch of one CTA per SM
+ * whose GEMM partition runs the gather and the grouped GEMMs while the combine partition adds
+ * finished y tiles into `out`.  The second and third are dependent launches (programmatic
+ * stream serialization): each starts while the one before it runs and waits for it before
+ * reading its results.  TL_ERR_UNSUPPORTED if the device cannot hold the persistent grid at
+ * once.
  * Shapes: T >= 1; 1 <= topk <= 8; topk <= E <= 256; H % 256 == 0; F % 128 == 0.
  */
 size_t tl_moe_workspace_bytes(int T, int H, int E, int F, int topk);
