@@ -51,11 +51,12 @@ MOE_LAUNCHES = 3  # routing, permutation, the persistent expert-GEMM + combine k
 # A kernel changed since the capture reports traffic null.
 NCU_TRAFFIC = {"ag_70b": {"fe1bb8d7778bd175": 587978240,   # profiles/ag_70b_persistent_kernel_ncu.md
                            "33004dd266fe890c": 587501056,   # its traffic re-captures
-                           "c63981ffce7b1bcf": 612093952},
+                           "c63981ffce7b1bcf": 612093952,
+                           "06013d50fb65ebef": 612273152},
                # GEMM+RS, owner-slot chain and ring order, captured back to back on one box
                # (profiles/rs_70b_ring_persistent_kernel_pair_ncu.md)
-               "rs_70b": {"c63981ffce7b1bcf": 5608278016},
-               "rs_70b_ring": {"c63981ffce7b1bcf": 8656728064}}
+               "rs_70b": {"c63981ffce7b1bcf": 5608278016, "06013d50fb65ebef": 5641131520},
+               "rs_70b_ring": {"c63981ffce7b1bcf": 8656728064, "06013d50fb65ebef": 7760482816}}
 
 
 # The sources the AllGather+GEMM kernel is compiled from: its translation unit and every
@@ -554,14 +555,14 @@ def sub_workloads(tl, ctx, flush, stream, device, pk, args):
     moe_bytes = 3.0 * E * H * F * 2 + T * H * 2 + T * E * 4 + T * H * 4 + 2.0 * T * kk * (H * 2 + F * 2 + H * 2)
     rec("moe_64e", lambda: tl.tl_moe_combine(ctx, xx, lg, kk, wg, wu, wd, oo, ws, stream=stream), moe_flops,
         moe_bytes, "hbm", MOE_LAUNCHES)
-    out["moe_64e"]["combine_sms"] = ctx.config.combine_ctas
-    # the workload as stated: the combine partition on 8 reserved SMs
-    with tl.Context(ctx.device, combine_ctas=8) as c8:
-        rec("moe_64e_8sm", lambda: tl.tl_moe_combine(c8, xx, lg, kk, wg, wu, wd, oo, ws, stream=stream), moe_flops,
+    out["moe_64e"]["combine_sms"] = ctx.config.combine_ctas  # the workload as stated: 8 reserved SMs
+    # the same layer with a 16-SM combine partition, for comparison
+    with tl.Context(ctx.device, combine_ctas=16) as c16:
+        rec("moe_64e_16sm", lambda: tl.tl_moe_combine(c16, xx, lg, kk, wg, wu, wd, oo, ws, stream=stream), moe_flops,
             moe_bytes, "hbm", MOE_LAUNCHES)
-        if c8.check() != tl.TL_OK:
-            raise RuntimeError("moe_64e_8sm: device status not OK")
-    out["moe_64e_8sm"]["combine_sms"] = 8
+        if c16.check() != tl.TL_OK:
+            raise RuntimeError("moe_64e_16sm: device status not OK")
+    out["moe_64e_16sm"]["combine_sms"] = 16
     oracle_time(out["moe_64e"], "moe_64e", inp, args)
     del xx, lg, wg, wu, wd, oo, ws
 

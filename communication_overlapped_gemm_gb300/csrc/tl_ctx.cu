@@ -79,7 +79,7 @@ int tl_config_default(tl_config* cfg) {
   cfg->chunks_per_slab = 32;
   cfg->swizzle = 1;
   cfg->grid_ctas = 0;
-  cfg->combine_ctas = 16;
+  cfg->combine_ctas = 8;
   cfg->debug_skip_chunk = -1;
   cfg->timeout_ns = 2000000000ull;
   cfg->pair_ctas = 2;

@@ -271,6 +271,10 @@ struct OpBase {
   // Work the epilogue warps may do before their first tile (they idle until then).
   template <bool Trace>
   static __device__ void epilogue_prologue(const P&, int, int) {}
+  // Work of a GEMM-partition CTA after its last tile (all threads; the shared memory and the
+  // tensor memory are free by then).
+  template <bool Trace>
+  static __device__ void after_gemm(const P&, int, int, uint8_t*) {}
   static constexpr int kEpiWarps = 4;   // epilogue warps (4, or 8 = one warpgroup per 128-row half)
   static constexpr int kMaxMovers = 4;  // mover warps the launch bounds allow
   // Dependent launch: the kernel is launched with programmatic stream serialization, so its
@@ -578,10 +582,14 @@ __global__ void __launch_bounds__(op_max_threads<Op>(), 1)
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (Trace) trace_end(p.common);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+  Op::template after_gemm<Trace>(p, warp, lane, smem_raw);
+  if constexpr (Trace) {
+    __syncthreads();
+    trace_end(p.common);
   }
 }
 

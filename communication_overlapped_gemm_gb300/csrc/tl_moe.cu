@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
                                                            int* __restrict__ tile_expert, int* __restrict__ tile_rows,
                                                            int* __restrict__ num_mtiles, int* __restrict__ counts,
                                                            int* __restrict__ perm_out, int* __restrict__ counts_out,
-                                                           float4* __restrict__ out, size_t out_vec) {
+                                                           float4* __restrict__ out, size_t out_vec,
+                                                           int* __restrict__ combine_next) {
   __shared__ int hist[kMaxExperts];
   __shared__ int off[kMaxExperts + 1];
   __shared__ int poff[kMaxExperts + 1];
@@ -227,7 +228,10 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int* __restrict
   if (tid == 0) {
     counts[e] = cnt;
     if (counts_out) counts_out[e] = cnt;
-    if (e == 0) *num_mtiles = poff[E] / kBM;
+    if (e == 0) {
+      *num_mtiles = poff[E] / kBM;
+      *combine_next = 0;
+    }
   }
 }
 
@@ -253,6 +257,7 @@ struct MoeParams {
   float* out;
   uint64_t* up_flags;  // [R/128][n_up]
   uint64_t* y_flags;   // [R/128][n_down]
+  int* combine_next;   // the next y tile to combine (claimed at run time)
   int T, H, E, F, topk, n_up, n_down, kb_up, kb_down, combine_ctas, chunk, lag;
 };
 
@@ -471,20 +476,23 @@ struct MoeOp : OpBase<MoeParams> {
     else
       st_release_gpu(p.y_flags + static_cast<size_t>(j.x0) * p.n_down + j.x1, p.common.epoch);
   }
-  // Combine partition: y tiles are taken in the order the GEMM partition produces them;
-  // for each valid row a = (t, j): out[t, cols] += gate_a * y[a, cols] (fp32 vector
-  // reductions; with a zeroed out and top-2, 0 + a + b == 0 + b + a, so the result
-  // does not depend on which contribution lands first).
+  // Combine: y tiles are claimed in the order the GEMM partition produces them, from a
+  // counter (combine_next); for each valid row a = (t, j): out[t, cols] += gate_a * y[a, cols]
+  // (fp32 vector reductions; with a zeroed out and top-2, 0 + a + b == 0 + b + a, so the
+  // result does not depend on which contribution lands first or which CTA adds it).  The
+  // combine partition claims tiles from the start; each GEMM-partition CTA joins after its
+  // last GEMM tile (after_gemm), so the tiles still waiting when the GEMM work ends are
+  // spread over the whole grid instead of queueing on the partition.
   //
-  // Each combine CTA runs two independent halves (warps 0-3 and 4-7), each with its own
-  // 64 KB shared-memory tile buffer: the half's first warp waits on the tile's signal, one
+  // A CTA runs two independent halves (warps 0-3 and 4-7), each with its own 64 KB
+  // shared-memory tile buffer: the half's first warp claims a tile, waits on its signal, one
   // lane TMA-loads the 128 x 256 y tile, and the half stages the 128 rows' (token, gate)
   // records.  Each warp then takes 32 rows: for every row, lane l scales columns
   // [4l, 4l+4) and [128+4l, 128+4l+4) by the gate and adds them into out[token] with two
   // fp32 vector reductions, so each warp instruction covers 512 contiguous bytes of the
   // output row.  While one half waits for its load the other reduces.
   template <bool Trace>
-  static __device__ void side_role(const Params& p, int warp, int lane, uint8_t* smem_raw) {
+  static __device__ void combine(const Params& p, int warp, int lane, uint8_t* smem_raw) {
     uint8_t* base =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int kTileBytes = kBM * kBN * 2;  // 64 KB of bf16 y
@@ -493,20 +501,24 @@ struct MoeOp : OpBase<MoeParams> {
     const int hw = warp & 3;  // warp inside the half
     uint8_t* buf = base + half * kTileBytes;
     int2* meta = reinterpret_cast<int2*>(base + 2 * kTileBytes) + half * kBM;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + 2 * kTileBytes + 2 * kBM * sizeof(int2)) + half;
+    uint8_t* ctl = base + 2 * kTileBytes + 2 * kBM * sizeof(int2);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(ctl) + half;
+    int* claim = reinterpret_cast<int*>(ctl + 2 * sizeof(uint64_t)) + half;  // the half's claimed tile
     if (hw == 0 && lane == 0) {
       mbar_init(bar, 1);
       fence_mbar_init();
     }
-    named_bar_sync(1 + half, 128);
-    const int cc = blockIdx.x - (gridDim.x - p.combine_ctas);
     const int m = mtiles(p);
     const int total = m * p.n_down;
     // This lane's two 4-column groups: box g (64 columns each), byte offset inside the 128-B row.
     const int g0 = lane >> 4, g1 = 2 + (lane >> 4);
     const int piece = (lane & 15) >> 1, sub = (lane & 1) * 8;
     uint32_t phase = 0;
-    for (int v = 2 * cc + half; v < total; v += 2 * p.combine_ctas) {
+    for (;;) {
+      if (hw == 0 && lane == 0) *claim = atomicAdd(p.combine_next, 1);
+      named_bar_sync(1 + half, 128);
+      const int v = *reinterpret_cast<volatile int*>(claim);
+      if (v >= total) break;
       const MoeSlot sl = down_slot(p, m, v);
       if (hw == 0) {
         const uint64_t w0 = Trace ? globaltimer() : 0;
@@ -548,9 +560,20 @@ struct MoeOp : OpBase<MoeParams> {
         red_add_v4(o, gt * fa.x, gt * fa.y, gt * fb.x, gt * fb.y);
         red_add_v4(o + 128, gt * fc.x, gt * fc.y, gt * fd.x, gt * fd.y);
       }
-      named_bar_sync(1 + half, 128);  // the tile buffer and records are free for the next tile
+      named_bar_sync(1 + half, 128);  // the tile buffer, records and claim are free again
       if (Trace && hw == 0 && lane == 0) trace_close(p.common, globaltimer());
     }
+  }
+  template <bool Trace>
+  static __device__ void side_role(const Params& p, int warp, int lane, uint8_t* smem_raw) {
+    combine<Trace>(p, warp, lane, smem_raw);
+  }
+  // The operand ring the tile buffers now reuse was last written by TMA and read by the
+  // tensor cores (the async proxy): order those accesses before this thread's own.
+  template <bool Trace>
+  static __device__ void after_gemm(const Params& p, int warp, int lane, uint8_t* smem_raw) {
+    fence_proxy_async_smem();
+    combine<Trace>(p, warp, lane, smem_raw);
   }
 };
 
@@ -563,7 +586,7 @@ static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct MoeLayout {
   size_t experts, gates, perm, row_meta, tile_expert, tile_rows, num_mtiles, counts, xp, h, y, up_flags, y_flags,
-      x_flags, total;
+      x_flags, combine_next, total;
   int rmax;
 };
 
@@ -588,6 +611,7 @@ static MoeLayout moe_layout(int T, int H, int E, int F, int topk) {
   L.up_flags = o; o += al256(tiles * (F / 128) * 8);
   L.y_flags = o; o += al256(tiles * (H / kBN) * 8);
   L.x_flags = o; o += al256(tiles * kGatherPieces * 8);
+  L.combine_next = o; o += 256;
   L.total = o;
   return L;
 }
@@ -652,6 +676,7 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   p.out = out;
   p.up_flags = reinterpret_cast<uint64_t*>(ws + L.up_flags);
   p.y_flags = reinterpret_cast<uint64_t*>(ws + L.y_flags);
+  p.combine_next = reinterpret_cast<int*>(ws + L.combine_next);
   p.T = T;
   p.H = H;
   p.E = E;
@@ -679,7 +704,7 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   if (cudaLaunchKernelEx(&lc, moe_permute_kernel, static_cast<const int*>(experts), T * topk, E, topk,
                          static_cast<const float*>(gates), perm, row_meta, tile_expert, tile_rows, num_mtiles, counts,
                          perm_out, counts_out, reinterpret_cast<float4*>(out),
-                         static_cast<size_t>(T) * H / 4) != cudaSuccess) {
+                         static_cast<size_t>(T) * H / 4, p.combine_next) != cudaSuccess) {
     (void)cudaGetLastError();
     return TL_ERR_CUDA;
   }

@@ -77,7 +77,7 @@ typedef struct tl_config {
   int chunks_per_slab;        /* mover chunks, hence signals, per 128-row slab (1..32; default 32)     */
   int swizzle;                /* 0: identity tile order; 1: rank-swizzled ([TD] §3.7; default)          */
   int grid_ctas;              /* persistent CTAs; 0 = one per SM (default)                              */
-  int combine_ctas;           /* MoE combine partition, CTAs = SMs ([RA]; default 16)                   */
+  int combine_ctas;           /* MoE combine partition, CTAs = SMs ([RA]; default 8)                    */
   int debug_skip_chunk;       /* fault injection: this mover chunk is copied but never signalled (-1 off) */
   unsigned long long timeout_ns; /* bound of every device wait (default 2e9 ns)                       */
   int pair_ctas;              /* where shards / owner blocks are 256-row multiples, 256 x 256 tiles run
@@ -304,7 +304,8 @@ int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const void* const* 
  * [TL] §4.1 (dynamic mapping tables filled by the routing), §7.2 (Gather + GroupGEMM, then
  * GroupGEMM + Scatter + TopK reduce), [RA] MoE abstract (persistent expert producer; a
  * persistent combine consumer on `combine_ctas` dedicated SMs that handles output tiles as
- * their ready signals arrive).
+ * their ready signals arrive; the GEMM partition's CTAs join it after their last GEMM tile,
+ * each y tile claimed once at run time).
  *
  * x: bf16 [T x H]; logits: fp32 [T x E]; w_gate, w_up: bf16 [E x H x F]; w_down: bf16 [E x F x H].
  * out: fp32 [T x H] (written, not accumulated into).

@@ -51,7 +51,7 @@ def test_built_for_sm103a_only():
 def test_config_defaults_and_strerror(tl):
     c = tl.Config()
     assert tl.lib().tl_config_default(ctypes.byref(c)) == tl.TL_OK
-    assert (c.mover_warps, c.chunks_per_slab, c.swizzle, c.grid_ctas, c.combine_ctas) == (4, 32, 1, 0, 16)
+    assert (c.mover_warps, c.chunks_per_slab, c.swizzle, c.grid_ctas, c.combine_ctas) == (4, 32, 1, 0, 8)
     assert c.debug_skip_chunk == -1 and c.timeout_ns == 2_000_000_000 and c.pair_ctas == 2 and c.moe_renorm == 0
     assert c.rs_ring == 0 and c.ag_push == 0 and c.mover_kparts == 0 and c.ag_ll == 0
     assert c.mover_tma == 0

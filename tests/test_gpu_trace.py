@@ -1,8 +1,8 @@
 """GPU checks of the per-CTA trace buffer (tl_ctx_set_trace).
 
 With tracing on, every tile of a fused call appears exactly once in the MMA warp's spans,
-once per epilogue warp, every mover chunk once, and every combined y tile of the MoE side
-partition once; the results are bit-identical to an untraced call.
+once per epilogue warp, every mover chunk once, and every combined y tile of the MoE layer
+once; the results are bit-identical to an untraced call.
 """
 import numpy as np
 import pytest
@@ -118,5 +118,7 @@ def test_trace_moe_side_partition():
         sp = tr["spans"]
         once_each(sp, 10, m * n_down)        # every y tile combined once
         once_each(sp, 4, m * (n_up + n_down))
+        # y tiles are claimed at run time by the combine partition and, after their last GEMM
+        # tile, by the GEMM partition's CTAs: each is combined exactly once, by some CTA
         side = sp["cta"][sp["kind"] == 10]
-        assert side.min() >= ctx.num_ctas - ctx.config.combine_ctas
+        assert side.min() >= 0 and side.max() < ctx.num_ctas
