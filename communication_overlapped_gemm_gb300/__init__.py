@@ -25,7 +25,7 @@ __all__ = [
     "tl_ag_gemm", "tl_ag_gemm_ll_capable", "tl_allgather", "tl_gemm_rs", "tl_reduce_scatter", "tl_mlp2",
     "tl_moe_combine",
     "tl_ag_gemm_workspace_bytes", "tl_gemm_rs_workspace_bytes", "tl_gemm_rs_ring_workspace_bytes",
-    "tl_mlp2_workspace_bytes", "tl_rs_ring_tile_order",
+    "tl_mlp2_workspace_bytes", "tl_rs_ring_tile_order", "tl_moe_tile_order", "tl_moe_combine_order",
     "tl_moe_workspace_bytes", "tl_ag_tile_order", "tl_rs_tile_order", "tl_trace_bytes", "tl_ag_attention",
     "tl_ag_attention_workspace_bytes", "EXPORTED_SYMBOLS",
 ]
@@ -97,6 +97,8 @@ _SIGS = {
     "tl_ag_tile_order": (_i, [_i, _i, _i, _i, _i, _vp, _vp, _vp, _i]),
     "tl_rs_tile_order": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _i]),
     "tl_rs_ring_tile_order": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i]),
+    "tl_moe_tile_order": (_i, [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i]),
+    "tl_moe_combine_order": (_i, [_i, _i, _i, _i, _i, _i, _vp, _vp, _i]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -401,6 +403,32 @@ def tl_rs_ring_tile_order(W, m, n):
     rc = L.tl_rs_ring_tile_order(W, m, n, *[o.ctypes.data for o in out], cnt)
     if rc < 0:
         raise TLError(rc, "tl_rs_ring_tile_order")
+    return tuple(out)
+
+
+def tl_moe_tile_order(T, H, E, F, topk, m_tiles):
+    import numpy as np
+    L = lib()
+    cnt = L.tl_moe_tile_order(T, H, E, F, topk, m_tiles, None, None, None, 0)
+    if cnt < 0:
+        raise TLError(cnt, "tl_moe_tile_order")
+    out = [np.zeros(cnt, dtype=np.int32) for _ in range(3)]
+    rc = L.tl_moe_tile_order(T, H, E, F, topk, m_tiles, *[o.ctypes.data for o in out], cnt)
+    if rc < 0:
+        raise TLError(rc, "tl_moe_tile_order")
+    return tuple(out)
+
+
+def tl_moe_combine_order(T, H, E, F, topk, m_tiles):
+    import numpy as np
+    L = lib()
+    cnt = L.tl_moe_combine_order(T, H, E, F, topk, m_tiles, None, None, 0)
+    if cnt < 0:
+        raise TLError(cnt, "tl_moe_combine_order")
+    out = [np.zeros(cnt, dtype=np.int32) for _ in range(2)]
+    rc = L.tl_moe_combine_order(T, H, E, F, topk, m_tiles, *[o.ctypes.data for o in out], cnt)
+    if rc < 0:
+        raise TLError(rc, "tl_moe_combine_order")
     return tuple(out)
 
 

@@ -270,6 +270,54 @@ struct MoeSlot {
   int nb;    // column block
 };
 
+// The tile order of the persistent kernel (see MoeOp) for m row tiles, n_up / n_down column
+// blocks, chunks of G row tiles and a down chunk `lag` chunks behind its up chunk.  Host and
+// device share it: the kernel's scheduler and tl_moe_tile_order / tl_moe_combine_order.
+struct MoeOrder {
+  int m, n_up, n_down, G, lag;
+};
+TL_HD int moe_rows_before(int c, int m, int G) { return c * G < m ? c * G : m; }
+// Tiles before group g: the up tiles of chunks 0 .. min(g, nc) - 1 and the down tiles of
+// chunks 0 .. g - lag - 1 (every chunk holds G row tiles but the last, which holds
+// m - (nc - 1) G).
+TL_HD int moe_group_start(const MoeOrder& o, int nc, int g) {
+  const int cu = g < nc ? g : nc;
+  int cd = g - o.lag < nc ? g - o.lag : nc;
+  cd = cd > 0 ? cd : 0;
+  return moe_rows_before(cu, o.m, o.G) * o.n_up + moe_rows_before(cd, o.m, o.G) * o.n_down;
+}
+TL_HD MoeSlot moe_slot(const MoeOrder& o, int t) {
+  const int G = o.G;
+  const int nc = (o.m + G - 1) / G;
+  // the last group g with group_start(g) <= t (binary search over g in [0, nc + lag))
+  int lo = 0, hi = nc + o.lag - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (moe_group_start(o, nc, mid) <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int g = lo;
+  int w = t - moe_group_start(o, nc, g);
+  if (g < nc) {
+    const int gc = o.m - g * G < G ? o.m - g * G : G;
+    if (w < gc * o.n_up) return MoeSlot{1, g * G + w % gc, w / gc};
+    w -= gc * o.n_up;
+  }
+  const int c = g - o.lag;
+  const int gc = o.m - c * G < G ? o.m - c * G : G;
+  return MoeSlot{2, c * G + w % gc, w / gc};
+}
+// The v-th down-projection tile in production order (the order the combine claims them in).
+TL_HD MoeSlot moe_down_slot(const MoeOrder& o, int v) {
+  const int G = o.G;
+  const int c = v / (G * o.n_down);
+  const int gc = o.m - c * G < G ? o.m - c * G : G;
+  const int w = v - c * G * o.n_down;
+  return MoeSlot{2, c * G + w % gc, w / gc};
+}
+
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
@@ -303,45 +351,11 @@ struct MoeOp : OpBase<MoeParams> {
   // at least the chunk count runs every up tile first, then every down tile, in chunk order.
   // Inside a chunk the row tile is the fastest index, so the row tiles of one expert, which
   // share its weight columns, run side by side.
-  // Tiles before group g: the up tiles of chunks 0 .. min(g, nc) - 1 and the down tiles of
-  // chunks 0 .. g - lag - 1 (every chunk holds G row tiles but the last, which holds
-  // m - (nc - 1) G).
-  static __device__ __forceinline__ int rows_before(int c, int m, int G) { return min(c * G, m); }
-  static __device__ __forceinline__ int group_start(const Params& p, int m, int nc, int g) {
-    const int cu = min(g, nc), cd = max(0, min(g - p.lag, nc));
-    return rows_before(cu, m, p.chunk) * p.n_up + rows_before(cd, m, p.chunk) * p.n_down;
+  static __device__ __forceinline__ MoeOrder order(const Params& p, int m) {
+    return MoeOrder{m, p.n_up, p.n_down, p.chunk, p.lag};
   }
-  static __device__ MoeSlot slot(const Params& p, int m, int t) {
-    const int G = p.chunk;
-    const int nc = (m + G - 1) / G;
-    // the last group g with group_start(g) <= t (binary search over g in [0, nc + lag))
-    int lo = 0, hi = nc + p.lag - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (group_start(p, m, nc, mid) <= t)
-        lo = mid;
-      else
-        hi = mid - 1;
-    }
-    const int g = lo;
-    int w = t - group_start(p, m, nc, g);
-    if (g < nc) {
-      const int gc = min(G, m - g * G);
-      if (w < gc * p.n_up) return MoeSlot{1, g * G + w % gc, w / gc};
-      w -= gc * p.n_up;
-    }
-    const int c = g - p.lag;
-    const int gc = min(G, m - c * G);
-    return MoeSlot{2, c * G + w % gc, w / gc};
-  }
-  // The v-th down-projection tile in production order (the combine partition's order).
-  static __device__ MoeSlot down_slot(const Params& p, int m, int v) {
-    const int G = p.chunk;
-    const int c = v / (G * p.n_down);
-    const int gc = min(G, m - c * G);
-    const int w = v - c * G * p.n_down;
-    return MoeSlot{2, c * G + w % gc, w / gc};
-  }
+  static __device__ MoeSlot slot(const Params& p, int m, int t) { return moe_slot(order(p, m), t); }
+  static __device__ MoeSlot down_slot(const Params& p, int m, int v) { return moe_down_slot(order(p, m), v); }
   static __device__ Job job(const Params& p, int t) {
     const MoeSlot sl = slot(p, mtiles(p), t);
     Job j;
@@ -617,6 +631,14 @@ static MoeLayout moe_layout(int T, int H, int E, int F, int topk) {
   return L;
 }
 
+// Row tiles per chunk of the tile order, and the lag of a down chunk behind its up chunk: at
+// least the number of chunks, so every up tile runs before the first down tile.  With the
+// GEMM CTAs joining the combine after their last tile, starting the down tiles (and the
+// combine) early no longer pays: 252.9 us against 267.3 us with a lag of 6 chunks on the
+// 4096-token, 64-expert layer.
+constexpr int kMoeChunk = 2;
+static int moe_lag(const MoeLayout& L) { return (L.rmax / kBM + kMoeChunk - 1) / kMoeChunk; }
+
 static bool moe_shape_ok(int T, int H, int E, int F, int topk) {
   return T >= 1 && topk >= 1 && topk <= kMaxTopk && E >= topk && E <= kMaxExperts && H > 0 && F > 0 &&
          H % kBN == 0 && F % 128 == 0 && static_cast<long long>(T) * topk < (1LL << 30);
@@ -625,6 +647,44 @@ static bool moe_shape_ok(int T, int H, int E, int F, int topk) {
 extern "C" size_t tl_moe_workspace_bytes(int T, int H, int E, int F, int topk) {
   if (!moe_shape_ok(T, H, E, F, topk)) return 0;
   return moe_layout(T, H, E, F, topk).total;
+}
+
+// The order tl_moe_combine's persistent kernel uses for a layer whose routing produced
+// m_tiles padded row tiles (kind 1 = up, 2 = down, row tile, column block).
+extern "C" int tl_moe_tile_order(int T, int H, int E, int F, int topk, int m_tiles, int* kind, int* row_tile,
+                                 int* col_block, int cap) {
+  if (!moe_shape_ok(T, H, E, F, topk)) return TL_ERR_INVALID;
+  const MoeLayout L = moe_layout(T, H, E, F, topk);
+  if (m_tiles < 0 || m_tiles > L.rmax / kBM) return TL_ERR_INVALID;
+  const MoeOrder o{m_tiles, F / 128, H / kBN, kMoeChunk, moe_lag(L)};
+  const int total = m_tiles * (o.n_up + o.n_down);
+  if (!kind && !row_tile && !col_block) return total;
+  if (!kind || !row_tile || !col_block || cap < total) return TL_ERR_INVALID;
+  for (int t = 0; t < total; ++t) {
+    const MoeSlot sl = moe_slot(o, t);
+    kind[t] = sl.kind;
+    row_tile[t] = sl.i;
+    col_block[t] = sl.nb;
+  }
+  return total;
+}
+
+// The order the combine claims y tiles in (row tile, column block).
+extern "C" int tl_moe_combine_order(int T, int H, int E, int F, int topk, int m_tiles, int* row_tile,
+                                    int* col_block, int cap) {
+  if (!moe_shape_ok(T, H, E, F, topk)) return TL_ERR_INVALID;
+  const MoeLayout L = moe_layout(T, H, E, F, topk);
+  if (m_tiles < 0 || m_tiles > L.rmax / kBM) return TL_ERR_INVALID;
+  const MoeOrder o{m_tiles, F / 128, H / kBN, kMoeChunk, moe_lag(L)};
+  const int total = m_tiles * o.n_down;
+  if (!row_tile && !col_block) return total;
+  if (!row_tile || !col_block || cap < total) return TL_ERR_INVALID;
+  for (int v = 0; v < total; ++v) {
+    const MoeSlot sl = moe_down_slot(o, v);
+    row_tile[v] = sl.i;
+    col_block[v] = sl.nb;
+  }
+  return total;
 }
 
 extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, int topk, const void* w_gate,
@@ -688,12 +748,8 @@ extern "C" int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, i
   p.kb_up = H / kBK;
   p.kb_down = F / kBK;
   p.combine_ctas = ctx->cfg.combine_ctas;
-  p.chunk = 2;  // row tiles per chunk
-  // Chunks of up work ahead of the down chunk that reads them: at least the number of
-  // chunks, so every up tile runs before the first down tile.  With the GEMM CTAs joining the
-  // combine after their last tile, starting the down tiles (and the combine) early no longer
-  // pays: 252.9 us against 267.3 us with a lag of 6 chunks on the 4096-token, 64-expert layer.
-  p.lag = (L.rmax / kBM + p.chunk - 1) / p.chunk;
+  p.chunk = kMoeChunk;
+  p.lag = moe_lag(L);
   moe_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, topk, ctx->cfg.moe_renorm, experts, gates);
   if (cudaGetLastError() != cudaSuccess) return TL_ERR_CUDA;
   const int zero_ctas = ctx->sms > E ? ctx->sms - E : 1;

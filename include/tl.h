@@ -327,6 +327,19 @@ int tl_mlp2(tl_ctx* ctx, int W, const void* const* x_shards, const void* const* 
  * Shapes: T >= 1; 1 <= topk <= 8; topk <= E <= 256; H % 256 == 0; F % 128 == 0.
  */
 size_t tl_moe_workspace_bytes(int T, int H, int E, int F, int topk);
+/* The tile order of tl_moe_combine's persistent kernel, for host-side checks ([TL] §4.1: the
+ * tile-to-work mapping is filled at run time; here the closed form behind it).  m_tiles is
+ * the number of 128-row padded row tiles the routing produced (sum over experts of
+ * ceil(count_e / 128)); 0 <= m_tiles <= the bound the workspace is sized for.
+ * tl_moe_tile_order: for t = 0..count-1, the tile's kind (1 = gate/up, 2 = down), row tile
+ *   and column block (128 columns of F for kind 1, 256 columns of H for kind 2).
+ * tl_moe_combine_order: for v = 0..count-1, the row tile and column block of the v-th y tile
+ *   the combine claims.
+ * Both return the number of tiles, or TL_ERR_INVALID (bad shape, m_tiles out of range, or
+ * arrays shorter than `cap`).  Arrays may all be NULL to query the count.  Host only. */
+int tl_moe_tile_order(int T, int H, int E, int F, int topk, int m_tiles, int* kind, int* row_tile, int* col_block,
+                      int cap);
+int tl_moe_combine_order(int T, int H, int E, int F, int topk, int m_tiles, int* row_tile, int* col_block, int cap);
 int tl_moe_combine(tl_ctx* ctx, const void* x, const float* logits, int topk, const void* w_gate,
                    const void* w_up, const void* w_down, float* out, int* perm_out, int* counts_out,
                    void* workspace, size_t workspace_bytes, int T, int H, int E, int F, tl_stream_t stream);

@@ -221,3 +221,44 @@ def test_static_scratch_binding_checks_shapes_before_any_call(tl):
     with pytest.raises(ValueError, match="inconsistent shapes"):
         tl.tl_ag_gemm_static_scratch(None, a, torch.zeros((128, 256), dtype=torch.bfloat16),
                                      torch.zeros((256, 256), dtype=torch.bfloat16))
+
+
+@pytest.mark.parametrize("T,H,E,F,k,m", [(4096, 2048, 64, 1408, 2, 96), (4096, 2048, 64, 1408, 2, 127),
+                                         (4096, 2048, 64, 1408, 2, 1), (300, 512, 16, 256, 2, 13),
+                                         (96, 256, 256, 128, 8, 1), (200, 256, 8, 384, 3, 7),
+                                         (64, 256, 4, 128, 2, 0)])
+def test_moe_tile_order(tl, T, H, E, F, k, m):
+    """The persistent MoE kernel's tile order ([TL] §4.1 dynamic mapping, its closed form):
+    every up and down tile exactly once; every down tile after all up tiles of its row tile,
+    so a co-resident grid taking tiles in this order never waits on a later tile; every up tile
+    before the first down tile; the down tiles in the order the combine claims them, and for
+    each column block their row tiles ascending (the tile of a token's lower expert comes
+    first)."""
+    n_up, n_down = F // 128, H // 256
+    kind, row, col = tl.tl_moe_tile_order(T, H, E, F, k, m)
+    tiles = list(zip(kind.tolist(), row.tolist(), col.tolist()))
+    assert len(tiles) == m * (n_up + n_down)
+    assert sorted(tiles) == sorted([(1, r, c) for r in range(m) for c in range(n_up)] +
+                                   [(2, r, c) for r in range(m) for c in range(n_down)])
+    pos = {t: i for i, t in enumerate(tiles)}
+    for r in range(m):
+        last_up = max(pos[(1, r, c)] for c in range(n_up))
+        assert all(pos[(2, r, c)] > last_up for c in range(n_down))
+    assert kind.tolist() == sorted(kind.tolist())  # all up tiles (1) before all down tiles (2)
+    crow, ccol = tl.tl_moe_combine_order(T, H, E, F, k, m)
+    downs = [(r, c) for (kk, r, c) in tiles if kk == 2]
+    assert list(zip(crow.tolist(), ccol.tolist())) == downs
+    for c in range(n_down):
+        rows_c = [r for (r, cc) in downs if cc == c]
+        assert rows_c == sorted(rows_c)
+
+
+def test_moe_tile_order_refuses_bad_queries(tl):
+    rmax_tiles = -(-(4096 * 2 + 127 * 64) // 128)  # the row-tile bound the workspace is sized for
+    assert tl.tl_moe_tile_order(4096, 2048, 64, 1408, 2, rmax_tiles)[0].size == rmax_tiles * (11 + 8)
+    for bad in ((4096, 2048, 64, 1408, 2, rmax_tiles + 1), (4096, 2048, 64, 1408, 2, -1),
+                (4096, 2000, 64, 1408, 2, 4)):
+        with pytest.raises(tl.TLError):
+            tl.tl_moe_tile_order(*bad)
+        with pytest.raises(tl.TLError):
+            tl.tl_moe_combine_order(*bad)
