@@ -52,11 +52,14 @@ MOE_LAUNCHES = 3  # routing, permutation, the persistent expert-GEMM + combine k
 NCU_TRAFFIC = {"ag_70b": {"fe1bb8d7778bd175": 587978240,   # profiles/ag_70b_persistent_kernel_ncu.md
                            "33004dd266fe890c": 587501056,   # its traffic re-captures
                            "c63981ffce7b1bcf": 612093952,
-                           "06013d50fb65ebef": 612273152},
+                           "06013d50fb65ebef": 612273152,
+                           "abcbff1dabca23fc": 612214528},
                # GEMM+RS, owner-slot chain and ring order, captured back to back on one box
                # (profiles/rs_70b_ring_persistent_kernel_pair_ncu.md)
-               "rs_70b": {"c63981ffce7b1bcf": 5608278016, "06013d50fb65ebef": 5641131520},
-               "rs_70b_ring": {"c63981ffce7b1bcf": 8656728064, "06013d50fb65ebef": 7760482816}}
+               "rs_70b": {"c63981ffce7b1bcf": 5608278016, "06013d50fb65ebef": 5641131520,
+                          "abcbff1dabca23fc": 5573654528},
+               "rs_70b_ring": {"c63981ffce7b1bcf": 8656728064, "06013d50fb65ebef": 7760482816,
+                               "abcbff1dabca23fc": 9909475584}}
 
 
 # The sources the AllGather+GEMM kernel is compiled from: its translation unit and every
