@@ -104,3 +104,18 @@ def test_moe_full_size_on_eight_combine_sms(ctx):
     assert_close(out8[toks], rows, "moe_64e on 8 combine SMs, sampled tokens")
     out16, _, _ = run_moe(ctx, inp, 2)
     assert np.array_equal(out8, out16)
+
+
+@pytest.mark.parametrize("cfg", [dict(combine_ctas=1), dict(grid_ctas=16, combine_ctas=2), dict(grid_ctas=3, combine_ctas=1)])
+def test_moe_small_grids_and_partitions(ctx, cfg):
+    """The combine's run-time claims with few CTAs: a one-SM partition, and grids of 16 and 3
+    CTAs where most y tiles are combined by GEMM CTAs after their last tile.  The result
+    matches the oracle and is bit-identical to the default configuration's."""
+    inp = make_inputs("moe", 95, T=300, H=512, E=16, F=256)
+    ref_out, _, _ = run_moe(ctx, inp, 2)
+    with tl.Context(0, **cfg) as c2:
+        out, perm, counts = run_moe(c2, inp, 2)
+    ref = oracle.moe(inp["x"], inp["logits"], inp["w_gate"], inp["w_up"], inp["w_down"], 2)
+    assert np.array_equal(perm, ref["perm"]) and np.array_equal(counts, ref["counts"])
+    assert_close(out, ref["out"], f"moe {cfg}")
+    assert np.array_equal(out, ref_out)
